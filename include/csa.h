@@ -1,0 +1,192 @@
+/*
+ * csa.h -- C ABI of the B300 (sm_103a) library for the DeepSeek-V4 hybrid
+ * compressed attention hot path: CSA (compressed sparse attention) and HCA
+ * (heavily compressed attention).
+ *
+ * Pages defining the operations (title, site):
+ *   [peacm]   "DeepSeek-V4百万上下文时代的开源宣言" (peacm.com), §三.2 混合注意力机制
+ *   [gitcode] "DeepSeek-V4 技术报告深度解析" (gitcode.csdn.net), §2.1 混合注意力机制
+ *   [wiki]    "DeepSeek V4 (Flash & Pro)：通往百万级上下文与万亿参数推理的新纪元",
+ *             混合注意力机制：CSA 与 HCA 的协同逻辑
+ *
+ * Conventions common to every entry point
+ *   - Every data pointer is a caller-owned DEVICE buffer unless stated.  The
+ *     library never allocates or frees memory, never keeps pointers after a
+ *     call returns, and launches all work on the given stream without
+ *     synchronising (csa_check_status is the one call that synchronises).
+ *   - Arguments are validated on the host before anything is launched; a
+ *     failed check returns CSA_ERR_INVALID_ARG or CSA_ERR_UNSUPPORTED, has no
+ *     side effect and launches nothing.  A failed launch returns CSA_ERR_CUDA.
+ *     csa_last_error() then holds a one-line reason (per host thread).
+ *   - Data-dependent errors that only the device can see (a top-k index that
+ *     is not a complete block, a window position missing from the window
+ *     buffer, a query position beyond the cache capacity) never fault: the
+ *     kernel skips the offending row and sets a bit in the status word at the
+ *     start of the workspace.  csa_check_status() reports and clears it.
+ *   - Row-major layouts; the last dimension is contiguous.  Every device
+ *     pointer must be 16-byte aligned.
+ *   - Positions are absolute token indices (int64).  A query at position i
+ *     sees compressed block b when b*m + m - 1 <= i ("causally complete"),
+ *     i.e. the first floor((i+1)/m) blocks, and the raw window tokens
+ *     max(0, i-W+1) .. i.
+ */
+#ifndef CSA_B300_H
+#define CSA_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI-compatible with cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st* csa_stream_t;
+
+typedef enum {
+    CSA_OK = 0,
+    CSA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or params     */
+    CSA_ERR_UNSUPPORTED = 2, /* valid request outside the shapes this build runs */
+    CSA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed              */
+    CSA_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required        */
+    CSA_ERR_DEVICE = 5       /* csa_check_status: the device flagged bad data     */
+} csa_status;
+
+/* Storage formats.
+ *   CSA_F32, CSA_BF16: D values per row.
+ *   CSA_FP8_MIXED (cache/window rows only) [gitcode §2.1.4 "KV 缓存精度":
+ *   RoPE dims in BF16, the other dims in FP8]: dims 0..D-65 as OCP E4M3 bytes,
+ *   then the 64 RoPE dims D-64..D-1 as bfloat16, then (D-64)/64 float32
+ *   scales, one per 64-dim group (value = code * scale; scale = group amax /
+ *   448, or 1 for an all-zero group), zero padding to a multiple of 16 bytes
+ *   (608 bytes for D = 512). */
+typedef enum { CSA_F32 = 0, CSA_BF16 = 1, CSA_FP8_MIXED = 2 } csa_format;
+
+/* Device status bits (csa_check_status). */
+#define CSA_DEV_BAD_TOPK_INDEX 0x1u /* selected block not complete or >= n_cap */
+#define CSA_DEV_BAD_WINDOW 0x2u     /* window position not in the window buffer */
+#define CSA_DEV_BAD_POSITION 0x4u   /* floor((i+1)/m) exceeds the cache capacity */
+#define CSA_DEV_TIMEOUT 0x8u        /* a bounded wait inside a kernel expired     */
+
+/* Layer hyper-parameters, passed by pointer (read during the call only). */
+typedef struct {
+    int32_t head_dim;        /* D: 128 or 512 (any multiple of 64 up to 512)          */
+    int32_t rope_dims;       /* rotated trailing dims; must be 64 [peacm 四项关键 Trick] */
+    float rope_base;         /* theta_j = rope_base^(-2j/rope_dims); 10000              */
+    float norm_eps;          /* RMSNorm epsilon (unit gain); 1e-6                       */
+    float softmax_scale;     /* logit scale; <= 0 selects 1/sqrt(D)                     */
+    int32_t ratio;           /* m: tokens per compressed block (CSA 4, HCA 128, 1 = window rows) */
+    int32_t topk;            /* k: blocks kept per query (CSA), 1..4096                 */
+    int32_t window;          /* W: raw sliding-window tokens per query, 0..1024         */
+    int32_t derotate_output; /* nonzero: rotate the output by RoPE at position -i       */
+    int32_t act_format;      /* CSA_F32 or CSA_BF16: q, raw kv, indexer q/keys, outputs */
+    int32_t kv_format;       /* CSA_F32 (with F32 act), CSA_BF16 or CSA_FP8_MIXED      */
+} csa_params;
+
+/* Bytes of one stored cache/window row of `head_dim` dims in `kv_format`
+ * (D*4, D*2, or the mixed layout above); -1 for an unsupported pair. */
+int64_t csa_row_bytes(int32_t kv_format, int32_t head_dim);
+
+/* Write float32 rows into the cache row format p->kv_format (the cache
+ * writer).  For CSA_FP8_MIXED each 64-dim group is quantised with
+ * scale = amax/448 (float32), code = E4M3 round-to-nearest-even of x/scale
+ * with saturation [gitcode §2.1.4 "KV 缓存精度"].
+ *   src: [n_rows, D] float32.  dst: [n_rows] rows of csa_row_bytes bytes. */
+csa_status csa_cache_pack(const csa_params* p, const float* src, int64_t n_rows, void* dst,
+                          csa_stream_t stream);
+
+/* Block compressor [peacm §三.2 CSA "Step 1: KV 压缩 每 m 个 token -> 1 个压缩
+ * KV entry" (attention-like pooling with learnable weights); HCA "压缩率 m'
+ * 128"; 四项关键 Trick "Q/KV Normalization", "Partial RoPE"].  For every
+ * complete block b of m = p->ratio tokens at positions pos0+b*m .. pos0+b*m+m-1:
+ *   z_t = kv_t . w_z + bias[t mod m];  alpha = softmax_t(z);  c = sum alpha_t kv_t
+ *   entry = RoPE(RMSNorm(c), pos0 + b*m + m - 1)
+ * stored in p->kv_format.  m = 1 produces the window rows RoPE(RMSNorm(kv_t), t).
+ *   kv_raw: B sequences of T raw tokens [.., D] in p->act_format; sequence s
+ *           starts at row s*kv_seq_stride.
+ *   pos0:   position of the first token (same for every sequence); must be a
+ *           multiple of m.  T need not be: a trailing partial block is skipped.
+ *   w_z: [D] float32; bias: [m] float32.
+ *   out:    the T/m entries of sequence s start at row s*out_seq_stride. */
+csa_status csa_compress(const csa_params* p, const void* kv_raw, int32_t B, int64_t T,
+                        int64_t kv_seq_stride, int64_t pos0, const float* w_z, const float* bias,
+                        void* out, int64_t out_seq_stride, csa_stream_t stream);
+
+/* Lightning indexer + top-k [peacm §三.2 CSA "Step 2: Lightning Indexer Top-K
+ * 选择"; gitcode §2.1.1].  For query q at position i = q_pos[q] in sequence
+ * s = q / (Q/B), over the complete blocks b < floor((i+1)/m):
+ *   score_b = sum_h w_idx[q,h] * relu(q_idx[q,h,:] . keys[s,b,:])
+ * and keeps the top min(k, floor((i+1)/m)) blocks, ties to the lower index.
+ *   q_idx:  [Q, n_idx_heads, idx_dim] in p->act_format; w_idx: [Q, n_idx_heads] f32
+ *   keys:   [B, n_cap, idx_dim] in p->act_format
+ *   q_pos:  [Q] int64 (device)
+ *   topk_idx:   [Q, k] int32, selected block indices in ascending index order,
+ *               padded with -1 at the end
+ *   topk_score: [Q, k] float32 scores in the same order (-inf padding) or NULL
+ *   ws: workspace of at least csa_workspace_bytes(p, CSA_OP_INDEX_TOPK, ...).
+ * Requires Q % B == 0, idx_dim in {64, 128}, n_idx_heads <= 64. */
+csa_status csa_index_topk(const csa_params* p, const void* q_idx, const float* w_idx,
+                          int32_t n_idx_heads, int32_t idx_dim, const void* keys, int64_t n_cap,
+                          int32_t B, int32_t Q, const int64_t* q_pos, int32_t* topk_idx,
+                          float* topk_score, void* ws, size_t ws_bytes, csa_stream_t stream);
+
+/* CSA core attention [peacm §三.2 CSA "Step 3: Core Attention Multi-Query
+ * Attention" over the top-k blocks; 四项关键 Trick: Q/KV Normalization, Partial
+ * RoPE and output RoPE at -i, Sliding Window (most recent W raw tokens),
+ * Attention Sink; gitcode §2.1.4].  For query q (position i, sequence s):
+ *   q'_h  = RoPE(RMSNorm(q[q,h,:]), i)
+ *   J     = { cache[s, topk_idx[q,j]] : topk_idx != -1 } U { window rows of
+ *           positions max(0, i-W+1) .. i }   (one KV head: key = value = row)
+ *   l_hj  = scale * q'_h . row_j
+ *   lse_h = log(exp(sink[h]) + sum_j exp(l_hj))
+ *   out_h = sum_j exp(l_hj - lse_h) row_j, then RoPE(out_h, -i) when
+ *           p->derotate_output is set.  Empty J with sink -inf gives out 0, lse -inf.
+ *   q:      [Q, H, D] in p->act_format (raw: normalised and rotated here)
+ *   cache:  [B, n_cap] rows in p->kv_format
+ *   topk_idx: [Q, k] int32 (-1 entries skipped), e.g. from csa_index_topk
+ *   window: [B, n_win] rows in p->kv_format; row r of sequence s holds
+ *           position win_pos0[s] + r (win_pos0: [B] int64, device)
+ *   sink:   [H] float32 (-inf allowed)
+ *   out:    [Q, H, D] in p->act_format;  lse: [Q, H] float32 or NULL
+ * Requires Q % B == 0, H <= 128. */
+csa_status csa_attend(const csa_params* p, const void* q, int32_t H, int32_t B, int32_t Q,
+                      const int64_t* q_pos, const void* cache, int64_t n_cap,
+                      const int32_t* topk_idx, const void* window, int64_t n_win,
+                      const int64_t* win_pos0, const float* sink, void* out, float* lse,
+                      void* ws, size_t ws_bytes, csa_stream_t stream);
+
+/* HCA core attention [peacm §三.2 HCA "无稀疏筛选 对所有压缩 KV 做 dense
+ * attention"; wiki "128:1 的比例压缩为稠密的 MQA 流 并辅以一个 128 令牌的滑动
+ * 窗口"]: as csa_attend with J = every complete block 0 .. floor((i+1)/m)-1
+ * of the sequence plus the same window; m = p->ratio (128 for HCA). */
+csa_status hca_attend(const csa_params* p, const void* q, int32_t H, int32_t B, int32_t Q,
+                      const int64_t* q_pos, const void* cache, int64_t n_cap, const void* window,
+                      int64_t n_win, const int64_t* win_pos0, const float* sink, void* out,
+                      float* lse, void* ws, size_t ws_bytes, csa_stream_t stream);
+
+/* Workspace */
+typedef enum { CSA_OP_INDEX_TOPK = 1, CSA_OP_ATTEND = 2, CSA_OP_HCA_ATTEND = 3 } csa_op;
+
+/* Bytes of workspace an operation needs for these sizes (0 on invalid input).
+ * The first 256 bytes of every workspace hold the device status word; one
+ * workspace may serve several operations in stream order. */
+size_t csa_workspace_bytes(const csa_params* p, int32_t op, int32_t B, int32_t Q, int32_t H,
+                           int32_t n_idx_heads, int64_t n_cap, int64_t n_win);
+
+/* Zero the status word (asynchronous; call once after allocating a workspace). */
+csa_status csa_workspace_init(void* ws, size_t ws_bytes, csa_stream_t stream);
+
+/* Synchronise `stream`, read and clear the status word.  Returns CSA_OK, or
+ * CSA_ERR_DEVICE with the CSA_DEV_* bits described by csa_last_error(). */
+csa_status csa_check_status(void* ws, csa_stream_t stream);
+
+/* Raw status bits of the last csa_check_status on this thread. */
+uint32_t csa_last_device_bits(void);
+
+const char* csa_status_string(csa_status s);
+const char* csa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA_B300_H */

@@ -1,0 +1,144 @@
+// common.cuh -- device helpers shared by the kernels of libcsa (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "csa.h"
+
+namespace csa {
+
+constexpr int kRopeDims = 64;
+constexpr uint32_t kStatusWordBytes = 256;  // head of every workspace
+
+// ---------------------------------------------------------------- formats
+__host__ __device__ inline int64_t fp8m_row_bytes(int D) {
+    int64_t raw = (int64_t)(D - kRopeDims) + kRopeDims * 2 + 4 * (int64_t)((D - kRopeDims) / 64);
+    return (raw + 15) / 16 * 16;
+}
+
+__host__ __device__ inline int64_t row_bytes(int fmt, int D) {
+    if (fmt == CSA_F32) return 4 * (int64_t)D;
+    if (fmt == CSA_BF16) return 2 * (int64_t)D;
+    if (fmt == CSA_FP8_MIXED) return fp8m_row_bytes(D);
+    return -1;
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(((uint32_t)h) << 16); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+    __nv_bfloat16 b = __float2bfloat16_rn(f);
+    return *reinterpret_cast<uint16_t*>(&b);
+}
+
+// E4M3 code -> float (exact); uses the hardware conversion.
+__device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
+    __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)c, __NV_E4M3);
+    return __half2float(*reinterpret_cast<__half*>(&hr));
+}
+
+// float -> E4M3, round to nearest even, saturating to +-448 (hardware conversion).
+__device__ __forceinline__ uint8_t f32_to_e4m3_sat(float f) {
+    return (uint8_t)__nv_cvt_float_to_fp8(f, __NV_SATFINITE, __NV_E4M3);
+}
+
+// Read element d of a row in an activation format (F32 / BF16).
+__device__ __forceinline__ float load_act(const void* row, int fmt, int d) {
+    if (fmt == CSA_F32) return reinterpret_cast<const float*>(row)[d];
+    return bf16_to_f32(reinterpret_cast<const uint16_t*>(row)[d]);
+}
+
+__device__ __forceinline__ void store_act(void* row, int fmt, int d, float v) {
+    if (fmt == CSA_F32)
+        reinterpret_cast<float*>(row)[d] = v;
+    else
+        reinterpret_cast<uint16_t*>(row)[d] = f32_to_bf16_rn(v);
+}
+
+// Decode element d of a stored cache row (F32 / BF16 / FP8_MIXED).
+__device__ __forceinline__ float load_kv(const uint8_t* row, int fmt, int D, int d) {
+    if (fmt == CSA_F32) return reinterpret_cast<const float*>(row)[d];
+    if (fmt == CSA_BF16) return bf16_to_f32(reinterpret_cast<const uint16_t*>(row)[d]);
+    int nf = D - kRopeDims;
+    if (d >= nf) return bf16_to_f32(reinterpret_cast<const uint16_t*>(row + nf)[d - nf]);
+    const float* scales = reinterpret_cast<const float*>(row + nf + 2 * kRopeDims);
+    return e4m3_to_f32(row[d]) * scales[d >> 6];
+}
+
+// ---------------------------------------------------------------- RoPE
+// cos/sin of pos * base^(-2j/R), evaluated in double so that positions up to
+// 2^20 and beyond keep a full-precision angle.
+__device__ __forceinline__ void rope_cos_sin(double pos, int j, int R, double base, float* c,
+                                             float* s) {
+    double theta = pow(base, -2.0 * (double)j / (double)R);
+    double sn, cs;
+    sincos(pos * theta, &sn, &cs);
+    *c = (float)cs;
+    *s = (float)sn;
+}
+
+// ---------------------------------------------------------------- reductions
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Store one row held in shared memory (float32, D values) into a cache row
+// format.  Executed by one full warp.  For FP8_MIXED every 64-dim group is
+// quantised with scale = amax/448 (1 for an all-zero group).
+__device__ inline void warp_pack_row(const float* __restrict__ src, int D, int fmt,
+                                     uint8_t* __restrict__ dst) {
+    const int lane = threadIdx.x & 31;
+    if (fmt == CSA_F32) {
+        float* o = reinterpret_cast<float*>(dst);
+        for (int d = lane; d < D; d += 32) o[d] = src[d];
+        return;
+    }
+    if (fmt == CSA_BF16) {
+        uint16_t* o = reinterpret_cast<uint16_t*>(dst);
+        for (int d = lane; d < D; d += 32) o[d] = f32_to_bf16_rn(src[d]);
+        return;
+    }
+    const int nf = D - kRopeDims;
+    float* scales = reinterpret_cast<float*>(dst + nf + 2 * kRopeDims);
+    // chunks of 16 dims: four consecutive lanes cover one 64-dim group
+    for (int c0 = 0; c0 < nf / 16; c0 += 32) {
+        int c = c0 + lane;
+        bool active = c < nf / 16;
+        float amax = 0.f;
+        if (active)
+            for (int e = 0; e < 16; e++) amax = fmaxf(amax, fabsf(src[16 * c + e]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        float scale = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+        if (active) {
+            uint32_t w[4];
+            for (int e4 = 0; e4 < 4; e4++) {
+                uint32_t v = 0;
+                for (int b = 0; b < 4; b++) {
+                    float x = __fdiv_rn(src[16 * c + 4 * e4 + b], scale);
+                    v |= (uint32_t)f32_to_e4m3_sat(x) << (8 * b);
+                }
+                w[e4] = v;
+            }
+            *reinterpret_cast<uint4*>(dst + 16 * c) = make_uint4(w[0], w[1], w[2], w[3]);
+            if ((c & 3) == 0) scales[c >> 2] = scale;
+        }
+    }
+    uint16_t* rope = reinterpret_cast<uint16_t*>(dst + nf);
+    for (int j = lane; j < kRopeDims; j += 32) rope[j] = f32_to_bf16_rn(src[nf + j]);
+    // zero padding after the scales
+    int64_t used = nf + 2 * kRopeDims + 4 * (nf / 64);
+    int64_t total = fp8m_row_bytes(D);
+    for (int64_t b = used + lane; b < total; b += 32) dst[b] = 0;
+}
+
+}  // namespace csa

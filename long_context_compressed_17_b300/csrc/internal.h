@@ -1,0 +1,63 @@
+// internal.h -- launchers behind the C ABI (host side, no validation here:
+// csa_capi.cu validates every argument before calling these).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "csa.h"
+
+namespace csa {
+
+struct Geometry {  // resolved layer constants
+    int D, R, m, k, W;
+    float base, eps, scale;
+    int derotate;
+    int act, kv;
+    int64_t kv_row_bytes;
+};
+
+Geometry resolve(const csa_params* p);
+
+// Workspace layout of an operation.  Offsets are in bytes from the start of
+// the workspace; every region is 256-byte aligned.
+struct IndexTopkPlan {
+    size_t scores_off, scores_bytes;  // [Q, n_cap_pad] float32
+    int64_t n_cap_pad;
+    size_t total;
+};
+IndexTopkPlan plan_index_topk(const Geometry& g, int B, int Q, int HI, int64_t n_cap);
+
+struct AttendPlan {
+    int splits;           // split-K factor over the row list
+    int64_t list_len;     // rows per query in the list (before masking)
+    int64_t rows_per_split;
+    int head_group;       // heads per CTA
+    int use_tc;           // tensor-core kernel
+    size_t part_o_off, part_ml_off;  // [Q, S, H, D] and [Q, S, H, 2] float32
+    size_t total;
+};
+AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int64_t n_cap);
+
+cudaError_t launch_cache_pack(const Geometry& g, const float* src, int64_t n, void* dst,
+                              cudaStream_t st);
+cudaError_t launch_compress(const Geometry& g, const void* kv, int B, int64_t T,
+                            int64_t kv_stride, int64_t pos0, const float* w_z, const float* bias,
+                            void* out, int64_t out_stride, cudaStream_t st);
+cudaError_t launch_indexer(const Geometry& g, const IndexTopkPlan& pl, const void* q_idx,
+                           const float* w_idx, int HI, int dI, const void* keys, int64_t n_cap,
+                           int B, int Q, const int64_t* q_pos, uint32_t* status, float* scores,
+                           cudaStream_t st);
+cudaError_t launch_topk(const Geometry& g, const IndexTopkPlan& pl, const float* scores,
+                        int64_t n_cap, int B, int Q, const int64_t* q_pos, int32_t* idx,
+                        float* sel, cudaStream_t st);
+cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, const void* q,
+                          int H, int B, int Q, const int64_t* q_pos, const void* cache,
+                          int64_t n_cap, const int32_t* topk_idx, const void* window,
+                          int64_t n_win, const int64_t* win_pos0, const float* sink, void* out,
+                          float* lse, uint8_t* ws, uint32_t* status, cudaStream_t st);
+
+int num_sms();
+
+}  // namespace csa

@@ -1,0 +1,329 @@
+// k_attend.cu -- CSA / HCA core attention, CUDA-core path, and the split-K
+// log-sum-exp combine shared by every attention path.
+//
+// "DeepSeek-V4百万上下文时代的开源宣言" §三.2: CSA Step 3 (multi-query attention
+// over the top-k blocks), HCA (dense attention over every compressed block),
+// and 四项关键 Trick: RMSNorm on q and KV, partial RoPE on the last 64 dims and
+// RoPE at -i on the output, a sliding window of the last 128 raw tokens, and a
+// learnable sink logit in the softmax denominator.
+//
+// A query's rows form one list: [selected blocks (CSA) | every block (HCA)]
+// followed by the W window positions i-W+1 .. i.  The list is cut into
+// `splits` contiguous ranges; each CTA reduces one range for a group of heads
+// into an unnormalised partial (m, l, o) and attend_combine_kernel merges the
+// partials, adds the sink once and applies the output rotation.  The split
+// count depends on the list length and the SM count only, never on the batch
+// composition of a single query.
+#include "common.cuh"
+#include "internal.h"
+
+namespace csa {
+
+constexpr int kAttThreads = 256;
+constexpr int kAttRows = 32;
+
+struct AttendArgs {
+    const uint8_t* q;
+    int act;
+    int H, qps;
+    const int64_t* q_pos;
+    const uint8_t* cache;
+    int64_t n_cap;
+    int64_t rb;  // stored row bytes
+    int kvfmt;
+    const int32_t* topk_idx;  // nullptr: dense (HCA)
+    int k;
+    const uint8_t* window;
+    int64_t n_win;
+    const int64_t* win_pos0;
+    int W, m, R;
+    double base;
+    float eps, scale;
+    float* part_o;   // [Q, S, H, D]
+    float* part_ml;  // [Q, S, H, 2]
+    int S;
+    int64_t list_base;  // k (CSA) or n_cap (HCA): list position of the first window row
+    int64_t rows_per_split;
+    uint32_t* status;
+};
+
+// Resolve list position p of query (seq, i) to a stored row, or nullptr when
+// the row is masked (padding, not yet complete, before position 0).
+__device__ __forceinline__ const uint8_t* resolve_row(const AttendArgs& a, int64_t qi, int seq,
+                                                      int64_t i, int64_t n_av, int64_t p) {
+    if (p < a.list_base) {
+        int64_t e;
+        if (a.topk_idx) {
+            e = a.topk_idx[qi * a.k + p];
+            if (e < 0) return nullptr;
+            if (e >= n_av) {
+                atomicOr(a.status, CSA_DEV_BAD_TOPK_INDEX);
+                return nullptr;
+            }
+        } else {
+            e = p;
+            if (e >= n_av) return nullptr;
+        }
+        return a.cache + ((int64_t)seq * a.n_cap + e) * a.rb;
+    }
+    int64_t wpos = i - a.W + 1 + (p - a.list_base);
+    if (wpos < 0) return nullptr;
+    int64_t wr = wpos - a.win_pos0[seq];
+    if (wr < 0 || wr >= a.n_win) {
+        atomicOr(a.status, CSA_DEV_BAD_WINDOW);
+        return nullptr;
+    }
+    return a.window + ((int64_t)seq * a.n_win + wr) * a.rb;
+}
+
+// Normalise and rotate the query heads [h0, h0+nh) into qs (float32).
+__device__ inline void prepare_q(const AttendArgs& a, int64_t qi, int64_t i, int h0, int nh, int D,
+                                 float* qs, float* cs) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int j = tid; j < a.R / 2; j += blockDim.x) rope_cos_sin((double)i, j, a.R, a.base, &cs[2 * j], &cs[2 * j + 1]);
+    const int act_es = a.act == CSA_F32 ? 4 : 2;
+    for (int h = warp; h < nh; h += blockDim.x / 32) {
+        const uint8_t* qr = a.q + ((int64_t)qi * a.H + h0 + h) * D * act_es;
+        float ss = 0.f;
+        for (int d = lane; d < D; d += 32) {
+            float x = load_act(qr, a.act, d);
+            qs[h * D + d] = x;
+            ss = fmaf(x, x, ss);
+        }
+        ss = warp_sum(ss);
+        float r = 1.f / sqrtf(ss / (float)D + a.eps);
+        for (int d = lane; d < D; d += 32) qs[h * D + d] *= r;
+    }
+    __syncthreads();
+    for (int e = tid; e < nh * (a.R / 2); e += blockDim.x) {
+        int h = e / (a.R / 2), j = e % (a.R / 2);
+        float c = cs[2 * j], s = cs[2 * j + 1];
+        float* x = qs + h * D + D - a.R + 2 * j;
+        float x0 = x[0], x1 = x[1];
+        x[0] = x0 * c - x1 * s;
+        x[1] = x0 * s + x1 * c;
+    }
+    __syncthreads();
+}
+
+template <int D, int HG>
+__global__ void __launch_bounds__(kAttThreads) attend_generic_kernel(AttendArgs a) {
+    constexpr int TPH = kAttThreads / HG;   // threads per head in the PV update
+    constexpr int OPT = D / TPH;            // output dims per thread
+    constexpr int ES = D + 1;               // padded row stride (bank-conflict free)
+    extern __shared__ float sm[];
+    float* qs = sm;                          // [HG][D]
+    float* es = qs + HG * D;                 // [kAttRows][ES]
+    float* pr = es + kAttRows * ES;          // [HG][kAttRows]
+    float* mh = pr + HG * kAttRows;          // [HG]
+    float* lh = mh + HG;                     // [HG]
+    float* al = lh + HG;                     // [HG]
+    float* cs = al + HG;                     // [R]
+    const uint8_t** rp = reinterpret_cast<const uint8_t**>(cs + 64);  // [kAttRows]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int split = blockIdx.z, h0 = blockIdx.y * HG;
+    const int64_t qi = blockIdx.x;
+    const int seq = (int)(qi / a.qps);
+    const int64_t i = a.q_pos[qi];
+    int64_t n_av = (i + 1) / a.m;
+    if (n_av > a.n_cap) {
+        if (tid == 0) atomicOr(a.status, CSA_DEV_BAD_POSITION);
+        n_av = a.n_cap;
+    }
+    prepare_q(a, qi, i, h0, HG, D, qs, cs);
+    if (tid < HG) {
+        mh[tid] = -INFINITY;
+        lh[tid] = 0.f;
+    }
+    float o[OPT];
+#pragma unroll
+    for (int u = 0; u < OPT; u++) o[u] = 0.f;
+    const int hl = tid / TPH, dl = tid % TPH;
+
+    const int64_t list_len = a.list_base + a.W;
+    const int64_t r0 = (int64_t)split * a.rows_per_split;
+    const int64_t r1 = min(list_len, r0 + a.rows_per_split);
+    for (int64_t t0 = r0; t0 < r1; t0 += kAttRows) {
+        if (tid < kAttRows) {
+            int64_t p = t0 + tid;
+            rp[tid] = (p < r1) ? resolve_row(a, qi, seq, i, n_av, p) : nullptr;
+        }
+        __syncthreads();
+        for (int e = tid; e < kAttRows * D; e += kAttThreads) {
+            int r = e / D, d = e % D;
+            const uint8_t* row = rp[r];
+            es[r * ES + d] = row ? load_kv(row, a.kvfmt, D, d) : 0.f;
+        }
+        __syncthreads();
+        for (int h = warp; h < HG; h += kAttThreads / 32) {
+            float s = 0.f;
+            const float* qh = qs + h * D;
+            const float* er = es + lane * ES;
+#pragma unroll 8
+            for (int d = 0; d < D; d++) s = fmaf(qh[d], er[d], s);
+            s = rp[lane] ? s * a.scale : -INFINITY;
+            float mt = warp_max(s);
+            float m_old = mh[h];
+            float m_new = fmaxf(m_old, mt);
+            float p = (m_new == -INFINITY) ? 0.f : expf(s - m_new);
+            float alpha = (m_new == -INFINITY) ? 1.f : expf(m_old - m_new);
+            float ps = warp_sum(p);
+            pr[h * kAttRows + lane] = p;
+            if (lane == 0) {
+                mh[h] = m_new;
+                lh[h] = lh[h] * alpha + ps;
+                al[h] = alpha;
+            }
+        }
+        __syncthreads();
+        const float alpha = al[hl];
+#pragma unroll
+        for (int u = 0; u < OPT; u++) o[u] *= alpha;
+        for (int r = 0; r < kAttRows; r++) {
+            float p = pr[hl * kAttRows + r];
+            const float* er = es + r * ES + dl;
+#pragma unroll
+            for (int u = 0; u < OPT; u++) o[u] = fmaf(p, er[u * TPH], o[u]);
+        }
+        __syncthreads();
+    }
+    const int64_t pbase = ((qi * a.S + split) * a.H + h0 + hl);
+#pragma unroll
+    for (int u = 0; u < OPT; u++) a.part_o[pbase * D + dl + u * TPH] = o[u];
+    if (tid < HG) {
+        int64_t pb = ((qi * a.S + split) * a.H + h0 + tid) * 2;
+        a.part_ml[pb] = mh[tid];
+        a.part_ml[pb + 1] = lh[tid];
+    }
+}
+
+// Merge split partials, add the sink, normalise, rotate by -i and store.
+// grid (Q*H), block 128, dynamic smem D + 64 floats.
+__global__ void __launch_bounds__(128)
+    attend_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
+                          int S, int H, int D, const float* __restrict__ sink,
+                          const int64_t* __restrict__ q_pos, int R, double base, int derotate,
+                          void* __restrict__ out, int act, float* __restrict__ lse) {
+    extern __shared__ float row[];
+    float* cs = row + D;
+    const int tid = threadIdx.x;
+    const int64_t qh = blockIdx.x;
+    const int64_t qi = qh / H;
+    const int h = (int)(qh % H);
+    const float sk = sink[h];
+    float mstar = sk;
+    for (int s = 0; s < S; s++) mstar = fmaxf(mstar, part_ml[((qi * S + s) * H + h) * 2]);
+    const int64_t i = q_pos[qi];
+    if (derotate)
+        for (int j = tid; j < R / 2; j += blockDim.x) rope_cos_sin(-(double)i, j, R, base, &cs[2 * j], &cs[2 * j + 1]);
+    float l = 0.f;
+    if (mstar != -INFINITY) {
+        l = expf(sk - mstar);
+        for (int s = 0; s < S; s++) {
+            const float* ml = part_ml + ((qi * S + s) * H + h) * 2;
+            if (ml[0] != -INFINITY) l += ml[1] * expf(ml[0] - mstar);
+        }
+    }
+    const float inv = (l > 0.f) ? 1.f / l : 0.f;
+    for (int d = tid; d < D; d += blockDim.x) {
+        float acc = 0.f;
+        if (l > 0.f)
+            for (int s = 0; s < S; s++) {
+                const float* ml = part_ml + ((qi * S + s) * H + h) * 2;
+                if (ml[0] != -INFINITY)
+                    acc = fmaf(expf(ml[0] - mstar), part_o[((qi * S + s) * H + h) * D + d], acc);
+            }
+        row[d] = acc * inv;
+    }
+    __syncthreads();
+    if (derotate) {
+        for (int j = tid; j < R / 2; j += blockDim.x) {
+            int d0 = D - R + 2 * j;
+            float c = cs[2 * j], s = cs[2 * j + 1];
+            float x0 = row[d0], x1 = row[d0 + 1];
+            row[d0] = x0 * c - x1 * s;
+            row[d0 + 1] = x0 * s + x1 * c;
+        }
+        __syncthreads();
+    }
+    uint8_t* orow = reinterpret_cast<uint8_t*>(out) + qh * D * (act == CSA_F32 ? 4 : 2);
+    for (int d = tid; d < D; d += blockDim.x) store_act(orow, act, d, row[d]);
+    if (lse && tid == 0) lse[qh] = (l > 0.f) ? mstar + logf(l) : -INFINITY;
+}
+
+cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool sparse, const void* q,
+                             int H, int B, int Q, const int64_t* q_pos, const void* cache,
+                             int64_t n_cap, const int32_t* topk_idx, const void* window,
+                             int64_t n_win, const int64_t* win_pos0, uint8_t* ws,
+                             uint32_t* status, cudaStream_t st);
+
+template <int D, int HG>
+static cudaError_t run_generic(const AttendArgs& a, int Q, int H, cudaStream_t st) {
+    size_t smem = (size_t)(HG * D + kAttRows * (D + 1) + HG * kAttRows + 3 * HG + 64) * sizeof(float) +
+                  kAttRows * sizeof(void*);
+    cudaError_t e = cudaFuncSetAttribute(attend_generic_kernel<D, HG>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)Q, (unsigned)(H / HG), (unsigned)a.S);
+    attend_generic_kernel<D, HG><<<grid, kAttThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, const void* q,
+                          int H, int B, int Q, const int64_t* q_pos, const void* cache,
+                          int64_t n_cap, const int32_t* topk_idx, const void* window,
+                          int64_t n_win, const int64_t* win_pos0, const float* sink, void* out,
+                          float* lse, uint8_t* ws, uint32_t* status, cudaStream_t st) {
+    if (Q == 0) return cudaSuccess;
+    float* part_o = reinterpret_cast<float*>(ws + pl.part_o_off);
+    float* part_ml = reinterpret_cast<float*>(ws + pl.part_ml_off);
+    cudaError_t e;
+    if (pl.use_tc) {
+        e = launch_attend_tc(g, pl, sparse, q, H, B, Q, q_pos, cache, n_cap, topk_idx, window,
+                             n_win, win_pos0, ws, status, st);
+    } else {
+        AttendArgs a;
+        a.q = reinterpret_cast<const uint8_t*>(q);
+        a.act = g.act;
+        a.H = H;
+        a.qps = Q / B;
+        a.q_pos = q_pos;
+        a.cache = reinterpret_cast<const uint8_t*>(cache);
+        a.n_cap = n_cap;
+        a.rb = g.kv_row_bytes;
+        a.kvfmt = g.kv;
+        a.topk_idx = sparse ? topk_idx : nullptr;
+        a.k = g.k;
+        a.window = reinterpret_cast<const uint8_t*>(window);
+        a.n_win = n_win;
+        a.win_pos0 = win_pos0;
+        a.W = g.W;
+        a.m = g.m;
+        a.R = g.R;
+        a.base = g.base;
+        a.eps = g.eps;
+        a.scale = g.scale;
+        a.part_o = part_o;
+        a.part_ml = part_ml;
+        a.S = pl.splits;
+        a.list_base = sparse ? g.k : n_cap;
+        a.rows_per_split = pl.rows_per_split;
+        a.status = status;
+        const int HG = pl.head_group;
+        if (g.D == 512 && HG == 16) e = run_generic<512, 16>(a, Q, H, st);
+        else if (g.D == 512 && HG == 8) e = run_generic<512, 8>(a, Q, H, st);
+        else if (g.D == 256 && HG == 16) e = run_generic<256, 16>(a, Q, H, st);
+        else if (g.D == 256 && HG == 8) e = run_generic<256, 8>(a, Q, H, st);
+        else if (g.D == 128 && HG == 16) e = run_generic<128, 16>(a, Q, H, st);
+        else if (g.D == 128 && HG == 8) e = run_generic<128, 8>(a, Q, H, st);
+        else return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return e;
+    attend_combine_kernel<<<(unsigned)((int64_t)Q * H), 128, (g.D + 64) * sizeof(float), st>>>(
+        part_o, part_ml, pl.splits, H, g.D, sink, q_pos, g.R, (double)g.base, g.derotate, out,
+        g.act, lse);
+    return cudaGetLastError();
+}
+
+}  // namespace csa

@@ -1,0 +1,130 @@
+// k_compress.cu -- block compressor (softmax pooling + RMSNorm + partial RoPE)
+// and the cache-row writer.
+//
+// Block compression follows "DeepSeek-V4百万上下文时代的开源宣言" §三.2, CSA
+// "Step 1: KV 压缩" (every m tokens pooled into one entry by an attention-like
+// mechanism with learnable weights) and HCA (m' = 128); the entry is
+// RMSNorm-ed and rotated on its last 64 dims at the block's last position
+// (四项关键 Trick).  The mixed FP8/BF16 row format follows
+// "DeepSeek-V4 技术报告深度解析" §2.1.4 "KV 缓存精度".
+//
+// Both kernels are HBM streams with a few FLOPs per byte: plain CUDA-core code,
+// coalesced row reads, one CTA per output entry.
+#include "common.cuh"
+#include "internal.h"
+
+namespace csa {
+
+constexpr int kCompressThreads = 128;
+
+// grid (n_blocks_out, B); dynamic smem: (m + D + 32) floats
+__global__ void __launch_bounds__(kCompressThreads)
+    compress_kernel(const uint8_t* __restrict__ kv, int act, int64_t act_row_bytes,
+                    int64_t kv_seq_bytes, int D, int m, int64_t pos0,
+                    const float* __restrict__ w_z, const float* __restrict__ bias,
+                    uint8_t* __restrict__ out, int kvfmt, int64_t kv_row_bytes,
+                    int64_t out_seq_bytes, int R, float eps, double base) {
+    extern __shared__ float sm[];
+    float* z = sm;            // [m]
+    float* row = sm + m;      // [D]
+    float* red = row + D;     // [32]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = kCompressThreads / 32;
+    const int64_t b = blockIdx.x;
+    const uint8_t* blk = kv + blockIdx.y * kv_seq_bytes + b * m * act_row_bytes;
+
+    // pooling scores z_t = kv_t . w_z + bias[t mod m]   (pos0 is a multiple of m)
+    for (int t = warp; t < m; t += nwarps) {
+        const uint8_t* r = blk + t * act_row_bytes;
+        float acc = 0.f;
+        for (int d = lane; d < D; d += 32) acc = fmaf(load_act(r, act, d), w_z[d], acc);
+        acc = warp_sum(acc);
+        if (lane == 0) z[t] = acc + bias[t];
+    }
+    __syncthreads();
+    float zmax = -INFINITY;
+    for (int t = 0; t < m; t++) zmax = fmaxf(zmax, z[t]);
+    float den = 0.f;
+    for (int t = 0; t < m; t++) den += expf(z[t] - zmax);
+    const float inv_den = 1.f / den;
+
+    // pooled vector and its sum of squares
+    float ss = 0.f;
+    for (int d = tid; d < D; d += kCompressThreads) {
+        float c = 0.f;
+        for (int t = 0; t < m; t++)
+            c = fmaf(expf(z[t] - zmax) * inv_den, load_act(blk + t * act_row_bytes, act, d), c);
+        row[d] = c;
+        ss = fmaf(c, c, ss);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    if (tid == 0) {
+        float tot = 0.f;
+        for (int w = 0; w < nwarps; w++) tot += red[w];
+        red[31] = 1.f / sqrtf(tot / (float)D + eps);
+    }
+    __syncthreads();
+    const float rn = red[31];
+    for (int d = tid; d < D; d += kCompressThreads) row[d] *= rn;
+    __syncthreads();
+
+    // partial RoPE at the block's last position
+    const double pos = (double)(pos0 + b * m + m - 1);
+    for (int j = tid; j < R / 2; j += kCompressThreads) {
+        float c, s;
+        rope_cos_sin(pos, j, R, base, &c, &s);
+        int d0 = D - R + 2 * j;
+        float x0 = row[d0], x1 = row[d0 + 1];
+        row[d0] = x0 * c - x1 * s;
+        row[d0 + 1] = x0 * s + x1 * c;
+    }
+    __syncthreads();
+    if (warp == 0) warp_pack_row(row, D, kvfmt, out + blockIdx.y * out_seq_bytes + b * kv_row_bytes);
+}
+
+// one warp per row; dynamic smem: 4 warps x D floats
+__global__ void __launch_bounds__(128)
+    pack_kernel(const float* __restrict__ src, int64_t n, int D, int kvfmt, int64_t rb,
+                uint8_t* __restrict__ dst) {
+    extern __shared__ float sm[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float* row = sm + warp * D;
+    int64_t r = (int64_t)blockIdx.x * 4 + warp;
+    if (r >= n) return;
+    for (int d = lane; d < D; d += 32) row[d] = src[r * D + d];
+    __syncwarp();
+    warp_pack_row(row, D, kvfmt, dst + r * rb);
+}
+
+cudaError_t launch_cache_pack(const Geometry& g, const float* src, int64_t n, void* dst,
+                              cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    int64_t blocks = (n + 3) / 4;
+    pack_kernel<<<(unsigned)blocks, 128, 4 * g.D * sizeof(float), st>>>(
+        src, n, g.D, g.kv, g.kv_row_bytes, reinterpret_cast<uint8_t*>(dst));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_compress(const Geometry& g, const void* kv, int B, int64_t T,
+                            int64_t kv_stride, int64_t pos0, const float* w_z, const float* bias,
+                            void* out, int64_t out_stride, cudaStream_t st) {
+    int64_t nb = T / g.m;
+    if (nb == 0 || B == 0) return cudaSuccess;
+    int64_t act_rb = row_bytes(g.act, g.D);
+    size_t smem = (size_t)(g.m + g.D + 32) * sizeof(float);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(compress_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    dim3 grid((unsigned)nb, (unsigned)B);
+    compress_kernel<<<grid, kCompressThreads, smem, st>>>(
+        reinterpret_cast<const uint8_t*>(kv), g.act, act_rb, kv_stride * act_rb, g.D, g.m, pos0,
+        w_z, bias, reinterpret_cast<uint8_t*>(out), g.kv, g.kv_row_bytes,
+        out_stride * g.kv_row_bytes, g.R, g.eps, (double)g.base);
+    return cudaGetLastError();
+}
+
+}  // namespace csa

@@ -1,0 +1,171 @@
+"""Call order of one CSA or HCA attention layer on top of the C ABI.
+
+These helpers own no arithmetic: they allocate device buffers with torch and
+issue the C-ABI calls in the order the layer needs them.
+
+Decode step (one new token per sequence, every sequence at the same length L):
+  1. append: when the new token completes a block, csa_compress(ratio=m) pools
+     the newest m raw tokens into cache entry L/m - 1; csa_compress(ratio=1)
+     writes the new token's normalised, rotated window row.
+  2. CSA: csa_index_topk then csa_attend.  HCA: hca_attend.
+Prefill (one sequence, a chunk of new tokens after `T_cached` cached ones):
+  csa_compress over the chunk (ratio=m) and over the window tokens (ratio=1),
+  then csa_index_topk and csa_attend for every new token.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import (BF16, F32, FP8_MIXED, OP_ATTEND, OP_HCA_ATTEND, OP_INDEX_TOPK, csa_attend,
+               csa_compress, csa_index_topk, csa_row_bytes, csa_workspace_bytes, hca_attend,
+               params, workspace)
+
+_ACT_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
+
+
+def _fmt(x):
+    return {"f32": F32, "bf16": BF16, "fp8m": FP8_MIXED}.get(x, x)
+
+
+@dataclass
+class LayerConfig:
+    D: int
+    H: int
+    m: int
+    W: int = 128
+    topk: int = 0          # 0: HCA layer
+    H_I: int = 0
+    d_I: int = 0
+    act: str = "bf16"
+    kv: str = "bf16"
+    rope_base: float = 10000.0
+    eps: float = 1e-6
+    derotate: bool = True
+
+    @property
+    def sparse(self) -> bool:
+        return self.topk > 0
+
+    def params(self, ratio=None):
+        return params(self.D, self.m if ratio is None else ratio, self.topk, self.W, self.act,
+                      self.kv, rope_base=self.rope_base, norm_eps=self.eps,
+                      derotate_output=self.derotate)
+
+    @property
+    def row_bytes(self) -> int:
+        return csa_row_bytes(_fmt(self.kv), self.D)
+
+    def empty_rows(self, *shape, device="cuda"):
+        """Device buffer of stored cache/window rows [*shape, D] in the kv format."""
+        if _fmt(self.kv) == FP8_MIXED:
+            return torch.zeros(*shape, self.row_bytes, dtype=torch.uint8, device=device)
+        dt = torch.float32 if _fmt(self.kv) == F32 else torch.bfloat16
+        return torch.zeros(*shape, self.D, dtype=dt, device=device)
+
+
+class DecodeLayer:
+    """Buffers and calls of one decode step for B sequences."""
+
+    def __init__(self, cfg: LayerConfig, B: int, n_cap: int, n_win: int, device="cuda"):
+        self.cfg, self.B, self.n_cap, self.n_win = cfg, B, n_cap, n_win
+        self.p = cfg.params()
+        self.p1 = cfg.params(ratio=1)
+        act = _ACT_DTYPE[_fmt(cfg.act)]
+        self.out = torch.empty(B, cfg.H, cfg.D, dtype=act, device=device)
+        self.lse = torch.empty(B, cfg.H, dtype=torch.float32, device=device)
+        nb = 0
+        if cfg.sparse:
+            self.topk_idx = torch.empty(B, cfg.topk, dtype=torch.int32, device=device)
+            self.topk_score = torch.empty(B, cfg.topk, dtype=torch.float32, device=device)
+            nb = csa_workspace_bytes(self.p, OP_INDEX_TOPK, B, B, cfg.H, cfg.H_I, n_cap, n_win)
+            nb = max(nb, csa_workspace_bytes(self.p, OP_ATTEND, B, B, cfg.H, cfg.H_I, n_cap, n_win))
+        else:
+            nb = csa_workspace_bytes(self.p, OP_HCA_ATTEND, B, B, cfg.H, 0, n_cap, n_win)
+        self.ws = workspace(nb, device)
+        self.ws_bytes = self.ws.numel()
+
+    def append(self, kv_new, pos_first, w_z, bias, cache, window, win_row, stream=None):
+        """kv_new [B, m, D] raw tokens at positions pos_first .. pos_first+m-1 (a
+        complete block): pool it into cache entry pos_first/m and write the last
+        token's window row into window row `win_row`."""
+        cfg = self.cfg
+        rb = cache.element_size() * (cache.shape[-1])
+        e = pos_first // cfg.m
+        csa_compress(self.p, kv_new, self.B, cfg.m, cfg.m, pos_first, w_z, bias,
+                     cache.data_ptr() + e * rb, self.n_cap, stream)
+        last = kv_new[:, cfg.m - 1:cfg.m]
+        csa_compress(self.p1, last.data_ptr(), self.B, 1, cfg.m, pos_first + cfg.m - 1, w_z,
+                     bias, window.data_ptr() + win_row * rb, self.n_win, stream)
+
+    def attend(self, q, cache, window, q_pos, win_pos0, sink, q_idx=None, w_idx=None, keys=None,
+               stream=None):
+        cfg = self.cfg
+        if cfg.sparse:
+            csa_index_topk(self.p, q_idx, w_idx, cfg.H_I, cfg.d_I, keys, self.n_cap, self.B,
+                           self.B, q_pos, self.topk_idx, self.topk_score, self.ws, self.ws_bytes,
+                           stream)
+            csa_attend(self.p, q, cfg.H, self.B, self.B, q_pos, cache, self.n_cap, self.topk_idx,
+                       window, self.n_win, win_pos0, sink, self.out, self.lse, self.ws,
+                       self.ws_bytes, stream)
+        else:
+            hca_attend(self.p, q, cfg.H, self.B, self.B, q_pos, cache, self.n_cap, window,
+                       self.n_win, win_pos0, sink, self.out, self.lse, self.ws, self.ws_bytes,
+                       stream)
+        return self.out, self.lse
+
+
+class PrefillLayer:
+    """Buffers and calls of a chunked prefill of one sequence (CSA)."""
+
+    def __init__(self, cfg: LayerConfig, T_cached: int, T_new: int, device="cuda"):
+        assert cfg.sparse and T_cached % cfg.m == 0
+        self.cfg, self.T_cached, self.T_new = cfg, T_cached, T_new
+        self.n_cap = (T_cached + T_new) // cfg.m
+        self.raw_pos0 = max(0, T_cached - (cfg.W - 1))
+        self.n_win = T_cached + T_new - self.raw_pos0
+        self.p = cfg.params()
+        self.p1 = cfg.params(ratio=1)
+        act = _ACT_DTYPE[_fmt(cfg.act)]
+        self.cache = cfg.empty_rows(self.n_cap, device=device)
+        self.window = cfg.empty_rows(self.n_win, device=device)
+        self.win_pos0 = torch.tensor([self.raw_pos0], dtype=torch.int64, device=device)
+        self.out = torch.empty(T_new, cfg.H, cfg.D, dtype=act, device=device)
+        self.lse = torch.empty(T_new, cfg.H, dtype=torch.float32, device=device)
+        self.topk_idx = torch.empty(T_new, cfg.topk, dtype=torch.int32, device=device)
+        self.topk_score = torch.empty(T_new, cfg.topk, dtype=torch.float32, device=device)
+        nb = max(csa_workspace_bytes(self.p, OP_INDEX_TOPK, 1, T_new, cfg.H, cfg.H_I, self.n_cap,
+                                     self.n_win),
+                 csa_workspace_bytes(self.p, OP_ATTEND, 1, T_new, cfg.H, cfg.H_I, self.n_cap,
+                                     self.n_win))
+        self.ws = workspace(nb, device)
+        self.ws_bytes = self.ws.numel()
+
+    def load_cached_rows(self, rows):
+        """Copy already-stored rows of the cached prefix into the cache."""
+        n = self.T_cached // self.cfg.m
+        if n:
+            self.cache[:n].copy_(rows)
+
+    def compress(self, kv_raw, w_z, bias, stream=None):
+        """kv_raw [n_win, D]: raw tokens from raw_pos0 to the last new token."""
+        cfg = self.cfg
+        rb = self.cache.element_size() * self.cache.shape[-1]
+        n_old = self.T_cached // cfg.m
+        off = self.T_cached - self.raw_pos0
+        act_rb = kv_raw.element_size() * kv_raw.shape[-1]
+        csa_compress(self.p, kv_raw.data_ptr() + off * act_rb, 1, self.T_new, self.T_new,
+                     self.T_cached, w_z, bias, self.cache.data_ptr() + n_old * rb, self.n_cap,
+                     stream)
+        csa_compress(self.p1, kv_raw, 1, self.n_win, self.n_win, self.raw_pos0, w_z, bias,
+                     self.window, self.n_win, stream)
+
+    def attend(self, q, q_idx, w_idx, keys, q_pos, sink, stream=None):
+        cfg = self.cfg
+        csa_index_topk(self.p, q_idx, w_idx, cfg.H_I, cfg.d_I, keys, self.n_cap, 1, self.T_new,
+                       q_pos, self.topk_idx, self.topk_score, self.ws, self.ws_bytes, stream)
+        csa_attend(self.p, q, cfg.H, 1, self.T_new, q_pos, self.cache, self.n_cap, self.topk_idx,
+                   self.window, self.n_win, self.win_pos0, sink, self.out, self.lse, self.ws,
+                   self.ws_bytes, stream)
+        return self.out, self.lse

@@ -66,6 +66,8 @@ def _declare(L):
     L.oracle_read_row.restype = None
     L.oracle_pack_fp8_rows.argtypes = [_vp, _i64, _i32, _vp]
     L.oracle_pack_fp8_rows.restype = None
+    L.oracle_store_rows.argtypes = [_vp, _i64, _i32, _i32, _vp]
+    L.oracle_store_rows.restype = None
     L.oracle_rmsnorm.argtypes = [_vp, _i32, _dbl, _vp]
     L.oracle_rmsnorm.restype = None
     L.oracle_rope.argtypes = [_vp, _i32, _i32, _dbl, _dbl]
@@ -152,6 +154,23 @@ def pack_fp8_rows(x: np.ndarray) -> np.ndarray:
     n = x.size // D
     out = np.zeros(x.shape[:-1] + (fp8m_row_bytes(D),), dtype=np.uint8)
     lib().oracle_pack_fp8_rows(_ptr(x), n, D, _ptr(out))
+    return out
+
+
+def store_rows(x: np.ndarray, fmt: int) -> np.ndarray:
+    """float64 [..., D] -> rows stored in `fmt` (float32, bf16 bits or FP8 rows)."""
+    x = _c(x, np.float64)
+    D = x.shape[-1]
+    n = x.size // D
+    if fmt == F64:
+        return x.copy()
+    if fmt == F32:
+        out = np.empty(x.shape, dtype=np.float32)
+    elif fmt == BF16:
+        out = np.empty(x.shape, dtype=np.uint16)
+    else:
+        out = np.zeros(x.shape[:-1] + (fp8m_row_bytes(D),), dtype=np.uint8)
+    lib().oracle_store_rows(_ptr(x), n, D, fmt, _ptr(out))
     return out
 
 

@@ -491,3 +491,27 @@ void oracle_pack_fp8_rows(const float* x, int64_t n, int D, uint8_t* out) {
 #pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < n; r++) oracle_pack_fp8_row(x + r * D, D, out + r * rb);
 }
+
+/* Store n double rows in a row format (the cache keeps compressor outputs in
+ * its storage format): float32 rounding first, then bfloat16 (RNE) or the
+ * mixed FP8 row quantiser. */
+void oracle_store_rows(const double* x, int64_t n, int D, int fmt, void* out) {
+    int64_t rb = oracle_row_bytes(fmt, D);
+    float* f = (float*)malloc(sizeof(float) * (size_t)D);
+    for (int64_t r = 0; r < n; r++) {
+        uint8_t* dst = (uint8_t*)out + r * rb;
+        const double* src = x + r * D;
+        if (fmt == ORC_F64) {
+            memcpy(dst, src, sizeof(double) * (size_t)D);
+            continue;
+        }
+        for (int d = 0; d < D; d++) f[d] = (float)src[d];
+        if (fmt == ORC_F32)
+            memcpy(dst, f, sizeof(float) * (size_t)D);
+        else if (fmt == ORC_BF16)
+            for (int d = 0; d < D; d++) ((uint16_t*)dst)[d] = oracle_f32_to_bf16(f[d]);
+        else
+            oracle_pack_fp8_row(f, D, dst);
+    }
+    free(f);
+}

@@ -1,0 +1,150 @@
+"""The C-ABI library: it loads without a GPU, exports every entry point the
+header declares, and rejects invalid arguments on the host before launching
+anything (these checks never touch device memory, so fake aligned addresses
+are safe here)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "csa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from long_context_compressed_17_b300 import build
+    build.build()
+    import long_context_compressed_17_b300 as pkg
+    return pkg
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\**\s+([a-z_0-9]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("csa_compress", "csa_index_topk", "csa_attend", "hca_attend", "csa_cache_pack",
+              "csa_workspace_bytes", "csa_workspace_init", "csa_check_status",
+              "csa_status_string", "csa_last_error", "csa_row_bytes"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(L):
+    lib = ctypes.CDLL(L.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    out = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if " T " in line)
+    for n in declared_functions():
+        assert n in exported, n
+
+
+def test_library_holds_sm103a_code(L):
+    out = subprocess.run(["cuobjdump", "--list-elf", L.LIB_PATH], capture_output=True, text=True)
+    assert "sm_103a" in out.stdout, out.stdout + out.stderr
+
+
+def test_row_bytes(L):
+    assert L.csa_row_bytes("bf16", 512) == 1024
+    assert L.csa_row_bytes("f32", 128) == 512
+    assert L.csa_row_bytes("fp8m", 512) == 608   # 448 E4M3 + 64 bf16 + 7 scales + pad
+    assert L.csa_row_bytes("fp8m", 128) == 208
+    assert L.csa_row_bytes("bf16", 100) == -1
+
+
+FAKE = 1 << 20  # aligned, never dereferenced: validation fails before any launch
+
+
+def _attend_args(L, p, **over):
+    a = dict(p=p, q=FAKE, H=64, B=2, Q=2, q_pos=FAKE, cache=FAKE, n_cap=100, topk_idx=FAKE,
+             window=FAKE, n_win=128, win_pos0=FAKE, sink=FAKE, out=FAKE, lse=None, ws=FAKE,
+             ws_bytes=1 << 40, stream=0)
+    a.update(over)
+    return a
+
+
+def _status_of(fn, **kw):
+    from long_context_compressed_17_b300 import CsaError
+    with pytest.raises(CsaError) as ei:
+        fn(**kw)
+    return ei.value.status
+
+
+def test_attend_validation(L):
+    p = L.params(512, 4, topk=64)
+    bad = {
+        "null q": dict(q=None),
+        "misaligned q": dict(q=FAKE + 2),
+        "Q not multiple of B": dict(Q=3),
+        "null sink": dict(sink=None),
+        "null topk": dict(topk_idx=None),
+        "H not multiple of 8": dict(H=12),
+        "negative n_cap": dict(n_cap=-1),
+    }
+    for what, over in bad.items():
+        st = _status_of(L.csa_attend, **_attend_args(L, p, **over))
+        assert st in (1, 2), what
+    assert _status_of(L.csa_attend, **_attend_args(L, p, H=12)) == 2
+    assert _status_of(L.csa_attend, **_attend_args(L, p, ws_bytes=100)) == 4
+    assert "workspace" in L.csa_last_error()
+
+
+def test_params_validation(L):
+    from long_context_compressed_17_b300 import CsaError
+    cases = [
+        (L.params(100, 4, topk=8), 2),                    # head_dim
+        (L.params(512, 4, topk=0), 1),                    # topk
+        (L.params(512, 0, topk=8), 1),                    # ratio
+        (L.params(512, 4, topk=8, rope_dims=32), 2),      # rope dims
+        (L.params(512, 4, topk=8, act="f32", kv="bf16"), 2),
+        (L.params(512, 4, topk=8, window=5000), 1),
+        (L.params(512, 4, topk=8, norm_eps=float("nan")), 1),
+    ]
+    for p, want in cases:
+        st = _status_of(L.csa_attend, **_attend_args(L, p))
+        assert st == want, (p.head_dim, p.topk, p.ratio, st)
+
+
+def test_index_topk_validation(L):
+    p = L.params(512, 4, topk=1024)
+    base = dict(p=p, q_idx=FAKE, w_idx=FAKE, n_idx_heads=64, idx_dim=128, keys=FAKE, n_cap=1000,
+                B=2, Q=4, q_pos=FAKE, topk_idx=FAKE, topk_score=None, ws=FAKE, ws_bytes=1 << 40)
+    assert _status_of(L.csa_index_topk, **dict(base, idx_dim=96)) == 2
+    assert _status_of(L.csa_index_topk, **dict(base, n_idx_heads=65)) == 2
+    assert _status_of(L.csa_index_topk, **dict(base, Q=3)) == 1
+    assert _status_of(L.csa_index_topk, **dict(base, q_pos=None)) == 1
+    assert _status_of(L.csa_index_topk, **dict(base, ws_bytes=1000)) == 4
+    assert _status_of(L.csa_index_topk, **dict(base, p=L.params(512, 4, topk=5000))) == 1
+
+
+def test_compress_validation(L):
+    p = L.params(512, 4)
+    base = dict(p=p, kv_raw=FAKE, B=2, T=16, kv_seq_stride=16, pos0=8, w_z=FAKE, bias=FAKE,
+                out=FAKE, out_seq_stride=4)
+    assert _status_of(L.csa_compress, **dict(base, pos0=6)) == 1       # not a multiple of m
+    assert _status_of(L.csa_compress, **dict(base, kv_seq_stride=8)) == 1
+    assert _status_of(L.csa_compress, **dict(base, out_seq_stride=3)) == 1
+    assert _status_of(L.csa_compress, **dict(base, w_z=FAKE + 4)) == 1
+
+
+def test_zero_sized_requests_are_no_ops(L):
+    p = L.params(512, 4, topk=8)
+    # Q = 0 and T < m return CSA_OK without touching any pointer or the device
+    L.csa_attend(**_attend_args(L, p, Q=0, q=None, out=None))
+    L.csa_compress(p, None, 1, 3, 3, 0, None, None, None, 1)
+
+
+def test_workspace_sizes(L):
+    p = L.params(512, 4, topk=1024)
+    n = L.csa_workspace_bytes(p, L.OP_INDEX_TOPK, 32, 32, 64, 64, 32768, 128)
+    assert n >= 256 + 32 * 32768 * 4
+    assert L.csa_workspace_bytes(p, L.OP_ATTEND, 32, 32, 64, 64, 32768, 128) > 256
+    assert L.csa_workspace_bytes(p, 99, 32, 32, 64, 64, 32768, 128) == 0
