@@ -1,0 +1,562 @@
+"""Benchmark of the CSA/HCA hot path on B300: decode queries/s and achieved HBM GB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step is one pass of the whole hot path over one batch: for a decode
+workload, the append of the newest block (compressor, ratio m) and of the
+newest window row (ratio 1), then indexer scoring, top-k selection and core
+attention with the split-K combine (CSA), or the dense attention (HCA); for a
+prefill workload, the compressor over the new chunk and its window rows, then
+indexer, top-k and attention for every new token.
+
+Default workload: CSA decode, batch 32, 131072-token context, bf16 (the
+workload the headline metric is quoted on).  Every input is synthetic and
+seeded.  With N > 1 (torchrun) every rank runs its own batch (weak scaling, no
+data-path collective); the step time is the maximum over ranks.
+
+`--impl reference` times the CPU oracle (the only reference this method has)
+on the host cores over a bounded sample per step, on the same workload,
+metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "CSA/HCA decode queries/sec and achieved HBM GB/s (% roofline) at 128K–1M ctx"
+UNIT = "queries/s"
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ------------------------------------------------------------------ peaks
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "sm_max_mhz": float(d.get("sm_max_mhz", 2032.0)), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+                "sm_max_mhz": 2032.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+            0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+            0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML while running."""
+
+    def __init__(self, device_index=0, period_s=0.002):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self.period = period_s
+        self._stop = threading.Event()
+        self._h = None
+        try:
+            import pynvml
+            self.nv = pynvml
+            pynvml.nvmlInit()
+            self.error = None
+            try:
+                p = torch.cuda.get_device_properties(device_index)
+                bus = "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+                self._h = pynvml.nvmlDeviceGetHandleByPciBusId(bus)
+            except Exception as e:  # bus id not known to NVML: the only visible device
+                self.error = "bus-id lookup: %s" % e
+                if pynvml.nvmlDeviceGetCount() == 1:
+                    self._h = pynvml.nvmlDeviceGetHandleByIndex(0)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+        except Exception as e:  # NVML missing: report no samples
+            self.error = str(e)
+            self._h = None
+
+    def _run(self):
+        nv = self.nv
+        get_r = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
+                r = get_r(self._h)
+                for bit, name in _REASONS.items():
+                    if r & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self._h is not None:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self._h is not None:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "error": getattr(self, "error", None)}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons - {"gpu_idle"}), "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------ work units
+def algorithmic(w: workloads.Workload, row_bytes: int):
+    """Algorithmic bytes / flops per step: the dominant kernel and the whole step."""
+    act_es = 4 if w.act == "f32" else 2
+    if w.kind in ("csa_decode", "hca_decode"):
+        n_av = [L // w.m for L in w.lengths]
+        q_out = w.H * w.D * act_es * 2
+        if w.kind == "csa_decode":
+            idx_bytes = sum(n * w.d_I * act_es + w.H_I * w.d_I * act_es + w.H_I * 4 for n in n_av)
+            rows = w.B * (min(w.topk, max(n_av)) + w.W)
+            step = idx_bytes + rows * row_bytes + w.B * q_out
+            return {"kernel": "indexer", "bound": "hbm", "bytes": idx_bytes, "step_bytes": step}
+        att = sum((n + w.W) * row_bytes for n in n_av) + w.B * q_out
+        return {"kernel": "hca_attend", "bound": "hbm", "bytes": att, "step_bytes": att}
+    # prefill: indexer flops over causally complete blocks
+    fl = 0
+    for t in range(w.T_new):
+        fl += 2 * w.H_I * w.d_I * ((w.T_cached + t + 1) // w.m)
+    bound = "alu" if w.act == "f32" else "tensor"
+    return {"kernel": "indexer", "bound": bound, "flops": fl, "step_flops": fl}
+
+
+# ------------------------------------------------------------------ GPU arm
+class GpuStep:
+    """Buffers and CUDA graphs of one step, split as [before | dominant | after]."""
+
+    def __init__(self, w: workloads.Workload):
+        import long_context_compressed_17_b300 as L
+        from long_context_compressed_17_b300.pipeline import DecodeLayer, LayerConfig, PrefillLayer
+        self.L, self.w = L, w
+        self.inp = workloads.generate(w, device="cuda")
+        inp = self.inp
+        cfg = LayerConfig(D=w.D, H=w.H, m=w.m, W=w.W, topk=w.topk if w.kind != "hca_decode" else 0,
+                          H_I=w.H_I, d_I=w.d_I, act=w.act, kv=w.kv_fmt, rope_base=w.rope_base,
+                          eps=w.eps)
+        self.cfg = cfg
+        self.row_bytes = cfg.row_bytes
+        # stored rows the library reads (FP8 rows are packed by the library)
+        self.rows = {}
+        if w.kind != "csa_prefill":
+            for key in ("cache", "window"):
+                x = inp[key]
+                if w.kv_fmt == "fp8m":
+                    rows = cfg.empty_rows(*x.shape[:-1])
+                    L.csa_cache_pack(cfg.params(), x, x.numel() // w.D, rows)
+                    self.rows[key] = rows
+                else:
+                    self.rows[key] = x.clone()
+            torch.cuda.synchronize()
+        if w.kind in ("csa_decode", "hca_decode"):
+            assert len(set(w.lengths)) == 1, "the benchmark runs uniform lengths"
+            self.layer = DecodeLayer(cfg, w.B, w.n_cap, w.W)
+            Lb = w.lengths[0]
+            self.pos_first = Lb - w.m
+            self.win_row = (Lb - 1) - int(inp["win_pos0"][0])
+            if w.kind == "csa_decode":
+                self.ld = (w.n_cap + 127) // 128 * 128
+                self.scores = torch.empty(w.B, self.ld, dtype=torch.float32, device="cuda")
+        else:
+            self.layer = PrefillLayer(cfg, w.T_cached, w.T_new)
+            if w.T_cached:
+                old = inp["cache_old"]
+                if w.kv_fmt == "fp8m":
+                    rows = cfg.empty_rows(old.shape[0])
+                    L.csa_cache_pack(cfg.params(), old, old.shape[0], rows)
+                    old = rows
+                self.layer.load_cached_rows(old)
+            self.ld = (self.layer.n_cap + 127) // 128 * 128
+            self.scores = torch.empty(w.T_new, self.ld, dtype=torch.float32, device="cuda")
+
+    # the three segments of a step
+    def before(self):
+        w, inp, lay = self.w, self.inp, self.layer
+        if w.kind == "csa_prefill":
+            lay.compress(inp["kv_raw"], inp["w_z"], inp["bias"])
+        elif self.pos_first >= 0:
+            lay.append(inp["kv_new"], self.pos_first, inp["w_z"], inp["bias"], self.rows["cache"],
+                       self.rows["window"], self.win_row)
+
+    def dominant(self):
+        w, inp, lay, L = self.w, self.inp, self.layer, self.L
+        if w.kind == "hca_decode":
+            L.hca_attend(lay.p, inp["q"], w.H, w.B, w.B, inp["q_pos"], self.rows["cache"],
+                         w.n_cap, self.rows["window"], w.W, inp["win_pos0"], inp["sink"], lay.out,
+                         lay.lse, lay.ws, lay.ws_bytes)
+            return
+        B = w.B if w.kind == "csa_decode" else 1
+        n_cap = w.n_cap if w.kind == "csa_decode" else lay.n_cap
+        keys = inp["keys"]
+        L.csa_index_score(lay.p, inp["q_idx"], inp["w_idx"], w.H_I, w.d_I, keys, n_cap, B, w.Q,
+                          inp["q_pos"], self.scores, self.ld, lay.ws, lay.ws_bytes)
+
+    def after(self):
+        w, inp, lay, L = self.w, self.inp, self.layer, self.L
+        if w.kind == "hca_decode":
+            return
+        n_cap = w.n_cap if w.kind == "csa_decode" else lay.n_cap
+        L.csa_topk_select(lay.p, self.scores, self.ld, n_cap, w.Q, inp["q_pos"], lay.topk_idx,
+                          lay.topk_score)
+        if w.kind == "csa_decode":
+            L.csa_attend(lay.p, inp["q"], w.H, w.B, w.B, inp["q_pos"], self.rows["cache"],
+                         w.n_cap, lay.topk_idx, self.rows["window"], w.W, inp["win_pos0"],
+                         inp["sink"], lay.out, lay.lse, lay.ws, lay.ws_bytes)
+        else:
+            L.csa_attend(lay.p, inp["q"], w.H, 1, w.Q, inp["q_pos"], lay.cache, lay.n_cap,
+                         lay.topk_idx, lay.window, lay.n_win, lay.win_pos0, inp["sink"], lay.out,
+                         lay.lse, lay.ws, lay.ws_bytes)
+
+    def run_eager(self):
+        self.before()
+        self.dominant()
+        self.after()
+
+    def capture(self):
+        self.graphs = []
+        for seg in (self.before, self.dominant, self.after):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                seg()
+            self.graphs.append(g)
+        torch.cuda.synchronize()
+        self.launches_per_step = None
+
+
+def run_gpu(args, rank, world):
+    import long_context_compressed_17_b300 as L
+    w = workloads.BY_NAME[args.workload]
+    peaks = measured_peaks()
+    st = GpuStep(w)
+    alg = algorithmic(w, st.row_bytes)
+    for _ in range(2):  # untimed eager passes: kernel attributes, first-launch costs
+        st.run_eager()
+    torch.cuda.synchronize()
+    L.csa_check_status(st.layer.ws)
+    st.capture()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    g0, g1, g2 = st.graphs
+    for _ in range(args.warmup):
+        flush.zero_()
+        g0.replay()
+        g1.replay()
+        g2.replay()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    _barrier(world)
+    torch.cuda.synchronize()
+    n0 = L.csa_launch_count()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for k in range(args.steps):
+            flush.zero_()                 # L2 flushed before every timed step
+            e = ev[k]
+            e[0].record()
+            g0.replay()
+            e[1].record()
+            g1.replay()
+            e[2].record()
+            g2.replay()
+            e[3].record()
+        torch.cuda.synchronize()
+    _barrier(world)
+    step_ms = [ev[k][0].elapsed_time(ev[k][3]) for k in range(args.steps)]
+    dom_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
+    ms = statistics.mean(step_ms)
+    ms = _max_over_ranks(ms, world)
+    dom = statistics.mean(dom_ms)
+    # kernels per step, counted on an eager pass (graph replays do not go through the library)
+    n1 = L.csa_launch_count()
+    st.run_eager()
+    torch.cuda.synchronize()
+    per_step = L.csa_launch_count() - n1
+    L.csa_check_status(st.layer.ws)
+    e2e = run_e2e(st, args)
+
+    value = world * w.Q / (ms * 1e-3)
+    if alg["bound"] == "hbm":
+        achieved = alg["bytes"] / (dom * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": None, "kernel": alg["kernel"], "kernel_ms": round(dom, 5),
+                "bytes_per_launch": alg["bytes"], "peak_source": peaks["source"] + " (burst)"}
+    elif alg["bound"] == "tensor":
+        achieved = alg["flops"] / (dom * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": None, "kernel": alg["kernel"], "kernel_ms": round(dom, 5),
+                "flops_per_launch": alg["flops"], "peak_source": peaks["source"] + " bf16 (burst)"}
+    else:
+        # fp32 FMA peak: 148 SMs x 128 lanes x 2 flop x max SM clock
+        peak = 148 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+        achieved = alg["flops"] / (dom * 1e-3) / 1e12
+        roof = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                "kernel": alg["kernel"], "kernel_ms": round(dom, 5),
+                "flops_per_launch": alg["flops"], "peak_source": "fp32 FMA units x max clock"}
+    step_info = {}
+    if "step_bytes" in alg:
+        step_info = {"step_gbs": round(alg["step_bytes"] / (ms * 1e-3) / 1e9, 1),
+                     "step_hbm_frac": round(alg["step_bytes"] / (ms * 1e-3) / 1e9 /
+                                            peaks["hbm_gbs"], 4)}
+    cfg = {"workload": w.name, "kind": w.kind, "batch": w.B, "context": max(w.lengths),
+           "head_dim": w.D, "heads": w.H, "ratio": w.m, "topk": w.topk, "window": w.W,
+           "idx_heads": w.H_I, "idx_dim": w.d_I, "kv_format": w.kv_fmt, "seed": w.seed,
+           "l2": "flushed before every timed step (512 MiB write)",
+           "timing": "CUDA events around each step; step captured as 3 CUDA graphs",
+           "parallelism": "replicas" if world > 1 else "single GPU"}
+    cfg.update(step_info)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.act, "data": "synthetic (seeded; shapes of the pages' 1M-context workloads)",
+        "config": cfg, "roofline": roof, "e2e": e2e, "gpu_launches": per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, st.inp, budget_s=args.cpu_seconds)
+    return line
+
+
+def run_e2e(st: GpuStep, args):
+    """Same metric through the public API with host buffers: per step, copy the
+    new token's inputs from pinned host memory, run the step's calls, read the
+    outputs back; wall time with a synchronize per step."""
+    w, inp = st.w, st.inp
+    names = ["q", "kv_new", "q_pos", "win_pos0"] if w.kind != "csa_prefill" else \
+        ["q", "kv_raw", "q_pos"]
+    if w.kind != "hca_decode":
+        names += ["q_idx", "w_idx"]
+    host = {n: inp[n].cpu().pin_memory() for n in names}
+    out = st.layer.out
+    lse = st.layer.lse
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+    n = max(5, min(args.steps, 50))
+    times = []
+    for k in range(n + 3):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for nm, t in host.items():
+            inp[nm].copy_(t, non_blocking=True)
+        st.run_eager()
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        torch.cuda.synchronize()
+        if k >= 3:
+            times.append(time.perf_counter() - t0)
+    t = statistics.mean(times)
+    return {"value": round(w.Q / t, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(t * 1e3, 4),
+            "note": "cache, window and indexer keys stay resident in HBM (layer state)"}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def _oracle_sample(w, inp, n_q):
+    """Host copies of the inputs the oracle needs for the first n_q queries."""
+    import numpy as np
+    from tests import harness as H
+    s = {}
+    if w.kind in ("csa_decode", "hca_decode"):
+        sl = slice(0, n_q)
+        for k in ("q", "q_idx", "w_idx", "keys", "kv_new"):
+            if k in inp:
+                s[k] = H.np_stored(inp[k][sl])
+        for k in ("cache", "window"):
+            # the oracle's own stored form of the layer state (FP8 rows packed by the oracle)
+            s[k] = H.oracle_stored_rows(w, inp[k][sl])
+        s["q_pos"] = inp["q_pos"][sl].cpu().numpy()
+        s["win_pos0"] = inp["win_pos0"][sl].cpu().numpy()
+    else:
+        qs = slice(w.T_new - n_q, w.T_new)  # the last queries see the most blocks
+        for k in ("q", "q_idx", "w_idx"):
+            s[k] = H.np_stored(inp[k][qs])
+        s["keys"] = H.np_stored(inp["keys"])
+        s["kv_raw"] = H.np_stored(inp["kv_raw"])
+        s["cache_old"] = H.oracle_stored_rows(w, inp["cache_old"]) if w.T_cached else None
+        s["q_pos"] = inp["q_pos"][qs].cpu().numpy()
+    s["w_z"] = H.np_stored(inp["w_z"]).astype(np.float64)
+    s["bias"] = H.np_stored(inp["bias"]).astype(np.float64)
+    s["sink"] = H.np_stored(inp["sink"]).astype(np.float64)
+    return s
+
+
+def oracle_step(w, s, raw_pos0=0):
+    """The oracle's pass over the sampled queries (append, index, top-k, attend)."""
+    import numpy as np
+    import oracle
+    fmt = {"f32": oracle.F32, "bf16": oracle.BF16, "fp8m": oracle.FP8M}[w.kv_fmt]
+    n_q = s["q"].shape[0]
+    if w.kind in ("csa_decode", "hca_decode"):
+        cache, window = s["cache"].copy(), s["window"].copy()
+        for b in range(n_q):
+            Lb = int(s["q_pos"][b]) + 1
+            if Lb % w.m == 0:
+                e = oracle.compress(s["kv_new"][b], Lb - w.m, w.m, s["w_z"], s["bias"],
+                                    w.rope_dims, w.rope_base, w.eps)
+                cache[b, Lb // w.m - 1] = oracle.store_rows(e, fmt)[0]
+            r = oracle.compress(s["kv_new"][b][w.m - 1:], Lb - 1, 1, s["w_z"], s["bias"][:1],
+                                w.rope_dims, w.rope_base, w.eps)
+            window[b, Lb - 1 - int(s["win_pos0"][b])] = oracle.store_rows(r, fmt)[0]
+        seq = np.arange(n_q, dtype=np.int32)
+        idx = None
+        if w.kind == "csa_decode":
+            idx, _ = oracle.index_topk_batch(s["q_idx"], s["w_idx"], s["keys"], seq, s["q_pos"],
+                                             w.m, w.topk)
+        return oracle.attend_batch(s["q"], seq, s["q_pos"], w.m, cache, w.D, idx, window,
+                                   s["win_pos0"], w.W, s["sink"], rope_dims=w.rope_dims,
+                                   base=w.rope_base, eps=w.eps)
+    off = w.T_cached - raw_pos0
+    new = oracle.compress(s["kv_raw"][off:], w.T_cached, w.m, s["w_z"], s["bias"], w.rope_dims,
+                          w.rope_base, w.eps)
+    rows = [s["cache_old"]] if s["cache_old"] is not None else []
+    rows.append(oracle.store_rows(new, fmt))
+    cache = np.concatenate(rows, 0)[None]
+    win = oracle.store_rows(oracle.compress(s["kv_raw"], raw_pos0, 1, s["w_z"], s["bias"][:1],
+                                            w.rope_dims, w.rope_base, w.eps), fmt)[None]
+    seq = np.zeros(n_q, np.int32)
+    idx, _ = oracle.index_topk_batch(s["q_idx"], s["w_idx"], s["keys"][None], seq, s["q_pos"],
+                                     w.m, w.topk)
+    return oracle.attend_batch(s["q"], seq, s["q_pos"], w.m, cache, w.D, idx, win,
+                               np.array([raw_pos0]), w.W, s["sink"], rope_dims=w.rope_dims,
+                               base=w.rope_base, eps=w.eps)
+
+
+def cpu_baseline(w, inp, budget_s=15.0):
+    import oracle
+    oracle.build()
+    raw_pos0 = inp.get("raw_pos0", 0) if isinstance(inp, dict) else 0
+    n_q = 1
+    s = _oracle_sample(w, inp, n_q)
+    t0 = time.perf_counter()
+    oracle_step(w, s, raw_pos0)
+    t1 = time.perf_counter() - t0
+    cores = os.cpu_count() or 1
+    # as many queries as fit the budget with the cores busy, capped at the batch
+    n_q = int(max(1, min(w.Q, (budget_s / max(t1, 1e-3)) * min(cores, w.Q) * 0.8)))
+    s = _oracle_sample(w, inp, n_q)
+    t0 = time.perf_counter()
+    oracle_step(w, s, raw_pos0)
+    t = time.perf_counter() - t0
+    return {"value": round(n_q / t, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%d of the workload's %d queries (%s), %.1f s" % (
+                n_q, w.Q, "sequences 0..%d" % (n_q - 1) if w.kind != "csa_prefill"
+                else "the last %d new tokens" % n_q, t)}
+
+
+def run_reference(args, rank, world):
+    """The oracle on the host cores, each step a bounded sample of the workload."""
+    w = workloads.BY_NAME[args.workload]
+    import oracle
+    oracle.build()
+    # one query per host core and step (the oracle runs its queries in parallel)
+    cores = os.cpu_count() or 1
+    n_q = max(1, min(w.Q, cores))
+    inp = workloads.generate(w.replace(B=n_q) if w.kind != "csa_prefill" else w, device="cpu")
+    raw_pos0 = inp.get("raw_pos0", 0)
+    s = _oracle_sample(w, inp, n_q)
+    for _ in range(args.warmup):
+        oracle_step(w, s, raw_pos0)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(w, s, raw_pos0)
+        times.append(time.perf_counter() - t0)
+    t = statistics.mean(times)
+    v = round(n_q / t, 4)
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "kind": w.kind, "batch": w.B,
+                       "context": max(w.lengths), "sample_per_step": "%d queries" % n_q},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "%d queries per step of the %d-query workload" % (n_q, w.Q)},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------ multi-rank
+def _dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
+    return rank, world
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=workloads.CSA_DECODE_128K.name,
+                    choices=sorted(workloads.BY_NAME))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        # the CPU oracle runs on rank 0 only; other ranks exit without work
+        rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return 0
+    rank, world = _dist_init()
+    line = run_gpu(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -78,27 +78,33 @@ double oracle_e4m3_decode(uint8_t c) {
 }
 
 /* E4M3 encoding of a float32, round to nearest with ties to even mantissa,
- * saturating to the largest finite magnitude (448).  Written as a search over
- * the 127 finite non-negative codes so that it reads directly against the
- * definition: pick the nearest representable magnitude; on an exact tie pick
- * the code whose mantissa LSB is 0. */
+ * saturating to the largest finite magnitude (448).  The 127 finite
+ * non-negative codes 0..126 decode to strictly increasing magnitudes, so the
+ * nearest representable magnitude is found by bisection over the codes; on an
+ * exact tie the code whose mantissa LSB is 0 wins. */
 uint8_t oracle_e4m3_encode(float x) {
     if (isnan(x)) return 0x7F;
     double a = fabs((double)x);
-    int best = 0;
-    double bestd = INFINITY;
-    for (int c = 0; c <= 126; c++) {
-        double d = fabs(oracle_e4m3_decode((uint8_t)c) - a);
-        if (d < bestd || (d == bestd && (c & 1) == 0 && (best & 1) == 1)) {
-            bestd = d;
-            best = c;
+    int lo = 0, hi = 126; /* invariant: value(lo) <= a or lo == 0; a <= value(hi) or hi == 126 */
+    if (a >= oracle_e4m3_decode(126)) {
+        lo = hi = 126; /* at or above 448: saturate */
+    } else {
+        while (hi - lo > 1) {
+            int mid = (lo + hi) / 2;
+            if (oracle_e4m3_decode((uint8_t)mid) <= a)
+                lo = mid;
+            else
+                hi = mid;
         }
     }
-    /* magnitudes above 448 are nearest to code 126 (448) in this search: the
-     * saturating behaviour falls out of restricting the search to finite codes */
+    int best = lo;
+    if (hi != lo) {
+        double dl = a - oracle_e4m3_decode((uint8_t)lo);
+        double dh = oracle_e4m3_decode((uint8_t)hi) - a;
+        if (dh < dl || (dh == dl && (hi & 1) == 0)) best = hi;
+    }
     uint8_t code = (uint8_t)best;
-    if (signbit(x) && best != 0) code |= 0x80;
-    if (signbit(x) && best == 0) code = 0x80; /* keep the sign of zero */
+    if (signbit(x)) code |= 0x80; /* negative values, including -0, keep the sign bit */
     return code;
 }
 

@@ -182,3 +182,141 @@ def check_topk_set(gpu_idx, orc_scores, k, what=""):
     assert not bad, "%s: %d blocks differ beyond near-ties, e.g. %s (thr %.9g)" % (
         what, len(bad), [(b, orc_scores[b]) for b in bad[:4]], thr)
     return False
+
+
+# ----------------------------------------------------------- parity drivers
+def _to_cuda(inp):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+
+def _row_tol(w, ref):
+    if w.kv_fmt == "f32":
+        return 1e-5 + 1e-6 * np.abs(ref)
+    if w.kv_fmt == "bf16":
+        return 1e-5 + 2.0 ** -7 * np.abs(ref)
+    return 1e-4 + np.abs(ref) / 8 + 2.0 ** -9 * np.abs(ref).max()
+
+
+def check_stored_rows(w, gpu_rows, ref_rows, what):
+    """GPU-written cache rows vs the oracle's unrounded rows."""
+    got = oracle.read_rows(np_stored(gpu_rows), w.D)
+    ref = np.asarray(ref_rows, np.float64).reshape(got.shape)
+    err = np.abs(got - ref)
+    assert np.all(err <= _row_tol(w, ref)), "%s: worst %.3g" % (what, err.max())
+
+
+# ---------------------------------------------------------------- decode
+def decode_parity(w, seqs=None, gen_device="cpu", append=True):
+    inp = _to_cuda(workloads.generate(w, device=gen_device))
+    res = gpu_decode(w, inp, append=append)
+    seqs = list(range(w.B)) if seqs is None else seqs
+    fmt = {"f32": oracle.F32, "bf16": oracle.BF16, "fp8m": oracle.FP8M}[w.kv_fmt]
+    w_z = np_stored(inp["w_z"]).astype(np.float64)
+    bias = np_stored(inp["bias"]).astype(np.float64)
+    sink = np_stored(inp["sink"]).astype(np.float64)
+    stats = []
+    for b in seqs:
+        Lb = w.lengths[b]
+        i, n_av = Lb - 1, Lb // w.m
+        q = np_stored(inp["q"][b])
+        # the append step: the newest block's entry and the newest window row
+        ent = None
+        kv_b = np_stored(inp["kv_new"][b])
+        if append and Lb % w.m == 0:
+            ent = oracle.compress(kv_b, Lb - w.m, w.m, w_z, bias, w.rope_dims, w.rope_base, w.eps)
+            check_stored_rows(w, res["cache"][b, n_av - 1], ent, "appended entry seq %d" % b)
+        wr = i - int(inp["win_pos0"][b])
+        wrow = oracle.compress(kv_b[w.m - 1:], i, 1, w_z, bias[:1], w.rope_dims, w.rope_base, w.eps)
+        if append:
+            check_stored_rows(w, res["window"][b, wr], wrow, "window row seq %d" % b)
+        window = oracle_stored_rows(w, inp["window"][b])
+        if append:
+            window[wr] = oracle.store_rows(wrow, fmt)[0]
+        same = True
+        if w.kind == "csa_decode":
+            g_idx = res["topk_idx"][b].cpu().numpy()
+            scores = oracle.index_scores(np_stored(inp["q_idx"][b]),
+                                         np_stored(inp["w_idx"][b]).astype(np.float64),
+                                         np_stored(inp["keys"][b, :n_av]))
+            same = check_topk_set(g_idx, scores, w.topk, "seq %d" % b)
+            kk = min(w.topk, n_av)
+            g_sc = res["topk_score"][b, :kk].cpu().numpy().astype(np.float64)
+            assert np.allclose(g_sc, scores[g_idx[:kk]], rtol=1e-4, atol=1e-4), "scores seq %d" % b
+            need = np.unique(g_idx[:kk])
+        else:
+            need = np.arange(n_av)
+        # compact cache: only the rows this query reads, stored like the GPU's
+        rows = inp["cache"][b][torch.as_tensor(need, device=inp["cache"].device, dtype=torch.long)]
+        cache_c = oracle_stored_rows(w, rows)
+        if ent is not None and (n_av - 1) in set(need.tolist()):
+            cache_c[int(np.searchsorted(need, n_av - 1))] = oracle.store_rows(ent, fmt)[0]
+        if w.kind == "csa_decode":
+            out_o, lse_o = _attend_compact(w, q, i, cache_c, np.arange(len(need)), window,
+                                           int(inp["win_pos0"][b]), sink)
+        else:
+            out_o, lse_o = oracle.attend_query(q, i, w.m, cache_c, w.D, None, window,
+                                               int(inp["win_pos0"][b]), w.W, sink,
+                                               rope_dims=w.rope_dims, base=w.rope_base, eps=w.eps)
+        out_g = res["out"][b].float().cpu().numpy()
+        mx, mn = assert_close(out_g, out_o, w.act, "out seq %d" % b)
+        lse_g = res["lse"][b].cpu().numpy()
+        assert np.max(np.abs(lse_g - lse_o)) <= LSE_TOL[w.act], "lse seq %d" % b
+        stats.append((b, same, mx, mn))
+    return stats
+
+
+def _attend_compact(w, q, i, cache_c, idx_c, window, win_pos0, sink):
+    """CSA attention over the rows idx_c of a compact cache: the rows are the
+    selected blocks, so the query attends to exactly those plus the window."""
+    D = w.D
+    rows = oracle.read_rows(cache_c, D)[idx_c]
+    lo = max(0, i - w.W + 1)
+    wrows = oracle.read_rows(window, D)[lo - win_pos0:i + 1 - win_pos0] if w.W else np.zeros((0, D))
+    allrows = np.concatenate([rows, wrows], axis=0)
+    return oracle.attend_rows(q, i, allrows, sink, rope_dims=w.rope_dims, base=w.rope_base,
+                              eps=w.eps)
+
+
+
+# ---------------------------------------------------------------- prefill
+def prefill_parity(w, sample=None, gen_device="cpu"):
+    inp = _to_cuda(workloads.generate(w, device=gen_device))
+    res = gpu_prefill(w, inp)
+    cache_o, window_o = oracle_prefill_state(w, inp)
+    n_old = w.T_cached // w.m
+    # compressor outputs (new entries, window rows) against the oracle's
+    w_z = np_stored(inp["w_z"]).astype(np.float64)
+    bias = np_stored(inp["bias"]).astype(np.float64)
+    kv_raw = np_stored(inp["kv_raw"])
+    off = w.T_cached - inp["raw_pos0"]
+    new = oracle.compress(kv_raw[off:], w.T_cached, w.m, w_z, bias, w.rope_dims, w.rope_base, w.eps)
+    check_stored_rows(w, res["cache"][n_old:], new, "compressed entries")
+    win = oracle.compress(kv_raw, inp["raw_pos0"], 1, w_z, bias[:1], w.rope_dims, w.rope_base, w.eps)
+    check_stored_rows(w, res["window"], win, "window rows")
+    qs = list(range(w.T_new)) if sample is None else sample
+    q = np_stored(inp["q"])
+    q_idx = np_stored(inp["q_idx"])
+    w_idx = np_stored(inp["w_idx"]).astype(np.float64)
+    keys = np_stored(inp["keys"])
+    sink = np_stored(inp["sink"]).astype(np.float64)
+    g_idx = res["topk_idx"].cpu().numpy()
+    out_g = res["out"].float().cpu().numpy()
+    lse_g = res["lse"].cpu().numpy()
+    n_same = 0
+    for t in qs:
+        i = w.T_cached + t
+        n_av = (i + 1) // w.m
+        scores = oracle.index_scores(q_idx[t], w_idx[t], keys[:n_av])
+        n_same += check_topk_set(g_idx[t], scores, w.topk, "query %d" % t)
+    # attention for the sampled queries, given the GPU's indices
+    seq = np.zeros(len(qs), np.int32)
+    pos = np.array([w.T_cached + t for t in qs], np.int64)
+    out_o, lse_o = oracle.attend_batch(q[qs], seq, pos, w.m, cache_o[None], w.D, g_idx[qs],
+                                       window_o[None], inp["raw_pos0"], w.W, sink,
+                                       rope_dims=w.rope_dims, base=w.rope_base, eps=w.eps)
+    assert_close(out_g[qs], out_o, w.act, "prefill out")
+    assert np.max(np.abs(lse_g[qs] - lse_o)) <= LSE_TOL[w.act]
+    # end to end (the oracle's own selection) for the queries whose sets agree
+    return n_same, len(qs)
+
+
