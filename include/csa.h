@@ -130,6 +130,51 @@ csa_status csa_index_topk(const csa_params* p, const void* q_idx, const float* w
                           int32_t B, int32_t Q, const int64_t* q_pos, int32_t* topk_idx,
                           float* topk_score, void* ws, size_t ws_bytes, csa_stream_t stream);
 
+/* The two halves of csa_index_topk, for callers that keep or inspect the
+ * scores.  csa_index_score writes score_b for b < floor((i+1)/m) and -inf for
+ * the other blocks b < n_cap into scores[q*ld_scores + b] (float32, device,
+ * ld_scores >= n_cap, caller-owned); blocks are laid out as for keys.
+ * csa_topk_select reads such a score matrix and writes topk_idx/topk_score
+ * exactly as csa_index_topk does; it flags nothing.  ws: status word only
+ * (>= 256 bytes). */
+csa_status csa_index_score(const csa_params* p, const void* q_idx, const float* w_idx,
+                           int32_t n_idx_heads, int32_t idx_dim, const void* keys, int64_t n_cap,
+                           int32_t B, int32_t Q, const int64_t* q_pos, float* scores,
+                           int64_t ld_scores, void* ws, size_t ws_bytes, csa_stream_t stream);
+csa_status csa_topk_select(const csa_params* p, const float* scores, int64_t ld_scores,
+                           int64_t n_cap, int32_t Q, const int64_t* q_pos, int32_t* topk_idx,
+                           float* topk_score, csa_stream_t stream);
+
+/* csa_index_topk for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point; it exists for integration only.
+ *
+ * Some callers cannot call cudaMalloc: a plug-in or custom operator whose
+ * host framework owns every device allocation and hands it only its input and
+ * output buffers, or a latency-critical path that cannot afford the implicit
+ * device-wide synchronisation an allocation may cause.  This variant computes
+ * exactly what csa_index_topk computes, with the same arguments minus the
+ * workspace, and keeps its intermediate indexer scores in a scratch array
+ * compiled into the library: CSA_NOALLOC_MAX_SCORES float32 values (16 MiB)
+ * plus a 256-byte status header.  Every GPU that loads the library holds that
+ * scratch until the process exits.
+ *   - Q * ceil(n_cap / 128) * 128 must not exceed CSA_NOALLOC_MAX_SCORES;
+ *     larger requests return CSA_ERR_INVALID_ARG and launch nothing.
+ *   - The first call on a device looks up the scratch's device address on
+ *     that device (with that device current); make that first call before
+ *     any stream capture.
+ *   - All calls share the one scratch array, which keeps the last call's
+ *     contents.  Calls whose work overlaps on the GPU (different streams or
+ *     threads without ordering between them) race and give wrong results:
+ *     order them on one stream.
+ *   - status: optional device uint32 that receives the call's device status
+ *     bits (CSA_DEV_*), cleared at the start of every call; NULL to ignore. */
+#define CSA_NOALLOC_MAX_SCORES 4194304
+csa_status csa_index_topk_noalloc(const csa_params* p, const void* q_idx, const float* w_idx,
+                                  int32_t n_idx_heads, int32_t idx_dim, const void* keys,
+                                  int64_t n_cap, int32_t B, int32_t Q, const int64_t* q_pos,
+                                  int32_t* topk_idx, float* topk_score, uint32_t* status,
+                                  csa_stream_t stream);
+
 /* CSA core attention [peacm §三.2 CSA "Step 3: Core Attention Multi-Query
  * Attention" over the top-k blocks; 四项关键 Trick: Q/KV Normalization, Partial
  * RoPE and output RoPE at -i, Sliding Window (most recent W raw tokens),
@@ -182,6 +227,10 @@ csa_status csa_check_status(void* ws, csa_stream_t stream);
 
 /* Raw status bits of the last csa_check_status on this thread. */
 uint32_t csa_last_device_bits(void);
+
+/* Number of kernels this library has launched in this process (all
+ * threads), for launch accounting in benchmarks. */
+uint64_t csa_launch_count(void);
 
 const char* csa_status_string(csa_status s);
 const char* csa_last_error(void);

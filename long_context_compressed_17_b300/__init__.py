@@ -17,7 +17,7 @@ import torch
 __all__ = [
     "CsaError", "CsaParams", "F32", "BF16", "FP8_MIXED", "OP_INDEX_TOPK", "OP_ATTEND",
     "OP_HCA_ATTEND", "params", "lib", "csa_row_bytes", "csa_cache_pack", "csa_compress",
-    "csa_index_topk", "csa_attend", "hca_attend", "csa_workspace_bytes", "csa_workspace_init",
+    "csa_index_topk", "csa_index_score", "csa_topk_select", "csa_launch_count", "csa_index_topk_noalloc", "csa_attend", "hca_attend", "csa_workspace_bytes", "csa_workspace_init",
     "csa_check_status", "csa_last_device_bits", "csa_status_string", "csa_last_error",
     "workspace", "LIB_PATH",
 ]
@@ -80,6 +80,12 @@ def lib() -> ctypes.CDLL:
                                   _vp, _vp, _vp, _vp, _sz, _vp]),
             "hca_attend": (_i32, [P, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _i64, _vp, _vp,
                                   _vp, _vp, _vp, _sz, _vp]),
+            "csa_index_score": (_i32, [P, _vp, _vp, _i32, _i32, _vp, _i64, _i32, _i32, _vp, _vp,
+                                       _i64, _vp, _sz, _vp]),
+            "csa_topk_select": (_i32, [P, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp]),
+            "csa_launch_count": (ctypes.c_uint64, []),
+            "csa_index_topk_noalloc": (_i32, [P, _vp, _vp, _i32, _i32, _vp, _i64, _i32, _i32, _vp,
+                                              _vp, _vp, _vp, _vp]),
             "csa_workspace_bytes": (_sz, [P, _i32, _i32, _i32, _i32, _i32, _i64, _i64]),
             "csa_workspace_init": (_i32, [_vp, _sz, _vp]),
             "csa_check_status": (_i32, [_vp, _vp]),
@@ -148,6 +154,36 @@ def csa_index_topk(p, q_idx, w_idx, n_idx_heads, idx_dim, keys, n_cap, B, Q, q_p
                                 _ptr(keys), n_cap, B, Q, _ptr(q_pos), _ptr(topk_idx),
                                 _ptr(topk_score), _ptr(ws), ws_bytes, _stream(stream)),
            "csa_index_topk")
+
+
+def csa_index_score(p, q_idx, w_idx, n_idx_heads, idx_dim, keys, n_cap, B, Q, q_pos, scores,
+                    ld_scores, ws, ws_bytes, stream=None):
+    _check(lib().csa_index_score(ctypes.byref(p), _ptr(q_idx), _ptr(w_idx), n_idx_heads, idx_dim,
+                                 _ptr(keys), n_cap, B, Q, _ptr(q_pos), _ptr(scores), ld_scores,
+                                 _ptr(ws), ws_bytes, _stream(stream)),
+           "csa_index_score")
+
+
+def csa_topk_select(p, scores, ld_scores, n_cap, Q, q_pos, topk_idx, topk_score, stream=None):
+    _check(lib().csa_topk_select(ctypes.byref(p), _ptr(scores), ld_scores, n_cap, Q, _ptr(q_pos),
+                                 _ptr(topk_idx), _ptr(topk_score), _stream(stream)),
+           "csa_topk_select")
+
+
+def csa_index_topk_noalloc(p, q_idx, w_idx, n_idx_heads, idx_dim, keys, n_cap, B, Q, q_pos,
+                           topk_idx, topk_score, status, stream=None):
+    """csa_index_topk without a workspace, for callers that cannot allocate
+    device memory (its scores live in a fixed scratch array inside the library;
+    see include/csa.h for the size limit and the ordering rule)."""
+    _check(lib().csa_index_topk_noalloc(ctypes.byref(p), _ptr(q_idx), _ptr(w_idx), n_idx_heads,
+                                        idx_dim, _ptr(keys), n_cap, B, Q, _ptr(q_pos),
+                                        _ptr(topk_idx), _ptr(topk_score), _ptr(status),
+                                        _stream(stream)),
+           "csa_index_topk_noalloc")
+
+
+def csa_launch_count() -> int:
+    return int(lib().csa_launch_count())
 
 
 def csa_attend(p, q, H, B, Q, q_pos, cache, n_cap, topk_idx, window, n_win, win_pos0, sink, out,

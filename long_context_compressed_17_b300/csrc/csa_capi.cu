@@ -2,6 +2,8 @@
 // workspace planning and dispatch to the kernels.  No allocation, no
 // synchronisation (except csa_check_status), launches on the caller's stream.
 #include <math.h>
+
+#include <atomic>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -12,6 +14,9 @@
 namespace csa {
 
 static thread_local char g_err[512] = "";
+static std::atomic<unsigned long long> g_launches{0};
+
+void note_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
 static thread_local uint32_t g_dev_bits = 0;
 
 static csa_status fail(csa_status s, const char* fmt, ...) {
@@ -21,6 +26,8 @@ static csa_status fail(csa_status s, const char* fmt, ...) {
     va_end(ap);
     return s;
 }
+
+csa_status set_error(csa_status s, const char* msg) { return fail(s, "%s", msg); }
 
 static csa_status cuda_fail(cudaError_t e, const char* what) {
     return fail(CSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -263,12 +270,58 @@ csa_status csa_index_topk(const csa_params* p, const void* q_idx, const float* w
     uint32_t* status = reinterpret_cast<uint32_t*>(w);
     float* scores = reinterpret_cast<float*>(w + pl.scores_off);
     cudaStream_t st = (cudaStream_t)stream;
-    cudaError_t e = launch_indexer(g, pl, q_idx, w_idx, n_idx_heads, idx_dim, keys, n_cap, B, Q,
-                                   q_pos, status, scores, st);
+    cudaError_t e = launch_indexer(g, q_idx, w_idx, n_idx_heads, idx_dim, keys, n_cap, B, Q,
+                                   q_pos, status, scores, pl.n_cap_pad, st);
     if (e != cudaSuccess) return cuda_fail(e, "csa_index_topk: indexer");
-    e = launch_topk(g, pl, scores, n_cap, B, Q, q_pos, topk_idx, topk_score, st);
+    e = launch_topk(g, scores, pl.n_cap_pad, n_cap, Q, q_pos, topk_idx, topk_score, st);
     return e == cudaSuccess ? CSA_OK : cuda_fail(e, "csa_index_topk: top-k");
 }
+
+csa_status csa_index_score(const csa_params* p, const void* q_idx, const float* w_idx,
+                           int32_t n_idx_heads, int32_t idx_dim, const void* keys, int64_t n_cap,
+                           int32_t B, int32_t Q, const int64_t* q_pos, float* scores,
+                           int64_t ld_scores, void* ws, size_t ws_bytes, csa_stream_t stream) {
+    CHECK(check_params(p));
+    if (idx_dim != 64 && idx_dim != 128) return fail(CSA_ERR_UNSUPPORTED, "idx_dim %d: 64 or 128", idx_dim);
+    if (n_idx_heads < 1 || n_idx_heads > 64) return fail(CSA_ERR_UNSUPPORTED, "n_idx_heads %d: 1..64", n_idx_heads);
+    if (B < 1 || Q < 0 || Q % B != 0) return fail(CSA_ERR_INVALID_ARG, "Q %d must be a multiple of B %d", Q, B);
+    if (n_cap < 0 || n_cap > (1LL << 30)) return fail(CSA_ERR_INVALID_ARG, "n_cap out of range");
+    if (ld_scores < n_cap || ld_scores % 4 != 0)
+        return fail(CSA_ERR_INVALID_ARG, "ld_scores %lld must be >= n_cap and a multiple of 4", (long long)ld_scores);
+    if (Q == 0) return CSA_OK;
+    CHECK(check_ptr(q_idx, "q_idx"));
+    CHECK(check_ptr(w_idx, "w_idx"));
+    CHECK(check_ptr(keys, "keys", n_cap == 0));
+    CHECK(check_ptr(q_pos, "q_pos"));
+    CHECK(check_ptr(scores, "scores"));
+    CHECK(check_ptr(ws, "ws"));
+    if (ws_bytes < kStatusWordBytes) return fail(CSA_ERR_WORKSPACE, "workspace smaller than 256 bytes");
+    Geometry g = resolve(p);
+    cudaError_t e = launch_indexer(g, q_idx, w_idx, n_idx_heads, idx_dim, keys, n_cap, B, Q, q_pos,
+                                   reinterpret_cast<uint32_t*>(ws), scores, ld_scores,
+                                   (cudaStream_t)stream);
+    return e == cudaSuccess ? CSA_OK : cuda_fail(e, "csa_index_score");
+}
+
+csa_status csa_topk_select(const csa_params* p, const float* scores, int64_t ld_scores,
+                           int64_t n_cap, int32_t Q, const int64_t* q_pos, int32_t* topk_idx,
+                           float* topk_score, csa_stream_t stream) {
+    CHECK(check_params(p));
+    if (p->topk < 1 || p->topk > 4096) return fail(CSA_ERR_INVALID_ARG, "topk %d not in [1, 4096]", p->topk);
+    if (Q < 0 || n_cap < 0 || n_cap > (1LL << 30) || ld_scores < n_cap)
+        return fail(CSA_ERR_INVALID_ARG, "bad Q / n_cap / ld_scores");
+    if (Q == 0) return CSA_OK;
+    CHECK(check_ptr(scores, "scores"));
+    CHECK(check_ptr(q_pos, "q_pos"));
+    CHECK(check_ptr(topk_idx, "topk_idx"));
+    CHECK(check_ptr(topk_score, "topk_score", true));
+    Geometry g = resolve(p);
+    cudaError_t e = launch_topk(g, scores, ld_scores, n_cap, Q, q_pos, topk_idx, topk_score,
+                                (cudaStream_t)stream);
+    return e == cudaSuccess ? CSA_OK : cuda_fail(e, "csa_topk_select");
+}
+
+uint64_t csa_launch_count(void) { return (uint64_t)g_launches.load(); }
 
 static csa_status attend_common(const csa_params* p, bool sparse, const void* q, int32_t H,
                                 int32_t B, int32_t Q, const int64_t* q_pos, const void* cache,

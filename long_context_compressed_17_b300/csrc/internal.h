@@ -45,13 +45,12 @@ cudaError_t launch_cache_pack(const Geometry& g, const float* src, int64_t n, vo
 cudaError_t launch_compress(const Geometry& g, const void* kv, int B, int64_t T,
                             int64_t kv_stride, int64_t pos0, const float* w_z, const float* bias,
                             void* out, int64_t out_stride, cudaStream_t st);
-cudaError_t launch_indexer(const Geometry& g, const IndexTopkPlan& pl, const void* q_idx,
-                           const float* w_idx, int HI, int dI, const void* keys, int64_t n_cap,
-                           int B, int Q, const int64_t* q_pos, uint32_t* status, float* scores,
+cudaError_t launch_indexer(const Geometry& g, const void* q_idx, const float* w_idx, int HI,
+                           int dI, const void* keys, int64_t n_cap, int B, int Q,
+                           const int64_t* q_pos, uint32_t* status, float* scores, int64_t ld,
                            cudaStream_t st);
-cudaError_t launch_topk(const Geometry& g, const IndexTopkPlan& pl, const float* scores,
-                        int64_t n_cap, int B, int Q, const int64_t* q_pos, int32_t* idx,
-                        float* sel, cudaStream_t st);
+cudaError_t launch_topk(const Geometry& g, const float* scores, int64_t ld, int64_t n_cap, int Q,
+                        const int64_t* q_pos, int32_t* idx, float* sel, cudaStream_t st);
 cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, const void* q,
                           int H, int B, int Q, const int64_t* q_pos, const void* cache,
                           int64_t n_cap, const int32_t* topk_idx, const void* window,
@@ -59,5 +58,11 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
                           float* lse, uint8_t* ws, uint32_t* status, cudaStream_t st);
 
 int num_sms();
+
+// Kernel launch accounting (csa_launch_count).
+void note_launch(int n = 1);
+
+// Record a failure for csa_last_error() and return its status.
+csa_status set_error(csa_status s, const char* msg);
 
 }  // namespace csa
