@@ -60,16 +60,71 @@ _REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_
             0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
 
 
+class _CtypesNvml:
+    """The few read-only NVML queries the sampler needs, straight from the
+    driver's libnvidia-ml (used when the pynvml module is not installed)."""
+    NVML_CLOCK_SM = 1
+
+    def __init__(self):
+        import ctypes
+        self._c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+
+    def _ok(self, r, what):
+        if r != 0:
+            raise RuntimeError("%s failed (%d)" % (what, r))
+
+    def nvmlInit(self):
+        self._ok(self.lib.nvmlInit_v2(), "nvmlInit")
+
+    def nvmlDeviceGetCount(self):
+        n = self._c.c_uint()
+        self._ok(self.lib.nvmlDeviceGetCount_v2(self._c.byref(n)), "count")
+        return n.value
+
+    def _handle(self, fn, arg):
+        h = self._c.c_void_p()
+        self._ok(fn(arg, self._c.byref(h)), "handle")
+        return h
+
+    def nvmlDeviceGetHandleByPciBusId(self, bus):
+        return self._handle(self.lib.nvmlDeviceGetHandleByPciBusId_v2, bus.encode())
+
+    def nvmlDeviceGetHandleByIndex(self, i):
+        return self._handle(self.lib.nvmlDeviceGetHandleByIndex_v2, self._c.c_uint(i))
+
+    def _clock(self, fn, h, typ):
+        v = self._c.c_uint()
+        self._ok(fn(h, self._c.c_int(typ), self._c.byref(v)), "clock")
+        return v.value
+
+    def nvmlDeviceGetClockInfo(self, h, typ):
+        return self._clock(self.lib.nvmlDeviceGetClockInfo, h, typ)
+
+    def nvmlDeviceGetMaxClockInfo(self, h, typ):
+        return self._clock(self.lib.nvmlDeviceGetMaxClockInfo, h, typ)
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h):
+        v = self._c.c_ulonglong()
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self._ok(fn(h, self._c.byref(v)), "reasons")
+        return v.value
+
+
 class ClockSampler:
     """Samples SM clock and clock-event reasons through NVML while running."""
 
-    def __init__(self, device_index=0, period_s=0.002):
+    def __init__(self, device_index=0, period_s=0.001):
         self.samples, self.reasons, self.max_mhz = [], set(), None
         self.period = period_s
         self._stop = threading.Event()
         self._h = None
         try:
-            import pynvml
+            try:
+                import pynvml
+            except ImportError:
+                pynvml = _CtypesNvml()
             self.nv = pynvml
             pynvml.nvmlInit()
             self.error = None

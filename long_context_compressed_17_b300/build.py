@@ -60,7 +60,9 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
                 print(err, file=sys.stderr)
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + ".tmp%d" % os.getpid()
-        cmd = [NVCC, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static"]
+        # --no-undefined: a launcher declared but not defined must fail the build
+        cmd = [NVCC, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static",
+                                                            "-Xlinker", "--no-undefined"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))

@@ -267,6 +267,7 @@ static cudaError_t run_generic(const AttendArgs& a, int Q, int H, cudaStream_t s
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)Q, (unsigned)(H / HG), (unsigned)a.S);
     attend_generic_kernel<D, HG><<<grid, kAttThreads, smem, st>>>(a);
+    note_launch();
     return cudaGetLastError();
 }
 
@@ -323,6 +324,7 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
     attend_combine_kernel<<<(unsigned)((int64_t)Q * H), 128, (g.D + 64) * sizeof(float), st>>>(
         part_o, part_ml, pl.splits, H, g.D, sink, q_pos, g.R, (double)g.base, g.derotate, out,
         g.act, lse);
+    note_launch();
     return cudaGetLastError();
 }
 

@@ -104,6 +104,7 @@ cudaError_t launch_cache_pack(const Geometry& g, const float* src, int64_t n, vo
     int64_t blocks = (n + 3) / 4;
     pack_kernel<<<(unsigned)blocks, 128, 4 * g.D * sizeof(float), st>>>(
         src, n, g.D, g.kv, g.kv_row_bytes, reinterpret_cast<uint8_t*>(dst));
+    note_launch();
     return cudaGetLastError();
 }
 
@@ -124,6 +125,7 @@ cudaError_t launch_compress(const Geometry& g, const void* kv, int B, int64_t T,
         reinterpret_cast<const uint8_t*>(kv), g.act, act_rb, kv_stride * act_rb, g.D, g.m, pos0,
         w_z, bias, reinterpret_cast<uint8_t*>(out), g.kv, g.kv_row_bytes,
         out_stride * g.kv_row_bytes, g.R, g.eps, (double)g.base);
+    note_launch();
     return cudaGetLastError();
 }
 

@@ -63,19 +63,19 @@ __global__ void __launch_bounds__(kIdxTile)
     }
 }
 
-cudaError_t launch_indexer_tc(const Geometry& g, const IndexTopkPlan& pl, const void* q_idx,
-                              const float* w_idx, int HI, int dI, const void* keys, int64_t n_cap,
-                              int B, int Q, const int64_t* q_pos, uint32_t* status, float* scores,
+cudaError_t launch_indexer_tc(const Geometry& g, const void* q_idx, const float* w_idx, int HI,
+                              int dI, const void* keys, int64_t n_cap, int B, int Q,
+                              const int64_t* q_pos, uint32_t* status, float* scores, int64_t ld,
                               cudaStream_t st, bool* launched);
 
-cudaError_t launch_indexer(const Geometry& g, const IndexTopkPlan& pl, const void* q_idx,
-                           const float* w_idx, int HI, int dI, const void* keys, int64_t n_cap,
-                           int B, int Q, const int64_t* q_pos, uint32_t* status, float* scores,
+cudaError_t launch_indexer(const Geometry& g, const void* q_idx, const float* w_idx, int HI,
+                           int dI, const void* keys, int64_t n_cap, int B, int Q,
+                           const int64_t* q_pos, uint32_t* status, float* scores, int64_t ld,
                            cudaStream_t st) {
     if (Q == 0 || n_cap == 0) return cudaSuccess;
     bool launched = false;
-    cudaError_t e = launch_indexer_tc(g, pl, q_idx, w_idx, HI, dI, keys, n_cap, B, Q, q_pos,
-                                      status, scores, st, &launched);
+    cudaError_t e = launch_indexer_tc(g, q_idx, w_idx, HI, dI, keys, n_cap, B, Q, q_pos, status,
+                                      scores, ld, st, &launched);
     if (launched || e != cudaSuccess) return e;
     const int qps = Q / B;
     int qpc = 1;
@@ -94,7 +94,8 @@ cudaError_t launch_indexer(const Geometry& g, const IndexTopkPlan& pl, const voi
         }
         kern<<<grid, kIdxTile, smem, st>>>(reinterpret_cast<const uint8_t*>(q_idx), w_idx, HI,
                                            reinterpret_cast<const uint8_t*>(keys), g.act, n_cap,
-                                           qps, qpc, q_pos, g.m, scores, pl.n_cap_pad, status);
+                                           qps, qpc, q_pos, g.m, scores, ld, status);
+        note_launch();
         return cudaGetLastError();
     };
     return dI == 64 ? run(indexer_generic_kernel<64>) : run(indexer_generic_kernel<128>);

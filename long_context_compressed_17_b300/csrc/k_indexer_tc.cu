@@ -1,14 +1,336 @@
-// k_indexer_tc.cu -- tensor-core (tcgen05) lightning indexer: not yet built.
+// k_indexer_tc.cu -- lightning-indexer scoring on the 5th-generation tensor
+// cores (tcgen05 + TMEM + TMA), for bf16 keys of 128 dims and 64 heads.
+//
+// "DeepSeek-V4百万上下文时代的开源宣言" §三.2, CSA "Step 2: Lightning Indexer
+// Top-K 选择": score_b = sum_h w_h * relu(q_h . k_b) over causally complete
+// blocks.  The q.K products are a dense contraction, so they run as
+//   D[128 keys, N] = K_tile[128 keys, 128 dims] x Q[N, 128 dims]^T
+// with the keys as the M = 128 side (swap-AB: a decode query has only 64
+// heads) and N = 64 * NQ columns for NQ queries of one sequence; the relu and
+// the head-weighted sum run in the epilogue straight out of TMEM, one key per
+// thread.  Decode (NQ = 1) is an HBM stream of the keys; prefill (NQ = 4)
+// reuses every key tile for four queries per MMA.
+//
+// Persistent CTAs walk a contiguous range of (query group, key tile) units.
+// Warp 0 issues TMA loads, warp 1 issues the MMAs, warps 2..5 are the
+// epilogue.  Every wait is bounded: on a timeout the kernel flags
+// CSA_DEV_TIMEOUT, all roles leave their loops and TMEM is freed.
 #include "common.cuh"
 #include "internal.h"
+#include "tc_util.cuh"
 
 namespace csa {
 
-cudaError_t launch_indexer_tc(const Geometry&, const IndexTopkPlan&, const void*, const float*, int,
-                              int, const void*, int64_t, int, int, const int64_t*, uint32_t*,
-                              float*, cudaStream_t, bool* launched) {
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box);
+
+namespace {
+
+constexpr int kHI = 64;            // indexer heads (per query)
+constexpr int kDI = 128;           // indexer dim
+constexpr int kTileKeys = 128;     // MMA M
+constexpr int kStages = 4;
+constexpr uint32_t kStageBytes = kTileKeys * kDI * 2;   // 32 KiB: two 64-dim boxes
+constexpr int kThreads = 192;
+
+template <int NQ>
+struct Cfg {
+    static constexpr int N = NQ * kHI;                  // MMA N
+    static constexpr int kAcc = NQ == 1 ? 4 : 2;        // TMEM accumulators in flight
+    static constexpr int kQBufs = NQ == 1 ? 2 : 1;
+    static constexpr uint32_t kQBytes = (uint32_t)N * kDI * 2;
+    static constexpr uint32_t kTmemCols = kAcc * N;     // 256 or 512
+    static constexpr size_t kBarBytes = 256;
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kQBufs * kQBytes + kBarBytes;
+};
+
+struct IdxArgs {
+    const float* w_idx;    // [Q, 64]
+    const int64_t* q_pos;  // [Q]
+    float* scores;         // [Q, ld]
+    int64_t ld;
+    int64_t n_cap;
+    int qps;               // queries per sequence
+    int m;
+    int n_tiles;           // key tiles per query group
+    int64_t total_units;   // groups * n_tiles
+    uint32_t* status;
+};
+
+// Blocks a query group sees: the largest floor((i+1)/m) of its queries, capped.
+template <int NQ>
+__device__ __forceinline__ int64_t group_avail(const IdxArgs& a, int64_t g) {
+    int64_t nav = 0;
+#pragma unroll
+    for (int qq = 0; qq < NQ; qq++) {
+        int64_t n = (a.q_pos[g * NQ + qq] + 1) / a.m;
+        nav = max(nav, min(n, a.n_cap));
+    }
+    return nav;
+}
+
+}  // namespace
+
+template <int NQ>
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
+                      const __grid_constant__ CUtensorMap tm_q, IdxArgs a) {
+    using C = Cfg<NQ>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = sm;
+    uint8_t* sB = sA + kStages * kStageBytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::kQBufs * C::kQBytes);
+    uint64_t* empty = full + kStages;
+    uint64_t* qfull = empty + kStages;
+    uint64_t* qempty = qfull + C::kQBufs;
+    uint64_t* tfull = qempty + C::kQBufs;
+    uint64_t* tempty = tfull + C::kAcc;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + C::kAcc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; s++) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < C::kQBufs; b++) {
+            tc::mbar_init(&qfull[b], 1);
+            tc::mbar_init(&qempty[b], 1);
+        }
+        for (int c = 0; c < C::kAcc; c++) {
+            tc::mbar_init(&tfull[c], 1);
+            tc::mbar_init(&tempty[c], 4);  // one arrival per epilogue warp
+        }
+        *abort_flag = 0;
+        tc::fence_barrier_init();
+        tc::fence_proxy_async_smem();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_slot, C::kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    const int64_t per = (a.total_units + gridDim.x - 1) / gridDim.x;
+    const int64_t u0 = (int64_t)blockIdx.x * per;
+    const int64_t u1 = min(a.total_units, u0 + per);
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        tc::tma_prefetch_map(&tm_keys);
+        tc::tma_prefetch_map(&tm_q);
+        int stage = 0;
+        uint32_t phase = 0;
+        int64_t cur_g = -1, last_loaded = -1, gnav = 0;
+        int qloads = 0;
+        for (int64_t u = u0; u < u1; ++u) {
+            const int64_t g = u / a.n_tiles;
+            const int t = (int)(u % a.n_tiles);
+            if (g != cur_g) {
+                cur_g = g;
+                gnav = group_avail<NQ>(a, g);
+            }
+            if ((int64_t)t * kTileKeys >= gnav) continue;  // no complete block in this tile
+            if (g != last_loaded) {
+                const int qb = qloads % C::kQBufs;
+                const uint32_t par = ((uint32_t)(qloads / C::kQBufs) & 1u) ^ 1u;
+                if (!tc::mbar_wait(&qempty[qb], par, abort_flag, a.status)) break;
+                tc::mbar_arrive_expect_tx(&qfull[qb], C::kQBytes);
+                uint8_t* dst = sB + qb * C::kQBytes;
+                tc::tma_load_2d(dst, &tm_q, &qfull[qb], 0, (int)(g * C::N));
+                tc::tma_load_2d(dst + C::kQBytes / 2, &tm_q, &qfull[qb], 64, (int)(g * C::N));
+                last_loaded = g;
+                qloads++;
+            }
+            if (!tc::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status)) break;
+            tc::mbar_arrive_expect_tx(&full[stage], kStageBytes);
+            const int seq = (int)((g * NQ) / a.qps);
+            uint8_t* dst = sA + stage * kStageBytes;
+            tc::tma_load_3d(dst, &tm_keys, &full[stage], 0, t * kTileKeys, seq);
+            tc::tma_load_3d(dst + kStageBytes / 2, &tm_keys, &full[stage], 64, t * kTileKeys, seq);
+            if (++stage == kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc = tc::idesc_bf16_f32(kTileKeys, C::N);
+        int stage = 0, acc = 0, quses = 0, qb = 0;
+        uint32_t phase = 0, aphase = 0;
+        int64_t cur_g = -1, last_used = -1, gnav = 0;
+        for (int64_t u = u0; u < u1; ++u) {
+            const int64_t g = u / a.n_tiles;
+            const int t = (int)(u % a.n_tiles);
+            if (g != cur_g) {
+                cur_g = g;
+                gnav = group_avail<NQ>(a, g);
+            }
+            if ((int64_t)t * kTileKeys >= gnav) continue;
+            if (g != last_used) {
+                if (quses > 0) tc::mma_commit(&qempty[qb]);  // the old queries are free once read
+                qb = quses % C::kQBufs;
+                const uint32_t par = (uint32_t)(quses / C::kQBufs) & 1u;
+                if (!tc::mbar_wait(&qfull[qb], par, abort_flag, a.status)) break;
+                last_used = g;
+                quses++;
+            }
+            if (!tc::mbar_wait(&tempty[acc], aphase ^ 1u, abort_flag, a.status)) break;
+            if (!tc::mbar_wait(&full[stage], phase, abort_flag, a.status)) break;
+            tc::fence_after_sync();
+            const uint32_t a_base = tc::smem_u32(sA + stage * kStageBytes);
+            const uint32_t b_base = tc::smem_u32(sB + qb * C::kQBytes);
+            const uint32_t d = tmem + (uint32_t)(acc * C::N);
+#pragma unroll
+            for (int kk = 0; kk < kDI / 16; kk++) {
+                const uint32_t ka = (uint32_t)(kk >> 2) * (kStageBytes / 2) + (uint32_t)(kk & 3) * 32u;
+                const uint32_t kb = (uint32_t)(kk >> 2) * (C::kQBytes / 2) + (uint32_t)(kk & 3) * 32u;
+                tc::mma_bf16_ss(d, tc::sdesc_kmajor_sw128(a_base + ka),
+                                tc::sdesc_kmajor_sw128(b_base + kb), idesc, kk > 0 ? 1u : 0u);
+            }
+            tc::mma_commit(&empty[stage]);  // key tile free when these MMAs finish
+            tc::mma_commit(&tfull[acc]);    // accumulator ready for the epilogue
+            if (++stage == kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+            if (++acc == C::kAcc) {
+                acc = 0;
+                aphase ^= 1u;
+            }
+        }
+    } else if (warp >= 2) {
+        // ------------------------------------------------ epilogue: one key per thread
+        const int quarter = warp & 3;          // TMEM lanes this warp may read
+        const int row = quarter * 32 + lane;   // key within the tile
+        int acc = 0;
+        uint32_t aphase = 0;
+        int64_t cur_g = -1, gnav = 0;
+        int64_t nav[NQ];
+        for (int64_t u = u0; u < u1; ++u) {
+            const int64_t g = u / a.n_tiles;
+            const int t = (int)(u % a.n_tiles);
+            if (g != cur_g) {
+                cur_g = g;
+                gnav = 0;
+#pragma unroll
+                for (int qq = 0; qq < NQ; qq++) {
+                    nav[qq] = min((a.q_pos[g * NQ + qq] + 1) / a.m, a.n_cap);
+                    gnav = max(gnav, nav[qq]);
+                }
+            }
+            const int64_t key = (int64_t)t * kTileKeys + row;
+            if ((int64_t)t * kTileKeys >= gnav) {  // nothing complete in this tile
+                if (key < a.n_cap)
+#pragma unroll
+                    for (int qq = 0; qq < NQ; qq++) a.scores[(g * NQ + qq) * a.ld + key] = -INFINITY;
+                continue;
+            }
+            // one lane waits, the whole warp follows its verdict (tcgen05.ld is warp-wide)
+            int ok = 1;
+            if (lane == 0) ok = tc::mbar_wait(&tfull[acc], aphase, abort_flag, a.status) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc::fence_after_sync();
+            const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::N);
+#pragma unroll
+            for (int qq = 0; qq < NQ; qq++) {
+                const float4* w4 = reinterpret_cast<const float4*>(a.w_idx + (g * NQ + qq) * kHI);
+                float s = 0.f;
+#pragma unroll
+                for (int half = 0; half < 2; half++) {
+                    float v[32];
+                    tc::tmem_ld32(tbase + (uint32_t)(qq * kHI + half * 32), v);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; j4++) {
+                        const float4 w = __ldg(w4 + half * 8 + j4);
+                        s = fmaf(w.x, fmaxf(v[4 * j4 + 0], 0.f), s);
+                        s = fmaf(w.y, fmaxf(v[4 * j4 + 1], 0.f), s);
+                        s = fmaf(w.z, fmaxf(v[4 * j4 + 2], 0.f), s);
+                        s = fmaf(w.w, fmaxf(v[4 * j4 + 3], 0.f), s);
+                    }
+                }
+                if (key < a.n_cap) a.scores[(g * NQ + qq) * a.ld + key] = key < nav[qq] ? s : -INFINITY;
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&tempty[acc]);
+            if (++acc == C::kAcc) {
+                acc = 0;
+                aphase ^= 1u;
+            }
+        }
+    }
+    // ---------------------------------------------------- teardown
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+cudaError_t launch_indexer_tc(const Geometry& g, const void* q_idx, const float* w_idx, int HI,
+                              int dI, const void* keys, int64_t n_cap, int B, int Q,
+                              const int64_t* q_pos, uint32_t* status, float* scores, int64_t ld,
+                              cudaStream_t st, bool* launched) {
     *launched = false;
-    return cudaSuccess;
+    if (g.act != CSA_BF16 || HI != kHI || dI != kDI || n_cap < kTileKeys || Q < 1) return cudaSuccess;
+    if (((uintptr_t)w_idx & 15u) || (ld % 4) != 0) return cudaSuccess;
+    const int qps = Q / B;
+    const int NQ = (qps % 4 == 0) ? 4 : 1;
+    CUtensorMap tm_keys, tm_q;
+    const uint64_t kd[3] = {(uint64_t)kDI, (uint64_t)n_cap, (uint64_t)B};
+    const uint64_t ks[2] = {(uint64_t)kDI * 2, (uint64_t)n_cap * kDI * 2};
+    const uint32_t kb[3] = {64, (uint32_t)kTileKeys, 1};
+    const uint64_t qd[2] = {(uint64_t)kDI, (uint64_t)Q * kHI};
+    const uint64_t qs[1] = {(uint64_t)kDI * 2};
+    const uint32_t qbox[2] = {64, (uint32_t)(NQ * kHI)};
+    if (!make_tmap_bf16(&tm_keys, keys, 3, kd, ks, kb) || !make_tmap_bf16(&tm_q, q_idx, 2, qd, qs, qbox))
+        return cudaSuccess;  // no tensor map: the CUDA-core path runs instead
+    IdxArgs a;
+    a.w_idx = w_idx;
+    a.q_pos = q_pos;
+    a.scores = scores;
+    a.ld = ld;
+    a.n_cap = n_cap;
+    a.qps = qps;
+    a.m = g.m;
+    a.n_tiles = (int)((n_cap + kTileKeys - 1) / kTileKeys);
+    a.total_units = (int64_t)(Q / NQ) * a.n_tiles;
+    a.status = status;
+    const int64_t sms = num_sms();
+    const int grid = (int)(a.total_units < sms ? a.total_units : sms);
+    cudaError_t e;
+    if (NQ == 1) {
+        static bool attr = false;
+        if (!attr) {
+            e = cudaFuncSetAttribute(indexer_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)Cfg<1>::kSmem);
+            if (e != cudaSuccess) return e;
+            attr = true;
+        }
+        indexer_tc_kernel<1><<<grid, kThreads, Cfg<1>::kSmem, st>>>(tm_keys, tm_q, a);
+    } else {
+        static bool attr = false;
+        if (!attr) {
+            e = cudaFuncSetAttribute(indexer_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)Cfg<4>::kSmem);
+            if (e != cudaSuccess) return e;
+            attr = true;
+        }
+        indexer_tc_kernel<4><<<grid, kThreads, Cfg<4>::kSmem, st>>>(tm_keys, tm_q, a);
+    }
+    note_launch();
+    *launched = true;
+    return cudaGetLastError();
 }
 
 }  // namespace csa

@@ -148,13 +148,11 @@ __global__ void __launch_bounds__(kTopkThreads)
     }
 }
 
-cudaError_t launch_topk(const Geometry& g, const IndexTopkPlan& pl, const float* scores,
-                        int64_t n_cap, int B, int Q, const int64_t* q_pos, int32_t* idx,
-                        float* sel, cudaStream_t st) {
-    (void)B;
+cudaError_t launch_topk(const Geometry& g, const float* scores, int64_t ld, int64_t n_cap, int Q,
+                        const int64_t* q_pos, int32_t* idx, float* sel, cudaStream_t st) {
     if (Q == 0) return cudaSuccess;
-    topk_radix_kernel<<<Q, kTopkThreads, 0, st>>>(scores, pl.n_cap_pad, n_cap, q_pos, g.m, g.k,
-                                                   idx, sel);
+    topk_radix_kernel<<<Q, kTopkThreads, 0, st>>>(scores, ld, n_cap, q_pos, g.m, g.k, idx, sel);
+    note_launch();
     return cudaGetLastError();
 }
 

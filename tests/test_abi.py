@@ -47,6 +47,13 @@ def test_library_exports_every_declared_symbol(L):
         assert n in exported, n
 
 
+def test_library_has_no_unresolved_symbols_of_its_own(L):
+    out = subprocess.run(["nm", "-D", "--undefined-only", L.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    own = [line for line in out.splitlines() if "csa" in line]
+    assert not own, own
+
+
 def test_library_holds_sm103a_code(L):
     out = subprocess.run(["cuobjdump", "--list-elf", L.LIB_PATH], capture_output=True, text=True)
     assert "sm_103a" in out.stdout, out.stdout + out.stderr
