@@ -75,19 +75,21 @@ IndexTopkPlan plan_index_topk(const Geometry& g, int B, int Q, int HI, int64_t n
     return pl;
 }
 
-bool attend_tc_supported(const Geometry& g, int H);
-int attend_tc_splits(const Geometry& g, bool sparse, int Q, int64_t list_len);
+bool attend_tc_supported(const Geometry& g, bool sparse, int H, int64_t n_cap, int64_t n_win);
+void plan_attend_tc(const Geometry& g, bool sparse, int Q, int64_t n_cap, AttendPlan* pl);
 
-AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int64_t n_cap) {
+AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int64_t n_cap,
+                       int64_t n_win) {
     (void)B;
     AttendPlan pl;
     pl.list_len = (sparse ? (int64_t)g.k : n_cap) + g.W;
-    pl.use_tc = attend_tc_supported(g, H) ? 1 : 0;
+    pl.use_tc = attend_tc_supported(g, sparse, H, n_cap, n_win) ? 1 : 0;
+    pl.tc_T_sel = pl.tc_T = pl.tc_grid = 0;
+    pl.tc_total = 0;
     if (pl.use_tc) {
         pl.head_group = H;
-        pl.splits = attend_tc_splits(g, sparse, Q, pl.list_len);
-        int64_t per = (pl.list_len + pl.splits - 1) / pl.splits;
-        pl.rows_per_split = (per + 127) / 128 * 128;
+        pl.rows_per_split = 0;
+        plan_attend_tc(g, sparse, Q, n_cap, &pl);
     } else {
         pl.head_group = (H % 16 == 0) ? 16 : 8;
         const int hgs = H / pl.head_group;
@@ -211,12 +213,11 @@ csa_status csa_compress(const csa_params* p, const void* kv_raw, int32_t B, int6
 
 size_t csa_workspace_bytes(const csa_params* p, int32_t op, int32_t B, int32_t Q, int32_t H,
                            int32_t n_idx_heads, int64_t n_cap, int64_t n_win) {
-    (void)n_win;
-    if (check_params(p) != CSA_OK || B <= 0 || Q < 0 || n_cap < 0) return 0;
+    if (check_params(p) != CSA_OK || B <= 0 || Q < 0 || n_cap < 0 || n_win < 0) return 0;
     Geometry g = resolve(p);
     if (op == CSA_OP_INDEX_TOPK) return plan_index_topk(g, B, Q, n_idx_heads, n_cap).total;
-    if (op == CSA_OP_ATTEND) return H > 0 ? plan_attend(g, true, B, Q, H, n_cap).total : 0;
-    if (op == CSA_OP_HCA_ATTEND) return H > 0 ? plan_attend(g, false, B, Q, H, n_cap).total : 0;
+    if (op == CSA_OP_ATTEND) return H > 0 ? plan_attend(g, true, B, Q, H, n_cap, n_win).total : 0;
+    if (op == CSA_OP_HCA_ATTEND) return H > 0 ? plan_attend(g, false, B, Q, H, n_cap, n_win).total : 0;
     return 0;
 }
 
@@ -349,7 +350,7 @@ static csa_status attend_common(const csa_params* p, bool sparse, const void* q,
     CHECK(check_ptr(lse, "lse", true));
     CHECK(check_ptr(ws, "ws"));
     Geometry g = resolve(p);
-    AttendPlan pl = plan_attend(g, sparse, B, Q, H, n_cap);
+    AttendPlan pl = plan_attend(g, sparse, B, Q, H, n_cap, n_win);
     if (ws_bytes < pl.total) return fail(CSA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", name, ws_bytes, pl.total);
     uint8_t* w = reinterpret_cast<uint8_t*>(ws);
     cudaError_t e = launch_attend(g, pl, sparse, q, H, B, Q, q_pos, cache, n_cap, topk_idx, window,

@@ -35,10 +35,15 @@ struct AttendPlan {
     int64_t rows_per_split;
     int head_group;       // heads per CTA
     int use_tc;           // tensor-core kernel
+    // tensor-core kernel: tiles of 128 rows per query (selected / cache part
+    // and all), Q * tc_T tiles dealt to tc_grid persistent CTAs
+    int tc_T_sel, tc_T, tc_grid;
+    int64_t tc_total;
     size_t part_o_off, part_ml_off;  // [Q, S, H, D] and [Q, S, H, 2] float32
     size_t total;
 };
-AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int64_t n_cap);
+AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int64_t n_cap,
+                       int64_t n_win);
 
 cudaError_t launch_cache_pack(const Geometry& g, const float* src, int64_t n, void* dst,
                               cudaStream_t st);

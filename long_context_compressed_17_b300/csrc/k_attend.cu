@@ -199,28 +199,40 @@ __global__ void __launch_bounds__(kAttThreads) attend_generic_kernel(AttendArgs 
 }
 
 // Merge split partials, add the sink, normalise, rotate by -i and store.
-// grid (Q*H), block 128, dynamic smem D + 64 floats.
+// grid (Q*H), block 128, dynamic smem D + 64 floats.  The partials of query
+// q occupy slots 0..S_q-1 of its S slots: S_q = S for the CUDA-core kernel;
+// for the tensor-core kernel (tiles > 0) S_q is the number of CTAs whose
+// balanced tile range [c*total/grid, (c+1)*total/grid) meets the query's
+// tiles [q*tiles, (q+1)*tiles).
 __global__ void __launch_bounds__(128)
     attend_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
-                          int S, int H, int D, const float* __restrict__ sink,
+                          int S_alloc, int H, int D, const float* __restrict__ sink,
                           const int64_t* __restrict__ q_pos, int R, double base, int derotate,
-                          void* __restrict__ out, int act, float* __restrict__ lse) {
+                          void* __restrict__ out, int act, float* __restrict__ lse, int64_t tiles,
+                          int64_t total, int grid) {
     extern __shared__ float row[];
     float* cs = row + D;
     const int tid = threadIdx.x;
     const int64_t qh = blockIdx.x;
     const int64_t qi = qh / H;
     const int h = (int)(qh % H);
+    const int S = S_alloc;
+    int Sq = S_alloc;
+    if (tiles > 0) {
+        const int64_t c0 = ((qi * tiles + 1) * grid - 1) / total;
+        const int64_t c1 = (((qi + 1) * tiles) * grid - 1) / total;
+        Sq = (int)(c1 - c0 + 1);
+    }
     const float sk = sink[h];
     float mstar = sk;
-    for (int s = 0; s < S; s++) mstar = fmaxf(mstar, part_ml[((qi * S + s) * H + h) * 2]);
+    for (int s = 0; s < Sq; s++) mstar = fmaxf(mstar, part_ml[((qi * S + s) * H + h) * 2]);
     const int64_t i = q_pos[qi];
     if (derotate)
         for (int j = tid; j < R / 2; j += blockDim.x) rope_cos_sin(-(double)i, j, R, base, &cs[2 * j], &cs[2 * j + 1]);
     float l = 0.f;
     if (mstar != -INFINITY) {
         l = expf(sk - mstar);
-        for (int s = 0; s < S; s++) {
+        for (int s = 0; s < Sq; s++) {
             const float* ml = part_ml + ((qi * S + s) * H + h) * 2;
             if (ml[0] != -INFINITY) l += ml[1] * expf(ml[0] - mstar);
         }
@@ -229,7 +241,7 @@ __global__ void __launch_bounds__(128)
     for (int d = tid; d < D; d += blockDim.x) {
         float acc = 0.f;
         if (l > 0.f)
-            for (int s = 0; s < S; s++) {
+            for (int s = 0; s < Sq; s++) {
                 const float* ml = part_ml + ((qi * S + s) * H + h) * 2;
                 if (ml[0] != -INFINITY)
                     acc = fmaf(expf(ml[0] - mstar), part_o[((qi * S + s) * H + h) * D + d], acc);
@@ -255,8 +267,8 @@ __global__ void __launch_bounds__(128)
 cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool sparse, const void* q,
                              int H, int B, int Q, const int64_t* q_pos, const void* cache,
                              int64_t n_cap, const int32_t* topk_idx, const void* window,
-                             int64_t n_win, const int64_t* win_pos0, uint8_t* ws,
-                             uint32_t* status, cudaStream_t st);
+                             int64_t n_win, const int64_t* win_pos0, float* part_o,
+                             float* part_ml, uint32_t* status, cudaStream_t st);
 
 template <int D, int HG>
 static cudaError_t run_generic(const AttendArgs& a, int Q, int H, cudaStream_t st) {
@@ -282,7 +294,7 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
     cudaError_t e;
     if (pl.use_tc) {
         e = launch_attend_tc(g, pl, sparse, q, H, B, Q, q_pos, cache, n_cap, topk_idx, window,
-                             n_win, win_pos0, ws, status, st);
+                             n_win, win_pos0, part_o, part_ml, status, st);
     } else {
         AttendArgs a;
         a.q = reinterpret_cast<const uint8_t*>(q);
@@ -323,7 +335,7 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
     if (e != cudaSuccess) return e;
     attend_combine_kernel<<<(unsigned)((int64_t)Q * H), 128, (g.D + 64) * sizeof(float), st>>>(
         part_o, part_ml, pl.splits, H, g.D, sink, q_pos, g.R, (double)g.base, g.derotate, out,
-        g.act, lse);
+        g.act, lse, pl.use_tc ? (int64_t)pl.tc_T : 0, pl.tc_total, pl.tc_grid);
     note_launch();
     return cudaGetLastError();
 }

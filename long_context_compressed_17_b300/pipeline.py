@@ -43,6 +43,7 @@ class LayerConfig:
     rope_base: float = 10000.0
     eps: float = 1e-6
     derotate: bool = True
+    scale: float = 0.0     # softmax scale; <= 0: 1/sqrt(D)
 
     @property
     def sparse(self) -> bool:
@@ -51,7 +52,7 @@ class LayerConfig:
     def params(self, ratio=None):
         return params(self.D, self.m if ratio is None else ratio, self.topk, self.W, self.act,
                       self.kv, rope_base=self.rope_base, norm_eps=self.eps,
-                      derotate_output=self.derotate)
+                      softmax_scale=self.scale, derotate_output=self.derotate)
 
     @property
     def row_bytes(self) -> int:

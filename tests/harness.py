@@ -28,7 +28,11 @@ def cfg_of(w: Workload):
     from long_context_compressed_17_b300.pipeline import LayerConfig
     return LayerConfig(D=w.D, H=w.H, m=w.m, W=w.W, topk=w.topk if w.kind != "hca_decode" else 0,
                        H_I=w.H_I, d_I=w.d_I, act=w.act, kv=w.kv_fmt, rope_base=w.rope_base,
-                       eps=w.eps)
+                       eps=w.eps, scale=w.softmax_scale)
+
+
+def _scale(w: Workload):
+    return w.softmax_scale if w.softmax_scale > 0 else None
 
 
 # ------------------------------------------------------------------ GPU side
@@ -206,8 +210,12 @@ def check_stored_rows(w, gpu_rows, ref_rows, what):
 
 
 # ---------------------------------------------------------------- decode
-def decode_parity(w, seqs=None, gen_device="cpu", append=True):
+def decode_parity(w, seqs=None, gen_device="cpu", append=True, mutate=None):
+    """Decode step on the GPU vs the oracle.  `mutate(inp)` may rewrite the
+    generated inputs in place before either side sees them."""
     inp = _to_cuda(workloads.generate(w, device=gen_device))
+    if mutate is not None:
+        mutate(inp)
     res = gpu_decode(w, inp, append=append)
     seqs = list(range(w.B)) if seqs is None else seqs
     fmt = {"f32": oracle.F32, "bf16": oracle.BF16, "fp8m": oracle.FP8M}[w.kv_fmt]
@@ -256,7 +264,8 @@ def decode_parity(w, seqs=None, gen_device="cpu", append=True):
         else:
             out_o, lse_o = oracle.attend_query(q, i, w.m, cache_c, w.D, None, window,
                                                int(inp["win_pos0"][b]), w.W, sink,
-                                               rope_dims=w.rope_dims, base=w.rope_base, eps=w.eps)
+                                               rope_dims=w.rope_dims, base=w.rope_base, eps=w.eps,
+                       scale=_scale(w))
         out_g = res["out"][b].float().cpu().numpy()
         mx, mn = assert_close(out_g, out_o, w.act, "out seq %d" % b)
         lse_g = res["lse"][b].cpu().numpy()
@@ -274,7 +283,7 @@ def _attend_compact(w, q, i, cache_c, idx_c, window, win_pos0, sink):
     wrows = oracle.read_rows(window, D)[lo - win_pos0:i + 1 - win_pos0] if w.W else np.zeros((0, D))
     allrows = np.concatenate([rows, wrows], axis=0)
     return oracle.attend_rows(q, i, allrows, sink, rope_dims=w.rope_dims, base=w.rope_base,
-                              eps=w.eps)
+                              eps=w.eps, scale=_scale(w))
 
 
 
@@ -313,7 +322,8 @@ def prefill_parity(w, sample=None, gen_device="cpu"):
     pos = np.array([w.T_cached + t for t in qs], np.int64)
     out_o, lse_o = oracle.attend_batch(q[qs], seq, pos, w.m, cache_o[None], w.D, g_idx[qs],
                                        window_o[None], inp["raw_pos0"], w.W, sink,
-                                       rope_dims=w.rope_dims, base=w.rope_base, eps=w.eps)
+                                       rope_dims=w.rope_dims, base=w.rope_base, eps=w.eps,
+                       scale=_scale(w))
     assert_close(out_g[qs], out_o, w.act, "prefill out")
     assert np.max(np.abs(lse_g[qs] - lse_o)) <= LSE_TOL[w.act]
     # end to end (the oracle's own selection) for the queries whose sets agree

@@ -51,8 +51,43 @@ def test_hca_decode_small():
     decode_parity(SMALL_HCA)
 
 
-def test_csa_decode_fp8_small():
-    decode_parity(SMALL_FP8)
+SMALL_HCA_TILES = workloads.HCA_DECODE_1M.replace(
+    name="hca_decode_tiles", B=3, L_per_seq=(128 * 300, 128 * 170 + 64, 128 * 129 - 1))
+
+
+def test_hca_decode_several_tiles():
+    """Caches of 300, 170 and 128 blocks: several 128-row tiles, a ragged last tile."""
+    decode_parity(SMALL_HCA_TILES)
+
+
+def _ramp_toward_q(inp, t_max):
+    """Every query head points along one unit direction u of the 448 unrotated
+    dims, and cache row j gains t_max * j / n along u.  Its logit is then about
+    scale' * t_j plus N(0, 1) noise, so the logits climb along the row list and
+    the running softmax reference is raised several times per query; the
+    output stays of order 1."""
+    dev = inp["q"].device
+    D = inp["q"].shape[-1]
+    u = torch.zeros(D, device=dev)
+    u[:D - 64] = 1.0 / (D - 64) ** 0.5
+    inp["q"].copy_(u.expand_as(inp["q"]).to(inp["q"].dtype))
+    n = inp["cache"].shape[1]
+    t = t_max * torch.arange(n, device=dev, dtype=torch.float32) / n
+    inp["cache"].copy_((inp["cache"].float() + t[None, :, None] * u).to(inp["cache"].dtype))
+
+
+def test_hca_decode_growing_logits_rescale():
+    # softmax scale 3/sqrt(D): 4 cache tiles whose maxima climb by ~9 nats each
+    w = SMALL_HCA_TILES.replace(name="hca_ramp", B=2, L_per_seq=(128 * 500, 128 * 380),
+                                softmax_scale=3.0 / 512 ** 0.5)
+    decode_parity(w, mutate=lambda inp: _ramp_toward_q(inp, 12.0))
+
+
+def test_csa_decode_growing_logits_rescale():
+    # the selected blocks are listed in index order, so their logits climb too
+    w = SMALL_CSA.replace(name="csa_ramp", B=2, L_per_seq=(20000, 9001), topk=600,
+                          softmax_scale=3.0 / 512 ** 0.5)
+    decode_parity(w, mutate=lambda inp: _ramp_toward_q(inp, 12.0))
 
 
 def test_fp8_pack_is_bit_exact():

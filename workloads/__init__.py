@@ -47,6 +47,7 @@ class Workload:
     rope_dims: int = 64
     rope_base: float = 10000.0
     eps: float = 1e-6
+    softmax_scale: float = 0.0  # <= 0: 1/sqrt(D)
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
