@@ -61,16 +61,18 @@ def test_hca_decode_several_tiles():
 
 
 def _ramp_toward_q(inp, t_max):
-    """Every query head points along one unit direction u of the 448 unrotated
-    dims, and cache row j gains t_max * j / n along u.  Its logit is then about
-    scale' * t_j plus N(0, 1) noise, so the logits climb along the row list and
-    the running softmax reference is raised several times per query; the
-    output stays of order 1."""
+    """Every query head is 1 on dims 0..127 and 0 elsewhere (unrotated dims), so
+    its normalised form is exactly 2 there -- exact in bf16 as well.  Cache
+    row j gains t_max * j / n along u = that direction / sqrt(128).  Its logit
+    is then about scale * 2 * sqrt(128) * t_j plus noise, climbing along the
+    row list, so the running softmax reference is raised several times per
+    query; the output stays of order 1."""
     dev = inp["q"].device
     D = inp["q"].shape[-1]
-    u = torch.zeros(D, device=dev)
-    u[:D - 64] = 1.0 / (D - 64) ** 0.5
-    inp["q"].copy_(u.expand_as(inp["q"]).to(inp["q"].dtype))
+    q = torch.zeros(D, device=dev)
+    q[:128] = 1.0
+    inp["q"].copy_(q.expand_as(inp["q"]).to(inp["q"].dtype))
+    u = q / 128 ** 0.5
     n = inp["cache"].shape[1]
     t = t_max * torch.arange(n, device=dev, dtype=torch.float32) / n
     inp["cache"].copy_((inp["cache"].float() + t[None, :, None] * u).to(inp["cache"].dtype))
