@@ -134,14 +134,19 @@ csa_status csa_index_topk(const csa_params* p, const void* q_idx, const float* w
  * scores.  csa_index_score writes score_b for b < floor((i+1)/m) and -inf for
  * the other blocks b < n_cap into scores[q*ld_scores + b] (float32, device,
  * ld_scores >= n_cap, caller-owned); blocks are laid out as for keys.
+ * ws: status word only (>= 256 bytes).
  * csa_topk_select reads such a score matrix and writes topk_idx/topk_score
- * exactly as csa_index_topk does; it flags nothing.  ws: status word only
- * (>= 256 bytes). */
+ * exactly as csa_index_topk does; it flags nothing.  It CONSUMES the score
+ * matrix: when a query's blocks are selected in several chunks, the chunks'
+ * candidates are written over the scores (copy them first to keep them).
+ * Sizes whose selection does not fit in shared memory (k * n_cap / 8192 above
+ * roughly 51200, e.g. k = 4096 with n_cap > ~100K) return CSA_ERR_UNSUPPORTED,
+ * as csa_index_topk does. */
 csa_status csa_index_score(const csa_params* p, const void* q_idx, const float* w_idx,
                            int32_t n_idx_heads, int32_t idx_dim, const void* keys, int64_t n_cap,
                            int32_t B, int32_t Q, const int64_t* q_pos, float* scores,
                            int64_t ld_scores, void* ws, size_t ws_bytes, csa_stream_t stream);
-csa_status csa_topk_select(const csa_params* p, const float* scores, int64_t ld_scores,
+csa_status csa_topk_select(const csa_params* p, float* scores, int64_t ld_scores,
                            int64_t n_cap, int32_t Q, const int64_t* q_pos, int32_t* topk_idx,
                            float* topk_score, csa_stream_t stream);
 

@@ -68,15 +68,15 @@ __device__ __forceinline__ float load_kv(const uint8_t* row, int fmt, int D, int
 }
 
 // ---------------------------------------------------------------- RoPE
-// cos/sin of pos * base^(-2j/R), evaluated in double so that positions up to
-// 2^20 and beyond keep a full-precision angle.
-__device__ __forceinline__ void rope_cos_sin(double pos, int j, int R, double base, float* c,
-                                             float* s) {
-    double theta = pow(base, -2.0 * (double)j / (double)R);
-    double sn, cs;
-    sincos(pos * theta, &sn, &cs);
-    *c = (float)cs;
-    *s = (float)sn;
+// cos/sin of pos * theta.  The angle (up to ~1e6 rad at 1M context) is formed
+// and reduced modulo 2*pi in double, so the float sincos sees |r| <= pi and
+// the result keeps full float accuracy at any position.
+__device__ __forceinline__ void rope_cs(double pos, double theta, float* c, float* s) {
+    const double kTwoPi = 6.283185307179586476925286766559;
+    const double a = pos * theta;
+    const double k = rint(a * (1.0 / kTwoPi));
+    const float r = (float)fma(-k, kTwoPi, a);
+    sincosf(r, s, c);
 }
 
 // ---------------------------------------------------------------- reductions

@@ -61,6 +61,13 @@ Geometry resolve(const csa_params* p) {
     return g;
 }
 
+RopeTheta rope_theta(const Geometry& g) {
+    RopeTheta t;
+    for (int j = 0; j < 32; j++)
+        t.t[j] = pow((double)g.base, -2.0 * (double)j / (double)g.R);
+    return t;
+}
+
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 IndexTopkPlan plan_index_topk(const Geometry& g, int B, int Q, int HI, int64_t n_cap) {
@@ -264,6 +271,9 @@ csa_status csa_index_topk(const csa_params* p, const void* q_idx, const float* w
     CHECK(check_ptr(topk_idx, "topk_idx"));
     CHECK(check_ptr(topk_score, "topk_score", true));
     CHECK(check_ptr(ws, "ws"));
+    if (topk_chunk(n_cap, Q, p->topk) == 0)
+        return fail(CSA_ERR_UNSUPPORTED, "top-%d of %lld blocks does not fit the selection's shared memory",
+                    p->topk, (long long)n_cap);
     Geometry g = resolve(p);
     IndexTopkPlan pl = plan_index_topk(g, B, Q, n_idx_heads, n_cap);
     if (ws_bytes < pl.total) return fail(CSA_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, pl.total);
@@ -304,7 +314,7 @@ csa_status csa_index_score(const csa_params* p, const void* q_idx, const float* 
     return e == cudaSuccess ? CSA_OK : cuda_fail(e, "csa_index_score");
 }
 
-csa_status csa_topk_select(const csa_params* p, const float* scores, int64_t ld_scores,
+csa_status csa_topk_select(const csa_params* p, float* scores, int64_t ld_scores,
                            int64_t n_cap, int32_t Q, const int64_t* q_pos, int32_t* topk_idx,
                            float* topk_score, csa_stream_t stream) {
     CHECK(check_params(p));
@@ -312,6 +322,9 @@ csa_status csa_topk_select(const csa_params* p, const float* scores, int64_t ld_
     if (Q < 0 || n_cap < 0 || n_cap > (1LL << 30) || ld_scores < n_cap)
         return fail(CSA_ERR_INVALID_ARG, "bad Q / n_cap / ld_scores");
     if (Q == 0) return CSA_OK;
+    if (topk_chunk(n_cap, Q, p->topk) == 0)
+        return fail(CSA_ERR_UNSUPPORTED, "top-%d of %lld blocks does not fit the selection's shared memory",
+                    p->topk, (long long)n_cap);
     CHECK(check_ptr(scores, "scores"));
     CHECK(check_ptr(q_pos, "q_pos"));
     CHECK(check_ptr(topk_idx, "topk_idx"));

@@ -10,6 +10,13 @@
 
 namespace csa {
 
+// RoPE frequencies theta_j = base^(-2j/R) of the 32 rotated pairs (R = 64),
+// computed once per call in double on the host and passed by value to the
+// kernels.
+struct RopeTheta {
+    double t[32];
+};
+
 struct Geometry {  // resolved layer constants
     int D, R, m, k, W;
     float base, eps, scale;
@@ -19,6 +26,9 @@ struct Geometry {  // resolved layer constants
 };
 
 Geometry resolve(const csa_params* p);
+
+// theta_j = base^(-2j/R) for the RoPE pairs of the last R dims.
+RopeTheta rope_theta(const Geometry& g);
 
 // Workspace layout of an operation.  Offsets are in bytes from the start of
 // the workspace; every region is 256-byte aligned.
@@ -54,8 +64,10 @@ cudaError_t launch_indexer(const Geometry& g, const void* q_idx, const float* w_
                            int dI, const void* keys, int64_t n_cap, int B, int Q,
                            const int64_t* q_pos, uint32_t* status, float* scores, int64_t ld,
                            cudaStream_t st);
-cudaError_t launch_topk(const Geometry& g, const float* scores, int64_t ld, int64_t n_cap, int Q,
+cudaError_t launch_topk(const Geometry& g, float* scores, int64_t ld, int64_t n_cap, int Q,
                         const int64_t* q_pos, int32_t* idx, float* sel, cudaStream_t st);
+// Chunk size of the top-k selection for these sizes; 0: does not fit.
+int64_t topk_chunk(int64_t n_cap, int Q, int k);
 cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, const void* q,
                           int H, int B, int Q, const int64_t* q_pos, const void* cache,
                           int64_t n_cap, const int32_t* topk_idx, const void* window,

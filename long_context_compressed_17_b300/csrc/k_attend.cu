@@ -37,7 +37,7 @@ struct AttendArgs {
     int64_t n_win;
     const int64_t* win_pos0;
     int W, m, R;
-    double base;
+    RopeTheta theta;
     float eps, scale;
     float* part_o;   // [Q, S, H, D]
     float* part_ml;  // [Q, S, H, 2]
@@ -80,7 +80,7 @@ __device__ __forceinline__ const uint8_t* resolve_row(const AttendArgs& a, int64
 __device__ inline void prepare_q(const AttendArgs& a, int64_t qi, int64_t i, int h0, int nh, int D,
                                  float* qs, float* cs) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int j = tid; j < a.R / 2; j += blockDim.x) rope_cos_sin((double)i, j, a.R, a.base, &cs[2 * j], &cs[2 * j + 1]);
+    for (int j = tid; j < a.R / 2; j += blockDim.x) rope_cs((double)i, a.theta.t[j], &cs[2 * j], &cs[2 * j + 1]);
     const int act_es = a.act == CSA_F32 ? 4 : 2;
     for (int h = warp; h < nh; h += blockDim.x / 32) {
         const uint8_t* qr = a.q + ((int64_t)qi * a.H + h0 + h) * D * act_es;
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(128)
                           int S_alloc, int H, int D, const float* __restrict__ sink,
                           const int64_t* __restrict__ q_pos, int R, double base, int derotate,
                           void* __restrict__ out, int act, float* __restrict__ lse, int64_t tiles,
-                          int64_t total, int grid) {
+                          int64_t total, int grid, RopeTheta theta) {
     extern __shared__ float row[];
     float* cs = row + D;
     const int tid = threadIdx.x;
@@ -222,13 +222,14 @@ __global__ void __launch_bounds__(128)
         const int64_t c0 = ((qi * tiles + 1) * grid - 1) / total;
         const int64_t c1 = (((qi + 1) * tiles) * grid - 1) / total;
         Sq = (int)(c1 - c0 + 1);
+        if (Sq == 1) return;  // finished (sink, normalisation, rotation) by its only CTA
     }
     const float sk = sink[h];
     float mstar = sk;
     for (int s = 0; s < Sq; s++) mstar = fmaxf(mstar, part_ml[((qi * S + s) * H + h) * 2]);
     const int64_t i = q_pos[qi];
     if (derotate)
-        for (int j = tid; j < R / 2; j += blockDim.x) rope_cos_sin(-(double)i, j, R, base, &cs[2 * j], &cs[2 * j + 1]);
+        for (int j = tid; j < R / 2; j += blockDim.x) rope_cs(-(double)i, theta.t[j], &cs[2 * j], &cs[2 * j + 1]);
     float l = 0.f;
     if (mstar != -INFINITY) {
         l = expf(sk - mstar);
@@ -267,8 +268,9 @@ __global__ void __launch_bounds__(128)
 cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool sparse, const void* q,
                              int H, int B, int Q, const int64_t* q_pos, const void* cache,
                              int64_t n_cap, const int32_t* topk_idx, const void* window,
-                             int64_t n_win, const int64_t* win_pos0, float* part_o,
-                             float* part_ml, uint32_t* status, cudaStream_t st);
+                             int64_t n_win, const int64_t* win_pos0, const float* sink,
+                             void* out, float* lse, float* part_o, float* part_ml,
+                             uint32_t* status, cudaStream_t st);
 
 template <int D, int HG>
 static cudaError_t run_generic(const AttendArgs& a, int Q, int H, cudaStream_t st) {
@@ -294,7 +296,7 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
     cudaError_t e;
     if (pl.use_tc) {
         e = launch_attend_tc(g, pl, sparse, q, H, B, Q, q_pos, cache, n_cap, topk_idx, window,
-                             n_win, win_pos0, part_o, part_ml, status, st);
+                             n_win, win_pos0, sink, out, lse, part_o, part_ml, status, st);
     } else {
         AttendArgs a;
         a.q = reinterpret_cast<const uint8_t*>(q);
@@ -314,7 +316,7 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
         a.W = g.W;
         a.m = g.m;
         a.R = g.R;
-        a.base = g.base;
+        a.theta = rope_theta(g);
         a.eps = g.eps;
         a.scale = g.scale;
         a.part_o = part_o;
@@ -335,7 +337,7 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
     if (e != cudaSuccess) return e;
     attend_combine_kernel<<<(unsigned)((int64_t)Q * H), 128, (g.D + 64) * sizeof(float), st>>>(
         part_o, part_ml, pl.splits, H, g.D, sink, q_pos, g.R, (double)g.base, g.derotate, out,
-        g.act, lse, pl.use_tc ? (int64_t)pl.tc_T : 0, pl.tc_total, pl.tc_grid);
+        g.act, lse, pl.use_tc ? (int64_t)pl.tc_T : 0, pl.tc_total, pl.tc_grid, rope_theta(g));
     note_launch();
     return cudaGetLastError();
 }

@@ -4,31 +4,36 @@
 // "DeepSeek-V4百万上下文时代的开源宣言" §三.2: CSA Step 3 (multi-query attention
 // over the top-k compressed blocks), HCA (dense attention over every block),
 // and 四项关键 Trick: RMSNorm and partial RoPE on q, a sliding window of the
-// last W raw tokens, a learnable sink in the softmax denominator.
+// last W raw tokens, a learnable sink in the softmax denominator, RoPE at -i
+// on the output.
 //
 // One query's row list is cut into tiles of 128 rows: ceil(k/128) tiles of
 // selected blocks (CSA, gathered row by row with TMA gather4) or
 // ceil(n_cap/128) tiles of consecutive blocks (HCA, TMA tiles), then
 // ceil(W/128) window tiles.  The (query, tile) pairs are dealt out in
 // contiguous, balanced ranges to one persistent CTA per SM; the run of one
-// query's tiles inside a CTA is a segment, reduced to an unnormalised partial
-// (m, l, o) that attend_combine_kernel merges with the sink.
+// query's tiles inside a CTA is a segment.  A segment that is the whole query
+// is finished in place (sink, normalisation, rotation, bf16 store); the others
+// leave an unnormalised partial (m, l, o) for attend_combine_kernel.
 //
 // Per tile (one shared KV head, so key = value = row e_j):
-//   S^T[128 rows, 64 heads] = E[128, 512] . Q'^T          (swap-AB: rows are M)
+//   S^T[128 rows, 64 heads] = E[128, 512] . Q'^T        (swap-AB: rows are M)
 //   P = 2^(S^T * scale * log2 e - m)  (bf16, per head running reference m)
-//   O^T[512, 64] += E^T[512, 128] . P^T                    (4 MMAs of M = 128)
-// The tile stays in shared memory (4 slices of 128 rows x 128 dims, 128-byte
-// swizzle) between the two products: E is the K-major A operand of the first
-// and, read along its rows, the MN-major A operand of the second.  A slice is
-// refilled with the next tile as soon as its PV product is done.  The running
-// reference m is raised only when a tile's maximum exceeds it by more than
+//   O^T[512, 64] += E^T[512, 128] . P^T                  (4 MMAs of M = 128)
+// Every MMA is M = 128 x N = 64: at N = 64 an MMA costs the same ~50 cycles
+// for M = 64 and M = 128, so the rows, not the heads, fill M.  The tile (4
+// slices of 128 rows x 128 dims, 128-byte swizzle) is the K-major A operand of
+// the first product and, read along its rows, the MN-major A operand of the
+// second; each slice is refilled with the next tile as soon as its PV product
+// is done, so the next loads overlap the PV products and the QK product of a
+// tile starts on its first slice.
+// The running reference m is raised only when a logit exceeds it by more than
 // 2^8; O^T (in TMEM) and the partial sums are then rescaled in place.
 //
-// Warp roles: warp 0 loads (TMA), warp 1 issues MMAs, warps 2..5 normalise
-// and rotate q, run the softmax and write the partials.  Every wait is
-// bounded; on a timeout the kernel sets CSA_DEV_TIMEOUT, every role leaves its
-// loop, outstanding copies and MMAs are waited for and TMEM is freed.
+// Warp roles: warp 0 loads (TMA), warp 1 issues MMAs, warps 2..9 normalise
+// and rotate q, run the softmax and the epilogue.  Every wait is bounded; on
+// a timeout the kernel sets CSA_DEV_TIMEOUT, every role leaves its loop,
+// outstanding copies and MMAs are waited for and TMEM is freed.
 #include <math.h>
 
 #include "common.cuh"
@@ -44,7 +49,7 @@ namespace {
 
 constexpr int kD = 512;
 constexpr int kH = 64;
-constexpr int kRows = 128;
+constexpr int kRows = 128;                          // rows per tile (MMA M)
 constexpr int kSlices = 4;                          // 128-dim slices of a tile
 constexpr uint32_t kBoxBytes = kRows * 128;         // 128 rows x 64 dims (bf16)
 constexpr uint32_t kSliceBytes = 2 * kBoxBytes;     // 128 rows x 128 dims
@@ -52,12 +57,17 @@ constexpr uint32_t kQBoxBytes = kH * 128;           // 64 heads x 64 dims
 constexpr uint32_t kQBytes = 8 * kQBoxBytes;        // 64 heads x 512 dims
 constexpr uint32_t kPBytes = kRows * kH * 2;        // 128 rows x 64 heads
 constexpr size_t kSmem = 1024 + kSlices * kSliceBytes + kQBytes + kPBytes;
-constexpr int kThreads = 192;
+constexpr int kSoftWarps = 8;                       // 4 TMEM lane quarters x 2 head halves
+constexpr int kSoftThreads = kSoftWarps * 32;
+constexpr int kThreads = 64 + kSoftThreads;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // S^T: 64 columns
 constexpr uint32_t kColO = 256;  // O^T: 4 x 64 columns
 constexpr float kRescaleLog2 = 8.f;
-constexpr int kBarSoftmax = 1;   // named barrier of the 4 softmax warps
+constexpr float kNoRef = -1e30f; // running reference before any valid logit
+constexpr int kBarSoftmax = 1;   // named barrier of the softmax warps
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 struct AttTcArgs {
     const uint16_t* q;        // [Q, 64, 512] bf16
@@ -67,7 +77,6 @@ struct AttTcArgs {
     int64_t n_cap, n_win;
     const int64_t* win_pos0;  // [B]
     int W, m, qps;
-    double base;
     float eps, scale_log2;
     int T_sel, T;             // tiles per query: selected / cache part, all
     int64_t total;            // Q * T
@@ -75,7 +84,12 @@ struct AttTcArgs {
     int S;                    // partial slots per query
     float* part_o;            // [Q, S, 64, 512]
     float* part_ml;           // [Q, S, 64, 2]
+    const float* sink;        // [64]
+    uint16_t* out;            // [Q, 64, 512] bf16 (queries finished in one CTA)
+    float* lse;               // [Q, 64] or nullptr
+    int derotate;
     uint32_t* status;
+    RopeTheta theta;
 };
 
 // CTA that owns global tile g (CTA c owns [c*total/grid, (c+1)*total/grid)).
@@ -119,53 +133,47 @@ __device__ __forceinline__ int last_live(const AttTcArgs& a, const QueryInfo& qi
 }
 
 // -------------------------------------------------------------- softmax helpers
-// Reduce-scatter 64 per-lane values over the warp: afterwards lane l holds the
-// reduction of entries 2l and 2l+1 over all 32 lanes.
+// Reduce 32 per-lane values over the warp so that lane l ends with the
+// reduction of entry l over all 32 lanes (a reduce-scatter, 31 shuffles).
 template <bool kMax>
-__device__ __forceinline__ float2 warp_reduce_scatter64(const float (&v)[64], int lane) {
+__device__ __forceinline__ float warp_reduce_scatter32(const float (&v)[32], int lane) {
     auto op = [](float x, float y) { return kMax ? fmaxf(x, y) : x + y; };
-    float a[32], b[16], c[8], d[4], e[2];
+    float a[16], b[8], c[4], d[2];
     {
         const bool up = lane & 16;
 #pragma unroll
-        for (int j = 0; j < 32; j++) {
-            float keep = up ? v[j + 32] : v[j], send = up ? v[j] : v[j + 32];
+        for (int j = 0; j < 16; j++) {
+            float keep = up ? v[j + 16] : v[j], send = up ? v[j] : v[j + 16];
             a[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
         }
     }
     {
         const bool up = lane & 8;
 #pragma unroll
-        for (int j = 0; j < 16; j++) {
-            float keep = up ? a[j + 16] : a[j], send = up ? a[j] : a[j + 16];
+        for (int j = 0; j < 8; j++) {
+            float keep = up ? a[j + 8] : a[j], send = up ? a[j] : a[j + 8];
             b[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
         }
     }
     {
         const bool up = lane & 4;
 #pragma unroll
-        for (int j = 0; j < 8; j++) {
-            float keep = up ? b[j + 8] : b[j], send = up ? b[j] : b[j + 8];
+        for (int j = 0; j < 4; j++) {
+            float keep = up ? b[j + 4] : b[j], send = up ? b[j] : b[j + 4];
             c[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
         }
     }
     {
         const bool up = lane & 2;
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-            float keep = up ? c[j + 4] : c[j], send = up ? c[j] : c[j + 4];
+        for (int j = 0; j < 2; j++) {
+            float keep = up ? c[j + 2] : c[j], send = up ? c[j] : c[j + 2];
             d[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
         }
     }
-    {
-        const bool up = lane & 1;
-#pragma unroll
-        for (int j = 0; j < 2; j++) {
-            float keep = up ? d[j + 2] : d[j], send = up ? d[j] : d[j + 2];
-            e[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 1));
-        }
-    }
-    return make_float2(e[0], e[1]);
+    const bool up = lane & 1;
+    float keep = up ? d[1] : d[0], send = up ? d[0] : d[1];
+    return op(keep, __shfl_xor_sync(0xffffffffu, send, 1));
 }
 
 __device__ __forceinline__ bool softmax_barrier_or(bool pred) {
@@ -173,15 +181,15 @@ __device__ __forceinline__ bool softmax_barrier_or(bool pred) {
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, 128, p;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)pred), "r"(kBarSoftmax)
+        : "r"((uint32_t)pred), "r"(kBarSoftmax), "r"(kSoftThreads)
         : "memory");
     return r != 0;
 }
 
-__device__ __forceinline__ void softmax_barrier() { tc::named_barrier(kBarSoftmax, 128); }
+__device__ __forceinline__ void softmax_barrier() { tc::named_barrier(kBarSoftmax, kSoftThreads); }
 
 // Wait by lane 0, verdict shared with the warp (tcgen05.ld is warp-wide).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -189,6 +197,13 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     int ok = 1;
     if (lane == 0) ok = tc::mbar_wait(bar, parity, abort_flag, status) ? 1 : 0;
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// 2^x with the hardware approximation (relative error ~2^-22; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -199,20 +214,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tm_sel,
-                     const __grid_constant__ CUtensorMap tm_win, AttTcArgs a) {
+                     const __grid_constant__ CUtensorMap tm_win, const __grid_constant__ AttTcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sE = sm;                              // kSlices x kSliceBytes
+    uint8_t* sE = sm;                              // kSlices x (2 boxes of 128 rows x 64 dims)
     uint8_t* sQ = sE + kSlices * kSliceBytes;      // 8 boxes of 64 heads x 64 dims
     uint8_t* sP = sQ + kQBytes;                    // 128 rows x 64 heads
 
     __shared__ __align__(8) uint64_t full[kSlices], empty[kSlices];
-    __shared__ __align__(8) uint64_t s_full, p_full, o_full, q_full, mma_done;
+    __shared__ __align__(8) uint64_t s_full, p_full, o_seg, q_full, mma_done;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_sh;
     __shared__ float red[4][kH];
-    __shared__ float mref[kH], alph[kH];
-    __shared__ float rope_cs[64];
+    __shared__ float mref_s[kH], alph_s[kH], fac_s[kH];
+    __shared__ float rot_cs[64];
     volatile int* abort_flag = &abort_sh;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -222,8 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_init(&empty[s], 1);
         }
         tc::mbar_init(&s_full, 1);
-        tc::mbar_init(&p_full, 4);
-        tc::mbar_init(&o_full, 1);
+        tc::mbar_init(&p_full, kSoftWarps);
+        tc::mbar_init(&o_seg, 1);   // after the last PV product of a segment
         tc::mbar_init(&q_full, 1);
         tc::mbar_init(&mma_done, 1);
         abort_sh = 0;
@@ -249,17 +264,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (a.W > 0) tc::tma_prefetch_map(&tm_win);
         }
         uint32_t tcount = 0;
-        uint32_t fills[kSlices] = {0, 0, 0, 0};  // loads issued into each slot
-        for (int64_t g = g_begin; g < g_end && !*abort_flag;) {
+        uint32_t fills[kSlices] = {0, 0, 0, 0};  // loads issued into each slice
+        bool stop = false;
+        for (int64_t g = g_begin; g < g_end && !stop;) {
             const int64_t qi = g / a.T;
             const int64_t seg_end = min(g_end, (qi + 1) * a.T);
             const QueryInfo inf = query_info(a, qi);
-            bool stop = false;
-            for (int lt = (int)(g - qi * a.T); lt < (int)(seg_end - qi * a.T); ++lt) {
+            for (int lt = (int)(g - qi * a.T); lt < (int)(seg_end - qi * a.T) && !stop; ++lt) {
                 if (!tile_live(a, inf, lt)) continue;
-                // gathered rows of this lane (CSA selected tiles): rows 4*lane .. 4*lane+3
-                int rows[4] = {0, 0, 0, 0};
                 const bool gather = lt < a.T_sel && a.topk_idx != nullptr;
+                int rows[4] = {0, 0, 0, 0};  // gathered rows of this lane: 4*lane .. 4*lane+3
+                int row0 = 0;
+                const CUtensorMap* map = &tm_sel;
                 if (gather) {
 #pragma unroll
                     for (int j = 0; j < 4; j++) {
@@ -268,6 +284,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (e < 0 || e >= inf.n_av) e = 0;  // masked by the softmax warps
                         rows[j] = (int)((int64_t)inf.seq * a.n_cap + e);
                     }
+                } else if (lt < a.T_sel) {
+                    row0 = lt * kRows;
+                } else {
+                    map = &tm_win;
+                    row0 = (int)(inf.i - a.W + 1 + (int64_t)(lt - a.T_sel) * kRows - a.win_pos0[inf.seq]);
                 }
                 for (int c = 0; c < kSlices; c++) {
                     if (!warp_wait(&empty[c], (tcount & 1u) ^ 1u, abort_flag, a.status, lane)) {
@@ -282,32 +303,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int b = 0; b < 2; b++)
                             tc::tma_gather4(dst + b * kBoxBytes + lane * 512, &tm_sel, &full[c],
                                             c * 128 + b * 64, rows[0], rows[1], rows[2], rows[3]);
-                    } else if (lane == 0) {
-                        int row0;
-                        const CUtensorMap* map;
-                        if (lt < a.T_sel) {
-                            map = &tm_sel;
-                            row0 = lt * kRows;
-                        } else {
-                            map = &tm_win;
-                            row0 = (int)(inf.i - a.W + 1 + (int64_t)(lt - a.T_sel) * kRows -
-                                         a.win_pos0[inf.seq]);
-                        }
-#pragma unroll
-                        for (int b = 0; b < 2; b++)
-                            tc::tma_load_3d(dst + b * kBoxBytes, map, &full[c], c * 128 + b * 64, row0,
-                                            inf.seq);
+                    } else if (lane < 2) {
+                        tc::tma_load_3d(dst + lane * kBoxBytes, map, &full[c], c * 128 + lane * 64, row0, inf.seq);
                     }
                     ++fills[c];
                 }
-                if (stop) break;
                 ++tcount;
             }
-            if (stop) break;
             g = seg_end;
         }
-        // Leave no copy in flight: the newest load of every slot must have
-        // landed (at most one phase of a slot is ever outstanding).
+        // Leave no copy in flight: the newest load of every slice must have
+        // landed (at most one phase of a slice is ever outstanding).
         if (lane == 0) {
             for (int c = 0; c < kSlices; c++) {
                 if (fills[c] == 0) continue;
@@ -317,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, kH, 0, 0);
+            constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kRows, kH, 0, 0);
             constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, kH, 1, 1);
             const uint32_t sE0 = tc::smem_u32(sE), sQ0 = tc::smem_u32(sQ), sP0 = tc::smem_u32(sP);
             uint32_t tcount = 0, nq = 0;
@@ -326,14 +332,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t qi = g / a.T;
                 const int64_t seg_end = min(g_end, (qi + 1) * a.T);
                 const QueryInfo inf = query_info(a, qi);
+                const int lt_last = last_live(a, inf, (int)(g - qi * a.T), (int)(seg_end - qi * a.T));
                 bool first = true;
-                for (int lt = (int)(g - qi * a.T); lt < (int)(seg_end - qi * a.T); ++lt) {
+                for (int lt = (int)(g - qi * a.T); lt <= lt_last; ++lt) {
                     if (!tile_live(a, inf, lt)) continue;
                     if (first) {
                         if (!tc::mbar_wait(&q_full, nq & 1u, abort_flag, a.status)) { stop = true; break; }
                         ++nq;
                     }
-                    // S^T = E . Q'^T over the 512 dims
+                    // S^T = E . Q'^T over the 512 dims, slice by slice as they land
                     for (int c = 0; c < kSlices && !stop; c++) {
                         if (!tc::mbar_wait(&full[c], tcount & 1u, abort_flag, a.status)) { stop = true; break; }
                         tc::fence_after_sync();
@@ -343,26 +350,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int kg = 8 * c + j;
                             const uint64_t ad = tc::sdesc_sw128(slice + (j >> 2) * kBoxBytes + (j & 3) * 32, 16, 1024);
                             const uint64_t bd = tc::sdesc_sw128(sQ0 + (kg >> 2) * kQBoxBytes + (kg & 3) * 32, 16, 1024);
-                            tc::mma_bf16_ss(tmem + kColS, ad, bd, idesc_qk, (c | j) != 0 ? 1u : 0u);
+                            tc::mma_bf16_ss(tmem + kColS, ad, bd, idesc_qk, kg != 0 ? 1u : 0u);
                         }
                     }
                     if (stop) break;
                     tc::mma_commit(&s_full);
                     if (!tc::mbar_wait(&p_full, tcount & 1u, abort_flag, a.status)) { stop = true; break; }
                     tc::fence_after_sync();
-                    // O^T += E^T . P^T, one 128-dim slice at a time
+                    // O^T += E^T . P^T, one 128-dim slice at a time; each slice is
+                    // released for the next tile as soon as its products are done
                     for (int c = 0; c < kSlices; c++) {
                         const uint32_t slice = sE0 + c * kSliceBytes;
 #pragma unroll
-                        for (int kk = 0; kk < 8; kk++) {
+                        for (int kk = 0; kk < kRows / 16; kk++) {
                             const uint64_t ad = tc::sdesc_sw128(slice + kk * 2048, kBoxBytes, 1024);
                             const uint64_t bd = tc::sdesc_sw128(sP0 + kk * 2048, kBoxBytes, 1024);
-                            tc::mma_bf16_ss(tmem + kColO + 64 * c, ad, bd, idesc_pv,
-                                            (first && kk == 0) ? 0u : 1u);
+                            tc::mma_bf16_ss(tmem + kColO + 64 * c, ad, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
                         }
                         tc::mma_commit(&empty[c]);
                     }
-                    tc::mma_commit(&o_full);
+                    if (lt == lt_last) tc::mma_commit(&o_seg);
                     first = false;
                     ++tcount;
                 }
@@ -374,25 +381,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
-        const int sw = warp - 2;                 // 0..3
-        const int tid = threadIdx.x - 64;        // 0..127
-        const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
-        const int row = quarter * 32 + lane;     // row of the tile / dim of an O^T slice
+        // Warp w owns TMEM lane quarter (w % 4) -- 32 tile rows, or 32 dims of
+        // every O^T slice -- and the 32 heads of half (w - 2) / 4.
+        const int sw = warp - 2;                 // 0..7
+        const int tid = threadIdx.x - 64;        // 0..255
+        const int quarter = warp & 3;
+        const int half = sw >> 2;
+        const int h0 = half * 32;
+        const int row = quarter * 32 + lane;     // tile row / dim within an O^T slice
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const float kLn2 = 0.6931471805599453f;
 
         // q' = RoPE(RMSNorm(q), i) of query qi into sQ (bf16, 128-byte swizzle)
         auto prep_q = [&](int64_t qi) {
             const int64_t i = a.q_pos[qi];
             if (tid < 32) {
                 float c, s;
-                rope_cos_sin((double)i, tid, kRopeDims, a.base, &c, &s);
-                rope_cs[2 * tid] = c;
-                rope_cs[2 * tid + 1] = s;
+                rope_cs((double)i, a.theta.t[tid], &c, &s);
+                rot_cs[2 * tid] = c;
+                rot_cs[2 * tid + 1] = s;
             }
             softmax_barrier();
-            for (int hh = 0; hh < 16; hh++) {
-                const int h = sw * 16 + hh;
+            for (int hh = 0; hh < kH / kSoftWarps; hh++) {
+                const int h = sw * (kH / kSoftWarps) + hh;
                 const uint4* src = reinterpret_cast<const uint4*>(a.q + (qi * kH + h) * kD) + lane * 2;
                 const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
                 const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
@@ -413,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 8; e++) {
                         const int j = (lane - 28) * 8 + e;
-                        const float c = rope_cs[2 * j], s = rope_cs[2 * j + 1];
+                        const float c = rot_cs[2 * j], s = rot_cs[2 * j + 1];
                         const float x0 = x[2 * e], x1 = x[2 * e + 1];
                         x[2 * e] = x0 * c - x1 * s;
                         x[2 * e + 1] = x0 * s + x1 * c;
@@ -454,9 +464,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t q0 = next_live_query(g_begin);
             if (q0 >= 0) prep_q(q0);
         }
-        uint32_t tcount = 0;
+        uint32_t tcount = 0, nseg = 0;
         bool stop = false;
-        float l_part[kH];
+        float l_part[32], mref[32];
         for (int64_t g = g_begin; g < g_end && !stop;) {
             const int64_t qi = g / a.T;
             const int64_t seg_end = min(g_end, (qi + 1) * a.T);
@@ -464,23 +474,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int lt0 = (int)(g - qi * a.T), lt1 = (int)(seg_end - qi * a.T);
             const int lt_last = last_live(a, inf, lt0, lt1);
             if (tid == 0 && (inf.i + 1) / a.m > a.n_cap) atomicOr(a.status, CSA_DEV_BAD_POSITION);
-            if (tid < kH) mref[tid] = -INFINITY;
 #pragma unroll
-            for (int h = 0; h < kH; h++) l_part[h] = 0.f;
+            for (int h = 0; h < 32; h++) {
+                l_part[h] = 0.f;
+                mref[h] = kNoRef;
+            }
             int seg_tiles = 0;
+            bool ref_set = false;  // mref_s holds this segment's reference
             for (int lt = lt0; lt <= lt_last; ++lt) {
                 if (!tile_live(a, inf, lt)) continue;
                 // row validity (and the device-side checks of the row list)
-                bool valid;
+                bool valid = false;
                 if (lt < a.T_sel) {
                     const int p = lt * kRows + row;
                     if (a.topk_idx) {
-                        valid = false;
                         if (p < a.k) {
                             const int64_t e = a.topk_idx[qi * a.k + p];
                             if (e >= 0) {
                                 if (e < inf.n_av) valid = true;
-                                else atomicOr(a.status, CSA_DEV_BAD_TOPK_INDEX);
+                                else if (half == 0) atomicOr(a.status, CSA_DEV_BAD_TOPK_INDEX);
                             }
                         }
                     } else {
@@ -489,76 +501,81 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     const int r = (lt - a.T_sel) * kRows + row;
                     const int64_t wpos = inf.i - a.W + 1 + r;
-                    valid = false;
                     if (r < a.W && wpos >= 0) {
                         const int64_t wr = wpos - a.win_pos0[inf.seq];
                         if (wr >= 0 && wr < a.n_win) valid = true;
-                        else atomicOr(a.status, CSA_DEV_BAD_WINDOW);
+                        else if (half == 0) atomicOr(a.status, CSA_DEV_BAD_WINDOW);
                     }
                 }
-                // all four warps leave together, or none does (named barriers follow)
-                if (softmax_barrier_or(!warp_wait(&s_full, tcount & 1u, abort_flag, a.status, lane))) {
-                    stop = true;
-                    break;
-                }
-                tc::fence_after_sync();
-                float x[kH];
-                {
-                    uint32_t r[64];
-                    tc::tmem_ld64(tmem + lane_off + kColS, r);
+                const float mask = valid ? 0.f : -INFINITY;  // x = s * scale + mask
+                const bool ok = warp_wait(&s_full, tcount & 1u, abort_flag, a.status, lane);
+                float x[32];
+                bool need = false;
+                if (ok) {
+                    tc::fence_after_sync();
+                    tc::tmem_ld32(tmem + lane_off + kColS + h0, x);
                     tc::tmem_ld_wait();
 #pragma unroll
-                    for (int h = 0; h < kH; h++) x[h] = valid ? __uint_as_float(r[h]) * a.scale_log2 : -INFINITY;
-                }
-                // per-head maximum of the tile, then the running reference
-                const float2 mx = warp_reduce_scatter64<true>(x, lane);
-                red[sw][2 * lane] = mx.x;
-                red[sw][2 * lane + 1] = mx.y;
-                softmax_barrier();
-                bool mine = false;
-                if (tid < kH) {
-                    const float tm = fmaxf(fmaxf(red[0][tid], red[1][tid]), fmaxf(red[2][tid], red[3][tid]));
-                    const float mo = mref[tid];
-                    float al = 1.f;
-                    if (tm > mo + kRescaleLog2) {
-                        al = (mo == -INFINITY) ? 0.f : exp2f(mo - tm);
-                        mine = mo != -INFINITY;
-                        mref[tid] = tm;
+                    for (int h = 0; h < 32; h++) {
+                        x[h] = fmaf(x[h], a.scale_log2, mask);
+                        need |= x[h] > mref[h] + kRescaleLog2;
                     }
-                    alph[tid] = al;
                 }
-                const bool resc = softmax_barrier_or(mine);
-                if (resc) {
+                // one barrier per tile: leave together on a failed wait, and
+                // raise the running reference when any logit outgrew it
+                if (softmax_barrier_or(!ok || need)) {
+                    if (softmax_barrier_or(!ok)) { stop = true; break; }
+                    // tile maximum per head (over this quarter's rows), then over quarters
+                    red[quarter][h0 + lane] = warp_reduce_scatter32<true>(x, lane);
+                    softmax_barrier();
+                    bool mine = false;
+                    if (tid < kH) {
+                        const float tm = fmaxf(fmaxf(red[0][tid], red[1][tid]), fmaxf(red[2][tid], red[3][tid]));
+                        float mn = ref_set ? mref_s[tid] : kNoRef;
+                        float al = 1.f;
+                        if (tm > mn + kRescaleLog2) {
+                            al = (mn == kNoRef) ? 0.f : ex2_approx(mn - tm);
+                            mine = mn != kNoRef;
+                            mn = tm;
+                        }
+                        mref_s[tid] = mn;
+                        alph_s[tid] = al;
+                    }
+                    const bool resc = softmax_barrier_or(mine);
+                    ref_set = true;
 #pragma unroll
-                    for (int h = 0; h < kH; h++) l_part[h] *= alph[h];
-                    if (seg_tiles > 0) {  // O^T holds this segment's earlier tiles
+                    for (int h = 0; h < 32; h++) mref[h] = mref_s[h0 + h];
+                    if (resc) {
+                        // O^T holds this segment's earlier tiles (their PV products are
+                        // complete: they were issued before this tile's QK product)
+#pragma unroll
+                        for (int h = 0; h < 32; h++) l_part[h] *= alph_s[h0 + h];
                         for (int c = 0; c < kSlices; c++) {
-                            uint32_t r[64];
-                            tc::tmem_ld64(tmem + lane_off + kColO + 64 * c, r);
+                            uint32_t r[32];
+                            tc::tmem_ld32(tmem + lane_off + kColO + 64 * c + h0, *reinterpret_cast<float(*)[32]>(r));
                             tc::tmem_ld_wait();
 #pragma unroll
-                            for (int h = 0; h < kH; h++) r[h] = __float_as_uint(__uint_as_float(r[h]) * alph[h]);
-                            tc::tmem_st64(tmem + lane_off + kColO + 64 * c, r);
+                            for (int h = 0; h < 32; h++) r[h] = __float_as_uint(__uint_as_float(r[h]) * alph_s[h0 + h]);
+                            tc::tmem_st32(tmem + lane_off + kColO + 64 * c + h0, r);
                         }
                         tc::tmem_st_wait();
                     }
                 }
-                // P row (bf16) into the MN-major B operand, 128-byte swizzle
+                // P row (bf16) into the MN-major B operand, 128-byte swizzle:
+                // this warp writes bytes 64*half .. 64*half+63 of its rows
                 uint8_t* prow = sP + row * 128;
 #pragma unroll
-                for (int ch = 0; ch < 8; ch++) {
+                for (int ch = 0; ch < 4; ch++) {
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; e++) {
                         const int h = ch * 8 + 2 * e;
-                        const float m0 = mref[h], m1 = mref[h + 1];
-                        const float p0 = (m0 == -INFINITY) ? 0.f : exp2f(x[h] - m0);
-                        const float p1 = (m1 == -INFINITY) ? 0.f : exp2f(x[h + 1] - m1);
-                        w[e] = pack_bf16x2(p0, p1);
+                        w[e] = pack_bf16x2(ex2_approx(x[h] - mref[h]), ex2_approx(x[h + 1] - mref[h + 1]));
                         l_part[h] += __uint_as_float(w[e] << 16);
                         l_part[h + 1] += __uint_as_float(w[e] & 0xffff0000u);
                     }
-                    *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    const int chunk = 4 * half + ch;
+                    *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
                 tc::fence_proxy_async_smem();
                 tc::fence_before_sync();
@@ -574,41 +591,77 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (stop) break;
             // ---------------------------------------------------- segment epilogue
-            const int64_t slot = (int64_t)blockIdx.x - cta_of(a, qi * a.T);
-            const float2 ls = warp_reduce_scatter64<false>(l_part, lane);
-            red[sw][2 * lane] = ls.x;
-            red[sw][2 * lane + 1] = ls.y;
+            const int64_t c_first = cta_of(a, qi * a.T);
+            const bool whole = c_first == cta_of(a, (qi + 1) * a.T - 1);  // no other CTA has tiles of qi
+            red[quarter][h0 + lane] = warp_reduce_scatter32<false>(l_part, lane);
             softmax_barrier();
-            const int64_t pbase = (qi * a.S + slot) * kH;
             if (tid < kH) {
                 const float l = (red[0][tid] + red[1][tid]) + (red[2][tid] + red[3][tid]);
-                const float mr = mref[tid];
-                a.part_ml[(pbase + tid) * 2] = (mr == -INFINITY) ? -INFINITY : mr * kLn2;
-                a.part_ml[(pbase + tid) * 2 + 1] = l;
-            }
-            if (seg_tiles > 0) {
-                if (softmax_barrier_or(!warp_wait(&o_full, (tcount - 1u) & 1u, abort_flag, a.status, lane))) {
-                    stop = true;
-                    break;
+                const float mr = ref_set ? mref_s[tid] : kNoRef;
+                const float m = (mr == kNoRef || l == 0.f) ? -INFINITY : mr * kLn2;
+                if (whole) {
+                    // merge with the sink here: out = o / (l + e^(sink - m)), lse
+                    const float sk = a.sink[tid];
+                    const float ms = fmaxf(m, sk);
+                    float L = 0.f, f = 0.f;
+                    if (ms != -INFINITY) {
+                        const float em = (m == -INFINITY) ? 0.f : expf(m - ms);
+                        L = l * em + ((sk == -INFINITY) ? 0.f : expf(sk - ms));
+                        f = L > 0.f ? em / L : 0.f;
+                    }
+                    fac_s[tid] = f;
+                    if (a.lse) a.lse[qi * kH + tid] = L > 0.f ? ms + logf(L) : -INFINITY;
+                } else {
+                    const int64_t pb = (qi * a.S + ((int64_t)blockIdx.x - c_first)) * kH + tid;
+                    a.part_ml[pb * 2] = m;
+                    a.part_ml[pb * 2 + 1] = l;
                 }
-                tc::fence_after_sync();
-                for (int c = 0; c < kSlices; c++) {
-                    uint32_t r[64];
-                    tc::tmem_ld64(tmem + lane_off + kColO + 64 * c, r);
+            }
+            if (whole && a.derotate && tid < 32) {
+                float c, s;
+                rope_cs((double)inf.i, a.theta.t[tid], &c, &s);
+                rot_cs[2 * tid] = c;
+                rot_cs[2 * tid + 1] = s;
+            }
+            bool okw = true;
+            if (seg_tiles > 0) okw = warp_wait(&o_seg, (nseg++) & 1u, abort_flag, a.status, lane);
+            if (softmax_barrier_or(!okw)) { stop = true; break; }  // also publishes fac_s, rot_cs
+            tc::fence_after_sync();
+            for (int c = 0; c < 4; c++) {
+                const int d = c * 128 + row;
+                float v[32];
+                if (seg_tiles > 0) {
+                    tc::tmem_ld32(tmem + lane_off + kColO + 64 * c + h0, v);
                     tc::tmem_ld_wait();
-                    float* dst = a.part_o + pbase * kD + c * 128 + row;
+                } else {
 #pragma unroll
-                    for (int h = 0; h < kH; h++) dst[(int64_t)h * kD] = __uint_as_float(r[h]);
+                    for (int h = 0; h < 32; h++) v[h] = 0.f;
                 }
-                tc::fence_before_sync();
-            } else {
-                for (int c = 0; c < kSlices; c++) {
-                    float* dst = a.part_o + pbase * kD + c * 128 + row;
-#pragma unroll 8
-                    for (int h = 0; h < kH; h++) dst[(int64_t)h * kD] = 0.f;
+                if (whole) {
+#pragma unroll
+                    for (int h = 0; h < 32; h++) v[h] *= fac_s[h0 + h];
+                    if (a.derotate && c == 3 && row >= 128 - kRopeDims) {
+                        // RoPE at -i on dims 448..511: pairs (d, d+1) sit on adjacent lanes
+                        const int j = (row - (128 - kRopeDims)) >> 1;
+                        const float cs = rot_cs[2 * j], sn = rot_cs[2 * j + 1];
+                        const bool odd = row & 1;
+#pragma unroll
+                        for (int h = 0; h < 32; h++) {
+                            const float other = __shfl_xor_sync(0xffffffffu, v[h], 1);
+                            v[h] = odd ? (v[h] * cs - other * sn) : (v[h] * cs + other * sn);
+                        }
+                    }
+                    uint16_t* dst = a.out + (qi * kH + h0) * kD + d;
+#pragma unroll
+                    for (int h = 0; h < 32; h++) dst[(int64_t)h * kD] = f32_to_bf16_rn(v[h]);
+                } else {
+                    float* dst = a.part_o + ((qi * a.S + ((int64_t)blockIdx.x - c_first)) * kH + h0) * kD + d;
+#pragma unroll
+                    for (int h = 0; h < 32; h++) dst[(int64_t)h * kD] = v[h];
                 }
             }
-            softmax_barrier();  // red[] and mref[] are free again
+            tc::fence_before_sync();
+            softmax_barrier();  // red[], fac_s[], rot_cs[] are free again
             g = seg_end;
         }
     }
@@ -651,8 +704,9 @@ void plan_attend_tc(const Geometry& g, bool sparse, int Q, int64_t n_cap, Attend
 cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool sparse, const void* q,
                              int H, int B, int Q, const int64_t* q_pos, const void* cache,
                              int64_t n_cap, const int32_t* topk_idx, const void* window,
-                             int64_t n_win, const int64_t* win_pos0, float* part_o,
-                             float* part_ml, uint32_t* status, cudaStream_t st) {
+                             int64_t n_win, const int64_t* win_pos0, const float* sink,
+                             void* out, float* lse, float* part_o, float* part_ml,
+                             uint32_t* status, cudaStream_t st) {
     (void)H;
     if (pl.tc_total == 0) return cudaSuccess;
     CUtensorMap tm_sel, tm_win;
@@ -686,9 +740,8 @@ cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool spars
     a.W = g.W;
     a.m = g.m;
     a.qps = Q / B;
-    a.base = (double)g.base;
     a.eps = g.eps;
-    a.scale_log2 = g.scale * 1.4426950408889634f;
+    a.scale_log2 = g.scale * kLog2e;
     a.T_sel = pl.tc_T_sel;
     a.T = pl.tc_T;
     a.total = pl.tc_total;
@@ -696,7 +749,12 @@ cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool spars
     a.S = pl.splits;
     a.part_o = part_o;
     a.part_ml = part_ml;
+    a.sink = sink;
+    a.out = reinterpret_cast<uint16_t*>(out);
+    a.lse = lse;
+    a.derotate = g.derotate;
     a.status = status;
+    a.theta = rope_theta(g);
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

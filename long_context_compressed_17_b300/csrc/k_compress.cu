@@ -9,51 +9,70 @@
 // "DeepSeek-V4 技术报告深度解析" §2.1.4 "KV 缓存精度".
 //
 // Both kernels are HBM streams with a few FLOPs per byte: plain CUDA-core code,
-// coalesced row reads, one CTA per output entry.
+// coalesced row reads, one CTA per output entry; the compressor stages its
+// block of raw rows in shared memory so HBM is read once.
 #include "common.cuh"
 #include "internal.h"
 
 namespace csa {
 
-constexpr int kCompressThreads = 128;
+constexpr int kCompressThreads = 256;
+constexpr size_t kCompressStageMax = 160 * 1024;  // raw block staged in smem up to this size
 
-// grid (n_blocks_out, B); dynamic smem: (m + D + 32) floats
+// grid (n_blocks_out, B).  Dynamic smem: (m + D + 32) floats, rounded up to
+// 16 bytes, then (when `staged`) the block's m raw rows.
 __global__ void __launch_bounds__(kCompressThreads)
     compress_kernel(const uint8_t* __restrict__ kv, int act, int64_t act_row_bytes,
                     int64_t kv_seq_bytes, int D, int m, int64_t pos0,
                     const float* __restrict__ w_z, const float* __restrict__ bias,
                     uint8_t* __restrict__ out, int kvfmt, int64_t kv_row_bytes,
-                    int64_t out_seq_bytes, int R, float eps, double base) {
-    extern __shared__ float sm[];
-    float* z = sm;            // [m]
+                    int64_t out_seq_bytes, float eps, RopeTheta theta, int staged) {
+    extern __shared__ __align__(16) float sm[];
+    float* z = sm;            // [m] scores, then pooling weights
     float* row = sm + m;      // [D]
     float* red = row + D;     // [32]
+    uint8_t* stage = reinterpret_cast<uint8_t*>(sm + ((m + D + 32 + 3) & ~3));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nwarps = kCompressThreads / 32;
+    constexpr int nwarps = kCompressThreads / 32;
     const int64_t b = blockIdx.x;
     const uint8_t* blk = kv + blockIdx.y * kv_seq_bytes + b * m * act_row_bytes;
+    const uint8_t* src = blk;
+    if (staged) {  // one coalesced pass over HBM; both sweeps below read smem
+        const int64_t n16 = (int64_t)m * act_row_bytes / 16;
+        const uint4* g = reinterpret_cast<const uint4*>(blk);
+        uint4* s = reinterpret_cast<uint4*>(stage);
+        for (int64_t i = tid; i < n16; i += kCompressThreads) s[i] = __ldg(g + i);
+        __syncthreads();
+        src = stage;
+    }
 
     // pooling scores z_t = kv_t . w_z + bias[t mod m]   (pos0 is a multiple of m)
     for (int t = warp; t < m; t += nwarps) {
-        const uint8_t* r = blk + t * act_row_bytes;
+        const uint8_t* r = src + t * act_row_bytes;
         float acc = 0.f;
-        for (int d = lane; d < D; d += 32) acc = fmaf(load_act(r, act, d), w_z[d], acc);
+        for (int d = lane; d < D; d += 32) acc = fmaf(load_act(r, act, d), __ldg(w_z + d), acc);
         acc = warp_sum(acc);
         if (lane == 0) z[t] = acc + bias[t];
     }
     __syncthreads();
-    float zmax = -INFINITY;
-    for (int t = 0; t < m; t++) zmax = fmaxf(zmax, z[t]);
-    float den = 0.f;
-    for (int t = 0; t < m; t++) den += expf(z[t] - zmax);
-    const float inv_den = 1.f / den;
+    // softmax over the block's tokens: z <- alpha
+    if (warp == 0) {
+        float zmax = -INFINITY;
+        for (int t = lane; t < m; t += 32) zmax = fmaxf(zmax, z[t]);
+        zmax = warp_max(zmax);
+        float den = 0.f;
+        for (int t = lane; t < m; t += 32) den += expf(z[t] - zmax);
+        den = warp_sum(den);
+        const float inv = 1.f / den;
+        for (int t = lane; t < m; t += 32) z[t] = expf(z[t] - zmax) * inv;
+    }
+    __syncthreads();
 
     // pooled vector and its sum of squares
     float ss = 0.f;
     for (int d = tid; d < D; d += kCompressThreads) {
         float c = 0.f;
-        for (int t = 0; t < m; t++)
-            c = fmaf(expf(z[t] - zmax) * inv_den, load_act(blk + t * act_row_bytes, act, d), c);
+        for (int t = 0; t < m; t++) c = fmaf(z[t], load_act(src + t * act_row_bytes, act, d), c);
         row[d] = c;
         ss = fmaf(c, c, ss);
     }
@@ -72,10 +91,11 @@ __global__ void __launch_bounds__(kCompressThreads)
 
     // partial RoPE at the block's last position
     const double pos = (double)(pos0 + b * m + m - 1);
-    for (int j = tid; j < R / 2; j += kCompressThreads) {
+    if (tid < kRopeDims / 2) {
+        const int j = tid;
         float c, s;
-        rope_cos_sin(pos, j, R, base, &c, &s);
-        int d0 = D - R + 2 * j;
+        rope_cs(pos, theta.t[j], &c, &s);
+        int d0 = D - kRopeDims + 2 * j;
         float x0 = row[d0], x1 = row[d0 + 1];
         row[d0] = x0 * c - x1 * s;
         row[d0 + 1] = x0 * s + x1 * c;
@@ -114,7 +134,10 @@ cudaError_t launch_compress(const Geometry& g, const void* kv, int B, int64_t T,
     int64_t nb = T / g.m;
     if (nb == 0 || B == 0) return cudaSuccess;
     int64_t act_rb = row_bytes(g.act, g.D);
-    size_t smem = (size_t)(g.m + g.D + 32) * sizeof(float);
+    size_t smem = (size_t)((g.m + g.D + 32 + 3) & ~3) * sizeof(float);
+    const size_t blk_bytes = (size_t)g.m * (size_t)act_rb;
+    const int staged = blk_bytes <= kCompressStageMax ? 1 : 0;
+    if (staged) smem += blk_bytes;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(compress_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -124,7 +147,7 @@ cudaError_t launch_compress(const Geometry& g, const void* kv, int B, int64_t T,
     compress_kernel<<<grid, kCompressThreads, smem, st>>>(
         reinterpret_cast<const uint8_t*>(kv), g.act, act_rb, kv_stride * act_rb, g.D, g.m, pos0,
         w_z, bias, reinterpret_cast<uint8_t*>(out), g.kv, g.kv_row_bytes,
-        out_stride * g.kv_row_bytes, g.R, g.eps, (double)g.base);
+        out_stride * g.kv_row_bytes, g.eps, rope_theta(g), staged);
     note_launch();
     return cudaGetLastError();
 }
