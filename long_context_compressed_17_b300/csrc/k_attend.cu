@@ -199,70 +199,98 @@ __global__ void __launch_bounds__(kAttThreads) attend_generic_kernel(AttendArgs 
 }
 
 // Merge split partials, add the sink, normalise, rotate by -i and store.
-// grid (Q*H), block 128, dynamic smem D + 64 floats.  The partials of query
-// q occupy slots 0..S_q-1 of its S slots: S_q = S for the CUDA-core kernel;
-// for the tensor-core kernel (tiles > 0) S_q is the number of CTAs whose
-// balanced tile range [c*total/grid, (c+1)*total/grid) meets the query's
-// tiles [q*tiles, (q+1)*tiles).
+// Block (q, h), 128 threads, each owning 4 consecutive dims (float4 loads);
+// dynamic smem: S_alloc floats of slot weights.
+//   CUDA-core kernel (tiles == 0): grid Q*H, query q has S_alloc partials.
+//   Tensor-core kernel (tiles > 0): CTA c of `grid` owns the tiles
+//   [c*total/grid, (c+1)*total/grid) of all queries' tile lists (tiles per
+//   query); only a query cut by a CTA boundary has partials (one per CTA
+//   meeting it), every other query was finished by its only CTA.  Grid
+//   (grid-1)*H: block (b-1, h) handles the query cut by boundary b, if b is
+//   the first boundary inside it.
 __global__ void __launch_bounds__(128)
     attend_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                           int S_alloc, int H, int D, const float* __restrict__ sink,
-                          const int64_t* __restrict__ q_pos, int R, double base, int derotate,
-                          void* __restrict__ out, int act, float* __restrict__ lse, int64_t tiles,
-                          int64_t total, int grid, RopeTheta theta) {
-    extern __shared__ float row[];
-    float* cs = row + D;
-    const int tid = threadIdx.x;
-    const int64_t qh = blockIdx.x;
-    const int64_t qi = qh / H;
-    const int h = (int)(qh % H);
-    const int S = S_alloc;
-    int Sq = S_alloc;
+                          const int64_t* __restrict__ q_pos, int derotate, void* __restrict__ out,
+                          int act, float* __restrict__ lse, int64_t tiles, int64_t total, int grid,
+                          RopeTheta theta) {
+    extern __shared__ float wts[];  // [S_alloc]
+    __shared__ float cs[kRopeDims];
+    __shared__ float s_inv;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int h = (int)(blockIdx.x % H);
+    int64_t qi;
+    int Sq;
     if (tiles > 0) {
+        const int64_t b = blockIdx.x / H + 1;
+        const int64_t g = b * total / grid;  // first tile of CTA b
+        if (g % tiles == 0) return;          // the boundary falls between queries
+        qi = g / tiles;
         const int64_t c0 = ((qi * tiles + 1) * grid - 1) / total;
+        if (c0 + 1 != b) return;             // handled at the query's first boundary
         const int64_t c1 = (((qi + 1) * tiles) * grid - 1) / total;
         Sq = (int)(c1 - c0 + 1);
-        if (Sq == 1) return;  // finished (sink, normalisation, rotation) by its only CTA
+    } else {
+        qi = blockIdx.x / H;
+        Sq = S_alloc;
     }
-    const float sk = sink[h];
-    float mstar = sk;
-    for (int s = 0; s < Sq; s++) mstar = fmaxf(mstar, part_ml[((qi * S + s) * H + h) * 2]);
+    const int S = S_alloc;
     const int64_t i = q_pos[qi];
-    if (derotate)
-        for (int j = tid; j < R / 2; j += blockDim.x) rope_cs(-(double)i, theta.t[j], &cs[2 * j], &cs[2 * j + 1]);
-    float l = 0.f;
-    if (mstar != -INFINITY) {
-        l = expf(sk - mstar);
-        for (int s = 0; s < Sq; s++) {
-            const float* ml = part_ml + ((qi * S + s) * H + h) * 2;
-            if (ml[0] != -INFINITY) l += ml[1] * expf(ml[0] - mstar);
+    if (derotate && tid < kRopeDims / 2) rope_cs(-(double)i, theta.t[tid], &cs[2 * tid], &cs[2 * tid + 1]);
+    if (tid < 32) {
+        const float sk = sink[h];
+        float mstar = sk;
+        for (int s2 = lane; s2 < Sq; s2 += 32) mstar = fmaxf(mstar, part_ml[((qi * S + s2) * H + h) * 2]);
+        mstar = warp_max(mstar);
+        float l = 0.f;
+        for (int s2 = lane; s2 < Sq; s2 += 32) {
+            const float* ml = part_ml + ((qi * S + s2) * H + h) * 2;
+            const float w = (mstar == -INFINITY || ml[0] == -INFINITY) ? 0.f : expf(ml[0] - mstar);
+            wts[s2] = w;
+            l += w * ml[1];
         }
-    }
-    const float inv = (l > 0.f) ? 1.f / l : 0.f;
-    for (int d = tid; d < D; d += blockDim.x) {
-        float acc = 0.f;
-        if (l > 0.f)
-            for (int s = 0; s < Sq; s++) {
-                const float* ml = part_ml + ((qi * S + s) * H + h) * 2;
-                if (ml[0] != -INFINITY)
-                    acc = fmaf(expf(ml[0] - mstar), part_o[((qi * S + s) * H + h) * D + d], acc);
-            }
-        row[d] = acc * inv;
+        l = warp_sum(l);
+        if (mstar != -INFINITY && sk != -INFINITY) l += expf(sk - mstar);
+        if (lane == 0) {
+            s_inv = l > 0.f ? 1.f / l : 0.f;
+            if (lse) lse[qi * H + h] = l > 0.f ? mstar + logf(l) : -INFINITY;
+        }
     }
     __syncthreads();
-    if (derotate) {
-        for (int j = tid; j < R / 2; j += blockDim.x) {
-            int d0 = D - R + 2 * j;
-            float c = cs[2 * j], s = cs[2 * j + 1];
-            float x0 = row[d0], x1 = row[d0 + 1];
-            row[d0] = x0 * c - x1 * s;
-            row[d0 + 1] = x0 * s + x1 * c;
+    const float inv = s_inv;
+    for (int d4 = tid; d4 < D / 4; d4 += blockDim.x) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s2 = 0; s2 < Sq; s2++) {
+            const float w = wts[s2];
+            if (w == 0.f) continue;
+            const float4 v = __ldg(reinterpret_cast<const float4*>(part_o + ((qi * S + s2) * H + h) * D) + d4);
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
         }
-        __syncthreads();
+        float o[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+        const int d0 = 4 * d4;
+        if (derotate && d0 >= D - kRopeDims) {
+#pragma unroll
+            for (int pr = 0; pr < 2; pr++) {
+                const int j = (d0 + 2 * pr - (D - kRopeDims)) >> 1;
+                const float c = cs[2 * j], sn = cs[2 * j + 1];
+                const float x0 = o[2 * pr], x1 = o[2 * pr + 1];
+                o[2 * pr] = x0 * c - x1 * sn;
+                o[2 * pr + 1] = x0 * sn + x1 * c;
+            }
+        }
+        if (act == CSA_F32) {
+            reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (qi * H + h) * D)[d4] =
+                make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+            uint2 pk;
+            pk.x = (uint32_t)f32_to_bf16_rn(o[0]) | ((uint32_t)f32_to_bf16_rn(o[1]) << 16);
+            pk.y = (uint32_t)f32_to_bf16_rn(o[2]) | ((uint32_t)f32_to_bf16_rn(o[3]) << 16);
+            reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(out) + (qi * H + h) * D)[d4] = pk;
+        }
     }
-    uint8_t* orow = reinterpret_cast<uint8_t*>(out) + qh * D * (act == CSA_F32 ? 4 : 2);
-    for (int d = tid; d < D; d += blockDim.x) store_act(orow, act, d, row[d]);
-    if (lse && tid == 0) lse[qh] = (l > 0.f) ? mstar + logf(l) : -INFINITY;
 }
 
 cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool sparse, const void* q,
@@ -335,9 +363,11 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
         else return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
-    attend_combine_kernel<<<(unsigned)((int64_t)Q * H), 128, (g.D + 64) * sizeof(float), st>>>(
-        part_o, part_ml, pl.splits, H, g.D, sink, q_pos, g.R, (double)g.base, g.derotate, out,
-        g.act, lse, pl.use_tc ? (int64_t)pl.tc_T : 0, pl.tc_total, pl.tc_grid, rope_theta(g));
+    const int64_t blocks = pl.use_tc ? (int64_t)(pl.tc_grid - 1) * H : (int64_t)Q * H;
+    if (blocks == 0) return cudaSuccess;  // every query was finished by its only CTA
+    attend_combine_kernel<<<(unsigned)blocks, 128, (size_t)pl.splits * sizeof(float), st>>>(
+        part_o, part_ml, pl.splits, H, g.D, sink, q_pos, g.derotate, out, g.act, lse,
+        pl.use_tc ? (int64_t)pl.tc_T : 0, pl.tc_total, pl.tc_grid, rope_theta(g));
     note_launch();
     return cudaGetLastError();
 }

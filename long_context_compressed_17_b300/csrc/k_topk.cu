@@ -122,31 +122,24 @@ __device__ Select block_radix_select(const uint32_t* keys, int n, int k, int* hi
 }
 
 // Keep the top `k` of keys[0, n) in index order: calls emit(pos, i) for the
-// kept entries with pos = 0 .. k-1 ascending in i.  Each thread owns a
-// contiguous index range, so one block scan preserves the order.
+// kept entries with pos = 0 .. k-1 ascending in i.  The keys are swept in
+// block-wide rounds (thread t reads entry r + t: no bank conflicts); one scan
+// of the packed (greater, equal) counts per round places every kept entry.
 template <class Emit>
 __device__ void block_compact(const uint32_t* keys, int n, Select sel, int* sw, Emit emit) {
-    const int nt = blockDim.x;
-    const int per = (n + nt - 1) / nt;
-    const int lo = threadIdx.x * per, hi = min(n, lo + per);
-    int gt = 0, eq = 0;
-    for (int i = lo; i < hi; i++) {
-        const uint32_t u = keys[i];
-        gt += (u > sel.T);
-        eq += (u == sel.T);
-    }
-    int tot;
-    const int eq_before = block_exclusive_scan(eq, sw, &tot);
-    int take = min(max(sel.take_eq - eq_before, 0), eq);
-    int pos = block_exclusive_scan(gt + take, sw, &tot);
-    for (int i = lo; i < hi; i++) {
-        const uint32_t u = keys[i];
-        bool keep = u > sel.T;
-        if (u == sel.T && take > 0) {
-            keep = true;
-            take--;
-        }
-        if (keep) emit(pos++, i);
+    int base = 0, eq_left = sel.take_eq;
+    for (int r0 = 0; r0 < n; r0 += blockDim.x) {
+        const int i = r0 + threadIdx.x;
+        const uint32_t u = i < n ? keys[i] : 0u;
+        const int gt = (i < n && u > sel.T) ? 1 : 0;
+        const int eq = (i < n && u == sel.T) ? 1 : 0;
+        int tot;
+        const int before = block_exclusive_scan(gt | (eq << 16), sw, &tot);
+        const int gt_before = before & 0xffff, eq_before = before >> 16;
+        if (gt || (eq && eq_before < eq_left)) emit(base + gt_before + min(eq_before, eq_left), i);
+        const int eq_tot = tot >> 16;
+        base += (tot & 0xffff) + min(eq_tot, eq_left);
+        eq_left -= min(eq_tot, eq_left);
     }
 }
 
