@@ -49,19 +49,20 @@ namespace {
 
 constexpr int kD = 512;
 constexpr int kH = 64;
-constexpr int kRows = 128;                          // rows per tile (MMA M)
-constexpr int kSlices = 4;                          // 128-dim slices of a tile
-constexpr uint32_t kBoxBytes = kRows * 128;         // 128 rows x 64 dims (bf16)
-constexpr uint32_t kSliceBytes = 2 * kBoxBytes;     // 128 rows x 128 dims
+constexpr int kRows = 64;                           // rows per tile (QK MMA M)
+constexpr int kStages = 2;
+constexpr uint32_t kBoxBytes = kRows * 128;         // 64 rows x 64 dims (bf16)
+constexpr uint32_t kStageBytes = 8 * kBoxBytes;     // 64 rows x 512 dims
 constexpr uint32_t kQBoxBytes = kH * 128;           // 64 heads x 64 dims
 constexpr uint32_t kQBytes = 8 * kQBoxBytes;        // 64 heads x 512 dims
-constexpr uint32_t kPBytes = kRows * kH * 2;        // 128 rows x 64 heads
-constexpr size_t kSmem = 1024 + kSlices * kSliceBytes + kQBytes + kPBytes;
-constexpr int kSoftWarps = 8;                       // 4 TMEM lane quarters x 2 head halves
+constexpr uint32_t kPBytes = kRows * kH * 2;        // 64 rows x 64 heads
+constexpr size_t kSmem = 1024 + kStages * kStageBytes + kQBytes + 2 * kPBytes;
+constexpr int kSoftWarps = 16;                      // 4 TMEM lane quarters x 4 head quarters
 constexpr int kSoftThreads = kSoftWarps * 32;
 constexpr int kThreads = 64 + kSoftThreads;
+constexpr int kHW = kH / 4;                         // heads per softmax warp
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;    // S^T: 64 columns
+constexpr uint32_t kColS = 0;    // S^T buffers: 2 x 64 columns
 constexpr uint32_t kColO = 256;  // O^T: 4 x 64 columns
 constexpr float kRescaleLog2 = 8.f;
 constexpr float kNoRef = -1e30f; // running reference before any valid logit
@@ -133,20 +134,14 @@ __device__ __forceinline__ int last_live(const AttTcArgs& a, const QueryInfo& qi
 }
 
 // -------------------------------------------------------------- softmax helpers
-// Reduce 32 per-lane values over the warp so that lane l ends with the
-// reduction of entry l over all 32 lanes (a reduce-scatter, 31 shuffles).
+// Reduce 16 per-lane values over the warp so that lanes l and l+16 end with
+// the reduction of entry (l % 16) over all 32 lanes (31 shuffles).
 template <bool kMax>
-__device__ __forceinline__ float warp_reduce_scatter32(const float (&v)[32], int lane) {
+__device__ __forceinline__ float warp_reduce_scatter16(const float (&v)[16], int lane) {
     auto op = [](float x, float y) { return kMax ? fmaxf(x, y) : x + y; };
     float a[16], b[8], c[4], d[2];
-    {
-        const bool up = lane & 16;
 #pragma unroll
-        for (int j = 0; j < 16; j++) {
-            float keep = up ? v[j + 16] : v[j], send = up ? v[j] : v[j + 16];
-            a[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
-        }
-    }
+    for (int j = 0; j < 16; j++) a[j] = op(v[j], __shfl_xor_sync(0xffffffffu, v[j], 16));
     {
         const bool up = lane & 8;
 #pragma unroll
@@ -217,12 +212,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_win, const __grid_constant__ AttTcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sE = sm;                              // kSlices x (2 boxes of 128 rows x 64 dims)
-    uint8_t* sQ = sE + kSlices * kSliceBytes;      // 8 boxes of 64 heads x 64 dims
-    uint8_t* sP = sQ + kQBytes;                    // 128 rows x 64 heads
+    uint8_t* sE = sm;                              // kStages x (8 boxes of 64 rows x 64 dims)
+    uint8_t* sQ = sE + kStages * kStageBytes;      // 8 boxes of 64 heads x 64 dims
+    uint8_t* sP = sQ + kQBytes;                    // 2 x (64 rows x 64 heads)
 
-    __shared__ __align__(8) uint64_t full[kSlices], empty[kSlices];
-    __shared__ __align__(8) uint64_t s_full, p_full, o_seg, q_full, mma_done;
+    __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
+    __shared__ __align__(8) uint64_t s_full[2], p_full[2];
+    __shared__ __align__(8) uint64_t o_full, o_seg, q_full, mma_done;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_sh;
     __shared__ float red[4][kH];
@@ -232,12 +228,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kSlices; s++) {
+        for (int s = 0; s < kStages; s++) {
             tc::mbar_init(&full[s], 1);
             tc::mbar_init(&empty[s], 1);
         }
-        tc::mbar_init(&s_full, 1);
-        tc::mbar_init(&p_full, kSoftWarps);
+        for (int b = 0; b < 2; b++) {
+            tc::mbar_init(&s_full[b], 1);
+            tc::mbar_init(&p_full[b], kSoftWarps);
+        }
+        tc::mbar_init(&o_full, 1);  // after every PV product
         tc::mbar_init(&o_seg, 1);   // after the last PV product of a segment
         tc::mbar_init(&q_full, 1);
         tc::mbar_init(&mma_done, 1);
@@ -264,116 +263,167 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (a.W > 0) tc::tma_prefetch_map(&tm_win);
         }
         uint32_t tcount = 0;
-        uint32_t fills[kSlices] = {0, 0, 0, 0};  // loads issued into each slice
-        bool stop = false;
-        for (int64_t g = g_begin; g < g_end && !stop;) {
-            const int64_t qi = g / a.T;
-            const int64_t seg_end = min(g_end, (qi + 1) * a.T);
-            const QueryInfo inf = query_info(a, qi);
-            for (int lt = (int)(g - qi * a.T); lt < (int)(seg_end - qi * a.T) && !stop; ++lt) {
-                if (!tile_live(a, inf, lt)) continue;
-                const bool gather = lt < a.T_sel && a.topk_idx != nullptr;
-                int rows[4] = {0, 0, 0, 0};  // gathered rows of this lane: 4*lane .. 4*lane+3
-                int row0 = 0;
-                const CUtensorMap* map = &tm_sel;
-                if (gather) {
+        uint32_t fills[kStages] = {0, 0};  // loads issued into each stage
+        // rows lane l gathers for tile lt of query qi: 4*(l%16) .. +3
+        auto gather_rows = [&](int64_t qi, const QueryInfo& inf, int lt, int (&rows)[4]) {
 #pragma unroll
-                    for (int j = 0; j < 4; j++) {
-                        const int p = lt * kRows + 4 * lane + j;
-                        int64_t e = p < a.k ? (int64_t)a.topk_idx[qi * a.k + p] : -1;
-                        if (e < 0 || e >= inf.n_av) e = 0;  // masked by the softmax warps
-                        rows[j] = (int)((int64_t)inf.seq * a.n_cap + e);
-                    }
-                } else if (lt < a.T_sel) {
-                    row0 = lt * kRows;
-                } else {
-                    map = &tm_win;
-                    row0 = (int)(inf.i - a.W + 1 + (int64_t)(lt - a.T_sel) * kRows - a.win_pos0[inf.seq]);
-                }
-                for (int c = 0; c < kSlices; c++) {
-                    if (!warp_wait(&empty[c], (tcount & 1u) ^ 1u, abort_flag, a.status, lane)) {
-                        stop = true;
-                        break;
-                    }
-                    uint8_t* dst = sE + c * kSliceBytes;
-                    if (lane == 0) tc::mbar_arrive_expect_tx(&full[c], kSliceBytes);
-                    __syncwarp();
-                    if (gather) {
-#pragma unroll
-                        for (int b = 0; b < 2; b++)
-                            tc::tma_gather4(dst + b * kBoxBytes + lane * 512, &tm_sel, &full[c],
-                                            c * 128 + b * 64, rows[0], rows[1], rows[2], rows[3]);
-                    } else if (lane < 2) {
-                        tc::tma_load_3d(dst + lane * kBoxBytes, map, &full[c], c * 128 + lane * 64, row0, inf.seq);
-                    }
-                    ++fills[c];
-                }
-                ++tcount;
+            for (int j = 0; j < 4; j++) {
+                const int p = lt * kRows + 4 * (lane & 15) + j;
+                int64_t e = p < a.k ? (int64_t)a.topk_idx[qi * a.k + p] : -1;
+                if (e < 0 || e >= inf.n_av) e = 0;  // masked by the softmax warps
+                rows[j] = (int)((int64_t)inf.seq * a.n_cap + e);
             }
-            g = seg_end;
+        };
+        auto box_row0 = [&](const QueryInfo& inf, int lt) {
+            return lt < a.T_sel ? lt * kRows
+                                : (int)(inf.i - a.W + 1 + (int64_t)(lt - a.T_sel) * kRows - a.win_pos0[inf.seq]);
+        };
+        // The next live TMA-tile (not gathered) after global tile g within this
+        // CTA's range is prefetched into L2 while the current one is loaded.
+        auto prefetch_after = [&](int64_t g) {
+            for (++g; g < g_end; ++g) {
+                const int64_t qi = g / a.T;
+                const int lt = (int)(g - qi * a.T);
+                const QueryInfo inf = query_info(a, qi);
+                if (!tile_live(a, inf, lt)) continue;
+                if (!(lt < a.T_sel && a.topk_idx != nullptr) && lane < 8) {
+                    const int r0 = box_row0(inf, lt);
+                    if (r0 >= 0)  // a window box that starts before row 0 is not prefetched
+                        tc::tma_prefetch_3d(lt < a.T_sel ? &tm_sel : &tm_win, lane * 64, r0, inf.seq);
+                }
+                return;
+            }
+        };
+        for (int64_t g = g_begin; g < g_end; ++g) {
+            const int64_t qi = g / a.T;
+            const int lt = (int)(g - qi * a.T);
+            const QueryInfo inf = query_info(a, qi);
+            if (!tile_live(a, inf, lt)) continue;
+            prefetch_after(g);
+            const int st = tcount & 1;
+            if (!warp_wait(&empty[st], ((tcount >> 1) & 1u) ^ 1u, abort_flag, a.status, lane)) break;
+            uint8_t* dst = sE + st * kStageBytes;
+            if (lane == 0) tc::mbar_arrive_expect_tx(&full[st], kStageBytes);
+            __syncwarp();
+            if (lt < a.T_sel && a.topk_idx != nullptr) {
+                int rows[4];
+                gather_rows(qi, inf, lt, rows);
+#pragma unroll
+                for (int bb = 0; bb < 4; bb++) {
+                    const int box = (lane >> 4) * 4 + bb;
+                    tc::tma_gather4(dst + box * kBoxBytes + (lane & 15) * 512, &tm_sel, &full[st], box * 64,
+                                    rows[0], rows[1], rows[2], rows[3]);
+                }
+            } else if (lane < 8) {
+                tc::tma_load_3d(dst + lane * kBoxBytes, lt < a.T_sel ? &tm_sel : &tm_win, &full[st], lane * 64,
+                                box_row0(inf, lt), inf.seq);
+            }
+            ++fills[st];
+            ++tcount;
         }
-        // Leave no copy in flight: the newest load of every slice must have
-        // landed (at most one phase of a slice is ever outstanding).
+        // Leave no copy in flight: the newest load of every stage must have
+        // landed (at most one phase of a stage is ever outstanding).
         if (lane == 0) {
-            for (int c = 0; c < kSlices; c++) {
-                if (fills[c] == 0) continue;
-                if (!tc::mbar_drain(&full[c], (fills[c] - 1u) & 1u)) atomicOr(a.status, CSA_DEV_TIMEOUT);
+            for (int st = 0; st < kStages; st++) {
+                if (fills[st] == 0) continue;
+                if (!tc::mbar_drain(&full[st], (fills[st] - 1u) & 1u)) atomicOr(a.status, CSA_DEV_TIMEOUT);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
+        // Issue order is dynamic: the PV product of tile t as soon as its P is
+        // written, the QK product of tile t+1 as soon as its stage has landed
+        // and the S^T buffer it reuses is free (PV of tile t-1 issued).
         if (lane == 0) {
             constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kRows, kH, 0, 0);
             constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, kH, 1, 1);
             const uint32_t sE0 = tc::smem_u32(sE), sQ0 = tc::smem_u32(sQ), sP0 = tc::smem_u32(sP);
-            uint32_t tcount = 0, nq = 0;
-            bool stop = false;
-            for (int64_t g = g_begin; g < g_end && !stop;) {
-                const int64_t qi = g / a.T;
-                const int64_t seg_end = min(g_end, (qi + 1) * a.T);
-                const QueryInfo inf = query_info(a, qi);
-                const int lt_last = last_live(a, inf, (int)(g - qi * a.T), (int)(seg_end - qi * a.T));
-                bool first = true;
-                for (int lt = (int)(g - qi * a.T); lt <= lt_last; ++lt) {
-                    if (!tile_live(a, inf, lt)) continue;
-                    if (first) {
-                        if (!tc::mbar_wait(&q_full, nq & 1u, abort_flag, a.status)) { stop = true; break; }
-                        ++nq;
+            uint32_t t_qk = 0, t_pv = 0, nq = 0;
+            bool first_of[4], last_of[4];  // segment flags of tiles t_pv .. t_qk-1 (at most 2)
+            // QK cursor over this CTA's live tiles
+            int64_t g = g_begin;
+            int64_t cur_q = -1;
+            QueryInfo inf{};
+            int lt_last = -1;
+            bool at_seg_start = true;
+            auto advance = [&]() -> bool {  // move g to the next live tile; false at the end
+                for (; g < g_end; ++g) {
+                    const int64_t qi = g / a.T;
+                    if (qi != cur_q) {
+                        cur_q = qi;
+                        inf = query_info(a, qi);
+                        const int64_t seg_end = min(g_end, (qi + 1) * a.T);
+                        lt_last = last_live(a, inf, (int)(g - qi * a.T), (int)(seg_end - qi * a.T));
+                        at_seg_start = true;
                     }
-                    // S^T = E . Q'^T over the 512 dims, slice by slice as they land
-                    for (int c = 0; c < kSlices && !stop; c++) {
-                        if (!tc::mbar_wait(&full[c], tcount & 1u, abort_flag, a.status)) { stop = true; break; }
-                        tc::fence_after_sync();
-                        const uint32_t slice = sE0 + c * kSliceBytes;
-#pragma unroll
-                        for (int j = 0; j < 8; j++) {
-                            const int kg = 8 * c + j;
-                            const uint64_t ad = tc::sdesc_sw128(slice + (j >> 2) * kBoxBytes + (j & 3) * 32, 16, 1024);
-                            const uint64_t bd = tc::sdesc_sw128(sQ0 + (kg >> 2) * kQBoxBytes + (kg & 3) * 32, 16, 1024);
-                            tc::mma_bf16_ss(tmem + kColS, ad, bd, idesc_qk, kg != 0 ? 1u : 0u);
-                        }
-                    }
-                    if (stop) break;
-                    tc::mma_commit(&s_full);
-                    if (!tc::mbar_wait(&p_full, tcount & 1u, abort_flag, a.status)) { stop = true; break; }
-                    tc::fence_after_sync();
-                    // O^T += E^T . P^T, one 128-dim slice at a time; each slice is
-                    // released for the next tile as soon as its products are done
-                    for (int c = 0; c < kSlices; c++) {
-                        const uint32_t slice = sE0 + c * kSliceBytes;
-#pragma unroll
-                        for (int kk = 0; kk < kRows / 16; kk++) {
-                            const uint64_t ad = tc::sdesc_sw128(slice + kk * 2048, kBoxBytes, 1024);
-                            const uint64_t bd = tc::sdesc_sw128(sP0 + kk * 2048, kBoxBytes, 1024);
-                            tc::mma_bf16_ss(tmem + kColO + 64 * c, ad, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
-                        }
-                        tc::mma_commit(&empty[c]);
-                    }
-                    if (lt == lt_last) tc::mma_commit(&o_seg);
-                    first = false;
-                    ++tcount;
+                    if (tile_live(a, inf, (int)(g - qi * a.T))) return true;
                 }
-                g = seg_end;
+                return false;
+            };
+            bool more = advance();
+            uint64_t idle_since = 0;
+            while (more || t_pv < t_qk) {
+                bool progress = false;
+                if (t_pv < t_qk) {
+                    const int b = t_pv & 1;
+                    if (tc::mbar_try_wait(&p_full[b], (t_pv >> 1) & 1u)) {
+                        tc::fence_after_sync();
+                        const uint32_t stage = sE0 + b * kStageBytes;
+                        const uint32_t pb = sP0 + b * kPBytes;
+                        const bool first = first_of[t_pv & 3];
+#pragma unroll
+                        for (int c = 0; c < 4; c++) {
+#pragma unroll
+                            for (int kk = 0; kk < kRows / 16; kk++) {
+                                const uint64_t ad = tc::sdesc_sw128(stage + 2 * c * kBoxBytes + kk * 2048, kBoxBytes, 1024);
+                                const uint64_t bd = tc::sdesc_sw128(pb + kk * 2048, kBoxBytes, 1024);
+                                tc::mma_bf16_ss(tmem + kColO + 64 * c, ad, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
+                            }
+                        }
+                        tc::mma_commit(&empty[b]);
+                        tc::mma_commit(&o_full);
+                        if (last_of[t_pv & 3]) tc::mma_commit(&o_seg);
+                        ++t_pv;
+                        progress = true;
+                    }
+                }
+                if (more && t_pv + 1 >= t_qk) {  // S^T buffer of tile t_qk is free
+                    const int b = t_qk & 1;
+                    bool ready = !at_seg_start || tc::mbar_try_wait(&q_full, nq & 1u);
+                    if (ready) ready = tc::mbar_try_wait(&full[b], (t_qk >> 1) & 1u);
+                    if (ready) {
+                        tc::fence_after_sync();
+                        const uint32_t stage = sE0 + b * kStageBytes;
+#pragma unroll 8
+                        for (int kg = 0; kg < kD / 16; kg++) {
+                            const uint64_t ad = tc::sdesc_sw128(stage + (kg >> 2) * kBoxBytes + (kg & 3) * 32, 16, 1024);
+                            const uint64_t bd = tc::sdesc_sw128(sQ0 + (kg >> 2) * kQBoxBytes + (kg & 3) * 32, 16, 1024);
+                            tc::mma_bf16_ss(tmem + kColS + 64 * b, ad, bd, idesc_qk, kg != 0 ? 1u : 0u);
+                        }
+                        tc::mma_commit(&s_full[b]);
+                        if (at_seg_start) ++nq;
+                        first_of[t_qk & 3] = at_seg_start;
+                        last_of[t_qk & 3] = (int)(g - cur_q * a.T) == lt_last;
+                        at_seg_start = false;
+                        ++t_qk;
+                        ++g;
+                        more = advance();
+                        progress = true;
+                    }
+                }
+                if (progress) {
+                    idle_since = 0;
+                } else {
+                    if (*abort_flag) break;
+                    const uint64_t now = tc::globaltimer_ns();
+                    if (idle_since == 0) {
+                        idle_since = now;
+                    } else if (now - idle_since > tc::kWaitLimitNs) {
+                        atomicOr(a.status, CSA_DEV_TIMEOUT);
+                        *abort_flag = 1;
+                        break;
+                    }
+                }
             }
             // every MMA issued so far must be complete before TMEM is freed
             tc::mma_commit(&mma_done);
@@ -381,14 +431,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
-        // Warp w owns TMEM lane quarter (w % 4) -- 32 tile rows, or 32 dims of
-        // every O^T slice -- and the 32 heads of half (w - 2) / 4.
-        const int sw = warp - 2;                 // 0..7
-        const int tid = threadIdx.x - 64;        // 0..255
+        // Warp w owns TMEM lane quarter (w % 4) and the 16 heads of head quarter
+        // (w - 2) / 4.  S^T rows (M = 64) sit in lanes 0..15 of each quarter:
+        // row = 16 * quarter + lane.  O^T rows (dims, M = 128) fill all lanes.
+        const int sw = warp - 2;                 // 0..15
+        const int tid = threadIdx.x - 64;        // 0..511
         const int quarter = warp & 3;
-        const int half = sw >> 2;
-        const int h0 = half * 32;
-        const int row = quarter * 32 + lane;     // tile row / dim within an O^T slice
+        const int h0 = (sw >> 2) * kHW;
+        const bool row_lane = lane < 16;
+        const int row = quarter * 16 + (lane & 15);  // tile row of this lane (lanes 0..15)
+        const int dim = quarter * 32 + lane;         // O^T lane: dim within a 128-dim slice
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
 
         // q' = RoPE(RMSNorm(q), i) of query qi into sQ (bf16, 128-byte swizzle)
@@ -466,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint32_t tcount = 0, nseg = 0;
         bool stop = false;
-        float l_part[32], mref[32];
+        float l_part[kHW], mref[kHW];
         for (int64_t g = g_begin; g < g_end && !stop;) {
             const int64_t qi = g / a.T;
             const int64_t seg_end = min(g_end, (qi + 1) * a.T);
@@ -475,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int lt_last = last_live(a, inf, lt0, lt1);
             if (tid == 0 && (inf.i + 1) / a.m > a.n_cap) atomicOr(a.status, CSA_DEV_BAD_POSITION);
 #pragma unroll
-            for (int h = 0; h < 32; h++) {
+            for (int h = 0; h < kHW; h++) {
                 l_part[h] = 0.f;
                 mref[h] = kNoRef;
             }
@@ -483,40 +535,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ref_set = false;  // mref_s holds this segment's reference
             for (int lt = lt0; lt <= lt_last; ++lt) {
                 if (!tile_live(a, inf, lt)) continue;
+                const int b = tcount & 1;
                 // row validity (and the device-side checks of the row list)
                 bool valid = false;
-                if (lt < a.T_sel) {
-                    const int p = lt * kRows + row;
-                    if (a.topk_idx) {
-                        if (p < a.k) {
-                            const int64_t e = a.topk_idx[qi * a.k + p];
-                            if (e >= 0) {
-                                if (e < inf.n_av) valid = true;
-                                else if (half == 0) atomicOr(a.status, CSA_DEV_BAD_TOPK_INDEX);
+                const bool report = row_lane && sw < 4;
+                if (row_lane) {
+                    if (lt < a.T_sel) {
+                        const int p = lt * kRows + row;
+                        if (a.topk_idx) {
+                            if (p < a.k) {
+                                const int64_t e = a.topk_idx[qi * a.k + p];
+                                if (e >= 0) {
+                                    if (e < inf.n_av) valid = true;
+                                    else if (report) atomicOr(a.status, CSA_DEV_BAD_TOPK_INDEX);
+                                }
                             }
+                        } else {
+                            valid = p < inf.n_av;
                         }
                     } else {
-                        valid = p < inf.n_av;
-                    }
-                } else {
-                    const int r = (lt - a.T_sel) * kRows + row;
-                    const int64_t wpos = inf.i - a.W + 1 + r;
-                    if (r < a.W && wpos >= 0) {
-                        const int64_t wr = wpos - a.win_pos0[inf.seq];
-                        if (wr >= 0 && wr < a.n_win) valid = true;
-                        else if (half == 0) atomicOr(a.status, CSA_DEV_BAD_WINDOW);
+                        const int r = (lt - a.T_sel) * kRows + row;
+                        const int64_t wpos = inf.i - a.W + 1 + r;
+                        if (r < a.W && wpos >= 0) {
+                            const int64_t wr = wpos - a.win_pos0[inf.seq];
+                            if (wr >= 0 && wr < a.n_win) valid = true;
+                            else if (report) atomicOr(a.status, CSA_DEV_BAD_WINDOW);
+                        }
                     }
                 }
                 const float mask = valid ? 0.f : -INFINITY;  // x = s * scale + mask
-                const bool ok = warp_wait(&s_full, tcount & 1u, abort_flag, a.status, lane);
-                float x[32];
+                const bool ok = warp_wait(&s_full[b], (tcount >> 1) & 1u, abort_flag, a.status, lane);
+                float x[kHW];
                 bool need = false;
                 if (ok) {
                     tc::fence_after_sync();
-                    tc::tmem_ld32(tmem + lane_off + kColS + h0, x);
+                    tc::tmem_ld16(tmem + lane_off + kColS + 64 * b + h0, x);
                     tc::tmem_ld_wait();
 #pragma unroll
-                    for (int h = 0; h < 32; h++) {
+                    for (int h = 0; h < kHW; h++) {
                         x[h] = fmaf(x[h], a.scale_log2, mask);
                         need |= x[h] > mref[h] + kRescaleLog2;
                     }
@@ -526,7 +582,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (softmax_barrier_or(!ok || need)) {
                     if (softmax_barrier_or(!ok)) { stop = true; break; }
                     // tile maximum per head (over this quarter's rows), then over quarters
-                    red[quarter][h0 + lane] = warp_reduce_scatter32<true>(x, lane);
+                    const float mx = warp_reduce_scatter16<true>(x, lane);
+                    if (row_lane) red[quarter][h0 + lane] = mx;
                     softmax_barrier();
                     bool mine = false;
                     if (tid < kH) {
@@ -544,43 +601,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool resc = softmax_barrier_or(mine);
                     ref_set = true;
 #pragma unroll
-                    for (int h = 0; h < 32; h++) mref[h] = mref_s[h0 + h];
+                    for (int h = 0; h < kHW; h++) mref[h] = mref_s[h0 + h];
                     if (resc) {
-                        // O^T holds this segment's earlier tiles (their PV products are
-                        // complete: they were issued before this tile's QK product)
 #pragma unroll
-                        for (int h = 0; h < 32; h++) l_part[h] *= alph_s[h0 + h];
-                        for (int c = 0; c < kSlices; c++) {
-                            uint32_t r[32];
-                            tc::tmem_ld32(tmem + lane_off + kColO + 64 * c + h0, *reinterpret_cast<float(*)[32]>(r));
+                        for (int h = 0; h < kHW; h++) l_part[h] *= alph_s[h0 + h];
+                        // O^T holds this segment's earlier tiles: once the previous
+                        // PV product is done, rescale this warp's block of it
+                        const bool okr = warp_wait(&o_full, (tcount - 1u) & 1u, abort_flag, a.status, lane);
+                        if (softmax_barrier_or(!okr)) { stop = true; break; }
+                        tc::fence_after_sync();
+                        for (int c = 0; c < 4; c++) {
+                            float r[kHW];
+                            tc::tmem_ld16(tmem + lane_off + kColO + 64 * c + h0, r);
                             tc::tmem_ld_wait();
 #pragma unroll
-                            for (int h = 0; h < 32; h++) r[h] = __float_as_uint(__uint_as_float(r[h]) * alph_s[h0 + h]);
-                            tc::tmem_st32(tmem + lane_off + kColO + 64 * c + h0, r);
+                            for (int h = 0; h < kHW; h++) r[h] *= alph_s[h0 + h];
+                            tc::tmem_st16(tmem + lane_off + kColO + 64 * c + h0, r);
                         }
                         tc::tmem_st_wait();
                     }
                 }
                 // P row (bf16) into the MN-major B operand, 128-byte swizzle:
-                // this warp writes bytes 64*half .. 64*half+63 of its rows
-                uint8_t* prow = sP + row * 128;
+                // this warp writes bytes 32*(w-2)/4 .. +31 of its rows
+                if (row_lane) {
+                    uint8_t* prow = sP + b * kPBytes + row * 128;
 #pragma unroll
-                for (int ch = 0; ch < 4; ch++) {
-                    uint32_t w[4];
+                    for (int ch = 0; ch < 2; ch++) {
+                        uint32_t w[4];
 #pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        const int h = ch * 8 + 2 * e;
-                        w[e] = pack_bf16x2(ex2_approx(x[h] - mref[h]), ex2_approx(x[h + 1] - mref[h + 1]));
-                        l_part[h] += __uint_as_float(w[e] << 16);
-                        l_part[h + 1] += __uint_as_float(w[e] & 0xffff0000u);
+                        for (int e = 0; e < 4; e++) {
+                            const int h = ch * 8 + 2 * e;
+                            w[e] = pack_bf16x2(ex2_approx(x[h] - mref[h]), ex2_approx(x[h + 1] - mref[h + 1]));
+                            l_part[h] += __uint_as_float(w[e] << 16);
+                            l_part[h + 1] += __uint_as_float(w[e] & 0xffff0000u);
+                        }
+                        const int chunk = 2 * (sw >> 2) + ch;
+                        *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
                     }
-                    const int chunk = 4 * half + ch;
-                    *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
                 tc::fence_proxy_async_smem();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&p_full);
+                if (lane == 0) tc::mbar_arrive(&p_full[b]);
                 ++seg_tiles;
                 ++tcount;
                 if (lt == lt_last) {
@@ -593,7 +655,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---------------------------------------------------- segment epilogue
             const int64_t c_first = cta_of(a, qi * a.T);
             const bool whole = c_first == cta_of(a, (qi + 1) * a.T - 1);  // no other CTA has tiles of qi
-            red[quarter][h0 + lane] = warp_reduce_scatter32<false>(l_part, lane);
+            {
+                const float ls = warp_reduce_scatter16<false>(l_part, lane);
+                if (row_lane) red[quarter][h0 + lane] = ls;
+            }
             softmax_barrier();
             if (tid < kH) {
                 const float l = (red[0][tid] + red[1][tid]) + (red[2][tid] + red[3][tid]);
@@ -628,36 +693,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (softmax_barrier_or(!okw)) { stop = true; break; }  // also publishes fac_s, rot_cs
             tc::fence_after_sync();
             for (int c = 0; c < 4; c++) {
-                const int d = c * 128 + row;
-                float v[32];
+                const int d = c * 128 + dim;
+                float v[kHW];
                 if (seg_tiles > 0) {
-                    tc::tmem_ld32(tmem + lane_off + kColO + 64 * c + h0, v);
+                    tc::tmem_ld16(tmem + lane_off + kColO + 64 * c + h0, v);
                     tc::tmem_ld_wait();
                 } else {
 #pragma unroll
-                    for (int h = 0; h < 32; h++) v[h] = 0.f;
+                    for (int h = 0; h < kHW; h++) v[h] = 0.f;
                 }
                 if (whole) {
 #pragma unroll
-                    for (int h = 0; h < 32; h++) v[h] *= fac_s[h0 + h];
-                    if (a.derotate && c == 3 && row >= 128 - kRopeDims) {
+                    for (int h = 0; h < kHW; h++) v[h] *= fac_s[h0 + h];
+                    if (a.derotate && c == 3 && dim >= 128 - kRopeDims) {  // uniform per warp
                         // RoPE at -i on dims 448..511: pairs (d, d+1) sit on adjacent lanes
-                        const int j = (row - (128 - kRopeDims)) >> 1;
+                        const int j = (dim - (128 - kRopeDims)) >> 1;
                         const float cs = rot_cs[2 * j], sn = rot_cs[2 * j + 1];
-                        const bool odd = row & 1;
+                        const bool odd = dim & 1;
 #pragma unroll
-                        for (int h = 0; h < 32; h++) {
+                        for (int h = 0; h < kHW; h++) {
                             const float other = __shfl_xor_sync(0xffffffffu, v[h], 1);
                             v[h] = odd ? (v[h] * cs - other * sn) : (v[h] * cs + other * sn);
                         }
                     }
                     uint16_t* dst = a.out + (qi * kH + h0) * kD + d;
 #pragma unroll
-                    for (int h = 0; h < 32; h++) dst[(int64_t)h * kD] = f32_to_bf16_rn(v[h]);
+                    for (int h = 0; h < kHW; h++) dst[(int64_t)h * kD] = f32_to_bf16_rn(v[h]);
                 } else {
                     float* dst = a.part_o + ((qi * a.S + ((int64_t)blockIdx.x - c_first)) * kH + h0) * kD + d;
 #pragma unroll
-                    for (int h = 0; h < 32; h++) dst[(int64_t)h * kD] = v[h];
+                    for (int h = 0; h < kHW; h++) dst[(int64_t)h * kD] = v[h];
                 }
             }
             tc::fence_before_sync();
@@ -678,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ host side
 bool attend_tc_supported(const Geometry& g, bool sparse, int H, int64_t n_cap, int64_t n_win) {
     if (g.act != CSA_BF16 || g.kv != CSA_BF16 || g.D != kD || g.R != 64 || H != kH) return false;
-    if (!sparse && n_cap < kRows) return false;     // tile boxes of 128 rows
+    if (!sparse && n_cap < kRows) return false;     // tile boxes of 64 rows
     if (sparse && (n_cap < 1 || g.k < 1)) return false;
     if (g.W > 0 && n_win < kRows) return false;
     return true;
