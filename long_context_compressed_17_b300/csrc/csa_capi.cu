@@ -91,7 +91,7 @@ AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int6
     AttendPlan pl;
     pl.list_len = (sparse ? (int64_t)g.k : n_cap) + g.W;
     pl.use_tc = attend_tc_supported(g, sparse, H, n_cap, n_win) ? 1 : 0;
-    pl.tc_T_sel = pl.tc_T = pl.tc_grid = 0;
+    pl.tc_T_sel = pl.tc_T = pl.tc_grid = pl.tc_deq = 0;
     pl.tc_total = 0;
     if (pl.use_tc) {
         pl.head_group = H;
@@ -114,7 +114,16 @@ AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int6
     size_t o_bytes = align256((size_t)Q * pl.splits * H * g.D * sizeof(float));
     pl.part_ml_off = pl.part_o_off + o_bytes;
     size_t ml_bytes = align256((size_t)Q * pl.splits * H * 2 * sizeof(float));
-    pl.total = pl.part_ml_off + ml_bytes;
+    pl.deq_off = pl.part_ml_off + ml_bytes;
+    size_t deq_bytes = 0;
+    if (pl.use_tc && g.kv == CSA_FP8_MIXED) {
+        // dequantise whichever is fewer rows: the ones the queries read or all
+        const size_t per_query = (size_t)Q * pl.tc_T * 64;
+        const size_t stored = (size_t)B * (size_t)(n_cap + (g.W > 0 ? n_win : 0));
+        pl.tc_deq = per_query <= stored ? 1 : 2;
+        deq_bytes = align256((pl.tc_deq == 1 ? per_query : stored) * g.D * 2);
+    }
+    pl.total = pl.deq_off + deq_bytes;
     return pl;
 }
 

@@ -45,11 +45,17 @@ struct AttendPlan {
     int64_t rows_per_split;
     int head_group;       // heads per CTA
     int use_tc;           // tensor-core kernel
-    // tensor-core kernel: tiles of 128 rows per query (selected / cache part
+    // tensor-core kernel: tiles of 64 rows per query (selected / cache part
     // and all), Q * tc_T tiles dealt to tc_grid persistent CTAs
     int tc_T_sel, tc_T, tc_grid;
     int64_t tc_total;
+    // FP8 rows reach the tensor-core kernel dequantised to bf16 in the
+    // workspace: 1 = the rows each query reads, [Q, tc_T * 64, D] in tile
+    // order; 2 = every stored row, [B, n_cap, D] then [B, n_win, D]; 0 = the
+    // stored rows are bf16 already
+    int tc_deq;
     size_t part_o_off, part_ml_off;  // [Q, S, H, D] and [Q, S, H, 2] float32
+    size_t deq_off;                  // bf16 rows of tc_deq
     size_t total;
 };
 AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int64_t n_cap,

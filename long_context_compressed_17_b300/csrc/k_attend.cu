@@ -205,15 +205,16 @@ __global__ void __launch_bounds__(kAttThreads) attend_generic_kernel(AttendArgs 
 //   Tensor-core kernel (tiles > 0): CTA c of `grid` owns the tiles
 //   [c*total/grid, (c+1)*total/grid) of all queries' tile lists (tiles per
 //   query); only a query cut by a CTA boundary has partials (one per CTA
-//   meeting it), every other query was finished by its only CTA.  Grid
-//   (grid-1)*H: block (b-1, h) handles the query cut by boundary b, if b is
-//   the first boundary inside it.
+//   meeting it), every other query was finished by its only CTA.  With
+//   by_query the grid is Q*H and block (q, h) takes query q if it was cut;
+//   otherwise the grid is (grid-1)*H and block (b-1, h) handles the query cut
+//   by boundary b, if b is the first boundary inside it.
 __global__ void __launch_bounds__(128)
     attend_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                           int S_alloc, int H, int D, const float* __restrict__ sink,
                           const int64_t* __restrict__ q_pos, int derotate, void* __restrict__ out,
                           int act, float* __restrict__ lse, int64_t tiles, int64_t total, int grid,
-                          RopeTheta theta) {
+                          int by_query, RopeTheta theta) {
     extern __shared__ float wts[];  // [S_alloc]
     __shared__ float cs[kRopeDims];
     __shared__ float s_inv;
@@ -222,13 +223,21 @@ __global__ void __launch_bounds__(128)
     int64_t qi;
     int Sq;
     if (tiles > 0) {
-        const int64_t b = blockIdx.x / H + 1;
-        const int64_t g = b * total / grid;  // first tile of CTA b
-        if (g % tiles == 0) return;          // the boundary falls between queries
-        qi = g / tiles;
-        const int64_t c0 = ((qi * tiles + 1) * grid - 1) / total;
-        if (c0 + 1 != b) return;             // handled at the query's first boundary
-        const int64_t c1 = (((qi + 1) * tiles) * grid - 1) / total;
+        auto cta_of = [&](int64_t g) { return ((g + 1) * grid - 1) / total; };
+        int64_t c0;
+        if (by_query) {
+            qi = blockIdx.x / H;
+            c0 = cta_of(qi * tiles);
+        } else {
+            const int64_t b = blockIdx.x / H + 1;
+            const int64_t g = b * total / grid;  // first tile of CTA b
+            if (g % tiles == 0) return;          // the boundary falls between queries
+            qi = g / tiles;
+            c0 = cta_of(qi * tiles);
+            if (c0 + 1 != b) return;             // handled at the query's first boundary
+        }
+        const int64_t c1 = cta_of((qi + 1) * tiles - 1);
+        if (c1 == c0) return;                    // finished by its only CTA
         Sq = (int)(c1 - c0 + 1);
     } else {
         qi = blockIdx.x / H;
@@ -260,14 +269,24 @@ __global__ void __launch_bounds__(128)
     const float inv = s_inv;
     for (int d4 = tid; d4 < D / 4; d4 += blockDim.x) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s2 = 0; s2 < Sq; s2++) {
-            const float w = wts[s2];
-            if (w == 0.f) continue;
-            const float4 v = __ldg(reinterpret_cast<const float4*>(part_o + ((qi * S + s2) * H + h) * D) + d4);
-            acc.x = fmaf(w, v.x, acc.x);
-            acc.y = fmaf(w, v.y, acc.y);
-            acc.z = fmaf(w, v.z, acc.z);
-            acc.w = fmaf(w, v.w, acc.w);
+        // eight partials in flight at a time; a slot of weight 0 is not added
+        // (its values are never used, whatever they hold)
+        for (int s0 = 0; s0 < Sq; s0 += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                if (s0 + j < Sq)
+                    v[j] = __ldg(reinterpret_cast<const float4*>(part_o + ((qi * S + s0 + j) * H + h) * D) + d4);
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                if (s0 + j >= Sq) break;
+                const float w = wts[s0 + j];
+                if (w == 0.f) continue;
+                acc.x = fmaf(w, v[j].x, acc.x);
+                acc.y = fmaf(w, v[j].y, acc.y);
+                acc.z = fmaf(w, v[j].z, acc.z);
+                acc.w = fmaf(w, v[j].w, acc.w);
+            }
         }
         float o[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
         const int d0 = 4 * d4;
@@ -297,7 +316,7 @@ cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool spars
                              int H, int B, int Q, const int64_t* q_pos, const void* cache,
                              int64_t n_cap, const int32_t* topk_idx, const void* window,
                              int64_t n_win, const int64_t* win_pos0, const float* sink,
-                             void* out, float* lse, float* part_o, float* part_ml,
+                             void* out, float* lse, float* part_o, float* part_ml, uint8_t* deq,
                              uint32_t* status, cudaStream_t st);
 
 template <int D, int HG>
@@ -324,7 +343,7 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
     cudaError_t e;
     if (pl.use_tc) {
         e = launch_attend_tc(g, pl, sparse, q, H, B, Q, q_pos, cache, n_cap, topk_idx, window,
-                             n_win, win_pos0, sink, out, lse, part_o, part_ml, status, st);
+                             n_win, win_pos0, sink, out, lse, part_o, part_ml, ws + pl.deq_off, status, st);
     } else {
         AttendArgs a;
         a.q = reinterpret_cast<const uint8_t*>(q);
@@ -363,11 +382,14 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
         else return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
-    const int64_t blocks = pl.use_tc ? (int64_t)(pl.tc_grid - 1) * H : (int64_t)Q * H;
+    // tensor-core kernel: a block per query when there are no more queries
+    // than CTA boundaries, else a block per boundary
+    const int by_query = pl.use_tc && Q <= pl.tc_grid - 1;
+    const int64_t blocks = (!pl.use_tc || by_query) ? (int64_t)Q * H : (int64_t)(pl.tc_grid - 1) * H;
     if (blocks == 0) return cudaSuccess;  // every query was finished by its only CTA
     attend_combine_kernel<<<(unsigned)blocks, 128, (size_t)pl.splits * sizeof(float), st>>>(
         part_o, part_ml, pl.splits, H, g.D, sink, q_pos, g.derotate, out, g.act, lse,
-        pl.use_tc ? (int64_t)pl.tc_T : 0, pl.tc_total, pl.tc_grid, rope_theta(g));
+        pl.use_tc ? (int64_t)pl.tc_T : 0, pl.tc_total, pl.tc_grid, by_query, rope_theta(g));
     note_launch();
     return cudaGetLastError();
 }

@@ -75,6 +75,7 @@ struct AttTcArgs {
     const int64_t* q_pos;     // [Q]
     const int32_t* topk_idx;  // [Q, k]; nullptr: dense (HCA)
     int k;
+    int pre;                  // tm_sel maps [Q, T * 64, 512]: each query's rows in tile order
     int64_t n_cap, n_win;
     const int64_t* win_pos0;  // [B]
     int W, m, qps;
@@ -205,6 +206,90 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return (uint32_t)f32_to_bf16_rn(lo) | ((uint32_t)f32_to_bf16_rn(hi) << 16);
 }
 
+
+// ------------------------------------------------------------- FP8 rows -> bf16
+// Stored FP8_MIXED row of 512 dims: 448 E4M3 codes, the 64 rotated dims as
+// bf16, then one float32 scale per 64-dim group of codes.
+constexpr int kNf = kD - kRopeDims;             // quantised dims
+constexpr int kScaleOff = kNf + 2 * kRopeDims;  // byte offset of the scales
+
+// One warp dequantises one row into 512 bf16 (code * group scale, rounded to
+// nearest even; the rotated dims are copied).  A null row writes zeros: a
+// masked row must hold finite values, as its weight P = 0 multiplies it.
+__device__ __forceinline__ void warp_dequant_row(const uint8_t* row, uint16_t* out, int lane) {
+    uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
+    if (row != nullptr) {
+        if (lane < kNf / 16) {  // 16 codes per lane, four lanes per group
+            const uint4 c = __ldg(reinterpret_cast<const uint4*>(row) + lane);
+            const float sc = __ldg(reinterpret_cast<const float*>(row + kScaleOff) + (lane >> 2));
+            const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+            uint32_t r[8];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                r[2 * e] = pack_bf16x2(e4m3_to_f32((uint8_t)w[e]) * sc, e4m3_to_f32((uint8_t)(w[e] >> 8)) * sc);
+                r[2 * e + 1] =
+                    pack_bf16x2(e4m3_to_f32((uint8_t)(w[e] >> 16)) * sc, e4m3_to_f32((uint8_t)(w[e] >> 24)) * sc);
+            }
+            o0 = make_uint4(r[0], r[1], r[2], r[3]);
+            o1 = make_uint4(r[4], r[5], r[6], r[7]);
+        } else {  // lanes 28..31: 16 rotated dims each, already bf16
+            const uint4* src = reinterpret_cast<const uint4*>(row + kNf) + 2 * (lane - kNf / 16);
+            o0 = __ldg(src);
+            o1 = __ldg(src + 1);
+        }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(out) + 2 * lane;
+    dst[0] = o0;
+    dst[1] = o1;
+}
+
+constexpr int kDeqThreads = 256;  // one row per warp
+
+// Every stored row of a buffer [n, rb bytes] -> [n, 512] bf16.
+__global__ void __launch_bounds__(kDeqThreads) dequant_rows_kernel(const uint8_t* __restrict__ src, int64_t rb,
+                                                                   int64_t n, uint16_t* __restrict__ out) {
+    const int64_t r = (int64_t)blockIdx.x * (kDeqThreads / 32) + (threadIdx.x >> 5);
+    if (r < n) warp_dequant_row(src + r * rb, out + r * kD, threadIdx.x & 31);
+}
+
+struct DeqGatherArgs {
+    const uint8_t* cache;     // [B, n_cap, rb]
+    const uint8_t* window;    // [B, n_win, rb]
+    int64_t rb, n_cap, n_win;
+    const int64_t* q_pos;     // [Q]
+    const int64_t* win_pos0;  // [B]
+    const int32_t* topk_idx;  // [Q, k]; nullptr: every cache row in order
+    int k, W, m, qps, T_sel, T;
+    int64_t rows;             // Q * T * 64
+    uint16_t* out;            // [Q, T * 64, 512]
+};
+
+// Row p of query qi's list in tile order: the p-th selected (or cache) row
+// for p < T_sel * 64, then window row p - T_sel * 64.  Rows the attention
+// masks (padding, index -1, out of range, before position 0) are zeros.
+__global__ void __launch_bounds__(kDeqThreads) dequant_gather_kernel(const DeqGatherArgs a) {
+    const int64_t r = (int64_t)blockIdx.x * (kDeqThreads / 32) + (threadIdx.x >> 5);
+    if (r >= a.rows) return;
+    const int64_t per = (int64_t)a.T * kRows;
+    const int64_t qi = r / per;
+    const int p = (int)(r - qi * per);
+    const int64_t i = a.q_pos[qi];
+    const int seq = (int)(qi / a.qps);
+    int64_t n_av = (i + 1) / a.m;
+    n_av = n_av < 0 ? 0 : (n_av < a.n_cap ? n_av : a.n_cap);
+    const uint8_t* src = nullptr;
+    if (p < a.T_sel * kRows) {
+        const int64_t e = a.topk_idx ? (p < a.k ? (int64_t)a.topk_idx[qi * a.k + p] : -1) : p;
+        if (e >= 0 && e < n_av) src = a.cache + ((int64_t)seq * a.n_cap + e) * a.rb;
+    } else {
+        const int rw = p - a.T_sel * kRows;
+        const int64_t wr = i - a.W + 1 + rw - a.win_pos0[seq];
+        if (rw < a.W && i - a.W + 1 + rw >= 0 && wr >= 0 && wr < a.n_win)
+            src = a.window + ((int64_t)seq * a.n_win + wr) * a.rb;
+    }
+    warp_dequant_row(src, a.out + r * kD, threadIdx.x & 31);
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -286,7 +371,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int lt = (int)(g - qi * a.T);
                 const QueryInfo inf = query_info(a, qi);
                 if (!tile_live(a, inf, lt)) continue;
-                if (!(lt < a.T_sel && a.topk_idx != nullptr) && lane < 8) {
+                if (a.pre) {
+                    if (lane < 8) tc::tma_prefetch_3d(&tm_sel, lane * 64, lt * kRows, (int)qi);
+                } else if (!(lt < a.T_sel && a.topk_idx != nullptr) && lane < 8) {
                     const int r0 = box_row0(inf, lt);
                     if (r0 >= 0)  // a window box that starts before row 0 is not prefetched
                         tc::tma_prefetch_3d(lt < a.T_sel ? &tm_sel : &tm_win, lane * 64, r0, inf.seq);
@@ -305,7 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* dst = sE + st * kStageBytes;
             if (lane == 0) tc::mbar_arrive_expect_tx(&full[st], kStageBytes);
             __syncwarp();
-            if (lt < a.T_sel && a.topk_idx != nullptr) {
+            if (a.pre) {
+                if (lane < 8)
+                    tc::tma_load_3d(dst + lane * kBoxBytes, &tm_sel, &full[st], lane * 64, lt * kRows, (int)qi);
+            } else if (lt < a.T_sel && a.topk_idx != nullptr) {
                 int rows[4];
                 gather_rows(qi, inf, lt, rows);
 #pragma unroll
@@ -742,7 +832,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ host side
 bool attend_tc_supported(const Geometry& g, bool sparse, int H, int64_t n_cap, int64_t n_win) {
-    if (g.act != CSA_BF16 || g.kv != CSA_BF16 || g.D != kD || g.R != 64 || H != kH) return false;
+    if (g.act != CSA_BF16 || (g.kv != CSA_BF16 && g.kv != CSA_FP8_MIXED)) return false;
+    if (g.D != kD || g.R != 64 || H != kH) return false;
     if (!sparse && n_cap < kRows) return false;     // tile boxes of 64 rows
     if (sparse && (n_cap < 1 || g.k < 1)) return false;
     if (g.W > 0 && n_win < kRows) return false;
@@ -770,35 +861,80 @@ cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool spars
                              int H, int B, int Q, const int64_t* q_pos, const void* cache,
                              int64_t n_cap, const int32_t* topk_idx, const void* window,
                              int64_t n_win, const int64_t* win_pos0, const float* sink,
-                             void* out, float* lse, float* part_o, float* part_ml,
+                             void* out, float* lse, float* part_o, float* part_ml, uint8_t* deq,
                              uint32_t* status, cudaStream_t st) {
     (void)H;
     if (pl.tc_total == 0) return cudaSuccess;
+    const int64_t rb = g.kv_row_bytes;
     CUtensorMap tm_sel, tm_win;
-    if (sparse) {
-        const uint64_t d[2] = {(uint64_t)kD, (uint64_t)B * (uint64_t)n_cap};
-        const uint64_t s[1] = {(uint64_t)kD * 2};
-        const uint32_t box[2] = {64, 1};
-        if (!make_tmap_bf16(&tm_sel, cache, 2, d, s, box)) return cudaErrorInvalidValue;
-    } else {
-        const uint64_t d[3] = {(uint64_t)kD, (uint64_t)n_cap, (uint64_t)B};
-        const uint64_t s[2] = {(uint64_t)kD * 2, (uint64_t)n_cap * kD * 2};
+    uint16_t* deq_rows = reinterpret_cast<uint16_t*>(deq);
+    if (pl.tc_deq == 1) {
+        DeqGatherArgs d;
+        d.cache = reinterpret_cast<const uint8_t*>(cache);
+        d.window = reinterpret_cast<const uint8_t*>(window);
+        d.rb = rb;
+        d.n_cap = n_cap;
+        d.n_win = n_win;
+        d.q_pos = q_pos;
+        d.win_pos0 = win_pos0;
+        d.topk_idx = sparse ? topk_idx : nullptr;
+        d.k = g.k;
+        d.W = g.W;
+        d.m = g.m;
+        d.qps = Q / B;
+        d.T_sel = pl.tc_T_sel;
+        d.T = pl.tc_T;
+        d.rows = (int64_t)Q * pl.tc_T * kRows;
+        d.out = deq_rows;
+        const int64_t blocks = (d.rows + kDeqThreads / 32 - 1) / (kDeqThreads / 32);
+        dequant_gather_kernel<<<(unsigned)blocks, kDeqThreads, 0, st>>>(d);
+        note_launch();
+        const uint64_t dm[3] = {(uint64_t)kD, (uint64_t)pl.tc_T * kRows, (uint64_t)Q};
+        const uint64_t sd[2] = {(uint64_t)kD * 2, (uint64_t)pl.tc_T * kRows * kD * 2};
         const uint32_t box[3] = {64, (uint32_t)kRows, 1};
-        if (!make_tmap_bf16(&tm_sel, cache, 3, d, s, box)) return cudaErrorInvalidValue;
-    }
-    if (g.W > 0) {
-        const uint64_t d[3] = {(uint64_t)kD, (uint64_t)n_win, (uint64_t)B};
-        const uint64_t s[2] = {(uint64_t)kD * 2, (uint64_t)n_win * kD * 2};
-        const uint32_t box[3] = {64, (uint32_t)kRows, 1};
-        if (!make_tmap_bf16(&tm_win, window, 3, d, s, box)) return cudaErrorInvalidValue;
-    } else {
+        if (!make_tmap_bf16(&tm_sel, deq_rows, 3, dm, sd, box)) return cudaErrorInvalidValue;
         tm_win = tm_sel;  // never read
+    } else {
+        if (pl.tc_deq == 2) {  // every stored row, then the bf16 copies stand in for the rows
+            const int64_t n_rows[2] = {(int64_t)B * n_cap, g.W > 0 ? (int64_t)B * n_win : 0};
+            const void* src[2] = {cache, window};
+            uint16_t* dst[2] = {deq_rows, deq_rows + n_rows[0] * kD};
+            for (int j = 0; j < 2; j++) {
+                if (n_rows[j] == 0) continue;
+                const int64_t blocks = (n_rows[j] + kDeqThreads / 32 - 1) / (kDeqThreads / 32);
+                dequant_rows_kernel<<<(unsigned)blocks, kDeqThreads, 0, st>>>(
+                    reinterpret_cast<const uint8_t*>(src[j]), rb, n_rows[j], dst[j]);
+                note_launch();
+            }
+            cache = dst[0];
+            window = dst[1];
+        }
+        if (sparse) {
+            const uint64_t d[2] = {(uint64_t)kD, (uint64_t)B * (uint64_t)n_cap};
+            const uint64_t s[1] = {(uint64_t)kD * 2};
+            const uint32_t box[2] = {64, 1};
+            if (!make_tmap_bf16(&tm_sel, cache, 2, d, s, box)) return cudaErrorInvalidValue;
+        } else {
+            const uint64_t d[3] = {(uint64_t)kD, (uint64_t)n_cap, (uint64_t)B};
+            const uint64_t s[2] = {(uint64_t)kD * 2, (uint64_t)n_cap * kD * 2};
+            const uint32_t box[3] = {64, (uint32_t)kRows, 1};
+            if (!make_tmap_bf16(&tm_sel, cache, 3, d, s, box)) return cudaErrorInvalidValue;
+        }
+        if (g.W > 0) {
+            const uint64_t d[3] = {(uint64_t)kD, (uint64_t)n_win, (uint64_t)B};
+            const uint64_t s[2] = {(uint64_t)kD * 2, (uint64_t)n_win * kD * 2};
+            const uint32_t box[3] = {64, (uint32_t)kRows, 1};
+            if (!make_tmap_bf16(&tm_win, window, 3, d, s, box)) return cudaErrorInvalidValue;
+        } else {
+            tm_win = tm_sel;  // never read
+        }
     }
     AttTcArgs a;
     a.q = reinterpret_cast<const uint16_t*>(q);
     a.q_pos = q_pos;
     a.topk_idx = sparse ? topk_idx : nullptr;
     a.k = g.k;
+    a.pre = pl.tc_deq == 1 ? 1 : 0;
     a.n_cap = n_cap;
     a.n_win = n_win;
     a.win_pos0 = win_pos0;

@@ -92,6 +92,15 @@ def test_csa_decode_growing_logits_rescale():
     decode_parity(w, mutate=lambda inp: _ramp_toward_q(inp, 12.0))
 
 
+def test_hca_decode_fp8_small():
+    """FP8 rows on the tensor-core path, in both dequantised layouts: a 37-block
+    capacity (fewer stored rows than tile rows: every stored row) and a
+    128-block one (the rows of each query's tiles)."""
+    decode_parity(SMALL_HCA.replace(name="hca_fp8_small", kv_fmt="fp8m"))
+    decode_parity(SMALL_HCA.replace(name="hca_fp8_rows", kv_fmt="fp8m", B=2,
+                                    L_per_seq=(128 * 128, 128 * 50 + 3)))
+
+
 def test_fp8_pack_is_bit_exact():
     from long_context_compressed_17_b300.pipeline import LayerConfig
     g = torch.Generator(device="cpu").manual_seed(11)
@@ -109,6 +118,13 @@ def test_fp8_pack_is_bit_exact():
 def test_csa_prefill_bf16_small():
     w = workloads.CSA_CHUNKED_PREFILL.replace(name="prefill_small", T_cached=512, T_new=300,
                                               topk=64)
+    n_same, n = prefill_parity(w)
+    assert n_same >= n - 2
+
+
+def test_csa_prefill_fp8_small():
+    w = workloads.CSA_CHUNKED_PREFILL.replace(name="prefill_fp8_small", kv_fmt="fp8m",
+                                              T_cached=512, T_new=300, topk=64)
     n_same, n = prefill_parity(w)
     assert n_same >= n - 2
 
