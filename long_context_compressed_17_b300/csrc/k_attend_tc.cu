@@ -36,6 +36,8 @@
 // outstanding copies and MMAs are waited for and TMEM is freed.
 #include <math.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc_util.cuh"
@@ -59,7 +61,8 @@ constexpr uint32_t kPBytes = kRows * kH * 2;        // 64 rows x 64 heads
 constexpr size_t kSmem = 1024 + kStages * kStageBytes + kQBytes + 2 * kPBytes;
 constexpr int kSoftWarps = 16;                      // 4 TMEM lane quarters x 4 head quarters
 constexpr int kSoftThreads = kSoftWarps * 32;
-constexpr int kThreads = 64 + kSoftThreads;
+constexpr int kLoadWarps = 2;                       // warps issuing TMA gathers (and warp 0)
+constexpr int kThreads = 64 + kSoftThreads + 32 * kLoadWarps;
 constexpr int kHW = kH / 4;                         // heads per softmax warp
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // S^T buffers: 2 x 64 columns
@@ -76,6 +79,7 @@ struct AttTcArgs {
     const int32_t* topk_idx;  // [Q, k]; nullptr: dense (HCA)
     int k;
     int pre;                  // tm_sel maps [Q, T * 64, 512]: each query's rows in tile order
+    const uint8_t* cache;     // [B, n_cap, 512] bf16 rows the gather warps copy
     int64_t n_cap, n_win;
     const int64_t* win_pos0;  // [B]
     int W, m, qps;
@@ -127,10 +131,61 @@ __device__ __forceinline__ bool tile_live(const AttTcArgs& a, const QueryInfo& q
     return qi.i - a.W + 1 + rlast >= 0;
 }
 
+// Boxes of a gathered tile fetched by the producer warp; the gather warps
+// share the others.  TMA gathers issued from several warps proceed in
+// parallel, so the 128 gather4 copies of a tile are spread over warps (two
+// gather warps saturate it: a third, the producer, gains nothing).
+constexpr int kProducerBoxes = 0;
+constexpr int kLoaderBoxes = (8 - kProducerBoxes) / kLoadWarps;
+
+// Whether tile lt is copied row by row from the selected cache rows (by
+// gather4) rather than loaded as a TMA tile.
+__device__ __forceinline__ bool is_gathered(const AttTcArgs& a, int lt) {
+    return !a.pre && a.topk_idx != nullptr && lt < a.T_sel;
+}
+
+// Cache rows of the selected blocks of gathered tile lt of query qi that
+// lane l gathers: tile rows 4*(l%16) .. +3 (a masked row fetches the
+// sequence's row 0; the softmax warps mask it).
+__device__ __forceinline__ void gather_rows(const AttTcArgs& a, int64_t qi, const QueryInfo& inf, int lt,
+                                            int lane, int (&rows)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const int p = lt * kRows + 4 * (lane & 15) + j;
+        int64_t e = p < a.k ? (int64_t)a.topk_idx[qi * a.k + p] : -1;
+        if (e < 0 || e >= inf.n_av) e = 0;
+        rows[j] = (int)((int64_t)inf.seq * a.n_cap + e);
+    }
+}
+
+// Boxes box0 .. box0+nbox-1 (64 dims each) of those rows into a stage, by
+// one warp.
+__device__ __forceinline__ void gather_boxes(const CUtensorMap* tm, uint64_t* bar, uint8_t* stage,
+                                             const int (&rows)[4], int box0, int nbox, int lane) {
+    const int rg = lane & 15;
+    for (int pi = lane; pi < 16 * nbox; pi += 32) {  // pi % 16 == rg
+        const int box = box0 + pi / 16;
+        tc::tma_gather4(stage + box * kBoxBytes + rg * 512, tm, bar, box * 64, rows[0], rows[1], rows[2], rows[3]);
+    }
+}
+
 // Last live tile of the segment [lt0, lt1) of a query, or -1.
 __device__ __forceinline__ int last_live(const AttTcArgs& a, const QueryInfo& qi, int lt0, int lt1) {
     for (int lt = lt1 - 1; lt >= lt0; --lt)
         if (tile_live(a, qi, lt)) return lt;
+    return -1;
+}
+
+// The first query from global tile g on (up to g_end) whose segment has a
+// live tile, or -1.
+__device__ __forceinline__ int64_t next_live_query(const AttTcArgs& a, int64_t g, int64_t g_end) {
+    while (g < g_end) {
+        const int64_t qi = g / a.T;
+        const int64_t seg_end = min(g_end, (qi + 1) * a.T);
+        const QueryInfo inf = query_info(a, qi);
+        if (last_live(a, inf, (int)(g - qi * a.T), (int)(seg_end - qi * a.T)) >= 0) return qi;
+        g = seg_end;
+    }
     return -1;
 }
 
@@ -200,6 +255,10 @@ __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -293,17 +352,17 @@ __global__ void __launch_bounds__(kDeqThreads) dequant_gather_kernel(const DeqGa
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
-    attend_tc_kernel(const __grid_constant__ CUtensorMap tm_sel,
-                     const __grid_constant__ CUtensorMap tm_win, const __grid_constant__ AttTcArgs a) {
+    attend_tc_kernel(const __grid_constant__ CUtensorMap tm_sel, const __grid_constant__ CUtensorMap tm_win,
+                     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ AttTcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sE = sm;                              // kStages x (8 boxes of 64 rows x 64 dims)
     uint8_t* sQ = sE + kStages * kStageBytes;      // 8 boxes of 64 heads x 64 dims
     uint8_t* sP = sQ + kQBytes;                    // 2 x (64 rows x 64 heads)
 
-    __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
+    __shared__ __align__(8) uint64_t full[kStages], empty[kStages], go[kStages];
     __shared__ __align__(8) uint64_t s_full[2], p_full[2];
-    __shared__ __align__(8) uint64_t o_full, o_seg, q_full, mma_done;
+    __shared__ __align__(8) uint64_t o_full, o_seg, q_full, q_raw, mma_done;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_sh;
     __shared__ float red[4][kH];
@@ -316,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; s++) {
             tc::mbar_init(&full[s], 1);
             tc::mbar_init(&empty[s], 1);
+            tc::mbar_init(&go[s], 1);
         }
         for (int b = 0; b < 2; b++) {
             tc::mbar_init(&s_full[b], 1);
@@ -324,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_init(&o_full, 1);  // after every PV product
         tc::mbar_init(&o_seg, 1);   // after the last PV product of a segment
         tc::mbar_init(&q_full, 1);
+        tc::mbar_init(&q_raw, 1);   // raw q of the CTA's first segment landed in sQ
         tc::mbar_init(&mma_done, 1);
         abort_sh = 0;
         tc::fence_barrier_init();
@@ -343,22 +404,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ loads
+        // The raw q rows of the first segment go into sQ ahead of any tile:
+        // the softmax warps normalise and rotate them in place.
+        const int64_t q_first = next_live_query(a, g_begin, g_end);
+        if (q_first >= 0) {
+            if (lane == 0) tc::mbar_arrive_expect_tx(&q_raw, kQBytes);
+            __syncwarp();
+            if (lane < 8) tc::tma_load_3d(sQ + lane * kQBoxBytes, &tm_q, &q_raw, lane * 64, 0, (int)q_first);
+        }
         if (lane == 0) {
             tc::tma_prefetch_map(&tm_sel);
             if (a.W > 0) tc::tma_prefetch_map(&tm_win);
         }
         uint32_t tcount = 0;
-        uint32_t fills[kStages] = {0, 0};  // loads issued into each stage
-        // rows lane l gathers for tile lt of query qi: 4*(l%16) .. +3
-        auto gather_rows = [&](int64_t qi, const QueryInfo& inf, int lt, int (&rows)[4]) {
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-                const int p = lt * kRows + 4 * (lane & 15) + j;
-                int64_t e = p < a.k ? (int64_t)a.topk_idx[qi * a.k + p] : -1;
-                if (e < 0 || e >= inf.n_av) e = 0;  // masked by the softmax warps
-                rows[j] = (int)((int64_t)inf.seq * a.n_cap + e);
-            }
-        };
+        uint32_t fills[kStages] = {0, 0};  // fills of each stage (by any warp)
         auto box_row0 = [&](const QueryInfo& inf, int lt) {
             return lt < a.T_sel ? lt * kRows
                                 : (int)(inf.i - a.W + 1 + (int64_t)(lt - a.T_sel) * kRows - a.win_pos0[inf.seq]);
@@ -373,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!tile_live(a, inf, lt)) continue;
                 if (a.pre) {
                     if (lane < 8) tc::tma_prefetch_3d(&tm_sel, lane * 64, lt * kRows, (int)qi);
-                } else if (!(lt < a.T_sel && a.topk_idx != nullptr) && lane < 8) {
+                } else if (!is_gathered(a, lt) && lane < 8) {
                     const int r0 = box_row0(inf, lt);
                     if (r0 >= 0)  // a window box that starts before row 0 is not prefetched
                         tc::tma_prefetch_3d(lt < a.T_sel ? &tm_sel : &tm_win, lane * 64, r0, inf.seq);
@@ -386,27 +445,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int lt = (int)(g - qi * a.T);
             const QueryInfo inf = query_info(a, qi);
             if (!tile_live(a, inf, lt)) continue;
-            prefetch_after(g);
             const int st = tcount & 1;
+            prefetch_after(g);
+            // every use of a stage is waited for here, in order, whoever fills it
             if (!warp_wait(&empty[st], ((tcount >> 1) & 1u) ^ 1u, abort_flag, a.status, lane)) break;
-            uint8_t* dst = sE + st * kStageBytes;
             if (lane == 0) tc::mbar_arrive_expect_tx(&full[st], kStageBytes);
-            __syncwarp();
-            if (a.pre) {
-                if (lane < 8)
-                    tc::tma_load_3d(dst + lane * kBoxBytes, &tm_sel, &full[st], lane * 64, lt * kRows, (int)qi);
-            } else if (lt < a.T_sel && a.topk_idx != nullptr) {
-                int rows[4];
-                gather_rows(qi, inf, lt, rows);
-#pragma unroll
-                for (int bb = 0; bb < 4; bb++) {
-                    const int box = (lane >> 4) * 4 + bb;
-                    tc::tma_gather4(dst + box * kBoxBytes + (lane & 15) * 512, &tm_sel, &full[st], box * 64,
-                                    rows[0], rows[1], rows[2], rows[3]);
+            if (is_gathered(a, lt)) {
+                if (lane == 0) tc::mbar_arrive(&go[st]);  // the gather warps join in
+                if (kProducerBoxes > 0) {
+                    int rows[4];
+                    gather_rows(a, qi, inf, lt, lane, rows);
+                    gather_boxes(&tm_sel, &full[st], sE + st * kStageBytes, rows, 0, kProducerBoxes, lane);
                 }
-            } else if (lane < 8) {
-                tc::tma_load_3d(dst + lane * kBoxBytes, lt < a.T_sel ? &tm_sel : &tm_win, &full[st], lane * 64,
-                                box_row0(inf, lt), inf.seq);
+            } else {
+                uint8_t* dst = sE + st * kStageBytes;
+                __syncwarp();
+                if (lane < 8) {
+                    if (a.pre)
+                        tc::tma_load_3d(dst + lane * kBoxBytes, &tm_sel, &full[st], lane * 64, lt * kRows, (int)qi);
+                    else
+                        tc::tma_load_3d(dst + lane * kBoxBytes, lt < a.T_sel ? &tm_sel : &tm_win, &full[st],
+                                        lane * 64, box_row0(inf, lt), inf.seq);
+                }
             }
             ++fills[st];
             ++tcount;
@@ -456,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool progress = false;
                 if (t_pv < t_qk) {
                     const int b = t_pv & 1;
-                    if (tc::mbar_try_wait(&p_full[b], (t_pv >> 1) & 1u)) {
+                    if (tc::mbar_test_wait(&p_full[b], (t_pv >> 1) & 1u)) {
                         tc::fence_after_sync();
                         const uint32_t stage = sE0 + b * kStageBytes;
                         const uint32_t pb = sP0 + b * kPBytes;
@@ -479,8 +539,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (more && t_pv + 1 >= t_qk) {  // S^T buffer of tile t_qk is free
                     const int b = t_qk & 1;
-                    bool ready = !at_seg_start || tc::mbar_try_wait(&q_full, nq & 1u);
-                    if (ready) ready = tc::mbar_try_wait(&full[b], (t_qk >> 1) & 1u);
+                    bool ready = !at_seg_start || tc::mbar_test_wait(&q_full, nq & 1u);
+                    if (ready) ready = tc::mbar_test_wait(&full[b], (t_qk >> 1) & 1u);
                     if (ready) {
                         tc::fence_after_sync();
                         const uint32_t stage = sE0 + b * kStageBytes;
@@ -519,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_commit(&mma_done);
             if (!tc::mbar_drain(&mma_done, 0)) atomicOr(a.status, CSA_DEV_TIMEOUT);
         }
-    } else {
+    } else if (warp < 2 + kSoftWarps) {
         // ------------------------------------------------------------ softmax + epilogue
         // Warp w owns TMEM lane quarter (w % 4) and the 16 heads of head quarter
         // (w - 2) / 4.  S^T rows (M = 64) sit in lanes 0..15 of each quarter:
@@ -533,82 +593,94 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int dim = quarter * 32 + lane;         // O^T lane: dim within a 128-dim slice
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
 
-        // q' = RoPE(RMSNorm(q), i) of query qi into sQ (bf16, 128-byte swizzle)
-        auto prep_q = [&](int64_t qi) {
+        // q' = RoPE(RMSNorm(q), i) of query qi into sQ (bf16, 128-byte
+        // swizzle).  staged: the raw rows were loaded into sQ by TMA (the
+        // CTA's first segment) and are normalised in place; otherwise they are
+        // read from global memory (L2: prefetched when the segment before
+        // started).  Lane l of a warp holds dims 16l .. 16l+15 of a head: two
+        // 16-byte chunks of box l/4 of that head's 128-byte row.
+        auto prep_q = [&](int64_t qi, auto staged_c) {
+            constexpr bool staged = decltype(staged_c)::value;
+            constexpr int kHq = kH / kSoftWarps;  // heads of this warp
             const int64_t i = a.q_pos[qi];
+            if constexpr (!staged)
+                for (int hh = 1; hh < kHq; hh++)  // on their way into L2 meanwhile
+                    prefetch_l2(a.q + (qi * kH + sw * kHq + hh) * kD + lane * 16);
+            const int ch = (lane & 3) * 2;
+            // this lane's chunk c (0, 1) of head h in sQ
+            uint8_t* const qbase = sQ + (lane >> 2) * kQBoxBytes;
+#define QCHUNK(h, c) reinterpret_cast<uint4*>(qbase + (h) * 128 + (((ch + (c)) ^ ((h) & 7)) << 4))
+            const uint4* gsrc = reinterpret_cast<const uint4*>(a.q + (qi * kH + sw * kHq) * kD) + lane * 2;
+            uint4 u0 = make_uint4(0u, 0u, 0u, 0u), u1 = u0;
+            if constexpr (!staged) {
+                u0 = __ldg(gsrc);
+                u1 = __ldg(gsrc + 1);
+            }
             if (tid < 32) {
                 float c, s;
                 rope_cs((double)i, a.theta.t[tid], &c, &s);
                 rot_cs[2 * tid] = c;
                 rot_cs[2 * tid + 1] = s;
             }
+            bool ok = true;
+            if constexpr (staged) ok = warp_wait(&q_raw, 0, abort_flag, a.status, lane);
             softmax_barrier();
-            for (int hh = 0; hh < kH / kSoftWarps; hh++) {
-                const int h = sw * (kH / kSoftWarps) + hh;
-                const uint4* src = reinterpret_cast<const uint4*>(a.q + (qi * kH + h) * kD) + lane * 2;
-                const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
-                const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-                float x[16];
-#pragma unroll
-                for (int e = 0; e < 8; e++) {
-                    x[2 * e] = __uint_as_float(w[e] << 16);
-                    x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-                }
-                float ss = 0.f;
-#pragma unroll
-                for (int e = 0; e < 16; e++) ss = fmaf(x[e], x[e], ss);
-                ss = warp_sum(ss);
-                const float r = 1.f / sqrtf(ss / (float)kD + a.eps);
-#pragma unroll
-                for (int e = 0; e < 16; e++) x[e] *= r;
-                if (lane >= 28) {  // dims 448..511: the rotated ones
+            if (ok) {
+#pragma unroll 1
+                for (int hh = 0; hh < kHq; hh++) {
+                    const int h = sw * kHq + hh;
+                    if constexpr (staged) {
+                        u0 = *QCHUNK(h, 0);
+                        u1 = *QCHUNK(h, 1);
+                    } else if (hh > 0) {
+                        u0 = __ldg(gsrc + hh * (kD / 8));
+                        u1 = __ldg(gsrc + hh * (kD / 8) + 1);
+                    }
+                    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                    float x[16];
 #pragma unroll
                     for (int e = 0; e < 8; e++) {
-                        const int j = (lane - 28) * 8 + e;
-                        const float c = rot_cs[2 * j], s = rot_cs[2 * j + 1];
-                        const float x0 = x[2 * e], x1 = x[2 * e + 1];
-                        x[2 * e] = x0 * c - x1 * s;
-                        x[2 * e + 1] = x0 * s + x1 * c;
+                        x[2 * e] = __uint_as_float(w[e] << 16);
+                        x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
                     }
+                    float ss = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 16; e++) ss = fmaf(x[e], x[e], ss);
+                    ss = warp_sum(ss);
+                    const float r = 1.f / sqrtf(ss / (float)kD + a.eps);
+#pragma unroll
+                    for (int e = 0; e < 16; e++) x[e] *= r;
+                    if (lane >= 28) {  // dims 448..511: the rotated ones
+#pragma unroll
+                        for (int e = 0; e < 8; e++) {
+                            const int j = (lane - 28) * 8 + e;
+                            const float c = rot_cs[2 * j], s = rot_cs[2 * j + 1];
+                            const float x0 = x[2 * e], x1 = x[2 * e + 1];
+                            x[2 * e] = x0 * c - x1 * s;
+                            x[2 * e + 1] = x0 * s + x1 * c;
+                        }
+                    }
+                    *QCHUNK(h, 0) = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
+                                              pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+                    *QCHUNK(h, 1) = make_uint4(pack_bf16x2(x[8], x[9]), pack_bf16x2(x[10], x[11]),
+                                              pack_bf16x2(x[12], x[13]), pack_bf16x2(x[14], x[15]));
                 }
-                uint4 o0, o1;
-                o0.x = pack_bf16x2(x[0], x[1]);
-                o0.y = pack_bf16x2(x[2], x[3]);
-                o0.z = pack_bf16x2(x[4], x[5]);
-                o0.w = pack_bf16x2(x[6], x[7]);
-                o1.x = pack_bf16x2(x[8], x[9]);
-                o1.y = pack_bf16x2(x[10], x[11]);
-                o1.z = pack_bf16x2(x[12], x[13]);
-                o1.w = pack_bf16x2(x[14], x[15]);
-                uint8_t* base = sQ + (lane >> 2) * kQBoxBytes + h * 128;
-                const int ch = (lane & 3) * 2;
-                *reinterpret_cast<uint4*>(base + (((ch) ^ (h & 7)) << 4)) = o0;
-                *reinterpret_cast<uint4*>(base + (((ch + 1) ^ (h & 7)) << 4)) = o1;
             }
+#undef QCHUNK
             tc::fence_proxy_async_smem();
             softmax_barrier();
             if (tid == 0) tc::mbar_arrive(&q_full);
         };
 
-        // the next segment (from global tile g) with a live tile, or -1
-        auto next_live_query = [&](int64_t g) -> int64_t {
-            while (g < g_end) {
-                const int64_t qi = g / a.T;
-                const int64_t seg_end = min(g_end, (qi + 1) * a.T);
-                const QueryInfo inf = query_info(a, qi);
-                if (last_live(a, inf, (int)(g - qi * a.T), (int)(seg_end - qi * a.T)) >= 0) return qi;
-                g = seg_end;
-            }
-            return -1;
-        };
 
         {
-            const int64_t q0 = next_live_query(g_begin);
-            if (q0 >= 0) prep_q(q0);
+            const int64_t q0 = next_live_query(a, g_begin, g_end);
+            if (q0 >= 0) prep_q(q0, std::true_type{});
         }
         uint32_t tcount = 0, nseg = 0;
         bool stop = false;
-        float l_part[kHW], mref[kHW];
+        float l_part[kHW];
+        const float* mref = mref_s + h0;  // running reference of this warp's heads (valid once ref_set)
         for (int64_t g = g_begin; g < g_end && !stop;) {
             const int64_t qi = g / a.T;
             const int64_t seg_end = min(g_end, (qi + 1) * a.T);
@@ -616,11 +688,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int lt0 = (int)(g - qi * a.T), lt1 = (int)(seg_end - qi * a.T);
             const int lt_last = last_live(a, inf, lt0, lt1);
             if (tid == 0 && (inf.i + 1) / a.m > a.n_cap) atomicOr(a.status, CSA_DEV_BAD_POSITION);
-#pragma unroll
-            for (int h = 0; h < kHW; h++) {
-                l_part[h] = 0.f;
-                mref[h] = kNoRef;
+            {  // the next segment's q rows head for L2 while this one runs
+                const int64_t qn = next_live_query(a, seg_end, g_end);
+                if (qn >= 0) prefetch_l2(a.q + (qn * kH + sw * (kH / kSoftWarps) + (lane >> 3)) * kD + (lane & 7) * 64);
             }
+#pragma unroll
+            for (int h = 0; h < kHW; h++) l_part[h] = 0.f;
             int seg_tiles = 0;
             bool ref_set = false;  // mref_s holds this segment's reference
             for (int lt = lt0; lt <= lt_last; ++lt) {
@@ -661,10 +734,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::fence_after_sync();
                     tc::tmem_ld16(tmem + lane_off + kColS + 64 * b + h0, x);
                     tc::tmem_ld_wait();
+                    need = !ref_set;  // the first tile of a segment sets the reference
 #pragma unroll
                     for (int h = 0; h < kHW; h++) {
                         x[h] = fmaf(x[h], a.scale_log2, mask);
-                        need |= x[h] > mref[h] + kRescaleLog2;
+                        if (ref_set) need |= x[h] > mref[h] + kRescaleLog2;
                     }
                 }
                 // one barrier per tile: leave together on a failed wait, and
@@ -690,8 +764,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const bool resc = softmax_barrier_or(mine);
                     ref_set = true;
-#pragma unroll
-                    for (int h = 0; h < kHW; h++) mref[h] = mref_s[h0 + h];
                     if (resc) {
 #pragma unroll
                         for (int h = 0; h < kHW; h++) l_part[h] *= alph_s[h0 + h];
@@ -737,8 +809,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++tcount;
                 if (lt == lt_last) {
                     // every QK product of this segment is done: q' of the next one may go in
-                    const int64_t qn = next_live_query(seg_end);
-                    if (qn >= 0) prep_q(qn);
+                    const int64_t qn = next_live_query(a, seg_end, g_end);
+                    if (qn >= 0) prep_q(qn, std::false_type{});
                 }
             }
             if (stop) break;
@@ -818,6 +890,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_before_sync();
             softmax_barrier();  // red[], fac_s[], rot_cs[] are free again
             g = seg_end;
+        }
+    } else {
+        // ------------------------------------------------------------ gathers
+        // The gathered tiles (selected rows) are fetched with TMA gather4 by
+        // the producer warp and the gather warps together, each its own boxes
+        // of every row; the producer warp, which waits for every use of a
+        // stage in order, arms the stage's full barrier with the tile's bytes
+        // and hands it over through go[stage].
+        const int lw = warp - 2 - kSoftWarps;
+        uint32_t tcount = 0, ngo[kStages] = {0, 0};
+        for (int64_t g = g_begin; g < g_end; ++g) {
+            const int64_t qi = g / a.T;
+            const int lt = (int)(g - qi * a.T);
+            const QueryInfo inf = query_info(a, qi);
+            if (!tile_live(a, inf, lt)) continue;
+            const int st = tcount & 1;
+            ++tcount;
+            if (!is_gathered(a, lt)) continue;
+            int rows[4];  // read while the stage is still in use
+            gather_rows(a, qi, inf, lt, lane, rows);
+            if (!warp_wait(&go[st], (ngo[st]++) & 1u, abort_flag, a.status, lane)) break;
+            gather_boxes(&tm_sel, &full[st], sE + st * kStageBytes, rows, kProducerBoxes + lw * kLoaderBoxes,
+                         kLoaderBoxes, lane);
         }
     }
     // ---------------------------------------------------------------- teardown
@@ -935,6 +1030,7 @@ cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool spars
     a.topk_idx = sparse ? topk_idx : nullptr;
     a.k = g.k;
     a.pre = pl.tc_deq == 1 ? 1 : 0;
+    a.cache = reinterpret_cast<const uint8_t*>(cache);
     a.n_cap = n_cap;
     a.n_win = n_win;
     a.win_pos0 = win_pos0;
@@ -963,7 +1059,14 @@ cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool spars
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    attend_tc_kernel<<<pl.tc_grid, kThreads, kSmem, st>>>(tm_sel, tm_win, a);
+    CUtensorMap tm_q;
+    {
+        const uint64_t d[3] = {(uint64_t)kD, (uint64_t)kH, (uint64_t)Q};
+        const uint64_t sd[2] = {(uint64_t)kD * 2, (uint64_t)kH * kD * 2};
+        const uint32_t box[3] = {64, (uint32_t)kH, 1};
+        if (!make_tmap_bf16(&tm_q, q, 3, d, sd, box)) return cudaErrorInvalidValue;
+    }
+    attend_tc_kernel<<<pl.tc_grid, kThreads, kSmem, st>>>(tm_sel, tm_win, tm_q, a);
     note_launch();
     return cudaGetLastError();
 }
