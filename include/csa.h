@@ -139,9 +139,9 @@ csa_status csa_index_topk(const csa_params* p, const void* q_idx, const float* w
  * exactly as csa_index_topk does; it flags nothing.  It CONSUMES the score
  * matrix: when a query's blocks are selected in several chunks, the chunks'
  * candidates are written over the scores (copy them first to keep them).
- * Sizes whose selection does not fit in shared memory (k * n_cap / 8192 above
- * roughly 51200, e.g. k = 4096 with n_cap > ~100K) return CSA_ERR_UNSUPPORTED,
- * as csa_index_topk does. */
+ * Sizes whose selection does not fit in shared memory (k * ceil(n_cap / 32768)
+ * above 40960, e.g. k = 4096 with n_cap > 327680, or k above 8192) return
+ * CSA_ERR_UNSUPPORTED, as csa_index_topk does. */
 csa_status csa_index_score(const csa_params* p, const void* q_idx, const float* w_idx,
                            int32_t n_idx_heads, int32_t idx_dim, const void* keys, int64_t n_cap,
                            int32_t B, int32_t Q, const int64_t* q_pos, float* scores,

@@ -899,20 +899,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         // stage in order, arms the stage's full barrier with the tile's bytes
         // and hands it over through go[stage].
         const int lw = warp - 2 - kSoftWarps;
+        // Cursor over this CTA's gathered tiles; the indices of the next one
+        // are read while the current one waits for its stage.
         uint32_t tcount = 0, ngo[kStages] = {0, 0};
-        for (int64_t g = g_begin; g < g_end; ++g) {
-            const int64_t qi = g / a.T;
-            const int lt = (int)(g - qi * a.T);
-            const QueryInfo inf = query_info(a, qi);
-            if (!tile_live(a, inf, lt)) continue;
-            const int st = tcount & 1;
-            ++tcount;
-            if (!is_gathered(a, lt)) continue;
-            int rows[4];  // read while the stage is still in use
-            gather_rows(a, qi, inf, lt, lane, rows);
+        int64_t g = g_begin;
+        auto next_gathered = [&](int64_t& qi, int& lt, int& st) -> bool {
+            for (; g < g_end; ++g) {
+                qi = g / a.T;
+                lt = (int)(g - qi * a.T);
+                const QueryInfo inf = query_info(a, qi);
+                if (!tile_live(a, inf, lt)) continue;
+                st = tcount & 1;
+                ++tcount;
+                if (is_gathered(a, lt)) {
+                    ++g;
+                    return true;
+                }
+            }
+            return false;
+        };
+        int64_t qi = 0;
+        int lt = 0, st = 0;
+        int rows[4];
+        bool have = next_gathered(qi, lt, st);
+        if (have) gather_rows(a, qi, query_info(a, qi), lt, lane, rows);
+        while (have) {
+            int64_t qi_n = 0;
+            int lt_n = 0, st_n = 0;
+            int rows_n[4];
+            const bool have_n = next_gathered(qi_n, lt_n, st_n);
+            if (have_n) gather_rows(a, qi_n, query_info(a, qi_n), lt_n, lane, rows_n);
             if (!warp_wait(&go[st], (ngo[st]++) & 1u, abort_flag, a.status, lane)) break;
             gather_boxes(&tm_sel, &full[st], sE + st * kStageBytes, rows, kProducerBoxes + lw * kLoaderBoxes,
                          kLoaderBoxes, lane);
+            have = have_n;
+            qi = qi_n;
+            lt = lt_n;
+            st = st_n;
+#pragma unroll
+            for (int j = 0; j < 4; j++) rows[j] = rows_n[j];
         }
     }
     // ---------------------------------------------------------------- teardown

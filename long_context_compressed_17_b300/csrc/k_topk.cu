@@ -3,20 +3,25 @@
 // "DeepSeek-V4百万上下文时代的开源宣言" §三.2, CSA "Step 2": keep the top-K
 // compressed blocks per query; ties go to the lower block index, so the
 // order is the total order (score descending, index ascending).  Scores are
-// mapped to order-preserving 32-bit keys; a radix select (four 8-bit digits,
-// most significant first) over keys held in shared memory finds the k-th
-// largest key T; every block with key > T is kept, and of the blocks with
-// key == T the lowest indices fill the remaining slots.  The output lists the
-// kept blocks in ascending index order.
+// mapped to order-preserving 32-bit keys.  A radix select over keys held in
+// shared memory finds the k-th largest key T: the keys' common leading bits
+// are skipped (block min / max), then 11-bit digits are resolved from the
+// first differing bit down, each pass over the keys that still match the
+// resolved prefix (copied to a short candidate list once they fit).  Every
+// block with key > T is kept, and of the blocks with key == T the lowest
+// indices fill the remaining slots; the kept blocks are listed in ascending
+// index order by a warp-segmented compaction (ballots within a warp, one
+// exclusive scan over the warps).
 //
-// Two stages.  A query's n complete blocks are cut into max(1, n / C) chunks
-// of C scores, the last one taking the remainder (C <= size < 2C); one CTA
-// per (chunk, query) selects the chunk's own top k.  Because the order is
-// total, the query's top k is a subset of the union of the chunks' top k.
-// With a single chunk that selection is already the answer; otherwise each
-// chunk CTA writes its k candidates (keys, then indices, in index order) over
-// the start of its own chunk of the score row (C >= 2k, so they fit) -- the
-// scores are consumed -- and one CTA per query selects the final k.
+// Two stages.  A query's n complete blocks are cut into ceil(n / C) chunks
+// of equal size (up to one), each of at least C / 2 >= 2k scores; one CTA per
+// (chunk, query) selects the chunk's own top k.  Because the order is total,
+// the query's top k is a subset of the union of the chunks' top k.  With a
+// single chunk that selection is already the answer; otherwise each chunk CTA
+// writes its k candidates (keys, then indices, in index order) over the
+// start of its own chunk of the score row -- the scores are consumed -- and
+// one CTA per query selects the final k from the concatenated candidates
+// (still in ascending index order).
 #include "common.cuh"
 #include "internal.h"
 
@@ -24,11 +29,13 @@ namespace csa {
 
 namespace {
 
-constexpr int kChunkThreads = 512;
-constexpr int kMergeThreads = 1024;
-constexpr int kMaxSingle = 32768;       // one chunk per query up to this many blocks (128 KiB of keys)
-constexpr int kMinChunk = 8192;         // C when queries are split
-constexpr int kMaxChunk = 16384;        // largest C (a chunk holds < 2C keys)
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+constexpr int kDigitBits = 11;
+constexpr int kBins = 1 << kDigitBits;  // two bins per thread in the digit search
+constexpr int kChunk = 32768;           // C: most scores one CTA holds (128 KiB of keys)
+constexpr int kCandCap = 4096;          // a digit's keys are copied out once this few
+constexpr int kMergeKeys = 40960;       // most candidates one merge CTA holds (160 KiB)
 
 // Order-preserving key of a float score (both zeros share one key).
 __device__ __forceinline__ uint32_t score_key(float f) {
@@ -41,31 +48,40 @@ __device__ __forceinline__ float key_score(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
 }
 
-// Exclusive scan over the CTA; returns the prefix, writes the total.
-// `sw` holds 32 ints of shared scratch.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* sw, int* total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+// Shared scratch of one selection (besides the keys).
+struct Scratch {
+    int hist[kBins];
+    uint32_t cand[kCandCap];
+    uint32_t red[2][kWarps];
+    int wcnt[2][kWarps];
+    int scan[kWarps];
+    int n_cand;
+    int digit, above;
+};
+
+// Exclusive scan of one int per thread over the CTA; returns the prefix.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* sw) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, x, o);
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
-    __syncthreads();
     if (lane == 31) sw[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int w = lane < nw ? sw[lane] : 0;
+        int w = sw[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int y = __shfl_up_sync(0xffffffffu, w, o);
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o) w += y;
         }
         sw[lane] = w;  // inclusive per-warp totals
     }
     __syncthreads();
     const int before = (warp > 0 ? sw[warp - 1] : 0) + x - v;
-    *total = sw[nw - 1];
+    __syncthreads();  // sw is free for the next scan
     return before;
 }
 
@@ -74,72 +90,161 @@ struct Select {
     int take_eq;  // how many keys equal to T are kept (the lowest indices)
 };
 
-// Radix select of the k-th largest of keys[0, n) (shared memory), 0 < k < n.
-__device__ Select block_radix_select(const uint32_t* keys, int n, int k, int* hist, uint32_t* s_digit,
-                                     int* s_above) {
-    uint32_t prefix = 0, mask = 0;
-    int remaining = k;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
-        __syncthreads();
-        for (int i = threadIdx.x; i < n; i += blockDim.x) {
-            const uint32_t u = keys[i];
-            if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1);
-        }
-        __syncthreads();
-        if (threadIdx.x < 32) {
-            // lane l owns digits 8l .. 8l+7; suffix sums from the top digit down
-            const int l = threadIdx.x;
-            int c[8], loc = 0;
-#pragma unroll
-            for (int e = 0; e < 8; e++) {
-                c[e] = hist[8 * l + e];
-                loc += c[e];
-            }
-            int suf = loc;  // inclusive suffix over lanes >= l
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                int y = __shfl_down_sync(0xffffffffu, suf, o);
-                if (l + o < 32) suf += y;
-            }
-            int above = suf - loc;  // keys with a digit in higher lanes
-#pragma unroll
-            for (int e = 7; e >= 0; e--) {
-                if (above < remaining && above + c[e] >= remaining) {
-                    *s_digit = (uint32_t)(8 * l + e);
-                    *s_above = above;
-                }
-                above += c[e];
-            }
-        }
-        __syncthreads();
-        prefix |= *s_digit << shift;
-        mask |= 255u << shift;
-        remaining -= *s_above;
-        __syncthreads();
+// Radix select of the k-th largest of keys[0, n) (shared memory), 0 < k <= n.
+__device__ Select radix_select(const uint32_t* keys, int n, int k, Scratch& s) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // the bits all keys share are skipped
+    uint32_t lo = 0xffffffffu, hi = 0u;
+    for (int i = tid; i < n; i += kThreads) {
+        const uint32_t u = keys[i];
+        lo = min(lo, u);
+        hi = max(hi, u);
     }
-    return Select{prefix, remaining};
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (lane == 0) {
+        s.red[0][warp] = lo;
+        s.red[1][warp] = hi;
+    }
+    __syncthreads();
+    lo = s.red[0][lane];
+    hi = s.red[1][lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (lo == hi) return Select{hi, k};
+    int top = 31 - __clz(lo ^ hi);  // highest bit in which keys differ
+    uint32_t prefix = top == 31 ? 0u : (hi & ~((2u << top) - 1u));
+    int remaining = k;
+    const uint32_t* src = keys;  // the keys matching the prefix are among src[0, m)
+    int m = n;
+    for (;;) {
+        const int shift = top >= kDigitBits - 1 ? top - (kDigitBits - 1) : 0;
+        const uint32_t himask = top == 31 ? 0u : ~((2u << top) - 1u);
+        for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0;
+        __syncthreads();
+        for (int i = tid; i < m; i += kThreads) {
+            const uint32_t u = src[i];
+            if ((u & himask) == prefix) atomicAdd(&s.hist[(u >> shift) & (kBins - 1)], 1);
+        }
+        __syncthreads();
+        // the digit d with (keys above d) < remaining <= (keys at or above d):
+        // thread t holds bins 2047-2t and 2046-2t, counted from the top bin
+        const int b0 = kBins - 1 - 2 * tid, b1 = b0 - 1;
+        const int c0 = s.hist[b0], c1 = s.hist[b1];
+        const int before = block_exclusive_scan(c0 + c1, s.scan);
+        if (before < remaining && before + c0 >= remaining) {
+            s.digit = b0;
+            s.above = before;
+        } else if (before + c0 < remaining && before + c0 + c1 >= remaining) {
+            s.digit = b1;
+            s.above = before + c0;
+        }
+        __syncthreads();
+        const int d = s.digit, cnt = s.hist[d];
+        remaining -= s.above;
+        prefix |= (uint32_t)d << shift;
+        if (shift == 0) return Select{prefix, remaining};
+        top = shift - 1;
+        if (cnt <= kCandCap && src != s.cand) {
+            // the keys of digit d go to the candidate list (their order is irrelevant)
+            if (tid == 0) s.n_cand = 0;
+            __syncthreads();
+            const uint32_t newmask = ~((2u << top) - 1u);
+            for (int i0 = 0; i0 < m; i0 += kThreads) {
+                const int i = i0 + tid;
+                const uint32_t u = i < m ? src[i] : 0u;
+                const bool hit = i < m && (u & newmask) == prefix;
+                const uint32_t bal = __ballot_sync(0xffffffffu, hit);
+                int base = 0;
+                if (lane == 0 && bal) base = atomicAdd(&s.n_cand, __popc(bal));
+                base = __shfl_sync(0xffffffffu, base, 0);
+                if (hit) s.cand[base + __popc(bal & ((1u << lane) - 1u))] = u;
+            }
+            __syncthreads();
+            src = s.cand;
+            m = s.n_cand;
+        }
+        __syncthreads();  // digit, above and hist are rewritten by the next pass
+    }
 }
 
 // Keep the top `k` of keys[0, n) in index order: calls emit(pos, i) for the
-// kept entries with pos = 0 .. k-1 ascending in i.  The keys are swept in
-// block-wide rounds (thread t reads entry r + t: no bank conflicts); one scan
-// of the packed (greater, equal) counts per round places every kept entry.
+// kept entries with pos = 0 .. k-1 ascending in i.  Warp w sweeps the
+// contiguous range [w*seg, (w+1)*seg) twice: once to count, once to place.
 template <class Emit>
-__device__ void block_compact(const uint32_t* keys, int n, Select sel, int* sw, Emit emit) {
-    int base = 0, eq_left = sel.take_eq;
-    for (int r0 = 0; r0 < n; r0 += blockDim.x) {
-        const int i = r0 + threadIdx.x;
-        const uint32_t u = i < n ? keys[i] : 0u;
-        const int gt = (i < n && u > sel.T) ? 1 : 0;
-        const int eq = (i < n && u == sel.T) ? 1 : 0;
-        int tot;
-        const int before = block_exclusive_scan(gt | (eq << 16), sw, &tot);
-        const int gt_before = before & 0xffff, eq_before = before >> 16;
-        if (gt || (eq && eq_before < eq_left)) emit(base + gt_before + min(eq_before, eq_left), i);
-        const int eq_tot = tot >> 16;
-        base += (tot & 0xffff) + min(eq_tot, eq_left);
-        eq_left -= min(eq_tot, eq_left);
+__device__ void block_compact(const uint32_t* keys, int n, Select sel, Scratch& s, Emit emit) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int seg = ((n + kWarps - 1) / kWarps + 31) & ~31;
+    const int i0 = warp * seg, i1 = min(n, i0 + seg);
+    int gt = 0, eq = 0;
+    for (int r = i0; r < i1; r += 32) {
+        const int i = r + lane;
+        const uint32_t u = i < i1 ? keys[i] : 0u;
+        gt += __popc(__ballot_sync(0xffffffffu, i < i1 && u > sel.T));
+        eq += __popc(__ballot_sync(0xffffffffu, i < i1 && u == sel.T));
+    }
+    if (lane == 0) {
+        s.wcnt[0][warp] = gt;
+        s.wcnt[1][warp] = eq;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int g0 = s.wcnt[0][lane], e0 = s.wcnt[1][lane];
+        int g = g0, e = e0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int yg = __shfl_up_sync(0xffffffffu, g, o), ye = __shfl_up_sync(0xffffffffu, e, o);
+            if (lane >= o) {
+                g += yg;
+                e += ye;
+            }
+        }
+        s.wcnt[0][lane] = g - g0;  // exclusive
+        s.wcnt[1][lane] = e - e0;
+    }
+    __syncthreads();
+    int gt_base = s.wcnt[0][warp], eq_base = s.wcnt[1][warp];
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int r = i0; r < i1; r += 32) {
+        const int i = r + lane;
+        const uint32_t u = i < i1 ? keys[i] : 0u;
+        const bool is_gt = i < i1 && u > sel.T, is_eq = i < i1 && u == sel.T;
+        const uint32_t bg = __ballot_sync(0xffffffffu, is_gt), be = __ballot_sync(0xffffffffu, is_eq);
+        const int g_before = gt_base + __popc(bg & lt_mask), e_before = eq_base + __popc(be & lt_mask);
+        if (is_gt || (is_eq && e_before < sel.take_eq)) emit(g_before + min(e_before, sel.take_eq), i);
+        gt_base += __popc(bg);
+        eq_base += __popc(be);
+    }
+}
+
+// keys[i] = score_key(src[i]) for i < n: 16-byte loads (every one issued
+// before any is used) when src is 16-byte aligned, else 4-byte loads.
+__device__ __forceinline__ void load_keys(const float* src, int n, uint32_t* keys) {
+    if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+        const float4* v = reinterpret_cast<const float4*>(src);
+        uint4* kv = reinterpret_cast<uint4*>(keys);
+        const int n4 = n / 4;
+        for (int j0 = threadIdx.x; j0 < n4; j0 += 8 * kThreads) {
+            float4 f[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++)
+                if (j0 + u * kThreads < n4) f[u] = __ldg(v + j0 + u * kThreads);
+#pragma unroll
+            for (int u = 0; u < 8; u++)
+                if (j0 + u * kThreads < n4)
+                    kv[j0 + u * kThreads] = make_uint4(score_key(f[u].x), score_key(f[u].y), score_key(f[u].z),
+                                                       score_key(f[u].w));
+        }
+        for (int i = 4 * n4 + threadIdx.x; i < n; i += kThreads) keys[i] = score_key(src[i]);
+    } else {
+#pragma unroll 8
+        for (int i = threadIdx.x; i < n; i += kThreads) keys[i] = score_key(src[i]);
     }
 }
 
@@ -149,120 +254,106 @@ __device__ __forceinline__ int64_t n_complete(const int64_t* q_pos, int64_t q, i
     return n < 0 ? 0 : n;
 }
 
-__device__ __forceinline__ int64_t n_chunks(int64_t n, int chunk) {
-    const int64_t c = n / chunk;
-    return c > 1 ? c : 1;
-}
+__device__ __forceinline__ int64_t n_chunks(int64_t n) { return n > kChunk ? (n + kChunk - 1) / kChunk : 1; }
+
+// Chunk c of nch over n blocks: [c*n/nch, (c+1)*n/nch).
+__device__ __forceinline__ int64_t chunk_lo(int64_t c, int64_t n, int64_t nch) { return c * n / nch; }
 
 // Stage 1: grid (max chunks, Q).  Writes the final selection when the query
-// has one chunk, its candidates otherwise.
-__global__ void __launch_bounds__(kChunkThreads)
+// has one chunk, its candidates otherwise.  Two CTAs fit an SM when a chunk
+// holds at most ~25K scores (one CTA's selection passes overlap the other's
+// loads).
+__global__ void __launch_bounds__(kThreads, 2)
     topk_chunk_kernel(float* __restrict__ scores, int64_t ld, int64_t n_cap,
-                      const int64_t* __restrict__ q_pos, int m, int k, int chunk,
+                      const int64_t* __restrict__ q_pos, int m, int k,
                       int32_t* __restrict__ idx, float* __restrict__ sel) {
-    extern __shared__ uint32_t keys[];  // [< 2 * chunk] (or the whole row)
-    __shared__ int hist[256];
-    __shared__ int sw[32];
-    __shared__ uint32_t s_digit;
-    __shared__ int s_above;
+    extern __shared__ uint32_t keys[];  // [<= kChunk]
+    __shared__ Scratch s;
     const int64_t q = blockIdx.y;
     const int64_t n = n_complete(q_pos, q, m, n_cap);
-    const int64_t nch = n_chunks(n, chunk);
+    const int64_t nch = n_chunks(n);
     if ((int64_t)blockIdx.x >= nch) return;
     float* row = scores + q * ld;
+    const int64_t lo = chunk_lo(blockIdx.x, n, nch);
+    const int nc = (int)(chunk_lo(blockIdx.x + 1, n, nch) - lo);
     if (nch == 1) {
         // a single chunk: this CTA writes the answer
         int32_t* oi = idx + q * k;
         float* os = sel ? sel + q * k : nullptr;
-        const int nc = (int)n;
         if (nc <= k) {
-            for (int j = threadIdx.x; j < k; j += blockDim.x) {
+            for (int j = threadIdx.x; j < k; j += kThreads) {
                 oi[j] = j < nc ? j : -1;
                 if (os) os[j] = j < nc ? row[j] : -INFINITY;
             }
             return;
         }
-        for (int i = threadIdx.x; i < nc; i += blockDim.x) keys[i] = score_key(row[i]);
+        load_keys(row, nc, keys);
         __syncthreads();
-        const Select s = block_radix_select(keys, nc, k, hist, &s_digit, &s_above);
-        block_compact(keys, nc, s, sw, [&](int pos, int i) {
+        const Select t = radix_select(keys, nc, k, s);
+        block_compact(keys, nc, t, s, [&](int pos, int i) {
             oi[pos] = i;
             if (os) os[pos] = key_score(keys[i]);
         });
         return;
     }
-    const int64_t lo = (int64_t)blockIdx.x * chunk;
-    const int nc = (int)((int64_t)blockIdx.x == nch - 1 ? n - lo : chunk);  // chunk <= nc < 2 chunk
-    for (int i = threadIdx.x; i < nc; i += blockDim.x) keys[i] = score_key(row[lo + i]);
+    load_keys(row + lo, nc, keys);
     __syncthreads();  // the chunk is in smem: its region of the row may be overwritten
     uint32_t* ck = reinterpret_cast<uint32_t*>(row + lo);      // [k] candidate keys
     int32_t* cidx = reinterpret_cast<int32_t*>(row + lo + k);  // [k] candidate indices
-    const Select s = block_radix_select(keys, nc, k, hist, &s_digit, &s_above);
-    block_compact(keys, nc, s, sw, [&](int pos, int i) {
+    const Select t = radix_select(keys, nc, k, s);
+    block_compact(keys, nc, t, s, [&](int pos, int i) {
         ck[pos] = keys[i];
         cidx[pos] = (int32_t)(lo + i);
     });
 }
 
 // Stage 2: one CTA per query with more than one chunk; chunk c's k
-// candidates sit at row[c*chunk ..]: k keys, then k indices.
-__global__ void __launch_bounds__(kMergeThreads)
+// candidates sit at the start of its range of the row: k keys, then k
+// indices.
+__global__ void __launch_bounds__(kThreads, 1)
     topk_merge_kernel(const float* __restrict__ scores, int64_t ld, int64_t n_cap,
-                      const int64_t* __restrict__ q_pos, int m, int k, int chunk,
+                      const int64_t* __restrict__ q_pos, int m, int k,
                       int32_t* __restrict__ idx, float* __restrict__ sel) {
     extern __shared__ uint32_t keys[];  // [nchunks * k]
-    __shared__ int hist[256];
-    __shared__ int sw[32];
-    __shared__ uint32_t s_digit;
-    __shared__ int s_above;
+    __shared__ Scratch s;
     const int64_t q = blockIdx.x;
     const int64_t n = n_complete(q_pos, q, m, n_cap);
-    const int64_t nch = n_chunks(n, chunk);
+    const int64_t nch = n_chunks(n);
     if (nch <= 1) return;
     const float* row = scores + q * ld;
     const int C = (int)(nch * k);
-    for (int i = threadIdx.x; i < C; i += blockDim.x)
-        keys[i] = reinterpret_cast<const uint32_t*>(row + (int64_t)(i / k) * chunk)[i % k];
+    for (int i = threadIdx.x; i < C; i += kThreads)
+        keys[i] = reinterpret_cast<const uint32_t*>(row + chunk_lo(i / k, n, nch))[i % k];
     __syncthreads();
     int32_t* oi = idx + q * k;
     float* os = sel ? sel + q * k : nullptr;
-    const Select s = block_radix_select(keys, C, k, hist, &s_digit, &s_above);
-    block_compact(keys, C, s, sw, [&](int pos, int i) {
-        oi[pos] = reinterpret_cast<const int32_t*>(row + (int64_t)(i / k) * chunk + k)[i % k];
+    const Select t = radix_select(keys, C, k, s);
+    block_compact(keys, C, t, s, [&](int pos, int i) {
+        oi[pos] = reinterpret_cast<const int32_t*>(row + chunk_lo(i / k, n, nch) + k)[i % k];
         if (os) os[pos] = key_score(keys[i]);
     });
 }
 
 }  // namespace
 
-// Chunk size C for n_cap blocks and Q queries, or 0 when the selection does
-// not fit in shared memory.
+// Chunk size for n_cap blocks, or 0 when the selection does not fit in
+// shared memory (the merge holds ceil(n_cap / C) * k keys) or a chunk could
+// not hold its k candidates twice over.
 int64_t topk_chunk(int64_t n_cap, int Q, int k) {
-    const int64_t sms = num_sms();
-    if (n_cap <= kMaxSingle && ((int64_t)Q >= 2 * sms || n_cap < 2 * kMinChunk))
-        return n_cap > 0 ? n_cap : 1;  // one chunk per query
-    int64_t chunk = kMinChunk;
-    while (chunk < kMaxChunk && (int64_t)Q * (n_cap / chunk) > 4 * sms) chunk *= 2;
-    while (chunk < 2 * (int64_t)k) chunk *= 2;
-    // the merge holds max(1, n_cap / C) * k keys in shared memory
-    while ((n_cap / chunk) * (int64_t)k * 4 > 200 * 1024 && chunk <= kMaxChunk) chunk *= 2;
-    if (chunk > kMaxChunk) return 0;
-    return chunk;
-}
-
-size_t topk_chunk_smem(int64_t n_cap, int64_t chunk) {
-    const int64_t keys = chunk >= n_cap ? n_cap : 2 * chunk - 1;
-    return (size_t)(keys > 0 ? keys : 1) * sizeof(uint32_t);
+    (void)Q;
+    if (n_cap <= kChunk) return n_cap > 0 ? n_cap : 1;  // one chunk per query
+    const int64_t nch = (n_cap + kChunk - 1) / kChunk;
+    if (nch * (int64_t)k > kMergeKeys || 2 * (int64_t)k > kChunk / 2) return 0;
+    return kChunk;
 }
 
 cudaError_t launch_topk(const Geometry& g, float* scores, int64_t ld, int64_t n_cap, int Q,
                         const int64_t* q_pos, int32_t* idx, float* sel, cudaStream_t st) {
     if (Q == 0) return cudaSuccess;
     const int k = g.k;
-    const int64_t chunk = topk_chunk(n_cap, Q, k);
-    if (chunk == 0) return cudaErrorInvalidValue;  // rejected earlier by the C ABI
-    const int64_t max_chunks = n_cap / chunk > 1 ? n_cap / chunk : 1;
-    const size_t smem1 = topk_chunk_smem(n_cap, chunk);
+    if (topk_chunk(n_cap, Q, k) == 0) return cudaErrorInvalidValue;  // rejected earlier by the C ABI
+    const int64_t max_chunks = n_cap > kChunk ? (n_cap + kChunk - 1) / kChunk : 1;
+    const size_t smem1 = (size_t)(n_cap < kChunk ? (n_cap > 0 ? n_cap : 1) : kChunk) * sizeof(uint32_t);
     static int attr1 = 0;
     if ((int)smem1 > attr1) {
         cudaError_t e = cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -271,7 +362,7 @@ cudaError_t launch_topk(const Geometry& g, float* scores, int64_t ld, int64_t n_
         attr1 = (int)smem1;
     }
     dim3 grid1((unsigned)max_chunks, (unsigned)Q);
-    topk_chunk_kernel<<<grid1, kChunkThreads, smem1, st>>>(scores, ld, n_cap, q_pos, g.m, k, (int)chunk, idx, sel);
+    topk_chunk_kernel<<<grid1, kThreads, smem1, st>>>(scores, ld, n_cap, q_pos, g.m, k, idx, sel);
     note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || max_chunks <= 1) return e;
@@ -282,7 +373,7 @@ cudaError_t launch_topk(const Geometry& g, float* scores, int64_t ld, int64_t n_
         if (e != cudaSuccess) return e;
         attr2 = (int)smem2;
     }
-    topk_merge_kernel<<<(unsigned)Q, kMergeThreads, smem2, st>>>(scores, ld, n_cap, q_pos, g.m, k, (int)chunk, idx, sel);
+    topk_merge_kernel<<<(unsigned)Q, kThreads, smem2, st>>>(scores, ld, n_cap, q_pos, g.m, k, idx, sel);
     note_launch();
     return cudaGetLastError();
 }

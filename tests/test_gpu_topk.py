@@ -73,3 +73,21 @@ def test_topk_one_million_blocks(L):
     rng = np.random.default_rng(7)
     n_av = [262144, 200000]
     _check(L, _scores(rng, 2, 262144, n_av), n_av, 4, 1024)
+
+
+def test_topk_continuous_scores_at_the_chunk_boundary(L):
+    """Distinct float scores; 32768 blocks fit one chunk, 32769 need two."""
+    rng = np.random.default_rng(8)
+    n_av = [32768, 32769, 32767]
+    s = (rng.standard_normal((3, 32769)) * 30 + 150).astype(np.float32)
+    for q in range(3):
+        s[q, n_av[q]:] = -np.inf
+    _check(L, s, n_av, 4, 1024)
+
+
+def test_topk_all_scores_equal(L):
+    """One distinct key: the lowest indices are kept."""
+    n_av = [5000, 70000]
+    s = np.full((2, 70000), 2.5, dtype=np.float32)
+    s[0, 5000:] = -np.inf
+    _check(L, s, n_av, 4, 1024)
