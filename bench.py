@@ -47,9 +47,13 @@ L2_FLUSH_BYTES = 512 << 20
 # captured build (sha256 prefix of the listed files); otherwise it is null.
 CAPTURED_TRAFFIC = {
     "csa_decode_bf16_b32_128k": (
-        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "95b89d51d9694302", 275556864),
+        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "c428605f4ea16fec", 274547200),
+    "csa_decode_fp8cache_b8_1m": (
+        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "c428605f4ea16fec", 546795776),
+    "csa_chunked_prefill_bf16_64k_8k": (
+        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "c428605f4ea16fec", 698945024),
     "hca_decode_bf16_b32_1m": (
-        ["k_attend_tc.cu", "tc_util.cuh", "common.cuh"], "5da83674cc972ab4", 287542784),
+        ["k_attend_tc.cu", "tc_util.cuh", "common.cuh"], "a42fd4ffbc28e7f9", 288056064),
 }
 
 

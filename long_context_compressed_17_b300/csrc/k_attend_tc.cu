@@ -7,33 +7,36 @@
 // last W raw tokens, a learnable sink in the softmax denominator, RoPE at -i
 // on the output.
 //
-// One query's row list is cut into tiles of 128 rows: ceil(k/128) tiles of
-// selected blocks (CSA, gathered row by row with TMA gather4) or
-// ceil(n_cap/128) tiles of consecutive blocks (HCA, TMA tiles), then
-// ceil(W/128) window tiles.  The (query, tile) pairs are dealt out in
+// One query's row list is cut into tiles of 64 rows: ceil(k/64) tiles of
+// selected blocks (CSA) or ceil(n_cap/64) tiles of consecutive blocks (HCA),
+// then ceil(W/64) window tiles.  The (query, tile) pairs are dealt out in
 // contiguous, balanced ranges to one persistent CTA per SM; the run of one
 // query's tiles inside a CTA is a segment.  A segment that is the whole query
 // is finished in place (sink, normalisation, rotation, bf16 store); the others
 // leave an unnormalised partial (m, l, o) for attend_combine_kernel.
 //
 // Per tile (one shared KV head, so key = value = row e_j):
-//   S^T[128 rows, 64 heads] = E[128, 512] . Q'^T        (swap-AB: rows are M)
+//   S^T[64 rows, 64 heads] = E[64, 512] . Q'^T          (swap-AB: rows are M)
 //   P = 2^(S^T * scale * log2 e - m)  (bf16, per head running reference m)
-//   O^T[512, 64] += E^T[512, 128] . P^T                  (4 MMAs of M = 128)
-// Every MMA is M = 128 x N = 64: at N = 64 an MMA costs the same ~50 cycles
-// for M = 64 and M = 128, so the rows, not the heads, fill M.  The tile (4
-// slices of 128 rows x 128 dims, 128-byte swizzle) is the K-major A operand of
-// the first product and, read along its rows, the MN-major A operand of the
-// second; each slice is refilled with the next tile as soon as its PV product
-// is done, so the next loads overlap the PV products and the QK product of a
-// tile starts on its first slice.
-// The running reference m is raised only when a logit exceeds it by more than
-// 2^8; O^T (in TMEM) and the partial sums are then rescaled in place.
+//   O^T[512, 64] += E^T[512, 64] . P^T                   (4 MMAs of M = 128)
+// The tile (8 boxes of 64 rows x 64 dims, 128-byte swizzle) is the K-major A
+// operand of the first product and, read along its rows, the MN-major A
+// operand of the second.  Two tile stages alternate; S^T and P are double
+// buffered, so the QK product of the next tile runs while the softmax of this
+// one does.  The running reference m is raised only when a logit exceeds it
+// by more than 2^8; O^T (in TMEM) and the partial sums are then rescaled in
+// place.
 //
-// Warp roles: warp 0 loads (TMA), warp 1 issues MMAs, warps 2..9 normalise
-// and rotate q, run the softmax and the epilogue.  Every wait is bounded; on
-// a timeout the kernel sets CSA_DEV_TIMEOUT, every role leaves its loop,
-// outstanding copies and MMAs are waited for and TMEM is freed.
+// Warp roles (20 warps): warp 0 orders every use of a stage, loads TMA tiles
+// (consecutive rows) and hands gathered tiles to warps 18..19, which fetch the
+// selected rows with TMA gather4 (two warps issue them twice as fast as one);
+// warp 1 issues the MMAs in a dynamic order (PV of a tile as soon as its P is
+// written, QK of the next as soon as its stage has landed); warps 2..17
+// prepare q', run the softmax and the epilogue.  FP8 rows are first
+// dequantised to bf16 in the workspace (dequant_gather_kernel or
+// dequant_rows_kernel).  Every wait is bounded; on a timeout the kernel sets
+// CSA_DEV_TIMEOUT, every role leaves its loop, outstanding copies and MMAs are
+// waited for and TMEM is freed.
 #include <math.h>
 
 #include <type_traits>
