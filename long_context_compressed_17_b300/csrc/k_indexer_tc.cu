@@ -12,8 +12,10 @@
 // reuses every key tile for four queries per MMA.
 //
 // Persistent CTAs walk a contiguous range of (query group, key tile) units.
-// Warp 0 issues TMA loads, warp 1 issues the MMAs, warps 2..5 are the
-// epilogue.  Every wait is bounded: on a timeout the kernel flags
+// Warp 0 issues TMA loads, warp 1 issues the MMAs, the other warps are the
+// epilogue: four (one per TMEM lane quarter) for NQ = 1, sixteen for NQ = 4,
+// where four warps share a quarter and take one of the four queries each (the
+// epilogue, 256 values per key, would otherwise hold the tensor pipe back).  Every wait is bounded: on a timeout the kernel flags
 // CSA_DEV_TIMEOUT, all roles leave their loops and TMEM is freed.
 #include "common.cuh"
 #include "internal.h"
@@ -31,13 +33,15 @@ constexpr int kDI = 128;           // indexer dim
 constexpr int kTileKeys = 128;     // MMA M
 constexpr int kStages = 4;
 constexpr uint32_t kStageBytes = kTileKeys * kDI * 2;   // 32 KiB: two 64-dim boxes
-constexpr int kThreads = 192;
 
 template <int NQ>
 struct Cfg {
     static constexpr int N = NQ * kHI;                  // MMA N
     static constexpr int kAcc = NQ == 1 ? 4 : 2;        // TMEM accumulators in flight
     static constexpr int kQBufs = NQ == 1 ? 2 : 1;
+    static constexpr int kEpiWarps = NQ == 1 ? 4 : 16;
+    static constexpr int kQPerWarp = NQ * 4 / kEpiWarps;  // queries of a key per epilogue warp
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
     static constexpr uint32_t kQBytes = (uint32_t)N * kDI * 2;
     static constexpr uint32_t kTmemCols = kAcc * N;     // 256 or 512
     static constexpr size_t kBarBytes = 256;
@@ -72,7 +76,7 @@ __device__ __forceinline__ int64_t group_avail(const IdxArgs& a, int64_t g) {
 }  // namespace
 
 template <int NQ>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                       const __grid_constant__ CUtensorMap tm_q, IdxArgs a) {
     using C = Cfg<NQ>;
@@ -101,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int c = 0; c < C::kAcc; c++) {
             tc::mbar_init(&tfull[c], 1);
-            tc::mbar_init(&tempty[c], 4);  // one arrival per epilogue warp
+            tc::mbar_init(&tempty[c], C::kEpiWarps);  // one arrival per epilogue warp
         }
         *abort_flag = 0;
         tc::fence_barrier_init();
@@ -208,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ epilogue: one key per thread
         const int quarter = warp & 3;          // TMEM lanes this warp may read
         const int row = quarter * 32 + lane;   // key within the tile
+        const int q0 = ((warp - 2) >> 2) * C::kQPerWarp;  // this warp's queries: q0 .. q0 + kQPerWarp - 1
         int acc = 0;
         uint32_t aphase = 0;
         int64_t cur_g = -1, gnav = 0;
@@ -228,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if ((int64_t)t * kTileKeys >= gnav) {  // nothing complete in this tile
                 if (key < a.n_cap)
 #pragma unroll
-                    for (int qq = 0; qq < NQ; qq++) a.scores[(g * NQ + qq) * a.ld + key] = -INFINITY;
+                    for (int qq = q0; qq < q0 + C::kQPerWarp; qq++) a.scores[(g * NQ + qq) * a.ld + key] = -INFINITY;
                 continue;
             }
             // one lane waits, the whole warp follows its verdict (tcgen05.ld is warp-wide)
@@ -239,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_after_sync();
             const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::N);
 #pragma unroll
-            for (int qq = 0; qq < NQ; qq++) {
+            for (int qq = q0; qq < q0 + C::kQPerWarp; qq++) {
                 const float4* w4 = reinterpret_cast<const float4*>(a.w_idx + (g * NQ + qq) * kHI);
                 float s = 0.f;
 #pragma unroll
@@ -317,7 +322,7 @@ cudaError_t launch_indexer_tc(const Geometry& g, const void* q_idx, const float*
             if (e != cudaSuccess) return e;
             attr = true;
         }
-        indexer_tc_kernel<1><<<grid, kThreads, Cfg<1>::kSmem, st>>>(tm_keys, tm_q, a);
+        indexer_tc_kernel<1><<<grid, Cfg<1>::kThreads, Cfg<1>::kSmem, st>>>(tm_keys, tm_q, a);
     } else {
         static bool attr = false;
         if (!attr) {
@@ -326,7 +331,7 @@ cudaError_t launch_indexer_tc(const Geometry& g, const void* q_idx, const float*
             if (e != cudaSuccess) return e;
             attr = true;
         }
-        indexer_tc_kernel<4><<<grid, kThreads, Cfg<4>::kSmem, st>>>(tm_keys, tm_q, a);
+        indexer_tc_kernel<4><<<grid, Cfg<4>::kThreads, Cfg<4>::kSmem, st>>>(tm_keys, tm_q, a);
     }
     note_launch();
     *launched = true;
