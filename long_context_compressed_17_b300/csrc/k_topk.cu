@@ -90,16 +90,9 @@ struct Select {
     int take_eq;  // how many keys equal to T are kept (the lowest indices)
 };
 
-// Radix select of the k-th largest of keys[0, n) (shared memory), 0 < k <= n.
-__device__ Select radix_select(const uint32_t* keys, int n, int k, Scratch& s) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // the bits all keys share are skipped
-    uint32_t lo = 0xffffffffu, hi = 0u;
-    for (int i = tid; i < n; i += kThreads) {
-        const uint32_t u = keys[i];
-        lo = min(lo, u);
-        hi = max(hi, u);
-    }
+// Each thread's smallest / largest key -> the CTA's (every thread).
+__device__ __forceinline__ void block_minmax(uint32_t& lo, uint32_t& hi, Scratch& s) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
@@ -117,6 +110,12 @@ __device__ Select radix_select(const uint32_t* keys, int n, int k, Scratch& s) {
         lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
         hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
     }
+}
+
+// Radix select of the k-th largest of keys[0, n) (shared memory), 0 < k <= n,
+// given the smallest and largest key (the bits all keys share are skipped).
+__device__ Select radix_select(const uint32_t* keys, int n, int k, uint32_t lo, uint32_t hi, Scratch& s) {
+    const int tid = threadIdx.x, lane = tid & 31;
     if (lo == hi) return Select{hi, k};
     int top = 31 - __clz(lo ^ hi);  // highest bit in which keys differ
     uint32_t prefix = top == 31 ? 0u : (hi & ~((2u << top) - 1u));
@@ -128,6 +127,7 @@ __device__ Select radix_select(const uint32_t* keys, int n, int k, Scratch& s) {
         const uint32_t himask = top == 31 ? 0u : ~((2u << top) - 1u);
         for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0;
         __syncthreads();
+#pragma unroll 4
         for (int i = tid; i < m; i += kThreads) {
             const uint32_t u = src[i];
             if ((u & himask) == prefix) atomicAdd(&s.hist[(u >> shift) & (kBins - 1)], 1);
@@ -156,6 +156,7 @@ __device__ Select radix_select(const uint32_t* keys, int n, int k, Scratch& s) {
             if (tid == 0) s.n_cand = 0;
             __syncthreads();
             const uint32_t newmask = ~((2u << top) - 1u);
+#pragma unroll 4
             for (int i0 = 0; i0 < m; i0 += kThreads) {
                 const int i = i0 + tid;
                 const uint32_t u = i < m ? src[i] : 0u;
@@ -183,6 +184,7 @@ __device__ void block_compact(const uint32_t* keys, int n, Select sel, Scratch& 
     const int seg = ((n + kWarps - 1) / kWarps + 31) & ~31;
     const int i0 = warp * seg, i1 = min(n, i0 + seg);
     int gt = 0, eq = 0;
+#pragma unroll 4
     for (int r = i0; r < i1; r += 32) {
         const int i = r + lane;
         const uint32_t u = i < i1 ? keys[i] : 0u;
@@ -211,6 +213,7 @@ __device__ void block_compact(const uint32_t* keys, int n, Select sel, Scratch& 
     __syncthreads();
     int gt_base = s.wcnt[0][warp], eq_base = s.wcnt[1][warp];
     const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll 4
     for (int r = i0; r < i1; r += 32) {
         const int i = r + lane;
         const uint32_t u = i < i1 ? keys[i] : 0u;
@@ -225,26 +228,38 @@ __device__ void block_compact(const uint32_t* keys, int n, Select sel, Scratch& 
 
 // keys[i] = score_key(src[i]) for i < n: 16-byte loads (every one issued
 // before any is used) when src is 16-byte aligned, else 4-byte loads.
-__device__ __forceinline__ void load_keys(const float* src, int n, uint32_t* keys) {
+template <int kBatch>
+__device__ __forceinline__ void load_keys(const float* src, int n, uint32_t* keys, uint32_t& lo, uint32_t& hi) {
+    lo = 0xffffffffu;
+    hi = 0u;
+    auto put = [&](int i, uint32_t q) {
+        keys[i] = q;
+        lo = min(lo, q);
+        hi = max(hi, q);
+    };
     if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
         const float4* v = reinterpret_cast<const float4*>(src);
         uint4* kv = reinterpret_cast<uint4*>(keys);
         const int n4 = n / 4;
-        for (int j0 = threadIdx.x; j0 < n4; j0 += 8 * kThreads) {
-            float4 f[8];
+        for (int j0 = threadIdx.x; j0 < n4; j0 += kBatch * kThreads) {
+            float4 f[kBatch];
 #pragma unroll
-            for (int u = 0; u < 8; u++)
+            for (int u = 0; u < kBatch; u++)
                 if (j0 + u * kThreads < n4) f[u] = __ldg(v + j0 + u * kThreads);
 #pragma unroll
-            for (int u = 0; u < 8; u++)
-                if (j0 + u * kThreads < n4)
-                    kv[j0 + u * kThreads] = make_uint4(score_key(f[u].x), score_key(f[u].y), score_key(f[u].z),
-                                                       score_key(f[u].w));
+            for (int u = 0; u < kBatch; u++)
+                if (j0 + u * kThreads < n4) {
+                    const uint4 q = make_uint4(score_key(f[u].x), score_key(f[u].y), score_key(f[u].z),
+                                               score_key(f[u].w));
+                    kv[j0 + u * kThreads] = q;
+                    lo = min(min(lo, min(q.x, q.y)), min(q.z, q.w));
+                    hi = max(max(hi, max(q.x, q.y)), max(q.z, q.w));
+                }
         }
-        for (int i = 4 * n4 + threadIdx.x; i < n; i += kThreads) keys[i] = score_key(src[i]);
+        for (int i = 4 * n4 + threadIdx.x; i < n; i += kThreads) put(i, score_key(src[i]));
     } else {
 #pragma unroll 8
-        for (int i = threadIdx.x; i < n; i += kThreads) keys[i] = score_key(src[i]);
+        for (int i = threadIdx.x; i < n; i += kThreads) put(i, score_key(src[i]));
     }
 }
 
@@ -260,13 +275,15 @@ __device__ __forceinline__ int64_t n_chunks(int64_t n) { return n > kChunk ? (n 
 __device__ __forceinline__ int64_t chunk_lo(int64_t c, int64_t n, int64_t nch) { return c * n / nch; }
 
 // Stage 1: grid (max chunks, Q).  Writes the final selection when the query
-// has one chunk, its candidates otherwise.  Two CTAs fit an SM when a chunk
-// holds at most ~25K scores (one CTA's selection passes overlap the other's
-// loads).
-__global__ void __launch_bounds__(kThreads, 2)
+// has one chunk, its candidates otherwise.  kMinBlocks = 2 when two CTAs fit
+// an SM (chunks of at most ~21K scores: one CTA's selection passes overlap
+// the other's loads), at the price of 32 registers a thread; else 1.
+template <int kMinBlocks>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
     topk_chunk_kernel(float* __restrict__ scores, int64_t ld, int64_t n_cap,
                       const int64_t* __restrict__ q_pos, int m, int k,
                       int32_t* __restrict__ idx, float* __restrict__ sel) {
+    constexpr int kLoadBatch = kMinBlocks == 2 ? 2 : 8;  // 16-byte loads in flight per thread
     extern __shared__ uint32_t keys[];  // [<= kChunk]
     __shared__ Scratch s;
     const int64_t q = blockIdx.y;
@@ -287,20 +304,22 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             return;
         }
-        load_keys(row, nc, keys);
-        __syncthreads();
-        const Select t = radix_select(keys, nc, k, s);
+        uint32_t lo_k, hi_k;
+        load_keys<kLoadBatch>(row, nc, keys, lo_k, hi_k);
+        block_minmax(lo_k, hi_k, s);  // also makes the keys visible to the CTA
+        const Select t = radix_select(keys, nc, k, lo_k, hi_k, s);
         block_compact(keys, nc, t, s, [&](int pos, int i) {
             oi[pos] = i;
             if (os) os[pos] = key_score(keys[i]);
         });
         return;
     }
-    load_keys(row + lo, nc, keys);
-    __syncthreads();  // the chunk is in smem: its region of the row may be overwritten
+    uint32_t lo_k, hi_k;
+    load_keys<kLoadBatch>(row + lo, nc, keys, lo_k, hi_k);
+    block_minmax(lo_k, hi_k, s);  // the chunk is in smem: its region of the row may be overwritten
     uint32_t* ck = reinterpret_cast<uint32_t*>(row + lo);      // [k] candidate keys
     int32_t* cidx = reinterpret_cast<int32_t*>(row + lo + k);  // [k] candidate indices
-    const Select t = radix_select(keys, nc, k, s);
+    const Select t = radix_select(keys, nc, k, lo_k, hi_k, s);
     block_compact(keys, nc, t, s, [&](int pos, int i) {
         ck[pos] = keys[i];
         cidx[pos] = (int32_t)(lo + i);
@@ -322,12 +341,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (nch <= 1) return;
     const float* row = scores + q * ld;
     const int C = (int)(nch * k);
-    for (int i = threadIdx.x; i < C; i += kThreads)
-        keys[i] = reinterpret_cast<const uint32_t*>(row + chunk_lo(i / k, n, nch))[i % k];
-    __syncthreads();
+    uint32_t lo_k = 0xffffffffu, hi_k = 0u;
+    for (int64_t c = 0; c < nch; c++) {  // chunk c's k candidate keys
+        const uint32_t* ck = reinterpret_cast<const uint32_t*>(row + chunk_lo(c, n, nch));
+#pragma unroll 4
+        for (int j = threadIdx.x; j < k; j += kThreads) {
+            const uint32_t u = ck[j];
+            keys[c * k + j] = u;
+            lo_k = min(lo_k, u);
+            hi_k = max(hi_k, u);
+        }
+    }
+    block_minmax(lo_k, hi_k, s);  // also makes the keys visible to the CTA
     int32_t* oi = idx + q * k;
     float* os = sel ? sel + q * k : nullptr;
-    const Select t = radix_select(keys, C, k, s);
+    const Select t = radix_select(keys, C, k, lo_k, hi_k, s);
     block_compact(keys, C, t, s, [&](int pos, int i) {
         oi[pos] = reinterpret_cast<const int32_t*>(row + chunk_lo(i / k, n, nch) + k)[i % k];
         if (os) os[pos] = key_score(keys[i]);
@@ -354,15 +382,22 @@ cudaError_t launch_topk(const Geometry& g, float* scores, int64_t ld, int64_t n_
     if (topk_chunk(n_cap, Q, k) == 0) return cudaErrorInvalidValue;  // rejected earlier by the C ABI
     const int64_t max_chunks = n_cap > kChunk ? (n_cap + kChunk - 1) / kChunk : 1;
     const size_t smem1 = (size_t)(n_cap < kChunk ? (n_cap > 0 ? n_cap : 1) : kChunk) * sizeof(uint32_t);
-    static int attr1 = 0;
-    if ((int)smem1 > attr1) {
-        cudaError_t e = cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem1);
+    // two CTAs an SM when both fit in its 228 KiB of shared memory
+    const bool two = smem1 + sizeof(Scratch) + 1024 <= 114 * 1024;
+    static int attr1[2] = {0, 0};
+    if ((int)smem1 > attr1[two]) {
+        cudaError_t e = two ? cudaFuncSetAttribute(topk_chunk_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)smem1)
+                            : cudaFuncSetAttribute(topk_chunk_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)smem1);
         if (e != cudaSuccess) return e;
-        attr1 = (int)smem1;
+        attr1[two] = (int)smem1;
     }
     dim3 grid1((unsigned)max_chunks, (unsigned)Q);
-    topk_chunk_kernel<<<grid1, kThreads, smem1, st>>>(scores, ld, n_cap, q_pos, g.m, k, idx, sel);
+    if (two)
+        topk_chunk_kernel<2><<<grid1, kThreads, smem1, st>>>(scores, ld, n_cap, q_pos, g.m, k, idx, sel);
+    else
+        topk_chunk_kernel<1><<<grid1, kThreads, smem1, st>>>(scores, ld, n_cap, q_pos, g.m, k, idx, sel);
     note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || max_chunks <= 1) return e;
