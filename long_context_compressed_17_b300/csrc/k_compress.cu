@@ -13,6 +13,7 @@
 // block of raw rows in shared memory so HBM is read once.
 #include "common.cuh"
 #include "internal.h"
+#include "tc_util.cuh"
 
 namespace csa {
 
@@ -104,6 +105,118 @@ __global__ void __launch_bounds__(kCompressThreads)
     if (warp == 0) warp_pack_row(row, D, kvfmt, out + blockIdx.y * out_seq_bytes + b * kv_row_bytes);
 }
 
+// Large blocks (HCA's m = 128) are split over a cluster of kSplit CTAs, each
+// pooling m / kSplit tokens with its own softmax reference:
+//   M_r = max z_t, S_r = sum e^(z_t - M_r), P_r = sum e^(z_t - M_r) kv_t
+// (t in slice r).  Every CTA stores (M_r, S_r, P_r) into slot r of CTA 0's
+// shared memory; after the cluster barrier CTA 0 merges them,
+//   pooled = sum_r e^(M_r - M) P_r / sum_r e^(M_r - M) S_r,  M = max_r M_r,
+// and finishes the entry as compress_kernel does (its pooled row goes where
+// its raw slice was).  grid (n_blocks_out * kSplit, B), clusters of (kSplit,
+// 1, 1).  Dynamic smem: the slice's raw rows (at least D floats), then
+// m / kSplit scores, then kSplit slots of (4 + D) floats, then 32 floats.
+constexpr int kSplit = 8;
+
+__global__ void __launch_bounds__(kCompressThreads)
+    compress_cluster_kernel(const uint8_t* __restrict__ kv, int act, int64_t act_row_bytes,
+                            int64_t kv_seq_bytes, int D, int m, int64_t pos0,
+                            const float* __restrict__ w_z, const float* __restrict__ bias,
+                            uint8_t* __restrict__ out, int kvfmt, int64_t kv_row_bytes,
+                            int64_t out_seq_bytes, float eps, RopeTheta theta) {
+    extern __shared__ __align__(16) float sm[];
+    const int mt = m / kSplit;                          // tokens of this CTA
+    const int rank = (int)tc::cluster_ctarank();        // == blockIdx.x % kSplit
+    const int64_t b = blockIdx.x / kSplit;              // output entry
+    const size_t slice_bytes = (size_t)mt * act_row_bytes;
+    uint8_t* stage = reinterpret_cast<uint8_t*>(sm);
+    float* z = reinterpret_cast<float*>(stage + ((slice_bytes + 15) & ~(size_t)15));
+    float* slots = z + ((mt + 3) & ~3);                 // [kSplit][4 + D]
+    float* red = slots + kSplit * (4 + D);              // [32]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int nwarps = kCompressThreads / 32;
+    const int t0 = rank * mt;                           // first token of the slice within the block
+    {
+        const uint4* g = reinterpret_cast<const uint4*>(kv + blockIdx.y * kv_seq_bytes +
+                                                        (b * m + t0) * act_row_bytes);
+        uint4* s = reinterpret_cast<uint4*>(stage);
+        const int64_t n16 = (int64_t)slice_bytes / 16;
+        for (int64_t i = tid; i < n16; i += kCompressThreads) s[i] = __ldg(g + i);
+    }
+    __syncthreads();
+    for (int t = warp; t < mt; t += nwarps) {
+        const uint8_t* r = stage + t * act_row_bytes;
+        float acc = 0.f;
+        for (int d = lane; d < D; d += 32) acc = fmaf(load_act(r, act, d), __ldg(w_z + d), acc);
+        acc = warp_sum(acc);
+        if (lane == 0) z[t] = acc + bias[t0 + t];
+    }
+    __syncthreads();
+    float zmax = -INFINITY;
+    for (int t = 0; t < mt; t++) zmax = fmaxf(zmax, z[t]);  // every thread: mt is small
+    __syncthreads();
+    if (tid < mt) z[tid] = expf(z[tid] - zmax);
+    __syncthreads();
+    float zsum = 0.f;
+    for (int t = 0; t < mt; t++) zsum += z[t];
+    // this slice's (M_r, S_r, P_r) into slot `rank` of CTA 0
+    const uint32_t slot0 = tc::mapa_shared(tc::smem_u32(slots + rank * (4 + D)), 0);
+    for (int d4 = tid; d4 < D / 4; d4 += kCompressThreads) {
+        float p[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            float c = 0.f;
+            for (int t = 0; t < mt; t++) c = fmaf(z[t], load_act(stage + t * act_row_bytes, act, 4 * d4 + e), c);
+            p[e] = c;
+        }
+        tc::st_cluster_v4(slot0 + 16u * (1 + d4), make_uint4(__float_as_uint(p[0]), __float_as_uint(p[1]),
+                                                               __float_as_uint(p[2]), __float_as_uint(p[3])));
+    }
+    if (tid == 0)
+        tc::st_cluster_v4(slot0, make_uint4(__float_as_uint(zmax), __float_as_uint(zsum), 0u, 0u));
+    tc::cluster_sync();  // every slot of CTA 0 is written and visible
+    if (rank != 0) return;
+    float* row = reinterpret_cast<float*>(stage);  // the raw slice is no longer needed
+    float M = -INFINITY;
+    for (int r = 0; r < kSplit; r++) M = fmaxf(M, slots[r * (4 + D)]);
+    float S = 0.f;
+    for (int r = 0; r < kSplit; r++) S += slots[r * (4 + D) + 1] * expf(slots[r * (4 + D)] - M);
+    const float invS = 1.f / S;
+    // merged pooled vector and its sum of squares
+    float ss = 0.f;
+    for (int d = tid; d < D; d += kCompressThreads) {
+        float c = 0.f;
+        for (int r = 0; r < kSplit; r++) c = fmaf(slots[r * (4 + D) + 4 + d], expf(slots[r * (4 + D)] - M), c);
+        c *= invS;
+        row[d] = c;
+        ss = fmaf(c, c, ss);
+    }
+    __syncthreads();
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    if (tid == 0) {
+        float tot = 0.f;
+        for (int w = 0; w < nwarps; w++) tot += red[w];
+        red[31] = 1.f / sqrtf(tot / (float)D + eps);
+    }
+    __syncthreads();
+    const float rn = red[31];
+    for (int d = tid; d < D; d += kCompressThreads) row[d] *= rn;
+    __syncthreads();
+    const double pos = (double)(pos0 + b * m + m - 1);
+    if (tid < kRopeDims / 2) {
+        const int j = tid;
+        float c, s;
+        rope_cs(pos, theta.t[j], &c, &s);
+        const int d0 = D - kRopeDims + 2 * j;
+        const float x0 = row[d0], x1 = row[d0 + 1];
+        row[d0] = x0 * c - x1 * s;
+        row[d0 + 1] = x0 * s + x1 * c;
+    }
+    __syncthreads();
+    if (warp == 0) warp_pack_row(row, D, kvfmt, out + blockIdx.y * out_seq_bytes + b * kv_row_bytes);
+}
+
 // one warp per row; dynamic smem: 4 warps x D floats
 __global__ void __launch_bounds__(128)
     pack_kernel(const float* __restrict__ src, int64_t n, int D, int kvfmt, int64_t rb,
@@ -134,6 +247,39 @@ cudaError_t launch_compress(const Geometry& g, const void* kv, int B, int64_t T,
     int64_t nb = T / g.m;
     if (nb == 0 || B == 0) return cudaSuccess;
     int64_t act_rb = row_bytes(g.act, g.D);
+    if (g.m >= 64 && g.m % kSplit == 0 && nb * kSplit <= 0x7fffffff) {
+        const int mt = g.m / kSplit;
+        const size_t slice = ((size_t)mt * act_rb + 15) & ~(size_t)15;
+        const size_t smem = slice + (size_t)(((mt + 3) & ~3) + kSplit * (4 + g.D) + 32) * sizeof(float);
+        if (slice >= (size_t)g.D * sizeof(float) && smem <= 200 * 1024) {
+            static size_t attr = 0;
+            if (smem > attr) {
+                cudaError_t e = cudaFuncSetAttribute(compress_cluster_kernel,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                if (e != cudaSuccess) return e;
+                attr = smem;
+            }
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(nb * kSplit), (unsigned)B, 1);
+            cfg.blockDim = dim3(kCompressThreads, 1, 1);
+            cfg.dynamicSmemBytes = smem;
+            cfg.stream = st;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = kSplit;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            cudaError_t e = cudaLaunchKernelEx(
+                &cfg, compress_cluster_kernel, reinterpret_cast<const uint8_t*>(kv), (int)g.act, act_rb,
+                kv_stride * act_rb, g.D, g.m, pos0, w_z, bias, reinterpret_cast<uint8_t*>(out), (int)g.kv,
+                g.kv_row_bytes, out_stride * g.kv_row_bytes, g.eps, rope_theta(g));
+            note_launch();
+            if (e != cudaSuccess) return e;
+            return cudaGetLastError();
+        }
+    }
     size_t smem = (size_t)((g.m + g.D + 32 + 3) & ~3) * sizeof(float);
     const size_t blk_bytes = (size_t)g.m * (size_t)act_rb;
     const int staged = blk_bytes <= kCompressStageMax ? 1 : 0;
