@@ -47,27 +47,33 @@ __global__ void __launch_bounds__(kCompressThreads)
         src = stage;
     }
 
-    // pooling scores z_t = kv_t . w_z + bias[t mod m]   (pos0 is a multiple of m)
-    for (int t = warp; t < m; t += nwarps) {
-        const uint8_t* r = src + t * act_row_bytes;
-        float acc = 0.f;
-        for (int d = lane; d < D; d += 32) acc = fmaf(load_act(r, act, d), __ldg(w_z + d), acc);
-        acc = warp_sum(acc);
-        if (lane == 0) z[t] = acc + bias[t];
+    if (m == 1) {
+        // a single token: its pooling weight is exactly 1 (window rows)
+        if (tid == 0) z[0] = 1.f;
+        __syncthreads();
+    } else {
+        // pooling scores z_t = kv_t . w_z + bias[t mod m]   (pos0 is a multiple of m)
+        for (int t = warp; t < m; t += nwarps) {
+            const uint8_t* r = src + t * act_row_bytes;
+            float acc = 0.f;
+            for (int d = lane; d < D; d += 32) acc = fmaf(load_act(r, act, d), __ldg(w_z + d), acc);
+            acc = warp_sum(acc);
+            if (lane == 0) z[t] = acc + bias[t];
+        }
+        __syncthreads();
+        // softmax over the block's tokens: z <- alpha
+        if (warp == 0) {
+            float zmax = -INFINITY;
+            for (int t = lane; t < m; t += 32) zmax = fmaxf(zmax, z[t]);
+            zmax = warp_max(zmax);
+            float den = 0.f;
+            for (int t = lane; t < m; t += 32) den += expf(z[t] - zmax);
+            den = warp_sum(den);
+            const float inv = 1.f / den;
+            for (int t = lane; t < m; t += 32) z[t] = expf(z[t] - zmax) * inv;
+        }
+        __syncthreads();
     }
-    __syncthreads();
-    // softmax over the block's tokens: z <- alpha
-    if (warp == 0) {
-        float zmax = -INFINITY;
-        for (int t = lane; t < m; t += 32) zmax = fmaxf(zmax, z[t]);
-        zmax = warp_max(zmax);
-        float den = 0.f;
-        for (int t = lane; t < m; t += 32) den += expf(z[t] - zmax);
-        den = warp_sum(den);
-        const float inv = 1.f / den;
-        for (int t = lane; t < m; t += 32) z[t] = expf(z[t] - zmax) * inv;
-    }
-    __syncthreads();
 
     // pooled vector and its sum of squares
     float ss = 0.f;
