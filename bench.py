@@ -47,11 +47,11 @@ L2_FLUSH_BYTES = 512 << 20
 # captured build (sha256 prefix of the listed files); otherwise it is null.
 CAPTURED_TRAFFIC = {
     "csa_decode_bf16_b32_128k": (
-        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "c428605f4ea16fec", 274547200),
+        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "0f560a0c071fc5b7", 274824704),
     "csa_decode_fp8cache_b8_1m": (
-        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "c428605f4ea16fec", 546795776),
+        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "0f560a0c071fc5b7", 546872832),
     "csa_chunked_prefill_bf16_64k_8k": (
-        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "c428605f4ea16fec", 698945024),
+        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "0f560a0c071fc5b7", 712652032),
     "hca_decode_bf16_b32_1m": (
         ["k_attend_tc.cu", "tc_util.cuh", "common.cuh"], "a42fd4ffbc28e7f9", 288056064),
 }
