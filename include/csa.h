@@ -112,6 +112,25 @@ csa_status csa_compress(const csa_params* p, const void* kv_raw, int32_t B, int6
                         int64_t kv_seq_stride, int64_t pos0, const float* w_z, const float* bias,
                         void* out, int64_t out_seq_stride, csa_stream_t stream);
 
+/* Decode append in one launch: the cache entry of one newly completed block
+ * per sequence and the window row of its last token -- exactly what
+ *   csa_compress(p, kv_new, B, m, kv_seq_stride, pos0, w_z, bias,
+ *                entry_out, out_seq_stride)
+ * and csa_compress with ratio 1 over the block's last token (position
+ * pos0+m-1) into win_out write (same arithmetic, bit for bit).  This entry
+ * point has no counterpart on the pages: it fuses the two steps of keeping a
+ * decode cache current [peacm §三.2 CSA "Step 1"; 四项关键 Trick "滑动窗口"].
+ *   kv_new: B blocks of m = p->ratio raw tokens [.., D] in p->act_format at
+ *           positions pos0 .. pos0+m-1 (pos0 a multiple of m); sequence s
+ *           starts at row s*kv_seq_stride.
+ *   entry_out: sequence s's entry at row s*out_seq_stride (p->kv_format rows).
+ *   win_out:   sequence s's window row at row s*win_seq_stride.
+ *   w_z: [D] float32; bias: [m] float32.  All buffers device, 16-byte aligned. */
+csa_status csa_append(const csa_params* p, const void* kv_new, int32_t B, int64_t kv_seq_stride,
+                      int64_t pos0, const float* w_z, const float* bias, void* entry_out,
+                      int64_t out_seq_stride, void* win_out, int64_t win_seq_stride,
+                      csa_stream_t stream);
+
 /* Lightning indexer + top-k [peacm §三.2 CSA "Step 2: Lightning Indexer Top-K
  * 选择"; gitcode §2.1.1].  For query q at position i = q_pos[q] in sequence
  * s = q / (Q/B), over the complete blocks b < floor((i+1)/m):

@@ -16,7 +16,7 @@ import torch
 
 __all__ = [
     "CsaError", "CsaParams", "F32", "BF16", "FP8_MIXED", "OP_INDEX_TOPK", "OP_ATTEND",
-    "OP_HCA_ATTEND", "params", "lib", "csa_row_bytes", "csa_cache_pack", "csa_compress",
+    "OP_HCA_ATTEND", "params", "lib", "csa_row_bytes", "csa_cache_pack", "csa_compress", "csa_append",
     "csa_index_topk", "csa_index_score", "csa_topk_select", "csa_launch_count", "csa_index_topk_noalloc", "csa_attend", "hca_attend", "csa_workspace_bytes", "csa_workspace_init",
     "csa_check_status", "csa_last_device_bits", "csa_status_string", "csa_last_error",
     "workspace", "LIB_PATH",
@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
             "csa_row_bytes": (_i64, [_i32, _i32]),
             "csa_cache_pack": (_i32, [P, _vp, _i64, _vp, _vp]),
             "csa_compress": (_i32, [P, _vp, _i32, _i64, _i64, _i64, _vp, _vp, _vp, _i64, _vp]),
+            "csa_append": (_i32, [P, _vp, _i32, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _vp]),
             "csa_index_topk": (_i32, [P, _vp, _vp, _i32, _i32, _vp, _i64, _i32, _i32, _vp, _vp,
                                       _vp, _vp, _sz, _vp]),
             "csa_attend": (_i32, [P, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _vp, _i64, _vp,
@@ -139,6 +140,13 @@ def csa_row_bytes(kv_format: int, head_dim: int) -> int:
 def csa_cache_pack(p, src, n_rows, dst, stream=None):
     _check(lib().csa_cache_pack(ctypes.byref(p), _ptr(src), n_rows, _ptr(dst), _stream(stream)),
            "csa_cache_pack")
+
+
+def csa_append(p, kv_new, B, kv_seq_stride, pos0, w_z, bias, entry_out, out_seq_stride, win_out,
+               win_seq_stride, stream=None):
+    _check(lib().csa_append(ctypes.byref(p), _ptr(kv_new), B, kv_seq_stride, pos0, _ptr(w_z),
+                            _ptr(bias), _ptr(entry_out), out_seq_stride, _ptr(win_out),
+                            win_seq_stride, _stream(stream)), "csa_append")
 
 
 def csa_compress(p, kv_raw, B, T, kv_seq_stride, pos0, w_z, bias, out, out_seq_stride,

@@ -223,8 +223,32 @@ csa_status csa_compress(const csa_params* p, const void* kv_raw, int32_t B, int6
     CHECK(check_ptr(out, "out"));
     Geometry g = resolve(p);
     cudaError_t e = launch_compress(g, kv_raw, B, T, kv_seq_stride, pos0, w_z, bias, out,
-                                    out_seq_stride, (cudaStream_t)stream);
+                                    out_seq_stride, nullptr, 0, (cudaStream_t)stream);
     return e == cudaSuccess ? CSA_OK : cuda_fail(e, "csa_compress");
+}
+
+csa_status csa_append(const csa_params* p, const void* kv_new, int32_t B, int64_t kv_seq_stride,
+                      int64_t pos0, const float* w_z, const float* bias, void* entry_out,
+                      int64_t out_seq_stride, void* win_out, int64_t win_seq_stride,
+                      csa_stream_t stream) {
+    CHECK(check_params(p));
+    if (B < 0 || B > 65535) return fail(CSA_ERR_INVALID_ARG, "B %d out of range", B);
+    if (pos0 < 0 || pos0 % p->ratio != 0)
+        return fail(CSA_ERR_INVALID_ARG, "pos0 %lld is not a non-negative multiple of ratio %d",
+                    (long long)pos0, p->ratio);
+    if (B == 0) return CSA_OK;
+    if (B > 1 && kv_seq_stride < p->ratio) return fail(CSA_ERR_INVALID_ARG, "kv_seq_stride < ratio");
+    if (B > 1 && (out_seq_stride < 1 || win_seq_stride < 1))
+        return fail(CSA_ERR_INVALID_ARG, "out_seq_stride / win_seq_stride < 1");
+    CHECK(check_ptr(kv_new, "kv_new"));
+    CHECK(check_ptr(w_z, "w_z"));
+    if (!bias) return fail(CSA_ERR_INVALID_ARG, "bias is NULL");
+    CHECK(check_ptr(entry_out, "entry_out"));
+    CHECK(check_ptr(win_out, "win_out"));
+    Geometry g = resolve(p);
+    cudaError_t e = launch_compress(g, kv_new, B, p->ratio, kv_seq_stride, pos0, w_z, bias, entry_out,
+                                    out_seq_stride, win_out, win_seq_stride, (cudaStream_t)stream);
+    return e == cudaSuccess ? CSA_OK : cuda_fail(e, "csa_append");
 }
 
 size_t csa_workspace_bytes(const csa_params* p, int32_t op, int32_t B, int32_t Q, int32_t H,

@@ -63,9 +63,12 @@ AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int6
 
 cudaError_t launch_cache_pack(const Geometry& g, const float* src, int64_t n, void* dst,
                               cudaStream_t st);
+// win_out (or nullptr): also the window row of every block's last token, at
+// row b of sequence s's win_stride rows.
 cudaError_t launch_compress(const Geometry& g, const void* kv, int B, int64_t T,
                             int64_t kv_stride, int64_t pos0, const float* w_z, const float* bias,
-                            void* out, int64_t out_stride, cudaStream_t st);
+                            void* out, int64_t out_stride, void* win_out, int64_t win_stride,
+                            cudaStream_t st);
 cudaError_t launch_indexer(const Geometry& g, const void* q_idx, const float* w_idx, int HI,
                            int dI, const void* keys, int64_t n_cap, int B, int Q,
                            const int64_t* q_pos, uint32_t* status, float* scores, int64_t ld,

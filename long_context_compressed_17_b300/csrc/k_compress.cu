@@ -20,6 +20,51 @@ namespace csa {
 constexpr int kCompressThreads = 256;
 constexpr size_t kCompressStageMax = 160 * 1024;  // raw block staged in smem up to this size
 
+// row[0, D) holds a pooled vector (shared memory) and ss each thread's partial
+// sum of its squares: RMSNorm it, rotate its last 64 dims at position pos and
+// store it into a cache row at dst (whole CTA; red: 32 floats of scratch).
+__device__ void norm_rope_store(float* row, float ss, float* red, int D, float eps, double pos,
+                                const RopeTheta& theta, int kvfmt, uint8_t* dst) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int nwarps = kCompressThreads / 32;
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    if (tid == 0) {
+        float tot = 0.f;
+        for (int w = 0; w < nwarps; w++) tot += red[w];
+        red[31] = 1.f / sqrtf(tot / (float)D + eps);
+    }
+    __syncthreads();
+    const float rn = red[31];
+    for (int d = tid; d < D; d += kCompressThreads) row[d] *= rn;
+    __syncthreads();
+    if (tid < kRopeDims / 2) {
+        const int j = tid;
+        float c, s;
+        rope_cs(pos, theta.t[j], &c, &s);
+        const int d0 = D - kRopeDims + 2 * j;
+        const float x0 = row[d0], x1 = row[d0 + 1];
+        row[d0] = x0 * c - x1 * s;
+        row[d0 + 1] = x0 * s + x1 * c;
+    }
+    __syncthreads();
+    if (warp == 0) warp_pack_row(row, D, kvfmt, dst);
+}
+
+// The window row of raw token `tok` (RMSNorm, RoPE at pos; what the
+// compressor with m = 1 writes), through row[0, D).
+__device__ void window_row(const uint8_t* tok, int act, float* row, float* red, int D, float eps, double pos,
+                           const RopeTheta& theta, int kvfmt, uint8_t* dst) {
+    float ss = 0.f;
+    for (int d = threadIdx.x; d < D; d += kCompressThreads) {
+        const float c = load_act(tok, act, d);
+        row[d] = c;
+        ss = fmaf(c, c, ss);
+    }
+    norm_rope_store(row, ss, red, D, eps, pos, theta, kvfmt, dst);
+}
+
 // grid (n_blocks_out, B).  Dynamic smem: (m + D + 32) floats, rounded up to
 // 16 bytes, then (when `staged`) the block's m raw rows.
 __global__ void __launch_bounds__(kCompressThreads)
@@ -27,7 +72,8 @@ __global__ void __launch_bounds__(kCompressThreads)
                     int64_t kv_seq_bytes, int D, int m, int64_t pos0,
                     const float* __restrict__ w_z, const float* __restrict__ bias,
                     uint8_t* __restrict__ out, int kvfmt, int64_t kv_row_bytes,
-                    int64_t out_seq_bytes, float eps, RopeTheta theta, int staged) {
+                    int64_t out_seq_bytes, float eps, RopeTheta theta, int staged,
+                    uint8_t* __restrict__ win_out, int64_t win_seq_bytes) {
     extern __shared__ __align__(16) float sm[];
     float* z = sm;            // [m] scores, then pooling weights
     float* row = sm + m;      // [D]
@@ -83,32 +129,14 @@ __global__ void __launch_bounds__(kCompressThreads)
         row[d] = c;
         ss = fmaf(c, c, ss);
     }
-    ss = warp_sum(ss);
-    if (lane == 0) red[warp] = ss;
-    __syncthreads();
-    if (tid == 0) {
-        float tot = 0.f;
-        for (int w = 0; w < nwarps; w++) tot += red[w];
-        red[31] = 1.f / sqrtf(tot / (float)D + eps);
-    }
-    __syncthreads();
-    const float rn = red[31];
-    for (int d = tid; d < D; d += kCompressThreads) row[d] *= rn;
-    __syncthreads();
-
-    // partial RoPE at the block's last position
+    // RMSNorm, partial RoPE at the block's last position, store
     const double pos = (double)(pos0 + b * m + m - 1);
-    if (tid < kRopeDims / 2) {
-        const int j = tid;
-        float c, s;
-        rope_cs(pos, theta.t[j], &c, &s);
-        int d0 = D - kRopeDims + 2 * j;
-        float x0 = row[d0], x1 = row[d0 + 1];
-        row[d0] = x0 * c - x1 * s;
-        row[d0 + 1] = x0 * s + x1 * c;
+    norm_rope_store(row, ss, red, D, eps, pos, theta, kvfmt, out + blockIdx.y * out_seq_bytes + b * kv_row_bytes);
+    if (win_out != nullptr) {  // the window row of the block's last token
+        __syncthreads();       // `row` is free again
+        window_row(src + (m - 1) * act_row_bytes, act, row, red, D, eps, pos, theta, kvfmt,
+                   win_out + blockIdx.y * win_seq_bytes + b * kv_row_bytes);
     }
-    __syncthreads();
-    if (warp == 0) warp_pack_row(row, D, kvfmt, out + blockIdx.y * out_seq_bytes + b * kv_row_bytes);
 }
 
 // Large blocks (HCA's m = 128) are split over a cluster of kSplit CTAs, each
@@ -128,7 +156,8 @@ __global__ void __launch_bounds__(kCompressThreads)
                             int64_t kv_seq_bytes, int D, int m, int64_t pos0,
                             const float* __restrict__ w_z, const float* __restrict__ bias,
                             uint8_t* __restrict__ out, int kvfmt, int64_t kv_row_bytes,
-                            int64_t out_seq_bytes, float eps, RopeTheta theta) {
+                            int64_t out_seq_bytes, float eps, RopeTheta theta,
+                            uint8_t* __restrict__ win_out, int64_t win_seq_bytes) {
     extern __shared__ __align__(16) float sm[];
     const int mt = m / kSplit;                          // tokens of this CTA
     const int rank = (int)tc::cluster_ctarank();        // == blockIdx.x % kSplit
@@ -180,6 +209,14 @@ __global__ void __launch_bounds__(kCompressThreads)
     if (tid == 0)
         tc::st_cluster_v4(slot0, make_uint4(__float_as_uint(zmax), __float_as_uint(zsum), 0u, 0u));
     tc::cluster_sync();  // every slot of CTA 0 is written and visible
+    const double pos = (double)(pos0 + b * m + m - 1);
+    if (rank == kSplit - 1 && win_out != nullptr) {
+        // the window row of the block's last token, the last row of this slice;
+        // this CTA's own slots are unused and hold the row
+        window_row(stage + (mt - 1) * act_row_bytes, act, slots, red, D, eps, pos, theta, kvfmt,
+                   win_out + blockIdx.y * win_seq_bytes + b * kv_row_bytes);
+        return;
+    }
     if (rank != 0) return;
     float* row = reinterpret_cast<float*>(stage);  // the raw slice is no longer needed
     float M = -INFINITY;
@@ -196,31 +233,7 @@ __global__ void __launch_bounds__(kCompressThreads)
         row[d] = c;
         ss = fmaf(c, c, ss);
     }
-    __syncthreads();
-    ss = warp_sum(ss);
-    if (lane == 0) red[warp] = ss;
-    __syncthreads();
-    if (tid == 0) {
-        float tot = 0.f;
-        for (int w = 0; w < nwarps; w++) tot += red[w];
-        red[31] = 1.f / sqrtf(tot / (float)D + eps);
-    }
-    __syncthreads();
-    const float rn = red[31];
-    for (int d = tid; d < D; d += kCompressThreads) row[d] *= rn;
-    __syncthreads();
-    const double pos = (double)(pos0 + b * m + m - 1);
-    if (tid < kRopeDims / 2) {
-        const int j = tid;
-        float c, s;
-        rope_cs(pos, theta.t[j], &c, &s);
-        const int d0 = D - kRopeDims + 2 * j;
-        const float x0 = row[d0], x1 = row[d0 + 1];
-        row[d0] = x0 * c - x1 * s;
-        row[d0 + 1] = x0 * s + x1 * c;
-    }
-    __syncthreads();
-    if (warp == 0) warp_pack_row(row, D, kvfmt, out + blockIdx.y * out_seq_bytes + b * kv_row_bytes);
+    norm_rope_store(row, ss, red, D, eps, pos, theta, kvfmt, out + blockIdx.y * out_seq_bytes + b * kv_row_bytes);
 }
 
 // one warp per row; dynamic smem: 4 warps x D floats
@@ -249,7 +262,8 @@ cudaError_t launch_cache_pack(const Geometry& g, const float* src, int64_t n, vo
 
 cudaError_t launch_compress(const Geometry& g, const void* kv, int B, int64_t T,
                             int64_t kv_stride, int64_t pos0, const float* w_z, const float* bias,
-                            void* out, int64_t out_stride, cudaStream_t st) {
+                            void* out, int64_t out_stride, void* win_out, int64_t win_stride,
+                            cudaStream_t st) {
     int64_t nb = T / g.m;
     if (nb == 0 || B == 0) return cudaSuccess;
     int64_t act_rb = row_bytes(g.act, g.D);
@@ -280,7 +294,8 @@ cudaError_t launch_compress(const Geometry& g, const void* kv, int B, int64_t T,
             cudaError_t e = cudaLaunchKernelEx(
                 &cfg, compress_cluster_kernel, reinterpret_cast<const uint8_t*>(kv), (int)g.act, act_rb,
                 kv_stride * act_rb, g.D, g.m, pos0, w_z, bias, reinterpret_cast<uint8_t*>(out), (int)g.kv,
-                g.kv_row_bytes, out_stride * g.kv_row_bytes, g.eps, rope_theta(g));
+                g.kv_row_bytes, out_stride * g.kv_row_bytes, g.eps, rope_theta(g),
+                reinterpret_cast<uint8_t*>(win_out), win_stride * g.kv_row_bytes);
             note_launch();
             if (e != cudaSuccess) return e;
             return cudaGetLastError();
@@ -299,7 +314,8 @@ cudaError_t launch_compress(const Geometry& g, const void* kv, int B, int64_t T,
     compress_kernel<<<grid, kCompressThreads, smem, st>>>(
         reinterpret_cast<const uint8_t*>(kv), g.act, act_rb, kv_stride * act_rb, g.D, g.m, pos0,
         w_z, bias, reinterpret_cast<uint8_t*>(out), g.kv, g.kv_row_bytes,
-        out_stride * g.kv_row_bytes, g.eps, rope_theta(g), staged);
+        out_stride * g.kv_row_bytes, g.eps, rope_theta(g), staged, reinterpret_cast<uint8_t*>(win_out),
+        win_stride * g.kv_row_bytes);
     note_launch();
     return cudaGetLastError();
 }

@@ -4,9 +4,10 @@ These helpers own no arithmetic: they allocate device buffers with torch and
 issue the C-ABI calls in the order the layer needs them.
 
 Decode step (one new token per sequence, every sequence at the same length L):
-  1. append: when the new token completes a block, csa_compress(ratio=m) pools
-     the newest m raw tokens into cache entry L/m - 1; csa_compress(ratio=1)
-     writes the new token's normalised, rotated window row.
+  1. append: when the new token completes a block, csa_append pools the newest
+     m raw tokens into cache entry L/m - 1 and writes the new token's
+     normalised, rotated window row (one launch; the same as csa_compress with
+     ratio m, then with ratio 1).
   2. CSA: csa_index_topk then csa_attend.  HCA: hca_attend.
 Prefill (one sequence, a chunk of new tokens after `T_cached` cached ones):
   csa_compress over the chunk (ratio=m) and over the window tokens (ratio=1),
@@ -18,9 +19,9 @@ from dataclasses import dataclass
 
 import torch
 
-from . import (BF16, F32, FP8_MIXED, OP_ATTEND, OP_HCA_ATTEND, OP_INDEX_TOPK, csa_attend,
-               csa_compress, csa_index_topk, csa_row_bytes, csa_workspace_bytes, hca_attend,
-               params, workspace)
+from . import (BF16, F32, FP8_MIXED, OP_ATTEND, OP_HCA_ATTEND, OP_INDEX_TOPK, csa_append,
+               csa_attend, csa_compress, csa_index_topk, csa_row_bytes, csa_workspace_bytes,
+               hca_attend, params, workspace)
 
 _ACT_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
 
@@ -94,11 +95,9 @@ class DecodeLayer:
         cfg = self.cfg
         rb = cache.element_size() * (cache.shape[-1])
         e = pos_first // cfg.m
-        csa_compress(self.p, kv_new, self.B, cfg.m, cfg.m, pos_first, w_z, bias,
-                     cache.data_ptr() + e * rb, self.n_cap, stream)
-        last = kv_new[:, cfg.m - 1:cfg.m]
-        csa_compress(self.p1, last.data_ptr(), self.B, 1, cfg.m, pos_first + cfg.m - 1, w_z,
-                     bias, window.data_ptr() + win_row * rb, self.n_win, stream)
+        # one launch: the entry and the last token's window row
+        csa_append(self.p, kv_new, self.B, cfg.m, pos_first, w_z, bias, cache.data_ptr() + e * rb,
+                   self.n_cap, window.data_ptr() + win_row * rb, self.n_win, stream)
 
     def attend(self, q, cache, window, q_pos, win_pos0, sink, q_idx=None, w_idx=None, keys=None,
                stream=None):

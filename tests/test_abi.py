@@ -30,7 +30,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("csa_compress", "csa_index_topk", "csa_attend", "hca_attend", "csa_cache_pack",
+    for n in ("csa_compress", "csa_append", "csa_index_topk", "csa_attend", "hca_attend", "csa_cache_pack",
               "csa_workspace_bytes", "csa_workspace_init", "csa_check_status",
               "csa_status_string", "csa_last_error", "csa_row_bytes"):
         assert n in names, n
@@ -140,6 +140,17 @@ def test_compress_validation(L):
     assert _status_of(L.csa_compress, **dict(base, kv_seq_stride=8)) == 1
     assert _status_of(L.csa_compress, **dict(base, out_seq_stride=3)) == 1
     assert _status_of(L.csa_compress, **dict(base, w_z=FAKE + 4)) == 1
+
+
+def test_append_validation(L):
+    p = L.params(512, 4)
+    base = dict(p=p, kv_new=FAKE, B=2, kv_seq_stride=4, pos0=8, w_z=FAKE, bias=FAKE,
+                entry_out=FAKE, out_seq_stride=4, win_out=FAKE, win_seq_stride=128)
+    assert _status_of(L.csa_append, **dict(base, pos0=6)) == 1       # not a multiple of m
+    assert _status_of(L.csa_append, **dict(base, kv_seq_stride=3)) == 1
+    assert _status_of(L.csa_append, **dict(base, win_out=None)) == 1
+    assert _status_of(L.csa_append, **dict(base, entry_out=FAKE + 8)) == 1  # not 16-byte aligned
+    assert _status_of(L.csa_append, **dict(base, B=-1)) == 1
 
 
 def test_zero_sized_requests_are_no_ops(L):

@@ -185,3 +185,37 @@ def test_full_size_chunked_prefill_sampled():
                         rng.choice(w.T_new, 16, replace=False).tolist()))
     n_same, n = prefill_parity(w, sample=sample, gen_device="cuda")
     assert n_same >= n - 2
+
+
+@pytest.mark.parametrize("m,kv", [(4, "bf16"), (128, "bf16"), (4, "fp8m"), (128, "fp8m")])
+def test_append_matches_two_compress_calls(m, kv):
+    """csa_append (one launch) writes the same bits as csa_compress over the
+    block plus csa_compress with ratio 1 over its last token."""
+    import long_context_compressed_17_b300 as L
+    from long_context_compressed_17_b300.pipeline import LayerConfig
+    B, D, n_cap, n_win = 5, 512, 40, 16
+    cfg = LayerConfig(D=D, H=64, m=m, kv=kv)
+    g = torch.Generator(device="cpu").manual_seed(21 + m)
+    kv_new = (torch.randn(B, m, D, generator=g) * 2).to(torch.bfloat16).cuda()
+    w_z = (torch.randn(D, generator=g) * 0.02).cuda()
+    bias = (torch.randn(m, generator=g) * 0.1).cuda()
+    pos0 = 37 * m
+    e, wr = 11, 9
+    outs = []
+    for fused in (True, False):
+        cache = cfg.empty_rows(B, n_cap)
+        window = cfg.empty_rows(B, n_win)
+        rb = cache.shape[-1] * cache.element_size()
+        if fused:
+            L.csa_append(cfg.params(), kv_new, B, m, pos0, w_z, bias, cache.data_ptr() + e * rb,
+                         n_cap, window.data_ptr() + wr * rb, n_win)
+        else:
+            L.csa_compress(cfg.params(), kv_new, B, m, m, pos0, w_z, bias,
+                           cache.data_ptr() + e * rb, n_cap)
+            L.csa_compress(cfg.params(ratio=1), kv_new[:, m - 1:].data_ptr(), B, 1, m,
+                           pos0 + m - 1, w_z, bias, window.data_ptr() + wr * rb, n_win)
+        torch.cuda.synchronize()
+        outs.append((cache.cpu(), window.cpu()))
+    assert torch.equal(outs[0][0], outs[1][0]), "entries differ"
+    assert torch.equal(outs[0][1], outs[1][1]), "window rows differ"
+    assert outs[0][0][:, e].abs().sum() > 0 and outs[0][1][:, wr].abs().sum() > 0
