@@ -78,6 +78,10 @@ def _declare(L):
     L.oracle_n_complete.restype = _i64
     L.oracle_index_scores.argtypes = [_vp, _i32, _vp, _i32, _i32, _vp, _i32, _i64, _vp]
     L.oracle_index_scores.restype = None
+    L.oracle_pack_idx_keys_fp8.argtypes = [_vp, _i64, _i32, _vp, _vp]
+    L.oracle_pack_idx_keys_fp8.restype = None
+    L.oracle_index_scores_fp8.argtypes = [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _i64, _vp]
+    L.oracle_index_scores_fp8.restype = None
     L.oracle_topk.argtypes = [_vp, _i64, _i32, _vp, _vp]
     L.oracle_topk.restype = _i64
     L.oracle_attend_rows.argtypes = [_vp, _i32, _i32, _i32, _i64, _vp, _i64, _vp, _dbl, _i32,
@@ -236,6 +240,32 @@ def index_scores(q: np.ndarray, w, keys: np.ndarray) -> np.ndarray:
     out = np.empty(n, dtype=np.float64)
     lib().oracle_index_scores(_ptr(q), fmt_of(q), _ptr(w), HI, dI, _ptr(keys), fmt_of(keys), n,
                               _ptr(out))
+    return out
+
+
+def pack_idx_keys_fp8(x: np.ndarray):
+    """float32 keys [n, dI] -> (E4M3 codes uint8 [n, dI], float32 scales [n]),
+    one scale per key row."""
+    x = _c(x, np.float32)
+    n, dI = x.shape
+    codes = np.empty((n, dI), dtype=np.uint8)
+    scales = np.empty(n, dtype=np.float32)
+    lib().oracle_pack_idx_keys_fp8(_ptr(x), n, dI, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def index_scores_fp8(q: np.ndarray, w, codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """q stored [HI, dI] (its heads quantised to FP8 inside), w [HI], FP8 keys
+    (codes [n, dI], scales [n]) -> float64 scores [n]."""
+    q = _c(q)
+    HI, dI = q.shape
+    w = _c(w, np.float64)
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.float32)
+    n = codes.shape[0]
+    out = np.empty(n, dtype=np.float64)
+    lib().oracle_index_scores_fp8(_ptr(q), fmt_of(q), _ptr(w), HI, dI, _ptr(codes), _ptr(scales), n,
+                                  _ptr(out))
     return out
 
 

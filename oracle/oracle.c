@@ -284,6 +284,68 @@ void oracle_index_scores(const void* q, int q_fmt, const double* w, int HI, int 
     free(kk);
 }
 
+/* Indexer keys in 8-bit floating point (the pages' lightning indexer runs
+ * in low precision [gitcode §2.1.1 "Lightning Indexer"]; this build's FP8
+ * variant): one float32 scale per key row, scale = amax/448 (1 for an
+ * all-zero row), code = E4M3(x / scale) with the division in float32 -- the
+ * same rule as a 64-dim group of the mixed cache row, over the whole row.
+ * x: [n, dI] float32 -> codes [n, dI], scales [n]. */
+static float orc_fp8_row_quant(const float* x, int dI, uint8_t* codes) {
+    float amax = 0.0f;
+    for (int d = 0; d < dI; d++) {
+        float a = fabsf(x[d]);
+        if (a > amax) amax = a;
+    }
+    float scale = (amax == 0.0f) ? 1.0f : amax / 448.0f;
+    for (int d = 0; d < dI; d++) {
+        volatile float q = x[d] / scale; /* float32 division, as stored */
+        codes[d] = oracle_e4m3_encode(q);
+    }
+    return scale;
+}
+
+void oracle_pack_idx_keys_fp8(const float* x, int64_t n, int dI, uint8_t* codes, float* scales) {
+    for (int64_t b = 0; b < n; b++) scales[b] = orc_fp8_row_quant(x + b * dI, dI, codes + b * dI);
+}
+
+/* Indexer score with FP8 keys; each query head row is quantised by the same
+ * rule (its float32 values, one scale per head):
+ *   score_b = sum_h w_h * relu(sum_d (q8_hd * sq_h) * (k8_bd * sk_b)),  b < n
+ * every dequantised value and the sums in double.
+ * q: [HI, dI] stored in q_fmt; w: [HI]; key_codes [n, dI]; key_scales [n]. */
+void oracle_index_scores_fp8(const void* q, int q_fmt, const double* w, int HI, int dI,
+                             const uint8_t* key_codes, const float* key_scales, int64_t n,
+                             double* scores) {
+    double* qq = (double*)malloc(sizeof(double) * (size_t)HI * (size_t)dI);
+    double* kk = (double*)malloc(sizeof(double) * (size_t)dI);
+    double* row = (double*)malloc(sizeof(double) * (size_t)dI);
+    float* rowf = (float*)malloc(sizeof(float) * (size_t)dI);
+    uint8_t* qc = (uint8_t*)malloc((size_t)dI);
+    for (int h = 0; h < HI; h++) {
+        oracle_read_row(q, q_fmt, dI, h, row);
+        for (int d = 0; d < dI; d++) rowf[d] = (float)row[d]; /* exact for bf16 / f32 storage */
+        float sq = orc_fp8_row_quant(rowf, dI, qc);
+        for (int d = 0; d < dI; d++) qq[(size_t)h * dI + d] = oracle_e4m3_decode(qc[d]) * (double)sq;
+    }
+    for (int64_t b = 0; b < n; b++) {
+        for (int d = 0; d < dI; d++)
+            kk[d] = oracle_e4m3_decode(key_codes[b * dI + d]) * (double)key_scales[b];
+        double s = 0.0;
+        for (int h = 0; h < HI; h++) {
+            double dot = 0.0;
+            for (int d = 0; d < dI; d++) dot += qq[(size_t)h * dI + d] * kk[d];
+            double relu = dot > 0.0 ? dot : 0.0;
+            s += w[h] * relu;
+        }
+        scores[b] = s;
+    }
+    free(qq);
+    free(kk);
+    free(row);
+    free(rowf);
+    free(qc);
+}
+
 typedef struct {
     double s;
     int64_t i;
