@@ -169,6 +169,29 @@ csa_status csa_topk_select(const csa_params* p, float* scores, int64_t ld_scores
                            int64_t n_cap, int32_t Q, const int64_t* q_pos, int32_t* topk_idx,
                            float* topk_score, csa_stream_t stream);
 
+/* The lightning indexer with 8-bit floating-point keys and queries (the
+ * pages' indexer runs in low precision [gitcode §2.1.1]; this FP8 variant is
+ * this library's).  Keys are stored as E4M3 codes with one float32 scale per
+ * key row: scale = amax/448 (1 for an all-zero row), code = E4M3 of
+ * x/scale (round to nearest even, saturating; both divisions in float32).
+ * csa_index_keys_pack writes that form:
+ *   keys: [n_rows, idx_dim] in p->act_format -> codes [n_rows, idx_dim] uint8,
+ *   scales [n_rows] float32 (device, 16-byte aligned); idx_dim must be 128.
+ * csa_index_topk_fp8 is csa_index_topk over such keys (key_codes
+ * [B, n_cap, 128], key_scales [B, n_cap]); every query head row of q_idx is
+ * quantised by the same rule inside the call, and
+ *   score_b = sum_h w_idx[q,h] * relu((q8_h * sq_h) . (k8_b * sk_b))
+ * with the E4M3 products accumulated in float32 on the tensor cores.
+ * Requires n_idx_heads = 64, idx_dim = 128, n_cap >= 128 (or 0), and a
+ * workspace of csa_workspace_bytes(p, CSA_OP_INDEX_TOPK_FP8, ...). */
+csa_status csa_index_keys_pack(const csa_params* p, const void* keys, int64_t n_rows, int32_t idx_dim,
+                               uint8_t* codes, float* scales, csa_stream_t stream);
+csa_status csa_index_topk_fp8(const csa_params* p, const void* q_idx, const float* w_idx,
+                              int32_t n_idx_heads, int32_t idx_dim, const uint8_t* key_codes,
+                              const float* key_scales, int64_t n_cap, int32_t B, int32_t Q,
+                              const int64_t* q_pos, int32_t* topk_idx, float* topk_score, void* ws,
+                              size_t ws_bytes, csa_stream_t stream);
+
 /* csa_index_topk for callers that cannot allocate device memory.  The pages
  * have no counterpart to this entry point; it exists for integration only.
  *
@@ -234,7 +257,12 @@ csa_status hca_attend(const csa_params* p, const void* q, int32_t H, int32_t B, 
                       float* lse, void* ws, size_t ws_bytes, csa_stream_t stream);
 
 /* Workspace */
-typedef enum { CSA_OP_INDEX_TOPK = 1, CSA_OP_ATTEND = 2, CSA_OP_HCA_ATTEND = 3 } csa_op;
+typedef enum {
+    CSA_OP_INDEX_TOPK = 1,
+    CSA_OP_ATTEND = 2,
+    CSA_OP_HCA_ATTEND = 3,
+    CSA_OP_INDEX_TOPK_FP8 = 4
+} csa_op;
 
 /* Bytes of workspace an operation needs for these sizes (0 on invalid input).
  * The first 256 bytes of every workspace hold the device status word; one

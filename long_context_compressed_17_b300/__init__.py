@@ -15,8 +15,8 @@ import os
 import torch
 
 __all__ = [
-    "CsaError", "CsaParams", "F32", "BF16", "FP8_MIXED", "OP_INDEX_TOPK", "OP_ATTEND",
-    "OP_HCA_ATTEND", "params", "lib", "csa_row_bytes", "csa_cache_pack", "csa_compress", "csa_append",
+    "CsaError", "CsaParams", "F32", "BF16", "FP8_MIXED", "OP_INDEX_TOPK", "OP_INDEX_TOPK_FP8", "OP_ATTEND",
+    "OP_HCA_ATTEND", "params", "lib", "csa_row_bytes", "csa_cache_pack", "csa_compress", "csa_append", "csa_index_keys_pack", "csa_index_topk_fp8",
     "csa_index_topk", "csa_index_score", "csa_topk_select", "csa_launch_count", "csa_index_topk_noalloc", "csa_attend", "hca_attend", "csa_workspace_bytes", "csa_workspace_init",
     "csa_check_status", "csa_last_device_bits", "csa_status_string", "csa_last_error",
     "workspace", "LIB_PATH",
@@ -25,7 +25,7 @@ __all__ = [
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcsa.so")
 
 F32, BF16, FP8_MIXED = 0, 1, 2
-OP_INDEX_TOPK, OP_ATTEND, OP_HCA_ATTEND = 1, 2, 3
+OP_INDEX_TOPK, OP_ATTEND, OP_HCA_ATTEND, OP_INDEX_TOPK_FP8 = 1, 2, 3, 4
 _FMT = {"f32": F32, "bf16": BF16, "fp8m": FP8_MIXED}
 
 
@@ -75,6 +75,9 @@ def lib() -> ctypes.CDLL:
             "csa_cache_pack": (_i32, [P, _vp, _i64, _vp, _vp]),
             "csa_compress": (_i32, [P, _vp, _i32, _i64, _i64, _i64, _vp, _vp, _vp, _i64, _vp]),
             "csa_append": (_i32, [P, _vp, _i32, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _vp]),
+            "csa_index_keys_pack": (_i32, [P, _vp, _i64, _i32, _vp, _vp, _vp]),
+            "csa_index_topk_fp8": (_i32, [P, _vp, _vp, _i32, _i32, _vp, _vp, _i64, _i32, _i32, _vp,
+                                          _vp, _vp, _vp, _sz, _vp]),
             "csa_index_topk": (_i32, [P, _vp, _vp, _i32, _i32, _vp, _i64, _i32, _i32, _vp, _vp,
                                       _vp, _vp, _sz, _vp]),
             "csa_attend": (_i32, [P, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _vp, _i64, _vp,
@@ -162,6 +165,19 @@ def csa_index_topk(p, q_idx, w_idx, n_idx_heads, idx_dim, keys, n_cap, B, Q, q_p
                                 _ptr(keys), n_cap, B, Q, _ptr(q_pos), _ptr(topk_idx),
                                 _ptr(topk_score), _ptr(ws), ws_bytes, _stream(stream)),
            "csa_index_topk")
+
+
+def csa_index_keys_pack(p, keys, n_rows, idx_dim, codes, scales, stream=None):
+    _check(lib().csa_index_keys_pack(ctypes.byref(p), _ptr(keys), n_rows, idx_dim, _ptr(codes),
+                                     _ptr(scales), _stream(stream)), "csa_index_keys_pack")
+
+
+def csa_index_topk_fp8(p, q_idx, w_idx, n_idx_heads, idx_dim, key_codes, key_scales, n_cap, B, Q,
+                       q_pos, topk_idx, topk_score, ws, ws_bytes, stream=None):
+    _check(lib().csa_index_topk_fp8(ctypes.byref(p), _ptr(q_idx), _ptr(w_idx), n_idx_heads, idx_dim,
+                                    _ptr(key_codes), _ptr(key_scales), n_cap, B, Q, _ptr(q_pos),
+                                    _ptr(topk_idx), _ptr(topk_score), _ptr(ws), ws_bytes,
+                                    _stream(stream)), "csa_index_topk_fp8")
 
 
 def csa_index_score(p, q_idx, w_idx, n_idx_heads, idx_dim, keys, n_cap, B, Q, q_pos, scores,

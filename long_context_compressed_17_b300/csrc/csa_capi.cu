@@ -70,7 +70,7 @@ RopeTheta rope_theta(const Geometry& g) {
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-IndexTopkPlan plan_index_topk(const Geometry& g, int B, int Q, int HI, int64_t n_cap) {
+IndexTopkPlan plan_index_topk(const Geometry& g, int B, int Q, int HI, int64_t n_cap, bool fp8) {
     (void)g;
     (void)B;
     (void)HI;
@@ -78,7 +78,12 @@ IndexTopkPlan plan_index_topk(const Geometry& g, int B, int Q, int HI, int64_t n
     pl.n_cap_pad = (n_cap + 127) / 128 * 128;
     pl.scores_off = kStatusWordBytes;
     pl.scores_bytes = align256((size_t)Q * (size_t)pl.n_cap_pad * sizeof(float));
+    pl.q8_off = pl.weff_off = pl.scores_off + pl.scores_bytes;
     pl.total = pl.scores_off + pl.scores_bytes;
+    if (fp8) {
+        pl.weff_off = pl.q8_off + align256((size_t)Q * 64 * 128);
+        pl.total = pl.weff_off + align256((size_t)Q * 64 * sizeof(float));
+    }
     return pl;
 }
 
@@ -256,6 +261,7 @@ size_t csa_workspace_bytes(const csa_params* p, int32_t op, int32_t B, int32_t Q
     if (check_params(p) != CSA_OK || B <= 0 || Q < 0 || n_cap < 0 || n_win < 0) return 0;
     Geometry g = resolve(p);
     if (op == CSA_OP_INDEX_TOPK) return plan_index_topk(g, B, Q, n_idx_heads, n_cap).total;
+    if (op == CSA_OP_INDEX_TOPK_FP8) return plan_index_topk(g, B, Q, n_idx_heads, n_cap, true).total;
     if (op == CSA_OP_ATTEND) return H > 0 ? plan_attend(g, true, B, Q, H, n_cap, n_win).total : 0;
     if (op == CSA_OP_HCA_ATTEND) return H > 0 ? plan_attend(g, false, B, Q, H, n_cap, n_win).total : 0;
     return 0;
@@ -403,6 +409,58 @@ static csa_status attend_common(const csa_params* p, bool sparse, const void* q,
                                   n_win, win_pos0, sink, out, lse, w,
                                   reinterpret_cast<uint32_t*>(w), (cudaStream_t)stream);
     return e == cudaSuccess ? CSA_OK : cuda_fail(e, name);
+}
+
+csa_status csa_index_keys_pack(const csa_params* p, const void* keys, int64_t n_rows, int32_t idx_dim,
+                               uint8_t* codes, float* scales, csa_stream_t stream) {
+    CHECK(check_params(p));
+    if (idx_dim != 128) return fail(CSA_ERR_UNSUPPORTED, "idx_dim %d: E4M3 keys take 128", idx_dim);
+    if (n_rows < 0) return fail(CSA_ERR_INVALID_ARG, "n_rows < 0");
+    if (n_rows == 0) return CSA_OK;
+    CHECK(check_ptr(keys, "keys"));
+    CHECK(check_ptr(codes, "codes"));
+    CHECK(check_ptr(scales, "scales"));
+    Geometry g = resolve(p);
+    cudaError_t e = launch_pack_idx_keys(g, keys, n_rows, codes, scales, (cudaStream_t)stream);
+    return e == cudaSuccess ? CSA_OK : cuda_fail(e, "csa_index_keys_pack");
+}
+
+csa_status csa_index_topk_fp8(const csa_params* p, const void* q_idx, const float* w_idx,
+                              int32_t n_idx_heads, int32_t idx_dim, const uint8_t* key_codes,
+                              const float* key_scales, int64_t n_cap, int32_t B, int32_t Q,
+                              const int64_t* q_pos, int32_t* topk_idx, float* topk_score, void* ws,
+                              size_t ws_bytes, csa_stream_t stream) {
+    CHECK(check_params(p));
+    if (p->topk < 1 || p->topk > 4096) return fail(CSA_ERR_INVALID_ARG, "topk %d not in [1, 4096]", p->topk);
+    if (idx_dim != 128 || n_idx_heads != 64)
+        return fail(CSA_ERR_UNSUPPORTED, "E4M3 keys take 64 heads of 128 dims (got %d x %d)", n_idx_heads, idx_dim);
+    if (B < 1 || Q < 0 || Q % B != 0) return fail(CSA_ERR_INVALID_ARG, "Q %d must be a multiple of B %d", Q, B);
+    if (n_cap < 0 || n_cap > (1LL << 30)) return fail(CSA_ERR_INVALID_ARG, "n_cap out of range");
+    if (Q == 0) return CSA_OK;
+    if (n_cap > 0 && n_cap < 128) return fail(CSA_ERR_UNSUPPORTED, "E4M3 keys need n_cap >= 128");
+    CHECK(check_ptr(q_idx, "q_idx"));
+    CHECK(check_ptr(w_idx, "w_idx"));
+    CHECK(check_ptr(key_codes, "key_codes", n_cap == 0));
+    CHECK(check_ptr(key_scales, "key_scales", n_cap == 0));
+    CHECK(check_ptr(q_pos, "q_pos"));
+    CHECK(check_ptr(topk_idx, "topk_idx"));
+    CHECK(check_ptr(topk_score, "topk_score", true));
+    CHECK(check_ptr(ws, "ws"));
+    if (topk_chunk(n_cap, Q, p->topk) == 0)
+        return fail(CSA_ERR_UNSUPPORTED, "top-%d of %lld blocks does not fit the selection's shared memory",
+                    p->topk, (long long)n_cap);
+    Geometry g = resolve(p);
+    IndexTopkPlan pl = plan_index_topk(g, B, Q, n_idx_heads, n_cap, true);
+    if (ws_bytes < pl.total) return fail(CSA_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, pl.total);
+    uint8_t* w = reinterpret_cast<uint8_t*>(ws);
+    uint32_t* status = reinterpret_cast<uint32_t*>(w);
+    float* scores = reinterpret_cast<float*>(w + pl.scores_off);
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = launch_indexer_fp8(g, q_idx, w_idx, key_codes, key_scales, n_cap, B, Q, q_pos, status, scores,
+                                       pl.n_cap_pad, w + pl.q8_off, reinterpret_cast<float*>(w + pl.weff_off), st);
+    if (e != cudaSuccess) return cuda_fail(e, "csa_index_topk_fp8: indexer");
+    e = launch_topk(g, scores, pl.n_cap_pad, n_cap, Q, q_pos, topk_idx, topk_score, st);
+    return e == cudaSuccess ? CSA_OK : cuda_fail(e, "csa_index_topk_fp8: top-k");
 }
 
 csa_status csa_attend(const csa_params* p, const void* q, int32_t H, int32_t B, int32_t Q,

@@ -35,9 +35,10 @@ RopeTheta rope_theta(const Geometry& g);
 struct IndexTopkPlan {
     size_t scores_off, scores_bytes;  // [Q, n_cap_pad] float32
     int64_t n_cap_pad;
+    size_t q8_off, weff_off;          // E4M3 keys: query codes [Q, 64, 128], weights [Q, 64] float32
     size_t total;
 };
-IndexTopkPlan plan_index_topk(const Geometry& g, int B, int Q, int HI, int64_t n_cap);
+IndexTopkPlan plan_index_topk(const Geometry& g, int B, int Q, int HI, int64_t n_cap, bool fp8 = false);
 
 struct AttendPlan {
     int splits;           // split-K factor over the row list
@@ -73,6 +74,12 @@ cudaError_t launch_indexer(const Geometry& g, const void* q_idx, const float* w_
                            int dI, const void* keys, int64_t n_cap, int B, int Q,
                            const int64_t* q_pos, uint32_t* status, float* scores, int64_t ld,
                            cudaStream_t st);
+cudaError_t launch_indexer_fp8(const Geometry& g, const void* q_idx, const float* w_idx, const uint8_t* key_codes,
+                               const float* key_scales, int64_t n_cap, int B, int Q, const int64_t* q_pos,
+                               uint32_t* status, float* scores, int64_t ld, uint8_t* q8, float* w_eff,
+                               cudaStream_t st);
+cudaError_t launch_pack_idx_keys(const Geometry& g, const void* rows, int64_t n, uint8_t* codes, float* scales,
+                                 cudaStream_t st);
 cudaError_t launch_topk(const Geometry& g, float* scores, int64_t ld, int64_t n_cap, int Q,
                         const int64_t* q_pos, int32_t* idx, float* sel, cudaStream_t st);
 // Chunk size of the top-k selection for these sizes; 0: does not fit.

@@ -64,8 +64,8 @@ __global__ void __launch_bounds__(kIdxTile)
 }
 
 cudaError_t launch_indexer_tc(const Geometry& g, const void* q_idx, const float* w_idx, int HI,
-                              int dI, const void* keys, int64_t n_cap, int B, int Q,
-                              const int64_t* q_pos, uint32_t* status, float* scores, int64_t ld,
+                              int dI, const void* keys, const float* key_scales, int64_t n_cap, int B,
+                              int Q, const int64_t* q_pos, uint32_t* status, float* scores, int64_t ld,
                               cudaStream_t st, bool* launched);
 
 cudaError_t launch_indexer(const Geometry& g, const void* q_idx, const float* w_idx, int HI,
@@ -74,7 +74,7 @@ cudaError_t launch_indexer(const Geometry& g, const void* q_idx, const float* w_
                            cudaStream_t st) {
     if (Q == 0 || n_cap == 0) return cudaSuccess;
     bool launched = false;
-    cudaError_t e = launch_indexer_tc(g, q_idx, w_idx, HI, dI, keys, n_cap, B, Q, q_pos, status,
+    cudaError_t e = launch_indexer_tc(g, q_idx, w_idx, HI, dI, keys, nullptr, n_cap, B, Q, q_pos, status,
                                       scores, ld, st, &launched);
     if (launched || e != cudaSuccess) return e;
     const int qps = Q / B;
@@ -99,6 +99,85 @@ cudaError_t launch_indexer(const Geometry& g, const void* q_idx, const float* w_
         return cudaGetLastError();
     };
     return dI == 64 ? run(indexer_generic_kernel<64>) : run(indexer_generic_kernel<128>);
+}
+
+// ------------------------------------------------------------ E4M3 indexer rows
+// One warp quantises a row of 128 values (4 per lane, lane l the dims
+// 4l .. 4l+3): scale = amax/448 (1 for an all-zero row), code = E4M3 of
+// x / scale, round to nearest even with saturation, both divisions in float32
+// (the rule of the mixed cache rows, over the whole row).  The lane's four
+// codes come back packed little-endian; the scale goes to every lane.
+__device__ __forceinline__ float warp_quant_row128(const uint8_t* row, int act, int lane, uint32_t* codes4) {
+    float x[4];
+#pragma unroll
+    for (int e = 0; e < 4; e++) x[e] = load_act(row, act, 4 * lane + e);
+    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    amax = warp_max(amax);
+    const float scale = amax == 0.f ? 1.f : __fdiv_rn(amax, 448.f);
+    uint32_t c = 0;
+#pragma unroll
+    for (int e = 0; e < 4; e++) c |= (uint32_t)f32_to_e4m3_sat(__fdiv_rn(x[e], scale)) << (8 * e);
+    *codes4 = c;
+    return scale;
+}
+
+// rows [n, 128] (act format) -> codes [n, 128], scales [n]; 8 rows a block.
+__global__ void __launch_bounds__(256)
+    pack_idx_keys_kernel(const uint8_t* __restrict__ rows, int act, int64_t n, uint8_t* __restrict__ codes,
+                         float* __restrict__ scales) {
+    const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= n) return;
+    const int64_t rb = act == CSA_F32 ? 4 * 128 : 2 * 128;
+    uint32_t c;
+    const float sc = warp_quant_row128(rows + r * rb, act, lane, &c);
+    reinterpret_cast<uint32_t*>(codes + r * 128)[lane] = c;
+    if (lane == 0) scales[r] = sc;
+}
+
+// Query heads [Q*64, 128] -> E4M3 codes, and the head weights times the head
+// scales: w_eff[q, h] = w_idx[q, h] * scale_qh (the score is
+// sk * sum_h w_h * scale_qh * relu(q8_h . k8), every scale positive).
+__global__ void __launch_bounds__(256)
+    quant_idx_queries_kernel(const uint8_t* __restrict__ q, int act, const float* __restrict__ w_idx, int64_t rows,
+                             uint8_t* __restrict__ q8, float* __restrict__ w_eff) {
+    const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= rows) return;
+    const int64_t rb = act == CSA_F32 ? 4 * 128 : 2 * 128;
+    uint32_t c;
+    const float sc = warp_quant_row128(q + r * rb, act, lane, &c);
+    reinterpret_cast<uint32_t*>(q8 + r * 128)[lane] = c;
+    if (lane == 0) w_eff[r] = w_idx[r] * sc;
+}
+
+cudaError_t launch_pack_idx_keys(const Geometry& g, const void* rows, int64_t n, uint8_t* codes, float* scales,
+                                 cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    pack_idx_keys_kernel<<<(unsigned)((n + 7) / 8), 256, 0, st>>>(reinterpret_cast<const uint8_t*>(rows), g.act,
+                                                                   n, codes, scales);
+    note_launch();
+    return cudaGetLastError();
+}
+
+// E4M3 indexer: the queries are quantised into q8 / w_eff (workspace), then
+// the tcgen05 kernel scores E4M3 keys against them.
+cudaError_t launch_indexer_fp8(const Geometry& g, const void* q_idx, const float* w_idx, const uint8_t* key_codes,
+                               const float* key_scales, int64_t n_cap, int B, int Q, const int64_t* q_pos,
+                               uint32_t* status, float* scores, int64_t ld, uint8_t* q8, float* w_eff,
+                               cudaStream_t st) {
+    if (Q == 0 || n_cap == 0) return cudaSuccess;
+    const int64_t rows = (int64_t)Q * 64;
+    quant_idx_queries_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(reinterpret_cast<const uint8_t*>(q_idx),
+                                                                          g.act, w_idx, rows, q8, w_eff);
+    note_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bool launched = false;
+    e = launch_indexer_tc(g, q8, w_eff, 64, 128, key_codes, key_scales, n_cap, B, Q, q_pos, status, scores, ld,
+                          st, &launched);
+    if (e == cudaSuccess && !launched) return cudaErrorInvalidValue;  // shapes checked by the C ABI
+    return e;
 }
 
 }  // namespace csa

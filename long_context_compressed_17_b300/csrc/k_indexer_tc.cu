@@ -25,6 +25,8 @@ namespace csa {
 
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                     const uint64_t* strides_bytes, const uint32_t* box);
+bool make_tmap_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                  const uint64_t* strides_bytes, const uint32_t* box);
 
 namespace {
 
@@ -32,24 +34,31 @@ constexpr int kHI = 64;            // indexer heads (per query)
 constexpr int kDI = 128;           // indexer dim
 constexpr int kTileKeys = 128;     // MMA M
 constexpr int kStages = 4;
-constexpr uint32_t kStageBytes = kTileKeys * kDI * 2;   // 32 KiB: two 64-dim boxes
 
-template <int NQ>
+// F8: keys and queries in E4M3 (kind::f8f6f4 MMAs, K = 32 per MMA), one
+// float32 scale per key row and per query head (folded into the head
+// weights); otherwise bf16 (kind::f16, K = 16).
+template <int NQ, bool F8>
 struct Cfg {
+    static constexpr int kEB = F8 ? 1 : 2;              // bytes per element
+    static constexpr uint32_t kStageBytes = kTileKeys * kDI * kEB;  // 32 KiB bf16 (two boxes), 16 KiB E4M3 (one)
+    static constexpr int kKSteps = kDI * kEB / 32;      // MMAs per key tile: 32 bytes of K each
     static constexpr int N = NQ * kHI;                  // MMA N
     static constexpr int kAcc = NQ == 1 ? 4 : 2;        // TMEM accumulators in flight
     static constexpr int kQBufs = NQ == 1 ? 2 : 1;
     static constexpr int kEpiWarps = NQ == 1 ? 4 : 16;
     static constexpr int kQPerWarp = NQ * 4 / kEpiWarps;  // queries of a key per epilogue warp
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
-    static constexpr uint32_t kQBytes = (uint32_t)N * kDI * 2;
+    static constexpr uint32_t kQBytes = (uint32_t)N * kDI * kEB;
     static constexpr uint32_t kTmemCols = kAcc * N;     // 256 or 512
     static constexpr size_t kBarBytes = 256;
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kQBufs * kQBytes + kBarBytes;
+    static constexpr uint32_t idesc = F8 ? tc::idesc_e4m3_f32(kTileKeys, N) : tc::idesc_bf16_f32(kTileKeys, N);
 };
 
 struct IdxArgs {
-    const float* w_idx;    // [Q, 64]
+    const float* w_idx;    // [Q, 64] (F8: the head weights times the query head scales)
+    const float* key_scales;  // F8: [B, n_cap] per key row; else nullptr
     const int64_t* q_pos;  // [Q]
     float* scores;         // [Q, ld]
     int64_t ld;
@@ -75,11 +84,12 @@ __device__ __forceinline__ int64_t group_avail(const IdxArgs& a, int64_t g) {
 
 }  // namespace
 
-template <int NQ>
-__global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
+template <int NQ, bool F8>
+__global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                       const __grid_constant__ CUtensorMap tm_q, IdxArgs a) {
-    using C = Cfg<NQ>;
+    using C = Cfg<NQ, F8>;
+    constexpr uint32_t kStageBytes = C::kStageBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = sm;
@@ -147,7 +157,7 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
                 tc::mbar_arrive_expect_tx(&qfull[qb], C::kQBytes);
                 uint8_t* dst = sB + qb * C::kQBytes;
                 tc::tma_load_2d(dst, &tm_q, &qfull[qb], 0, (int)(g * C::N));
-                tc::tma_load_2d(dst + C::kQBytes / 2, &tm_q, &qfull[qb], 64, (int)(g * C::N));
+                if (!F8) tc::tma_load_2d(dst + C::kQBytes / 2, &tm_q, &qfull[qb], 64, (int)(g * C::N));
                 last_loaded = g;
                 qloads++;
             }
@@ -156,7 +166,7 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
             const int seq = (int)((g * NQ) / a.qps);
             uint8_t* dst = sA + stage * kStageBytes;
             tc::tma_load_3d(dst, &tm_keys, &full[stage], 0, t * kTileKeys, seq);
-            tc::tma_load_3d(dst + kStageBytes / 2, &tm_keys, &full[stage], 64, t * kTileKeys, seq);
+            if (!F8) tc::tma_load_3d(dst + kStageBytes / 2, &tm_keys, &full[stage], 64, t * kTileKeys, seq);
             if (++stage == kStages) {
                 stage = 0;
                 phase ^= 1u;
@@ -164,7 +174,7 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = tc::idesc_bf16_f32(kTileKeys, C::N);
+        constexpr uint32_t idesc = C::idesc;
         int stage = 0, acc = 0, quses = 0, qb = 0;
         uint32_t phase = 0, aphase = 0;
         int64_t cur_g = -1, last_used = -1, gnav = 0;
@@ -191,11 +201,16 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
             const uint32_t b_base = tc::smem_u32(sB + qb * C::kQBytes);
             const uint32_t d = tmem + (uint32_t)(acc * C::N);
 #pragma unroll
-            for (int kk = 0; kk < kDI / 16; kk++) {
-                const uint32_t ka = (uint32_t)(kk >> 2) * (kStageBytes / 2) + (uint32_t)(kk & 3) * 32u;
-                const uint32_t kb = (uint32_t)(kk >> 2) * (C::kQBytes / 2) + (uint32_t)(kk & 3) * 32u;
-                tc::mma_bf16_ss(d, tc::sdesc_kmajor_sw128(a_base + ka),
-                                tc::sdesc_kmajor_sw128(b_base + kb), idesc, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < C::kKSteps; kk++) {
+                if (F8) {  // one 128-byte row per key / head: 32 bytes of K per MMA
+                    tc::mma_f8_ss(d, tc::sdesc_kmajor_sw128(a_base + (uint32_t)kk * 32u),
+                                  tc::sdesc_kmajor_sw128(b_base + (uint32_t)kk * 32u), idesc, kk > 0 ? 1u : 0u);
+                } else {   // two 64-dim boxes of 128-byte rows
+                    const uint32_t ka = (uint32_t)(kk >> 2) * (kStageBytes / 2) + (uint32_t)(kk & 3) * 32u;
+                    const uint32_t kb = (uint32_t)(kk >> 2) * (C::kQBytes / 2) + (uint32_t)(kk & 3) * 32u;
+                    tc::mma_bf16_ss(d, tc::sdesc_kmajor_sw128(a_base + ka),
+                                    tc::sdesc_kmajor_sw128(b_base + kb), idesc, kk > 0 ? 1u : 0u);
+                }
             }
             tc::mma_commit(&empty[stage]);  // key tile free when these MMAs finish
             tc::mma_commit(&tfull[acc]);    // accumulator ready for the epilogue
@@ -261,6 +276,7 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
                         s = fmaf(w.w, fmaxf(v[4 * j4 + 3], 0.f), s);
                     }
                 }
+                if (F8 && key < a.n_cap) s *= __ldg(a.key_scales + (g * NQ / a.qps) * a.n_cap + key);
                 if (key < a.n_cap) a.scores[(g * NQ + qq) * a.ld + key] = key < nav[qq] ? s : -INFINITY;
             }
             tc::fence_before_sync();
@@ -282,26 +298,47 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
     }
 }
 
+template <int NQ, bool F8>
+static cudaError_t run_indexer(const CUtensorMap& tm_keys, const CUtensorMap& tm_q, const IdxArgs& a, int grid,
+                               cudaStream_t st) {
+    using C = Cfg<NQ, F8>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<NQ, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)C::kSmem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    indexer_tc_kernel<NQ, F8><<<grid, C::kThreads, C::kSmem, st>>>(tm_keys, tm_q, a);
+    note_launch();
+    return cudaGetLastError();
+}
+
 cudaError_t launch_indexer_tc(const Geometry& g, const void* q_idx, const float* w_idx, int HI,
-                              int dI, const void* keys, int64_t n_cap, int B, int Q,
-                              const int64_t* q_pos, uint32_t* status, float* scores, int64_t ld,
+                              int dI, const void* keys, const float* key_scales, int64_t n_cap, int B,
+                              int Q, const int64_t* q_pos, uint32_t* status, float* scores, int64_t ld,
                               cudaStream_t st, bool* launched) {
     *launched = false;
-    if (g.act != CSA_BF16 || HI != kHI || dI != kDI || n_cap < kTileKeys || Q < 1) return cudaSuccess;
+    const bool f8 = key_scales != nullptr;  // q_idx: E4M3 codes, w_idx: weights x head scales
+    if ((!f8 && g.act != CSA_BF16) || HI != kHI || dI != kDI || n_cap < kTileKeys || Q < 1) return cudaSuccess;
     if (((uintptr_t)w_idx & 15u) || (ld % 4) != 0) return cudaSuccess;
     const int qps = Q / B;
     const int NQ = (qps % 4 == 0) ? 4 : 1;
+    const uint64_t eb = f8 ? 1 : 2;
     CUtensorMap tm_keys, tm_q;
     const uint64_t kd[3] = {(uint64_t)kDI, (uint64_t)n_cap, (uint64_t)B};
-    const uint64_t ks[2] = {(uint64_t)kDI * 2, (uint64_t)n_cap * kDI * 2};
-    const uint32_t kb[3] = {64, (uint32_t)kTileKeys, 1};
+    const uint64_t ks[2] = {(uint64_t)kDI * eb, (uint64_t)n_cap * kDI * eb};
+    const uint32_t kb[3] = {(uint32_t)(128 / eb), (uint32_t)kTileKeys, 1};  // 128-byte rows
     const uint64_t qd[2] = {(uint64_t)kDI, (uint64_t)Q * kHI};
-    const uint64_t qs[1] = {(uint64_t)kDI * 2};
-    const uint32_t qbox[2] = {64, (uint32_t)(NQ * kHI)};
-    if (!make_tmap_bf16(&tm_keys, keys, 3, kd, ks, kb) || !make_tmap_bf16(&tm_q, q_idx, 2, qd, qs, qbox))
-        return cudaSuccess;  // no tensor map: the CUDA-core path runs instead
+    const uint64_t qs[1] = {(uint64_t)kDI * eb};
+    const uint32_t qbox[2] = {(uint32_t)(128 / eb), (uint32_t)(NQ * kHI)};
+    const bool maps = f8 ? (make_tmap_u8(&tm_keys, keys, 3, kd, ks, kb) && make_tmap_u8(&tm_q, q_idx, 2, qd, qs, qbox))
+                         : (make_tmap_bf16(&tm_keys, keys, 3, kd, ks, kb) &&
+                            make_tmap_bf16(&tm_q, q_idx, 2, qd, qs, qbox));
+    if (!maps) return f8 ? cudaErrorInvalidValue : cudaSuccess;  // bf16: the CUDA-core path runs instead
     IdxArgs a;
     a.w_idx = w_idx;
+    a.key_scales = key_scales;
     a.q_pos = q_pos;
     a.scores = scores;
     a.ld = ld;
@@ -314,28 +351,12 @@ cudaError_t launch_indexer_tc(const Geometry& g, const void* q_idx, const float*
     const int64_t sms = num_sms();
     const int grid = (int)(a.total_units < sms ? a.total_units : sms);
     cudaError_t e;
-    if (NQ == 1) {
-        static bool attr = false;
-        if (!attr) {
-            e = cudaFuncSetAttribute(indexer_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)Cfg<1>::kSmem);
-            if (e != cudaSuccess) return e;
-            attr = true;
-        }
-        indexer_tc_kernel<1><<<grid, Cfg<1>::kThreads, Cfg<1>::kSmem, st>>>(tm_keys, tm_q, a);
-    } else {
-        static bool attr = false;
-        if (!attr) {
-            e = cudaFuncSetAttribute(indexer_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)Cfg<4>::kSmem);
-            if (e != cudaSuccess) return e;
-            attr = true;
-        }
-        indexer_tc_kernel<4><<<grid, Cfg<4>::kThreads, Cfg<4>::kSmem, st>>>(tm_keys, tm_q, a);
-    }
-    note_launch();
-    *launched = true;
-    return cudaGetLastError();
+    if (NQ == 1)
+        e = f8 ? run_indexer<1, true>(tm_keys, tm_q, a, grid, st) : run_indexer<1, false>(tm_keys, tm_q, a, grid, st);
+    else
+        e = f8 ? run_indexer<4, true>(tm_keys, tm_q, a, grid, st) : run_indexer<4, false>(tm_keys, tm_q, a, grid, st);
+    if (e == cudaSuccess) *launched = true;
+    return e;
 }
 
 }  // namespace csa

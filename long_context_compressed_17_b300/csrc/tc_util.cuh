@@ -227,6 +227,17 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// The same for kind::f8f6f4 operands (8-bit floating point, K = 32 per MMA).
+__device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread is complete.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile(
@@ -387,6 +398,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn = 0
            | ((uint32_t)(b_mn & 1) << 16)  // B major: 0 K, 1 MN
            | ((uint32_t)(N >> 3) << 17)    // N / 8
            | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// Instruction descriptor of tcgen05.mma kind::f8f6f4: E4M3 A and B (format
+// code 0), fp32 accumulator, both K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+    return (1u << 4)                      // D format: f32
+           | (0u << 7)                    // A format: E4M3
+           | (0u << 10)                   // B format: E4M3
+           | ((uint32_t)(N >> 3) << 17)   // N / 8
+           | ((uint32_t)(M >> 4) << 24);  // M / 16
 }
 
 // Shared-memory matrix descriptor for a K-major operand stored with the

@@ -166,3 +166,23 @@ def test_workspace_sizes(L):
     assert n >= 256 + 32 * 32768 * 4
     assert L.csa_workspace_bytes(p, L.OP_ATTEND, 32, 32, 64, 64, 32768, 128) > 256
     assert L.csa_workspace_bytes(p, 99, 32, 32, 64, 64, 32768, 128) == 0
+
+
+def test_index_topk_fp8_validation(L):
+    import torch
+    p = L.params(512, 4, topk=64)
+    base = dict(p=p, q_idx=FAKE, w_idx=FAKE, n_idx_heads=64, idx_dim=128, key_codes=FAKE,
+                key_scales=FAKE, n_cap=1024, B=2, Q=2, q_pos=FAKE, topk_idx=FAKE, topk_score=None,
+                ws=FAKE, ws_bytes=1 << 30)
+    assert _status_of(L.csa_index_topk_fp8, **dict(base, idx_dim=64)) == 2      # unsupported
+    assert _status_of(L.csa_index_topk_fp8, **dict(base, n_idx_heads=32)) == 2
+    assert _status_of(L.csa_index_topk_fp8, **dict(base, n_cap=100)) == 2       # < one key tile
+    assert _status_of(L.csa_index_topk_fp8, **dict(base, Q=3)) == 1             # Q % B
+    assert _status_of(L.csa_index_topk_fp8, **dict(base, key_scales=None)) == 1
+    assert _status_of(L.csa_index_topk_fp8, **dict(base, ws_bytes=1024)) == 4   # workspace
+    assert _status_of(L.csa_index_keys_pack, p=p, keys=FAKE, n_rows=4, idx_dim=64, codes=FAKE,
+                      scales=FAKE) == 2
+    # the E4M3 workspace adds the query codes and weights to the bf16 one
+    a = L.csa_workspace_bytes(p, L.OP_INDEX_TOPK, 2, 8, 64, 64, 4096, 128)
+    b = L.csa_workspace_bytes(p, L.OP_INDEX_TOPK_FP8, 2, 8, 64, 64, 4096, 128)
+    assert b >= a + 8 * 64 * 128 + 8 * 64 * 4
