@@ -213,7 +213,10 @@ def algorithmic(w: workloads.Workload, row_bytes: int):
         n_av = [L // w.m for L in w.lengths]
         q_out = w.H * w.D * act_es * 2
         if w.kind == "csa_decode":
-            idx_bytes = sum(n * w.d_I * act_es + w.H_I * w.d_I * act_es + w.H_I * 4 for n in n_av)
+            if w.idx_fmt == "fp8":  # E4M3 codes and a float32 scale per key; bf16 queries quantised in the step
+                idx_bytes = sum(n * (w.d_I + 4) + w.H_I * w.d_I * act_es + w.H_I * 4 for n in n_av)
+            else:
+                idx_bytes = sum(n * w.d_I * act_es + w.H_I * w.d_I * act_es + w.H_I * 4 for n in n_av)
             rows = w.B * (min(w.topk, max(n_av)) + w.W)
             step = idx_bytes + rows * row_bytes + w.B * q_out
             return {"kernel": "indexer", "bound": "hbm", "bytes": idx_bytes, "step_bytes": step}
@@ -263,6 +266,15 @@ class GpuStep:
             if w.kind == "csa_decode":
                 self.ld = (w.n_cap + 127) // 128 * 128
                 self.scores = torch.empty(w.B, self.ld, dtype=torch.float32, device="cuda")
+                if w.idx_fmt == "fp8":  # layer state: the keys in E4M3, packed once
+                    keys = inp["keys"]
+                    self.key_codes = torch.empty(keys.shape, dtype=torch.uint8, device="cuda")
+                    self.key_scales = torch.empty(keys.shape[:-1], dtype=torch.float32, device="cuda")
+                    L.csa_index_keys_pack(cfg.params(), keys, keys.numel() // w.d_I, w.d_I, self.key_codes,
+                                          self.key_scales)
+                    self.idx_ws_bytes = 256 + (w.B * 64 * 128 + 255) // 256 * 256 + (w.B * 64 * 4 + 255) // 256 * 256
+                    self.idx_ws = L.workspace(self.idx_ws_bytes)
+                    torch.cuda.synchronize()
         else:
             self.layer = PrefillLayer(cfg, w.T_cached, w.T_new)
             if w.T_cached:
@@ -294,6 +306,11 @@ class GpuStep:
         B = w.B if w.kind == "csa_decode" else 1
         n_cap = w.n_cap if w.kind == "csa_decode" else lay.n_cap
         keys = inp["keys"]
+        if w.idx_fmt == "fp8":
+            L.csa_index_score_fp8(lay.p, inp["q_idx"], inp["w_idx"], w.H_I, w.d_I, self.key_codes,
+                                  self.key_scales, n_cap, B, w.Q, inp["q_pos"], self.scores, self.ld,
+                                  self.idx_ws, self.idx_ws_bytes)
+            return
         L.csa_index_score(lay.p, inp["q_idx"], inp["w_idx"], w.H_I, w.d_I, keys, n_cap, B, w.Q,
                           inp["q_pos"], self.scores, self.ld, lay.ws, lay.ws_bytes)
 
@@ -523,7 +540,15 @@ def oracle_step(w, s, raw_pos0=0):
             window[b, Lb - 1 - int(s["win_pos0"][b])] = oracle.store_rows(r, fmt)[0]
         seq = np.arange(n_q, dtype=np.int32)
         idx = None
-        if w.kind == "csa_decode":
+        if w.kind == "csa_decode" and w.idx_fmt == "fp8":
+            idx = np.empty((n_q, w.topk), np.int32)
+            for b in range(n_q):
+                n_av = (int(s["q_pos"][b]) + 1) // w.m
+                keys = (s["keys"][b, :n_av].astype(np.uint32) << 16).view(np.float32)  # bf16 bits
+                codes, scales = oracle.pack_idx_keys_fp8(keys)
+                sc = oracle.index_scores_fp8(s["q_idx"][b], s["w_idx"][b], codes, scales)
+                idx[b], _ = oracle.topk(sc, w.topk)
+        elif w.kind == "csa_decode":
             idx, _ = oracle.index_topk_batch(s["q_idx"], s["w_idx"], s["keys"], seq, s["q_pos"],
                                              w.m, w.topk)
         return oracle.attend_batch(s["q"], seq, s["q_pos"], w.m, cache, w.D, idx, window,

@@ -183,9 +183,18 @@ csa_status csa_topk_select(const csa_params* p, float* scores, int64_t ld_scores
  *   score_b = sum_h w_idx[q,h] * relu((q8_h * sq_h) . (k8_b * sk_b))
  * with the E4M3 products accumulated in float32 on the tensor cores.
  * Requires n_idx_heads = 64, idx_dim = 128, n_cap >= 128 (or 0), and a
- * workspace of csa_workspace_bytes(p, CSA_OP_INDEX_TOPK_FP8, ...). */
+ * workspace of csa_workspace_bytes(p, CSA_OP_INDEX_TOPK_FP8, ...).
+ * csa_index_score_fp8 is its scoring half, as csa_index_score is for bf16
+ * keys (scores [Q, ld_scores] float32); its workspace needs 256 bytes plus
+ * Q*64*128 bytes and Q*64 floats, each rounded up to 256 bytes (no more than
+ * the CSA_OP_INDEX_TOPK_FP8 size for the same shapes). */
 csa_status csa_index_keys_pack(const csa_params* p, const void* keys, int64_t n_rows, int32_t idx_dim,
                                uint8_t* codes, float* scales, csa_stream_t stream);
+csa_status csa_index_score_fp8(const csa_params* p, const void* q_idx, const float* w_idx,
+                               int32_t n_idx_heads, int32_t idx_dim, const uint8_t* key_codes,
+                               const float* key_scales, int64_t n_cap, int32_t B, int32_t Q,
+                               const int64_t* q_pos, float* scores, int64_t ld_scores, void* ws,
+                               size_t ws_bytes, csa_stream_t stream);
 csa_status csa_index_topk_fp8(const csa_params* p, const void* q_idx, const float* w_idx,
                               int32_t n_idx_heads, int32_t idx_dim, const uint8_t* key_codes,
                               const float* key_scales, int64_t n_cap, int32_t B, int32_t Q,

@@ -16,7 +16,7 @@ import torch
 
 __all__ = [
     "CsaError", "CsaParams", "F32", "BF16", "FP8_MIXED", "OP_INDEX_TOPK", "OP_INDEX_TOPK_FP8", "OP_ATTEND",
-    "OP_HCA_ATTEND", "params", "lib", "csa_row_bytes", "csa_cache_pack", "csa_compress", "csa_append", "csa_index_keys_pack", "csa_index_topk_fp8",
+    "OP_HCA_ATTEND", "params", "lib", "csa_row_bytes", "csa_cache_pack", "csa_compress", "csa_append", "csa_index_keys_pack", "csa_index_score_fp8", "csa_index_topk_fp8",
     "csa_index_topk", "csa_index_score", "csa_topk_select", "csa_launch_count", "csa_index_topk_noalloc", "csa_attend", "hca_attend", "csa_workspace_bytes", "csa_workspace_init",
     "csa_check_status", "csa_last_device_bits", "csa_status_string", "csa_last_error",
     "workspace", "LIB_PATH",
@@ -76,6 +76,8 @@ def lib() -> ctypes.CDLL:
             "csa_compress": (_i32, [P, _vp, _i32, _i64, _i64, _i64, _vp, _vp, _vp, _i64, _vp]),
             "csa_append": (_i32, [P, _vp, _i32, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _vp]),
             "csa_index_keys_pack": (_i32, [P, _vp, _i64, _i32, _vp, _vp, _vp]),
+            "csa_index_score_fp8": (_i32, [P, _vp, _vp, _i32, _i32, _vp, _vp, _i64, _i32, _i32, _vp,
+                                           _vp, _i64, _vp, _sz, _vp]),
             "csa_index_topk_fp8": (_i32, [P, _vp, _vp, _i32, _i32, _vp, _vp, _i64, _i32, _i32, _vp,
                                           _vp, _vp, _vp, _sz, _vp]),
             "csa_index_topk": (_i32, [P, _vp, _vp, _i32, _i32, _vp, _i64, _i32, _i32, _vp, _vp,
@@ -170,6 +172,14 @@ def csa_index_topk(p, q_idx, w_idx, n_idx_heads, idx_dim, keys, n_cap, B, Q, q_p
 def csa_index_keys_pack(p, keys, n_rows, idx_dim, codes, scales, stream=None):
     _check(lib().csa_index_keys_pack(ctypes.byref(p), _ptr(keys), n_rows, idx_dim, _ptr(codes),
                                      _ptr(scales), _stream(stream)), "csa_index_keys_pack")
+
+
+def csa_index_score_fp8(p, q_idx, w_idx, n_idx_heads, idx_dim, key_codes, key_scales, n_cap, B, Q,
+                        q_pos, scores, ld_scores, ws, ws_bytes, stream=None):
+    _check(lib().csa_index_score_fp8(ctypes.byref(p), _ptr(q_idx), _ptr(w_idx), n_idx_heads,
+                                     idx_dim, _ptr(key_codes), _ptr(key_scales), n_cap, B, Q,
+                                     _ptr(q_pos), _ptr(scores), ld_scores, _ptr(ws), ws_bytes,
+                                     _stream(stream)), "csa_index_score_fp8")
 
 
 def csa_index_topk_fp8(p, q_idx, w_idx, n_idx_heads, idx_dim, key_codes, key_scales, n_cap, B, Q,

@@ -425,6 +425,40 @@ csa_status csa_index_keys_pack(const csa_params* p, const void* keys, int64_t n_
     return e == cudaSuccess ? CSA_OK : cuda_fail(e, "csa_index_keys_pack");
 }
 
+csa_status csa_index_score_fp8(const csa_params* p, const void* q_idx, const float* w_idx,
+                               int32_t n_idx_heads, int32_t idx_dim, const uint8_t* key_codes,
+                               const float* key_scales, int64_t n_cap, int32_t B, int32_t Q,
+                               const int64_t* q_pos, float* scores, int64_t ld_scores, void* ws,
+                               size_t ws_bytes, csa_stream_t stream) {
+    CHECK(check_params(p));
+    if (idx_dim != 128 || n_idx_heads != 64)
+        return fail(CSA_ERR_UNSUPPORTED, "E4M3 keys take 64 heads of 128 dims (got %d x %d)", n_idx_heads, idx_dim);
+    if (B < 1 || Q < 0 || Q % B != 0) return fail(CSA_ERR_INVALID_ARG, "Q %d must be a multiple of B %d", Q, B);
+    if (n_cap < 0 || n_cap > (1LL << 30)) return fail(CSA_ERR_INVALID_ARG, "n_cap out of range");
+    if (ld_scores < n_cap || ld_scores % 4 != 0)
+        return fail(CSA_ERR_INVALID_ARG, "ld_scores %lld must be >= n_cap and a multiple of 4", (long long)ld_scores);
+    if (Q == 0) return CSA_OK;
+    if (n_cap > 0 && n_cap < 128) return fail(CSA_ERR_UNSUPPORTED, "E4M3 keys need n_cap >= 128");
+    CHECK(check_ptr(q_idx, "q_idx"));
+    CHECK(check_ptr(w_idx, "w_idx"));
+    CHECK(check_ptr(key_codes, "key_codes", n_cap == 0));
+    CHECK(check_ptr(key_scales, "key_scales", n_cap == 0));
+    CHECK(check_ptr(q_pos, "q_pos"));
+    CHECK(check_ptr(scores, "scores"));
+    CHECK(check_ptr(ws, "ws"));
+    // workspace: status word, then the query codes and weights
+    const size_t q8_off = kStatusWordBytes;
+    const size_t weff_off = q8_off + align256((size_t)Q * 64 * 128);
+    const size_t need = weff_off + align256((size_t)Q * 64 * sizeof(float));
+    if (ws_bytes < need) return fail(CSA_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+    Geometry g = resolve(p);
+    uint8_t* w = reinterpret_cast<uint8_t*>(ws);
+    cudaError_t e = launch_indexer_fp8(g, q_idx, w_idx, key_codes, key_scales, n_cap, B, Q, q_pos,
+                                       reinterpret_cast<uint32_t*>(w), scores, ld_scores, w + q8_off,
+                                       reinterpret_cast<float*>(w + weff_off), (cudaStream_t)stream);
+    return e == cudaSuccess ? CSA_OK : cuda_fail(e, "csa_index_score_fp8");
+}
+
 csa_status csa_index_topk_fp8(const csa_params* p, const void* q_idx, const float* w_idx,
                               int32_t n_idx_heads, int32_t idx_dim, const uint8_t* key_codes,
                               const float* key_scales, int64_t n_cap, int32_t B, int32_t Q,

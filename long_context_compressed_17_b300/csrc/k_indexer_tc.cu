@@ -33,7 +33,6 @@ namespace {
 constexpr int kHI = 64;            // indexer heads (per query)
 constexpr int kDI = 128;           // indexer dim
 constexpr int kTileKeys = 128;     // MMA M
-constexpr int kStages = 4;
 
 // F8: keys and queries in E4M3 (kind::f8f6f4 MMAs, K = 32 per MMA), one
 // float32 scale per key row and per query head (folded into the head
@@ -44,14 +43,22 @@ struct Cfg {
     static constexpr uint32_t kStageBytes = kTileKeys * kDI * kEB;  // 32 KiB bf16 (two boxes), 16 KiB E4M3 (one)
     static constexpr int kKSteps = kDI * kEB / 32;      // MMAs per key tile: 32 bytes of K each
     static constexpr int N = NQ * kHI;                  // MMA N
-    static constexpr int kAcc = NQ == 1 ? 4 : 2;        // TMEM accumulators in flight
+    // key tiles and TMEM accumulators in flight: E4M3 tiles are half the bytes,
+    // so twice as many are in flight for the same shared memory
+    static constexpr int kStages = F8 ? 8 : 4;
+    static constexpr int kAcc = NQ == 1 ? (F8 ? 8 : 4) : 2;
     static constexpr int kQBufs = NQ == 1 ? 2 : 1;
-    static constexpr int kEpiWarps = NQ == 1 ? 4 : 16;
-    static constexpr int kQPerWarp = NQ * 4 / kEpiWarps;  // queries of a key per epilogue warp
+    // Epilogue warps: for NQ = 4, sixteen (four per TMEM lane quarter, one
+    // query each); for NQ = 1, two groups of four that take alternate
+    // accumulators (a tile's epilogue is latency-bound: two in flight).
+    static constexpr int kEpiWarps = NQ == 1 ? 8 : 16;
+    static constexpr int kEpiGroups = NQ == 1 ? 2 : 1;
+    static constexpr int kQPerWarp = NQ * 4 * kEpiGroups / kEpiWarps;  // queries of a key per epilogue warp
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
     static constexpr uint32_t kQBytes = (uint32_t)N * kDI * kEB;
     static constexpr uint32_t kTmemCols = kAcc * N;     // 256 or 512
-    static constexpr size_t kBarBytes = 256;
+    static constexpr size_t kBarBytes = 512;
+    static_assert((2 * kStages + 2 * kQBufs + 2 * kAcc) * 8 + 8 <= kBarBytes, "barrier area too small");
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kQBufs * kQBytes + kBarBytes;
     static constexpr uint32_t idesc = F8 ? tc::idesc_e4m3_f32(kTileKeys, N) : tc::idesc_bf16_f32(kTileKeys, N);
 };
@@ -93,10 +100,10 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = sm;
-    uint8_t* sB = sA + kStages * kStageBytes;
+    uint8_t* sB = sA + C::kStages * kStageBytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::kQBufs * C::kQBytes);
-    uint64_t* empty = full + kStages;
-    uint64_t* qfull = empty + kStages;
+    uint64_t* empty = full + C::kStages;
+    uint64_t* qfull = empty + C::kStages;
     uint64_t* qempty = qfull + C::kQBufs;
     uint64_t* tfull = qempty + C::kQBufs;
     uint64_t* tempty = tfull + C::kAcc;
@@ -105,7 +112,7 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; s++) {
+        for (int s = 0; s < C::kStages; s++) {
             tc::mbar_init(&full[s], 1);
             tc::mbar_init(&empty[s], 1);
         }
@@ -115,7 +122,7 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
         }
         for (int c = 0; c < C::kAcc; c++) {
             tc::mbar_init(&tfull[c], 1);
-            tc::mbar_init(&tempty[c], C::kEpiWarps);  // one arrival per epilogue warp
+            tc::mbar_init(&tempty[c], C::kEpiWarps / C::kEpiGroups);  // one arrival per warp of its group
         }
         *abort_flag = 0;
         tc::fence_barrier_init();
@@ -167,7 +174,7 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
             uint8_t* dst = sA + stage * kStageBytes;
             tc::tma_load_3d(dst, &tm_keys, &full[stage], 0, t * kTileKeys, seq);
             if (!F8) tc::tma_load_3d(dst + kStageBytes / 2, &tm_keys, &full[stage], 64, t * kTileKeys, seq);
-            if (++stage == kStages) {
+            if (++stage == C::kStages) {
                 stage = 0;
                 phase ^= 1u;
             }
@@ -214,7 +221,7 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
             }
             tc::mma_commit(&empty[stage]);  // key tile free when these MMAs finish
             tc::mma_commit(&tfull[acc]);    // accumulator ready for the epilogue
-            if (++stage == kStages) {
+            if (++stage == C::kStages) {
                 stage = 0;
                 phase ^= 1u;
             }
@@ -227,11 +234,19 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
         // ------------------------------------------------ epilogue: one key per thread
         const int quarter = warp & 3;          // TMEM lanes this warp may read
         const int row = quarter * 32 + lane;   // key within the tile
-        const int q0 = ((warp - 2) >> 2) * C::kQPerWarp;  // this warp's queries: q0 .. q0 + kQPerWarp - 1
+        static_assert(C::kQPerWarp == 1, "one query per epilogue warp");
+        const int wq = (warp - 2) >> 2;
+        const int grp = C::kEpiGroups > 1 ? wq : 0;  // this warp takes the accumulators acc % groups == grp
+        const int q0 = C::kEpiGroups > 1 ? 0 : wq;   // this warp's query within the query group
         int acc = 0;
         uint32_t aphase = 0;
         int64_t cur_g = -1, gnav = 0;
         int64_t nav[NQ];
+        // the query's head weights: in registers for decode (loaded once per query
+        // group), read through L1 per tile in prefill (the registers go to the
+        // sixteen epilogue warps there)
+        constexpr bool kWRegs = NQ == 1;
+        float wr[kWRegs ? kHI : 1];
         for (int64_t u = u0; u < u1; ++u) {
             const int64_t g = u / a.n_tiles;
             const int t = (int)(u % a.n_tiles);
@@ -243,14 +258,32 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
                     nav[qq] = min((a.q_pos[g * NQ + qq] + 1) / a.m, a.n_cap);
                     gnav = max(gnav, nav[qq]);
                 }
+                if constexpr (kWRegs) {
+                    const float4* w4 = reinterpret_cast<const float4*>(a.w_idx + (g * NQ + q0) * kHI);
+#pragma unroll
+                    for (int j4 = 0; j4 < kHI / 4; j4++) {
+                        const float4 w = __ldg(w4 + j4);
+                        wr[4 * j4] = w.x;
+                        wr[4 * j4 + 1] = w.y;
+                        wr[4 * j4 + 2] = w.z;
+                        wr[4 * j4 + 3] = w.w;
+                    }
+                }
             }
             const int64_t key = (int64_t)t * kTileKeys + row;
             if ((int64_t)t * kTileKeys >= gnav) {  // nothing complete in this tile
-                if (key < a.n_cap)
-#pragma unroll
-                    for (int qq = q0; qq < q0 + C::kQPerWarp; qq++) a.scores[(g * NQ + qq) * a.ld + key] = -INFINITY;
+                if (key < a.n_cap && grp == 0) a.scores[(g * NQ + q0) * a.ld + key] = -INFINITY;
                 continue;
             }
+            if ((acc % C::kEpiGroups) != grp) {  // the other group's accumulator
+                if (++acc == C::kAcc) {
+                    acc = 0;
+                    aphase ^= 1u;
+                }
+                continue;
+            }
+            // E4M3 keys: this key's scale is on its way while the accumulator is awaited
+            const float ksc = (F8 && key < a.n_cap) ? __ldg(a.key_scales + (g * NQ / a.qps) * a.n_cap + key) : 1.f;
             // one lane waits, the whole warp follows its verdict (tcgen05.ld is warp-wide)
             int ok = 1;
             if (lane == 0) ok = tc::mbar_wait(&tfull[acc], aphase, abort_flag, a.status) ? 1 : 0;
@@ -258,26 +291,31 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
             if (!ok) break;
             tc::fence_after_sync();
             const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::N);
-#pragma unroll
-            for (int qq = q0; qq < q0 + C::kQPerWarp; qq++) {
-                const float4* w4 = reinterpret_cast<const float4*>(a.w_idx + (g * NQ + qq) * kHI);
-                float s = 0.f;
+            {
+                float acc4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
 #pragma unroll
                 for (int half = 0; half < 2; half++) {
                     float v[32];
-                    tc::tmem_ld32(tbase + (uint32_t)(qq * kHI + half * 32), v);
+                    tc::tmem_ld32(tbase + (uint32_t)(q0 * kHI + half * 32), v);
                     tc::tmem_ld_wait();
+                    if constexpr (kWRegs) {
 #pragma unroll
-                    for (int j4 = 0; j4 < 8; j4++) {
-                        const float4 w = __ldg(w4 + half * 8 + j4);
-                        s = fmaf(w.x, fmaxf(v[4 * j4 + 0], 0.f), s);
-                        s = fmaf(w.y, fmaxf(v[4 * j4 + 1], 0.f), s);
-                        s = fmaf(w.z, fmaxf(v[4 * j4 + 2], 0.f), s);
-                        s = fmaf(w.w, fmaxf(v[4 * j4 + 3], 0.f), s);
+                        for (int j = 0; j < 32; j++) acc4[j & 3] = fmaf(wr[half * 32 + j], fmaxf(v[j], 0.f), acc4[j & 3]);
+                    } else {
+                        const float4* w4 = reinterpret_cast<const float4*>(a.w_idx + (g * NQ + q0) * kHI) + half * 8;
+#pragma unroll
+                        for (int j4 = 0; j4 < 8; j4++) {
+                            const float4 w = __ldg(w4 + j4);
+                            acc4[0] = fmaf(w.x, fmaxf(v[4 * j4 + 0], 0.f), acc4[0]);
+                            acc4[1] = fmaf(w.y, fmaxf(v[4 * j4 + 1], 0.f), acc4[1]);
+                            acc4[2] = fmaf(w.z, fmaxf(v[4 * j4 + 2], 0.f), acc4[2]);
+                            acc4[3] = fmaf(w.w, fmaxf(v[4 * j4 + 3], 0.f), acc4[3]);
+                        }
                     }
                 }
-                if (F8 && key < a.n_cap) s *= __ldg(a.key_scales + (g * NQ / a.qps) * a.n_cap + key);
-                if (key < a.n_cap) a.scores[(g * NQ + qq) * a.ld + key] = key < nav[qq] ? s : -INFINITY;
+                float s = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+                if (F8) s *= ksc;
+                if (key < a.n_cap) a.scores[(g * NQ + q0) * a.ld + key] = key < nav[q0] ? s : -INFINITY;
             }
             tc::fence_before_sync();
             __syncwarp();

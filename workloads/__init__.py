@@ -48,6 +48,7 @@ class Workload:
     rope_base: float = 10000.0
     eps: float = 1e-6
     softmax_scale: float = 0.0  # <= 0: 1/sqrt(D)
+    idx_fmt: str = "bf16"  # "bf16" | "fp8": indexer keys stored as E4M3 codes + a scale per row
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -88,7 +89,11 @@ CSA_DECODE_1M_FP8 = Workload(
     D=512, H=64, m=4, W=128, L=1048576, H_I=64, d_I=128, topk=1024)
 
 FULL = [CSA_PREFILL_F32, CSA_DECODE_128K, HCA_DECODE_1M, CSA_CHUNKED_PREFILL, CSA_DECODE_1M_FP8]
-BY_NAME = {w.name: w for w in FULL}
+# The headline decode shape with the indexer keys in E4M3 (the keys are the
+# same N(0,1) draws; each side quantises them itself).
+CSA_DECODE_128K_FP8IDX = CSA_DECODE_128K.replace(name="csa_decode_fp8idx_b32_128k", idx_fmt="fp8")
+EXTRA = [CSA_DECODE_128K_FP8IDX]
+BY_NAME = {w.name: w for w in FULL + EXTRA}
 
 
 def _gen(seed: int, stream: int, device) -> torch.Generator:
