@@ -234,7 +234,7 @@ def algorithmic(w: workloads.Workload, row_bytes: int):
 class GpuStep:
     """Buffers and CUDA graphs of one step, split as [before | dominant | after]."""
 
-    def __init__(self, w: workloads.Workload):
+    def __init__(self, w: workloads.Workload, batch_invariant: bool = False):
         import long_context_compressed_17_b300 as L
         from long_context_compressed_17_b300.pipeline import DecodeLayer, LayerConfig, PrefillLayer
         self.L, self.w = L, w
@@ -242,7 +242,7 @@ class GpuStep:
         inp = self.inp
         cfg = LayerConfig(D=w.D, H=w.H, m=w.m, W=w.W, topk=w.topk if w.kind != "hca_decode" else 0,
                           H_I=w.H_I, d_I=w.d_I, act=w.act, kv=w.kv_fmt, rope_base=w.rope_base,
-                          eps=w.eps)
+                          eps=w.eps, batch_invariant=batch_invariant)
         self.cfg = cfg
         self.row_bytes = cfg.row_bytes
         # stored rows the library reads (FP8 rows are packed by the library)
@@ -350,7 +350,7 @@ def run_gpu(args, rank, world):
     import long_context_compressed_17_b300 as L
     w = workloads.BY_NAME[args.workload]
     peaks = measured_peaks()
-    st = GpuStep(w)
+    st = GpuStep(w, batch_invariant=args.batch_invariant)
     alg = algorithmic(w, st.row_bytes)
     for _ in range(2):  # untimed eager passes: kernel attributes, first-launch costs
         st.run_eager()
@@ -426,7 +426,8 @@ def run_gpu(args, rank, world):
            "idx_heads": w.H_I, "idx_dim": w.d_I, "kv_format": w.kv_fmt, "seed": w.seed,
            "l2": "flushed before every timed step (512 MiB write)",
            "timing": "CUDA events around each step; step captured as 3 CUDA graphs",
-           "parallelism": "replicas" if world > 1 else "single GPU"}
+           "parallelism": "replicas" if world > 1 else "single GPU",
+           "batch_invariant": bool(args.batch_invariant)}
     cfg.update(step_info)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -664,6 +665,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch-invariant", action="store_true",
+                    help="attention with fixed splits: each query's result independent of the batch")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -81,6 +81,7 @@ typedef struct {
     int32_t derotate_output; /* nonzero: rotate the output by RoPE at position -i       */
     int32_t act_format;      /* CSA_F32 or CSA_BF16: q, raw kv, indexer q/keys, outputs */
     int32_t kv_format;       /* CSA_F32 (with F32 act), CSA_BF16 or CSA_FP8_MIXED      */
+    int32_t batch_invariant; /* nonzero: attention outputs bit-identical in any batch  */
 } csa_params;
 
 /* Bytes of one stored cache/window row of `head_dim` dims in `kv_format`
@@ -249,7 +250,22 @@ csa_status csa_index_topk_noalloc(const csa_params* p, const void* q_idx, const 
  *           position win_pos0[s] + r (win_pos0: [B] int64, device)
  *   sink:   [H] float32 (-inf allowed)
  *   out:    [Q, H, D] in p->act_format;  lse: [Q, H] float32 or NULL
- * Requires Q % B == 0, H <= 128. */
+ * Requires Q % B == 0, H <= 128.
+ *
+ * Batch invariance [gitcode §5.3 "批次不变且确定性内核": with split-KV a
+ * query's output depends on where it sits in the batch].  By default the
+ * row lists of all Q queries are dealt out to the SMs in balanced ranges, so
+ * where a query's list is split, and hence the rounding of its result,
+ * depends on the other queries.  With p->batch_invariant set, every query's
+ * list is cut at fixed points that depend only on its length: with T the
+ * list's tiles of 64 rows (tensor-core path: ceil(k/64) + ceil(W/64) tiles,
+ * HCA ceil(n_cap/64) + ceil(W/64); CUDA-core path: ceil((k + W)/64), HCA
+ * ceil((n_cap + W)/64)), one split every s tiles, s = the largest power of
+ * two <= T/8 clamped to [2, 16].  Every split leaves a partial and the
+ * partials are merged in split order, so a query's out and lse are
+ * bit-identical for any Q, B, batch order and companion queries, and from
+ * run to run.  The price is coarser load balance (whole splits) and one
+ * partial per split. */
 csa_status csa_attend(const csa_params* p, const void* q, int32_t H, int32_t B, int32_t Q,
                       const int64_t* q_pos, const void* cache, int64_t n_cap,
                       const int32_t* topk_idx, const void* window, int64_t n_win,

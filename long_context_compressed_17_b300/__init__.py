@@ -48,14 +48,17 @@ class CsaParams(ctypes.Structure):
         ("derotate_output", ctypes.c_int32),
         ("act_format", ctypes.c_int32),
         ("kv_format", ctypes.c_int32),
+        ("batch_invariant", ctypes.c_int32),
     ]
 
 
 def params(head_dim: int, ratio: int, topk: int = 0, window: int = 128, act="bf16", kv="bf16",
            rope_dims: int = 64, rope_base: float = 10000.0, norm_eps: float = 1e-6,
-           softmax_scale: float = 0.0, derotate_output: bool = True) -> CsaParams:
+           softmax_scale: float = 0.0, derotate_output: bool = True,
+           batch_invariant: bool = False) -> CsaParams:
     return CsaParams(head_dim, rope_dims, rope_base, norm_eps, softmax_scale, ratio, topk, window,
-                     int(bool(derotate_output)), _FMT.get(act, act), _FMT.get(kv, kv))
+                     int(bool(derotate_output)), _FMT.get(act, act), _FMT.get(kv, kv),
+                     int(bool(batch_invariant)))
 
 
 _lib = None

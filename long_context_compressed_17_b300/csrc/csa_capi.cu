@@ -58,6 +58,7 @@ Geometry resolve(const csa_params* p) {
     g.act = p->act_format;
     g.kv = p->kv_format;
     g.kv_row_bytes = row_bytes(p->kv_format, p->head_dim);
+    g.inv = p->batch_invariant != 0;
     return g;
 }
 
@@ -96,7 +97,7 @@ AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int6
     AttendPlan pl;
     pl.list_len = (sparse ? (int64_t)g.k : n_cap) + g.W;
     pl.use_tc = attend_tc_supported(g, sparse, H, n_cap, n_win) ? 1 : 0;
-    pl.tc_T_sel = pl.tc_T = pl.tc_grid = pl.tc_deq = 0;
+    pl.tc_T_sel = pl.tc_T = pl.tc_grid = pl.tc_deq = pl.tc_seg = pl.tc_nseg = 0;
     pl.tc_total = 0;
     if (pl.use_tc) {
         pl.head_group = H;
@@ -105,13 +106,17 @@ AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int6
     } else {
         pl.head_group = (H % 16 == 0) ? 16 : 8;
         const int hgs = H / pl.head_group;
-        const int64_t target = 4LL * num_sms();
-        int64_t s = (target + (int64_t)Q * hgs - 1) / ((int64_t)Q * hgs);
-        int64_t max_s = (pl.list_len + 31) / 32;
-        if (s > max_s) s = max_s;
-        if (s < 1) s = 1;
-        int64_t per = (pl.list_len + s - 1) / s;
-        pl.rows_per_split = (per + 31) / 32 * 32;
+        if (g.inv) {  // fixed splits: a function of the list length only
+            pl.rows_per_split = 64LL * inv_split_tiles((pl.list_len + 63) / 64);
+        } else {
+            const int64_t target = 4LL * num_sms();
+            int64_t s = (target + (int64_t)Q * hgs - 1) / ((int64_t)Q * hgs);
+            int64_t max_s = (pl.list_len + 31) / 32;
+            if (s > max_s) s = max_s;
+            if (s < 1) s = 1;
+            int64_t per = (pl.list_len + s - 1) / s;
+            pl.rows_per_split = (per + 31) / 32 * 32;
+        }
         pl.splits = (int)((pl.list_len + pl.rows_per_split - 1) / pl.rows_per_split);
         if (pl.splits < 1) pl.splits = 1;
     }

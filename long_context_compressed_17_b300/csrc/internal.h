@@ -23,7 +23,17 @@ struct Geometry {  // resolved layer constants
     int derotate;
     int act, kv;
     int64_t kv_row_bytes;
+    int inv;  // batch-invariant attention splits
 };
+
+// Batch-invariant attention: split length, in tiles of 64 rows, of a row
+// list of T tiles -- the largest power of two <= T/8, clamped to [2, 16]; a
+// function of the list's length only.
+inline int inv_split_tiles(int64_t T) {
+    int s = 2;
+    while (s < 16 && (int64_t)s * 16 <= T) s *= 2;
+    return s;
+}
 
 Geometry resolve(const csa_params* p);
 
@@ -50,6 +60,9 @@ struct AttendPlan {
     // and all), Q * tc_T tiles dealt to tc_grid persistent CTAs
     int tc_T_sel, tc_T, tc_grid;
     int64_t tc_total;
+    // batch-invariant splits: tc_seg tiles each (0: balanced ranges), tc_nseg
+    // per query
+    int tc_seg, tc_nseg;
     // FP8 rows reach the tensor-core kernel dequantised to bf16 in the
     // workspace: 1 = the rows each query reads, [Q, tc_T * 64, D] in tile
     // order; 2 = every stored row, [B, n_cap, D] then [B, n_win, D]; 0 = the

@@ -201,7 +201,8 @@ __global__ void __launch_bounds__(kAttThreads) attend_generic_kernel(AttendArgs 
 // Merge split partials, add the sink, normalise, rotate by -i and store.
 // Block (q, h), 128 threads, each owning 4 consecutive dims (float4 loads);
 // dynamic smem: S_alloc floats of slot weights.
-//   CUDA-core kernel (tiles == 0): grid Q*H, query q has S_alloc partials.
+//   CUDA-core kernel, or fixed splits (tiles == 0): grid Q*H, query q has
+//   S_alloc partials.
 //   Tensor-core kernel (tiles > 0): CTA c of `grid` owns the tiles
 //   [c*total/grid, (c+1)*total/grid) of all queries' tile lists (tiles per
 //   query); only a query cut by a CTA boundary has partials (one per CTA
@@ -382,14 +383,17 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
         else return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
-    // tensor-core kernel: a block per query when there are no more queries
-    // than CTA boundaries, else a block per boundary
-    const int by_query = pl.use_tc && Q <= pl.tc_grid - 1;
-    const int64_t blocks = (!pl.use_tc || by_query) ? (int64_t)Q * H : (int64_t)(pl.tc_grid - 1) * H;
+    // tensor-core kernel with balanced ranges: a block per query when there
+    // are no more queries than CTA boundaries, else a block per boundary.
+    // Fixed splits (and the CUDA-core kernel): every query has pl.splits
+    // partials, merged in split order by a block per query.
+    const bool ranges = pl.use_tc && pl.tc_seg == 0;
+    const int by_query = ranges && Q <= pl.tc_grid - 1;
+    const int64_t blocks = (!ranges || by_query) ? (int64_t)Q * H : (int64_t)(pl.tc_grid - 1) * H;
     if (blocks == 0) return cudaSuccess;  // every query was finished by its only CTA
     attend_combine_kernel<<<(unsigned)blocks, 128, (size_t)pl.splits * sizeof(float), st>>>(
         part_o, part_ml, pl.splits, H, g.D, sink, q_pos, g.derotate, out, g.act, lse,
-        pl.use_tc ? (int64_t)pl.tc_T : 0, pl.tc_total, pl.tc_grid, by_query, rope_theta(g));
+        ranges ? (int64_t)pl.tc_T : 0, pl.tc_total, pl.tc_grid, by_query, rope_theta(g));
     note_launch();
     return cudaGetLastError();
 }

@@ -13,7 +13,12 @@
 // contiguous, balanced ranges to one persistent CTA per SM; the run of one
 // query's tiles inside a CTA is a segment.  A segment that is the whole query
 // is finished in place (sink, normalisation, rotation, bf16 store); the others
-// leave an unnormalised partial (m, l, o) for attend_combine_kernel.
+// leave an unnormalised partial (m, l, o) for attend_combine_kernel.  In the
+// batch-invariant mode [gitcode §5.3 "批次不变且确定性内核"] every query's tiles
+// are cut into fixed splits of `seg` tiles (a function of the list length),
+// CTAs take whole splits, every split leaves a partial and the combine merges
+// them in split order, so the rounding of a query's result never depends on
+// the rest of the batch.
 //
 // Per tile (one shared KV head, so key = value = row e_j):
 //   S^T[64 rows, 64 heads] = E[64, 512] . Q'^T          (swap-AB: rows are M)
@@ -90,6 +95,7 @@ struct AttTcArgs {
     int T_sel, T;             // tiles per query: selected / cache part, all
     int64_t total;            // Q * T
     int grid;
+    int seg, nseg;            // batch-invariant splits of seg tiles, nseg per query (seg 0: off)
     int S;                    // partial slots per query
     float* part_o;            // [Q, S, 64, 512]
     float* part_ml;           // [Q, S, 64, 2]
@@ -104,6 +110,25 @@ struct AttTcArgs {
 // CTA that owns global tile g (CTA c owns [c*total/grid, (c+1)*total/grid)).
 __device__ __forceinline__ int64_t cta_of(const AttTcArgs& a, int64_t g) {
     return ((g + 1) * a.grid - 1) / a.total;
+}
+
+// First global tile of CTA c's range: balanced over tiles, or, with fixed
+// splits, over whole splits (CTA c takes splits [c*n/grid, (c+1)*n/grid) of
+// the n = Q * nseg in query order).
+__device__ __forceinline__ int64_t range_begin(const AttTcArgs& a, int64_t c) {
+    if (a.seg == 0) return c * a.total / a.grid;
+    const int64_t sp = c * (a.total / a.T * a.nseg) / a.grid;
+    const int64_t qi = sp / a.nseg;
+    return qi * a.T + min((int64_t)a.T, (sp % a.nseg) * a.seg);
+}
+
+// End of the segment that starts at global tile g: the end of the query's
+// tiles, of the fixed split holding g, or of the CTA's range.
+__device__ __forceinline__ int64_t seg_end_of(const AttTcArgs& a, int64_t g, int64_t g_end) {
+    const int64_t qi = g / a.T;
+    int64_t e = (qi + 1) * a.T;
+    if (a.seg > 0) e = min(e, qi * a.T + ((g - qi * a.T) / a.seg + 1) * a.seg);
+    return min(g_end, e);
 }
 
 struct QueryInfo {
@@ -184,7 +209,7 @@ __device__ __forceinline__ int last_live(const AttTcArgs& a, const QueryInfo& qi
 __device__ __forceinline__ int64_t next_live_query(const AttTcArgs& a, int64_t g, int64_t g_end) {
     while (g < g_end) {
         const int64_t qi = g / a.T;
-        const int64_t seg_end = min(g_end, (qi + 1) * a.T);
+        const int64_t seg_end = seg_end_of(a, g, g_end);
         const QueryInfo inf = query_info(a, qi);
         if (last_live(a, inf, (int)(g - qi * a.T), (int)(seg_end - qi * a.T)) >= 0) return qi;
         g = seg_end;
@@ -402,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_sync();
     const uint32_t tmem = tmem_slot;
 
-    const int64_t g_begin = (int64_t)blockIdx.x * a.total / a.grid;
-    const int64_t g_end = (int64_t)(blockIdx.x + 1) * a.total / a.grid;
+    const int64_t g_begin = range_begin(a, blockIdx.x);
+    const int64_t g_end = range_begin(a, blockIdx.x + 1);
 
     if (warp == 0) {
         // ------------------------------------------------------------ loads
@@ -495,18 +520,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool first_of[4], last_of[4];  // segment flags of tiles t_pv .. t_qk-1 (at most 2)
             // QK cursor over this CTA's live tiles
             int64_t g = g_begin;
-            int64_t cur_q = -1;
+            int64_t cur_q = -1, cur_end = g_begin, q_in = -1;  // q_in: query whose q' is in sQ
             QueryInfo inf{};
             int lt_last = -1;
             bool at_seg_start = true;
             auto advance = [&]() -> bool {  // move g to the next live tile; false at the end
                 for (; g < g_end; ++g) {
                     const int64_t qi = g / a.T;
-                    if (qi != cur_q) {
+                    if (g >= cur_end) {
                         cur_q = qi;
                         inf = query_info(a, qi);
-                        const int64_t seg_end = min(g_end, (qi + 1) * a.T);
-                        lt_last = last_live(a, inf, (int)(g - qi * a.T), (int)(seg_end - qi * a.T));
+                        cur_end = seg_end_of(a, g, g_end);
+                        lt_last = last_live(a, inf, (int)(g - qi * a.T), (int)(cur_end - qi * a.T));
                         at_seg_start = true;
                     }
                     if (tile_live(a, inf, (int)(g - qi * a.T))) return true;
@@ -542,7 +567,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (more && t_pv + 1 >= t_qk) {  // S^T buffer of tile t_qk is free
                     const int b = t_qk & 1;
-                    bool ready = !at_seg_start || tc::mbar_test_wait(&q_full, nq & 1u);
+                    // q' is prepared once per query: a later split of the same
+                    // query in this CTA reuses it
+                    const bool need_q = at_seg_start && cur_q != q_in;
+                    bool ready = !need_q || tc::mbar_test_wait(&q_full, nq & 1u);
                     if (ready) ready = tc::mbar_test_wait(&full[b], (t_qk >> 1) & 1u);
                     if (ready) {
                         tc::fence_after_sync();
@@ -554,7 +582,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tc::mma_bf16_ss(tmem + kColS + 64 * b, ad, bd, idesc_qk, kg != 0 ? 1u : 0u);
                         }
                         tc::mma_commit(&s_full[b]);
-                        if (at_seg_start) ++nq;
+                        if (need_q) {
+                            ++nq;
+                            q_in = cur_q;
+                        }
                         first_of[t_qk & 3] = at_seg_start;
                         last_of[t_qk & 3] = (int)(g - cur_q * a.T) == lt_last;
                         at_seg_start = false;
@@ -686,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* mref = mref_s + h0;  // running reference of this warp's heads (valid once ref_set)
         for (int64_t g = g_begin; g < g_end && !stop;) {
             const int64_t qi = g / a.T;
-            const int64_t seg_end = min(g_end, (qi + 1) * a.T);
+            const int64_t seg_end = seg_end_of(a, g, g_end);
             const QueryInfo inf = query_info(a, qi);
             const int lt0 = (int)(g - qi * a.T), lt1 = (int)(seg_end - qi * a.T);
             const int lt_last = last_live(a, inf, lt0, lt1);
@@ -811,15 +842,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++seg_tiles;
                 ++tcount;
                 if (lt == lt_last) {
-                    // every QK product of this segment is done: q' of the next one may go in
+                    // every QK product of this segment is done: q' of the next
+                    // query may go in (a further split of this one keeps it)
                     const int64_t qn = next_live_query(a, seg_end, g_end);
-                    if (qn >= 0) prep_q(qn, std::false_type{});
+                    if (qn >= 0 && qn != qi) prep_q(qn, std::false_type{});
                 }
             }
             if (stop) break;
             // ---------------------------------------------------- segment epilogue
-            const int64_t c_first = cta_of(a, qi * a.T);
-            const bool whole = c_first == cta_of(a, (qi + 1) * a.T - 1);  // no other CTA has tiles of qi
+            // partial slot: the split's index, or the CTA's rank among those
+            // meeting the query; a query no other CTA meets is finished here
+            // (never with fixed splits: their merge order is the same in any batch)
+            const int64_t c_first = a.seg ? 0 : cta_of(a, qi * a.T);
+            const int64_t slot = a.seg ? lt0 / a.seg : (int64_t)blockIdx.x - c_first;
+            const bool whole = !a.seg && c_first == cta_of(a, (qi + 1) * a.T - 1);
             {
                 const float ls = warp_reduce_scatter16<false>(l_part, lane);
                 if (row_lane) red[quarter][h0 + lane] = ls;
@@ -842,7 +878,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fac_s[tid] = f;
                     if (a.lse) a.lse[qi * kH + tid] = L > 0.f ? ms + logf(L) : -INFINITY;
                 } else {
-                    const int64_t pb = (qi * a.S + ((int64_t)blockIdx.x - c_first)) * kH + tid;
+                    const int64_t pb = (qi * a.S + slot) * kH + tid;
                     a.part_ml[pb * 2] = m;
                     a.part_ml[pb * 2 + 1] = l;
                 }
@@ -885,7 +921,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int h = 0; h < kHW; h++) dst[(int64_t)h * kD] = f32_to_bf16_rn(v[h]);
                 } else {
-                    float* dst = a.part_o + ((qi * a.S + ((int64_t)blockIdx.x - c_first)) * kH + h0) * kD + d;
+                    float* dst = a.part_o + ((qi * a.S + slot) * kH + h0) * kD + d;
 #pragma unroll
                     for (int h = 0; h < kHW; h++) dst[(int64_t)h * kD] = v[h];
                 }
@@ -968,6 +1004,14 @@ void plan_attend_tc(const Geometry& g, bool sparse, int Q, int64_t n_cap, Attend
     pl->tc_T = pl->tc_T_sel + (g.W + kRows - 1) / kRows;
     pl->tc_total = (int64_t)Q * pl->tc_T;
     const int64_t sms = num_sms();
+    if (g.inv) {  // fixed splits of tc_seg tiles, whole splits per CTA
+        pl->tc_seg = inv_split_tiles(pl->tc_T);
+        pl->tc_nseg = (pl->tc_T + pl->tc_seg - 1) / pl->tc_seg;
+        const int64_t segs = (int64_t)Q * pl->tc_nseg;
+        pl->tc_grid = (int)(segs < sms ? segs : sms);
+        pl->splits = pl->tc_nseg;
+        return;
+    }
     pl->tc_grid = (int)(pl->tc_total < sms ? pl->tc_total : sms);
     int smax = 1;
     if (pl->tc_total > 0) {
@@ -1071,6 +1115,8 @@ cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool spars
     a.T = pl.tc_T;
     a.total = pl.tc_total;
     a.grid = pl.tc_grid;
+    a.seg = pl.tc_seg;
+    a.nseg = pl.tc_nseg;
     a.S = pl.splits;
     a.part_o = part_o;
     a.part_ml = part_ml;

@@ -45,6 +45,7 @@ class LayerConfig:
     eps: float = 1e-6
     derotate: bool = True
     scale: float = 0.0     # softmax scale; <= 0: 1/sqrt(D)
+    batch_invariant: bool = False  # attention splits fixed per query (bit-identical in any batch)
 
     @property
     def sparse(self) -> bool:
@@ -53,7 +54,8 @@ class LayerConfig:
     def params(self, ratio=None):
         return params(self.D, self.m if ratio is None else ratio, self.topk, self.W, self.act,
                       self.kv, rope_base=self.rope_base, norm_eps=self.eps,
-                      softmax_scale=self.scale, derotate_output=self.derotate)
+                      softmax_scale=self.scale, derotate_output=self.derotate,
+                      batch_invariant=self.batch_invariant)
 
     @property
     def row_bytes(self) -> int:

@@ -168,6 +168,50 @@ def test_workspace_sizes(L):
     assert L.csa_workspace_bytes(p, 99, 32, 32, 64, 64, 32768, 128) == 0
 
 
+def _al(x):
+    return (x + 255) // 256 * 256
+
+
+def _inv_splits(T):
+    """Fixed splits of a T-tile list: one every s tiles, s the largest power of
+    two <= T/8 clamped to [2, 16] (the documented batch-invariant rule)."""
+    import math
+    s = min(16, max(2, 2 ** math.floor(math.log2(T / 8))))
+    return -(-T // s)
+
+
+@pytest.mark.parametrize("k,W,n_cap,Q,B", [(1024, 128, 32768, 32, 32), (1024, 128, 4096, 5, 5),
+                                           (64, 0, 4096, 3, 3), (100, 128, 4096, 8, 2)])
+def test_batch_invariant_csa_workspace_follows_the_split_rule(L, k, W, n_cap, Q, B):
+    """Tensor-core path (bf16, D = 512, 64 heads): ceil(k/64) + ceil(W/64)
+    tiles, one partial per fixed split for every query, whatever Q."""
+    p = L.params(512, 4, topk=k, window=W, batch_invariant=True)
+    S = _inv_splits(-(-k // 64) + -(-W // 64))
+    want = 256 + _al(Q * S * 64 * 512 * 4) + _al(Q * S * 64 * 2 * 4)
+    assert L.csa_workspace_bytes(p, L.OP_ATTEND, B, Q, 64, 0, n_cap, 128) == want
+
+
+@pytest.mark.parametrize("n_cap,Q", [(8192, 32), (2048, 12), (100, 1), (64, 7)])
+def test_batch_invariant_hca_workspace_follows_the_split_rule(L, n_cap, Q):
+    p = L.params(512, 128, window=128, batch_invariant=True)
+    S = _inv_splits(-(-n_cap // 64) + 2)
+    want = 256 + _al(Q * S * 64 * 512 * 4) + _al(Q * S * 64 * 2 * 4)
+    assert L.csa_workspace_bytes(p, L.OP_HCA_ATTEND, Q, Q, 64, 0, n_cap, 128) == want
+
+
+def test_batch_invariant_cuda_core_splits_follow_the_rule(L):
+    """fp32, D = 128, 8 heads: the list of k + W rows in splits of 64*s rows."""
+    import math
+    for k, W, Q in [(64, 128, 4096), (1000, 128, 3), (20, 0, 1)]:
+        p = L.params(128, 4, topk=k, window=W, act="f32", kv="f32", batch_invariant=True)
+        n = k + W
+        T = -(-n // 64)
+        s = min(16, max(2, 2 ** math.floor(math.log2(T / 8))))
+        S = -(-n // (64 * s))
+        want = 256 + _al(Q * S * 8 * 128 * 4) + _al(Q * S * 8 * 2 * 4)
+        assert L.csa_workspace_bytes(p, L.OP_ATTEND, Q, Q, 8, 0, 4096, 128) == want, (k, W, Q)
+
+
 def test_index_topk_fp8_validation(L):
     import torch
     p = L.params(512, 4, topk=64)
