@@ -54,7 +54,14 @@ struct Cfg {
     static constexpr int kEpiWarps = NQ == 1 ? 8 : 16;
     static constexpr int kEpiGroups = NQ == 1 ? 2 : 1;
     static constexpr int kQPerWarp = NQ * 4 * kEpiGroups / kEpiWarps;  // queries of a key per epilogue warp
-    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    // MMA-issuing warps: a thread issuing tcgen05.mma back to back waits on
+    // each instruction longer than an N = 64 product takes to run, so decode
+    // has two issuers on alternate key tiles (even stage and accumulator
+    // counts: each barrier still hears from one issuer only)
+    static constexpr int kIssuers = NQ == 1 ? 2 : 1;
+    static_assert(kStages % kIssuers == 0 && kAcc % kIssuers == 0, "issuers own whole stages");
+    static constexpr int kEpi0 = 1 + kIssuers;          // first epilogue warp
+    static constexpr int kThreads = 32 * kEpi0 + 32 * kEpiWarps;
     static constexpr uint32_t kQBytes = (uint32_t)N * kDI * kEB;
     static constexpr uint32_t kTmemCols = kAcc * N;     // 256 or 512
     static constexpr size_t kBarBytes = 512;
@@ -118,7 +125,7 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
         }
         for (int b = 0; b < C::kQBufs; b++) {
             tc::mbar_init(&qfull[b], 1);
-            tc::mbar_init(&qempty[b], 1);
+            tc::mbar_init(&qempty[b], C::kIssuers);  // every issuer releases the queries
         }
         for (int c = 0; c < C::kAcc; c++) {
             tc::mbar_init(&tfull[c], 1);
@@ -140,6 +147,9 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
     const int64_t per = (a.total_units + gridDim.x - 1) / gridDim.x;
     const int64_t u0 = (int64_t)blockIdx.x * per;
     const int64_t u1 = min(a.total_units, u0 + per);
+    // (query group, key tile) of unit u0; every role steps it along without dividing
+    const int64_t g0 = u0 / a.n_tiles;
+    const int64_t t0 = u0 - g0 * a.n_tiles;
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
@@ -148,13 +158,17 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         int64_t cur_g = -1, last_loaded = -1, gnav = 0;
-        int qloads = 0;
-        for (int64_t u = u0; u < u1; ++u) {
-            const int64_t g = u / a.n_tiles;
-            const int t = (int)(u % a.n_tiles);
+        int qloads = 0, seq = 0;
+        int64_t g = g0;
+        for (int64_t u = u0, t = t0; u < u1; ++u, ++t) {
+            if (t == a.n_tiles) {
+                t = 0;
+                ++g;
+            }
             if (g != cur_g) {
                 cur_g = g;
                 gnav = group_avail<NQ>(a, g);
+                seq = (int)((g * NQ) / a.qps);
             }
             if ((int64_t)t * kTileKeys >= gnav) continue;  // no complete block in this tile
             if (g != last_loaded) {
@@ -170,24 +184,29 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
             }
             if (!tc::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status)) break;
             tc::mbar_arrive_expect_tx(&full[stage], kStageBytes);
-            const int seq = (int)((g * NQ) / a.qps);
             uint8_t* dst = sA + stage * kStageBytes;
-            tc::tma_load_3d(dst, &tm_keys, &full[stage], 0, t * kTileKeys, seq);
-            if (!F8) tc::tma_load_3d(dst + kStageBytes / 2, &tm_keys, &full[stage], 64, t * kTileKeys, seq);
+            tc::tma_load_3d(dst, &tm_keys, &full[stage], 0, (int)(t * kTileKeys), seq);
+            if (!F8) tc::tma_load_3d(dst + kStageBytes / 2, &tm_keys, &full[stage], 64, (int)(t * kTileKeys), seq);
             if (++stage == C::kStages) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
-    } else if (warp == 1 && lane == 0) {
-        // ------------------------------------------------ MMA issuer
+    } else if (warp >= 1 && warp < C::kEpi0 && lane == 0) {
+        // ------------------------------------------------ MMA issuers
+        // Issuer `me` takes the live units j with j % kIssuers == me; every
+        // issuer follows the query buffers through all of them.
         constexpr uint32_t idesc = C::idesc;
-        int stage = 0, acc = 0, quses = 0, qb = 0;
-        uint32_t phase = 0, aphase = 0;
+        const uint32_t me = (uint32_t)(warp - 1);
+        uint32_t j = 0;  // live units so far
+        int quses = 0, qb = 0;
         int64_t cur_g = -1, last_used = -1, gnav = 0;
-        for (int64_t u = u0; u < u1; ++u) {
-            const int64_t g = u / a.n_tiles;
-            const int t = (int)(u % a.n_tiles);
+        int64_t g = g0;
+        for (int64_t u = u0, t = t0; u < u1; ++u, ++t) {
+            if (t == a.n_tiles) {
+                t = 0;
+                ++g;
+            }
             if (g != cur_g) {
                 cur_g = g;
                 gnav = group_avail<NQ>(a, g);
@@ -201,6 +220,10 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
                 last_used = g;
                 quses++;
             }
+            const uint32_t jj = j++;
+            if (jj % C::kIssuers != me) continue;
+            const int stage = (int)(jj % C::kStages), acc = (int)(jj % C::kAcc);
+            const uint32_t phase = (jj / C::kStages) & 1u, aphase = (jj / C::kAcc) & 1u;
             if (!tc::mbar_wait(&tempty[acc], aphase ^ 1u, abort_flag, a.status)) break;
             if (!tc::mbar_wait(&full[stage], phase, abort_flag, a.status)) break;
             tc::fence_after_sync();
@@ -221,35 +244,32 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
             }
             tc::mma_commit(&empty[stage]);  // key tile free when these MMAs finish
             tc::mma_commit(&tfull[acc]);    // accumulator ready for the epilogue
-            if (++stage == C::kStages) {
-                stage = 0;
-                phase ^= 1u;
-            }
-            if (++acc == C::kAcc) {
-                acc = 0;
-                aphase ^= 1u;
-            }
         }
-    } else if (warp >= 2) {
+    } else if (warp >= C::kEpi0) {
         // ------------------------------------------------ epilogue: one key per thread
         const int quarter = warp & 3;          // TMEM lanes this warp may read
         const int row = quarter * 32 + lane;   // key within the tile
         static_assert(C::kQPerWarp == 1, "one query per epilogue warp");
-        const int wq = (warp - 2) >> 2;
+        const int wq = (warp - C::kEpi0) >> 2;
         const int grp = C::kEpiGroups > 1 ? wq : 0;  // this warp takes the accumulators acc % groups == grp
         const int q0 = C::kEpiGroups > 1 ? 0 : wq;   // this warp's query within the query group
         int acc = 0;
         uint32_t aphase = 0;
         int64_t cur_g = -1, gnav = 0;
         int64_t nav[NQ];
+        float* srow = a.scores;            // this warp's query's score row
+        const float* krow = a.key_scales;  // F8: the sequence's key scales
         // the query's head weights: in registers for decode (loaded once per query
         // group), read through L1 per tile in prefill (the registers go to the
         // sixteen epilogue warps there)
         constexpr bool kWRegs = NQ == 1;
         float wr[kWRegs ? kHI : 1];
-        for (int64_t u = u0; u < u1; ++u) {
-            const int64_t g = u / a.n_tiles;
-            const int t = (int)(u % a.n_tiles);
+        int64_t g = g0;
+        for (int64_t u = u0, t = t0; u < u1; ++u, ++t) {
+            if (t == a.n_tiles) {
+                t = 0;
+                ++g;
+            }
             if (g != cur_g) {
                 cur_g = g;
                 gnav = 0;
@@ -258,6 +278,8 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
                     nav[qq] = min((a.q_pos[g * NQ + qq] + 1) / a.m, a.n_cap);
                     gnav = max(gnav, nav[qq]);
                 }
+                if (NQ == 1) srow = a.scores + (g * NQ + q0) * a.ld;
+                if (F8 && NQ == 1) krow = a.key_scales + (g * NQ / a.qps) * a.n_cap;
                 if constexpr (kWRegs) {
                     const float4* w4 = reinterpret_cast<const float4*>(a.w_idx + (g * NQ + q0) * kHI);
 #pragma unroll
@@ -271,8 +293,9 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
                 }
             }
             const int64_t key = (int64_t)t * kTileKeys + row;
+            if (NQ != 1) srow = a.scores + (g * NQ + q0) * a.ld;
             if ((int64_t)t * kTileKeys >= gnav) {  // nothing complete in this tile
-                if (key < a.n_cap && grp == 0) a.scores[(g * NQ + q0) * a.ld + key] = -INFINITY;
+                if (key < a.n_cap && grp == 0) srow[key] = -INFINITY;
                 continue;
             }
             if ((acc % C::kEpiGroups) != grp) {  // the other group's accumulator
@@ -283,7 +306,10 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
                 continue;
             }
             // E4M3 keys: this key's scale is on its way while the accumulator is awaited
-            const float ksc = (F8 && key < a.n_cap) ? __ldg(a.key_scales + (g * NQ / a.qps) * a.n_cap + key) : 1.f;
+            // (prefill keeps no row pointer: its sixteen warps are short of registers)
+            const float ksc = (F8 && key < a.n_cap)
+                                  ? __ldg((NQ == 1 ? krow : a.key_scales + (g * NQ / a.qps) * a.n_cap) + key)
+                                  : 1.f;
             // one lane waits, the whole warp follows its verdict (tcgen05.ld is warp-wide)
             int ok = 1;
             if (lane == 0) ok = tc::mbar_wait(&tfull[acc], aphase, abort_flag, a.status) ? 1 : 0;
@@ -315,7 +341,7 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
                 }
                 float s = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
                 if (F8) s *= ksc;
-                if (key < a.n_cap) a.scores[(g * NQ + q0) * a.ld + key] = key < nav[q0] ? s : -INFINITY;
+                if (key < a.n_cap) srow[key] = key < nav[q0] ? s : -INFINITY;
             }
             tc::fence_before_sync();
             __syncwarp();
