@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
         uint32_t phase = 0;
         int64_t cur_g = -1, last_loaded = -1, gnav = 0;
         int qloads = 0, seq = 0;
+        const float* ksrow = nullptr;  // F8: the sequence's key scales
         int64_t g = g0;
         for (int64_t u = u0, t = t0; u < u1; ++u, ++t) {
             if (t == a.n_tiles) {
@@ -169,6 +170,7 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
                 cur_g = g;
                 gnav = group_avail<NQ>(a, g);
                 seq = (int)((g * NQ) / a.qps);
+                if (F8) ksrow = a.key_scales + (int64_t)seq * a.n_cap;
             }
             if ((int64_t)t * kTileKeys >= gnav) continue;  // no complete block in this tile
             if (g != last_loaded) {
@@ -187,6 +189,11 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
             uint8_t* dst = sA + stage * kStageBytes;
             tc::tma_load_3d(dst, &tm_keys, &full[stage], 0, (int)(t * kTileKeys), seq);
             if (!F8) tc::tma_load_3d(dst + kStageBytes / 2, &tm_keys, &full[stage], 64, (int)(t * kTileKeys), seq);
+            if (F8) {  // the tile's key scales head for L2 now: the epilogue reads them thousands of cycles later
+                const int64_t k0 = t * kTileKeys, kn = min((int64_t)kTileKeys, a.n_cap - k0);
+                for (int64_t o = 0; o < kn; o += 32) tc::prefetch_l2_line(ksrow + k0 + o);
+                tc::prefetch_l2_line(ksrow + k0 + kn - 1);
+            }
             if (++stage == C::kStages) {
                 stage = 0;
                 phase ^= 1u;

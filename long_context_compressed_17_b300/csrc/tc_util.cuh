@@ -170,6 +170,11 @@ __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
     }
 }
 
+// The 128-byte line holding p into L2 (no alignment requirement).
+__device__ __forceinline__ void prefetch_l2_line(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
