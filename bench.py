@@ -51,13 +51,15 @@ L2_DRAIN_BYTES = 256 << 20
 # captured build (sha256 prefix of the listed files); otherwise it is null.
 CAPTURED_TRAFFIC = {
     "csa_decode_bf16_b32_128k": (
-        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "0f560a0c071fc5b7", 274824704),
+        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "c0862ebfda1d3a07", 274823936),
     "csa_decode_fp8cache_b8_1m": (
-        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "0f560a0c071fc5b7", 546872832),
+        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "c0862ebfda1d3a07", 546898176),
+    "csa_decode_fp8idx_b32_128k": (
+        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "c0862ebfda1d3a07", 143117568),
     "csa_chunked_prefill_bf16_64k_8k": (
-        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "0f560a0c071fc5b7", 712652032),
+        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "c0862ebfda1d3a07", 712744448),
     "hca_decode_bf16_b32_1m": (
-        ["k_attend_tc.cu", "tc_util.cuh", "common.cuh"], "a42fd4ffbc28e7f9", 288056064),
+        ["k_attend_tc.cu", "tc_util.cuh", "common.cuh"], "84ef9bc304f614c2", 284567936),
 }
 
 
@@ -417,7 +419,7 @@ def run_gpu(args, rank, world):
         achieved = alg["flops"] / (dom * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "traffic": None, "kernel": alg["kernel"], "kernel_ms": round(dom, 5),
+                "traffic": captured_traffic(w.name), "kernel": alg["kernel"], "kernel_ms": round(dom, 5),
                 "flops_per_launch": alg["flops"], "peak_source": peaks["source"] + " bf16 (burst)"}
     else:
         # fp32 FMA peak: 148 SMs x 128 lanes x 2 flop x max SM clock
