@@ -270,6 +270,10 @@ class GpuStep:
             self.pos_first = Lb - w.m
             self.win_row = (Lb - 1) - int(inp["win_pos0"][0])
             if w.kind == "csa_decode":
+                # the append feeds only the attention: it runs on a side stream
+                # beside the indexer's top-k (one CTA per query leaves most SMs free)
+                self.side = torch.cuda.Stream()
+                self.ev_fork, self.ev_join = torch.cuda.Event(), torch.cuda.Event()
                 self.ld = (w.n_cap + 127) // 128 * 128
                 self.scores = torch.empty(w.B, self.ld, dtype=torch.float32, device="cuda")
                 if w.idx_fmt == "fp8":  # layer state: the keys in E4M3, packed once
@@ -294,11 +298,14 @@ class GpuStep:
             self.scores = torch.empty(w.T_new, self.ld, dtype=torch.float32, device="cuda")
 
     # the three segments of a step
+    def has_before(self):
+        return self.w.kind == "csa_prefill" or (self.w.kind == "hca_decode" and self.pos_first >= 0)
+
     def before(self):
         w, inp, lay = self.w, self.inp, self.layer
         if w.kind == "csa_prefill":
             lay.compress(inp["kv_raw"], inp["w_z"], inp["bias"])
-        elif self.pos_first >= 0:
+        elif w.kind == "hca_decode" and self.pos_first >= 0:
             lay.append(inp["kv_new"], self.pos_first, inp["w_z"], inp["bias"], self.rows["cache"],
                        self.rows["window"], self.win_row)
 
@@ -325,8 +332,18 @@ class GpuStep:
         if w.kind == "hca_decode":
             return
         n_cap = w.n_cap if w.kind == "csa_decode" else lay.n_cap
+        forked = w.kind == "csa_decode" and self.pos_first >= 0
+        if forked:
+            main = torch.cuda.current_stream()
+            self.ev_fork.record(main)
+            self.side.wait_event(self.ev_fork)
+            lay.append(inp["kv_new"], self.pos_first, inp["w_z"], inp["bias"], self.rows["cache"],
+                       self.rows["window"], self.win_row, stream=self.side)
+            self.ev_join.record(self.side)
         L.csa_topk_select(lay.p, self.scores, self.ld, n_cap, w.Q, inp["q_pos"], lay.topk_idx,
                           lay.topk_score)
+        if forked:
+            main.wait_event(self.ev_join)
         if w.kind == "csa_decode":
             L.csa_attend(lay.p, inp["q"], w.H, w.B, w.B, inp["q_pos"], self.rows["cache"],
                          w.n_cap, lay.topk_idx, self.rows["window"], w.W, inp["win_pos0"],
@@ -344,6 +361,9 @@ class GpuStep:
     def capture(self):
         self.graphs = []
         for seg in (self.before, self.dominant, self.after):
+            if seg == self.before and not self.has_before():
+                self.graphs.append(None)
+                continue
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 seg()
@@ -374,7 +394,8 @@ def run_gpu(args, rank, world):
     g0, g1, g2 = st.graphs
     for _ in range(args.warmup):
         flush_l2()
-        g0.replay()
+        if g0 is not None:
+            g0.replay()
         g1.replay()
         g2.replay()
     torch.cuda.synchronize()
@@ -387,7 +408,8 @@ def run_gpu(args, rank, world):
             flush_l2()                    # L2 flushed before every timed step
             e = ev[k]
             e[0].record()
-            g0.replay()
+            if g0 is not None:
+                g0.replay()
             e[1].record()
             g1.replay()
             e[2].record()

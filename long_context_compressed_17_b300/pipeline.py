@@ -89,6 +89,8 @@ class DecodeLayer:
             nb = csa_workspace_bytes(self.p, OP_HCA_ATTEND, B, B, cfg.H, 0, n_cap, n_win)
         self.ws = workspace(nb, device)
         self.ws_bytes = self.ws.numel()
+        self._side = torch.cuda.Stream(device=device) if cfg.sparse else None
+        self._fork, self._join = torch.cuda.Event(), torch.cuda.Event()
 
     def append(self, kv_new, pos_first, w_z, bias, cache, window, win_row, stream=None):
         """kv_new [B, m, D] raw tokens at positions pos_first .. pos_first+m-1 (a
@@ -101,13 +103,38 @@ class DecodeLayer:
         csa_append(self.p, kv_new, self.B, cfg.m, pos_first, w_z, bias, cache.data_ptr() + e * rb,
                    self.n_cap, window.data_ptr() + win_row * rb, self.n_win, stream)
 
+    def step(self, kv_new, pos_first, w_z, bias, q, cache, window, win_row, q_pos, win_pos0, sink,
+             q_idx=None, w_idx=None, keys=None):
+        """One decode step on the current stream: append the newest block's entry
+        and window row, then attend.  For CSA the append feeds only the
+        attention, so it runs on a side stream beside the indexer and top-k
+        (whose one CTA per query leaves most SMs free) and the attention waits
+        for both; HCA attends to the new entry, so it appends first."""
+        if not self.cfg.sparse:
+            self.append(kv_new, pos_first, w_z, bias, cache, window, win_row)
+            return self.attend(q, cache, window, q_pos, win_pos0, sink)
+        main = torch.cuda.current_stream()
+        self._fork.record(main)
+        self._side.wait_event(self._fork)
+        self.append(kv_new, pos_first, w_z, bias, cache, window, win_row, stream=self._side)
+        self._join.record(self._side)
+        self.index_topk(q_idx, w_idx, keys, q_pos, stream=main)
+        main.wait_event(self._join)
+        return self.attend(q, cache, window, q_pos, win_pos0, sink, stream=main, selected=True)
+
+    def index_topk(self, q_idx, w_idx, keys, q_pos, stream=None):
+        cfg = self.cfg
+        csa_index_topk(self.p, q_idx, w_idx, cfg.H_I, cfg.d_I, keys, self.n_cap, self.B, self.B,
+                       q_pos, self.topk_idx, self.topk_score, self.ws, self.ws_bytes, stream)
+
     def attend(self, q, cache, window, q_pos, win_pos0, sink, q_idx=None, w_idx=None, keys=None,
-               stream=None):
+               stream=None, selected=False):
+        """CSA: index and select (unless `selected`: topk_idx holds this step's
+        selection), then attend; HCA: attend to every complete block."""
         cfg = self.cfg
         if cfg.sparse:
-            csa_index_topk(self.p, q_idx, w_idx, cfg.H_I, cfg.d_I, keys, self.n_cap, self.B,
-                           self.B, q_pos, self.topk_idx, self.topk_score, self.ws, self.ws_bytes,
-                           stream)
+            if not selected:
+                self.index_topk(q_idx, w_idx, keys, q_pos, stream)
             csa_attend(self.p, q, cfg.H, self.B, self.B, q_pos, cache, self.n_cap, self.topk_idx,
                        window, self.n_win, win_pos0, sink, self.out, self.lse, self.ws,
                        self.ws_bytes, stream)

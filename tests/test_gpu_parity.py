@@ -219,3 +219,36 @@ def test_append_matches_two_compress_calls(m, kv):
     assert torch.equal(outs[0][0], outs[1][0]), "entries differ"
     assert torch.equal(outs[0][1], outs[1][1]), "window rows differ"
     assert outs[0][0][:, e].abs().sum() > 0 and outs[0][1][:, wr].abs().sum() > 0
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8m"])
+def test_decode_step_with_side_stream_append_matches_sequential(kv):
+    """DecodeLayer.step runs the CSA append on a side stream beside the
+    indexer and top-k; outputs, cache and window rows equal those of the
+    sequential append-then-attend, bit for bit."""
+    from long_context_compressed_17_b300.pipeline import DecodeLayer
+    w = SMALL_CSA.replace(name="csa_step_overlap", B=4, L_per_seq=(8192,) * 4, kv_fmt=kv)
+    inp = _to_cuda(workloads.generate(w))
+    cfg = H.cfg_of(w)
+    Lb = w.lengths[0]
+    win_row = (Lb - 1) - int(inp["win_pos0"][0])
+    res = []
+    for overlapped in (False, True):
+        cache = H.gpu_pack(w, inp["cache"])
+        window = H.gpu_pack(w, inp["window"])
+        layer = DecodeLayer(cfg, w.B, w.n_cap, w.W)
+        args = (inp["kv_new"], Lb - w.m, inp["w_z"], inp["bias"])
+        if overlapped:
+            out, lse = layer.step(*args, inp["q"], cache, window, win_row, inp["q_pos"], inp["win_pos0"],
+                                  inp["sink"], q_idx=inp["q_idx"], w_idx=inp["w_idx"], keys=inp["keys"])
+        else:
+            layer.append(*args, cache, window, win_row)
+            out, lse = layer.attend(inp["q"], cache, window, inp["q_pos"], inp["win_pos0"], inp["sink"],
+                                    q_idx=inp["q_idx"], w_idx=inp["w_idx"], keys=inp["keys"])
+        torch.cuda.synchronize()
+        import long_context_compressed_17_b300 as L
+        L.csa_check_status(layer.ws)
+        res.append([t.clone() for t in (out, lse, cache, window, layer.topk_idx)])
+    for a, b, what in zip(res[0], res[1], ("out", "lse", "cache", "window", "topk_idx")):
+        assert torch.equal(a.view(torch.uint8) if a.dtype != torch.uint8 else a,
+                           b.view(torch.uint8) if b.dtype != torch.uint8 else b), what
