@@ -115,6 +115,19 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
     return r;
 }
 
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t caddr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(caddr) : "memory");
+    return v;
+}
+
+// Two consecutive words (caddr 8-byte aligned).
+__device__ __forceinline__ uint2 ld_cluster_v2_u32(uint32_t caddr) {
+    uint2 v;
+    asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(caddr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void st_cluster_v4(uint32_t caddr, uint4 v) {
     asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)
