@@ -199,8 +199,10 @@ __global__ void __launch_bounds__(kAttThreads) attend_generic_kernel(AttendArgs 
 }
 
 // Merge split partials, add the sink, normalise, rotate by -i and store.
-// Block (q, h), 128 threads, each owning 4 consecutive dims (float4 loads);
-// dynamic smem: S_alloc floats of slot weights.
+// Block (q, h), 128 threads, thread t owning dims 4t .. 4t+3 (D <= 512).
+// Every warp derives the slot weights and the denominator itself (the same
+// expressions over the same values, so the same bits in every warp): no
+// block barrier, and the partial rows are requested before the weights.
 //   CUDA-core kernel, or fixed splits (tiles == 0): grid Q*H, query q has
 //   S_alloc partials.
 //   Tensor-core kernel (tiles > 0): CTA c of `grid` owns the tiles
@@ -216,9 +218,6 @@ __global__ void __launch_bounds__(128)
                           const int64_t* __restrict__ q_pos, int derotate, void* __restrict__ out,
                           int act, float* __restrict__ lse, int64_t tiles, int64_t total, int grid,
                           int by_query, RopeTheta theta) {
-    extern __shared__ float wts[];  // [S_alloc]
-    __shared__ float cs[kRopeDims];
-    __shared__ float s_inv;
     const int tid = threadIdx.x, lane = tid & 31;
     const int h = (int)(blockIdx.x % H);
     int64_t qi;
@@ -246,70 +245,74 @@ __global__ void __launch_bounds__(128)
     }
     const int S = S_alloc;
     const int64_t i = q_pos[qi];
-    if (derotate && tid < kRopeDims / 2) rope_cs(-(double)i, theta.t[tid], &cs[2 * tid], &cs[2 * tid + 1]);
-    if (tid < 32) {
-        const float sk = sink[h];
-        float mstar = sk;
-        for (int s2 = lane; s2 < Sq; s2 += 32) mstar = fmaxf(mstar, part_ml[((qi * S + s2) * H + h) * 2]);
-        mstar = warp_max(mstar);
-        float l = 0.f;
-        for (int s2 = lane; s2 < Sq; s2 += 32) {
-            const float* ml = part_ml + ((qi * S + s2) * H + h) * 2;
-            const float w = (mstar == -INFINITY || ml[0] == -INFINITY) ? 0.f : expf(ml[0] - mstar);
-            wts[s2] = w;
-            l += w * ml[1];
+    const float* ml = part_ml + (qi * S * H + h) * 2;  // slot s: ml[s * 2H], ml[s * 2H + 1]
+    const int64_t mstep = (int64_t)H * 2;
+    const float4* po = reinterpret_cast<const float4*>(part_o + (qi * S * H + h) * D);  // slot s: po[s * H*D/4]
+    const int64_t ostep = (int64_t)H * D / 4;
+    const int d4 = tid;
+    const bool active = d4 < D / 4;
+    // the first eight slots' rows head out first: they do not wait for the weights
+    constexpr int kBatch = 8;
+    float4 v[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; j++)
+        if (active && j < Sq) v[j] = __ldg(po + j * ostep + d4);
+    const float sk = sink[h];
+    float mstar = sk;
+    for (int s2 = lane; s2 < Sq; s2 += 32) mstar = fmaxf(mstar, __ldg(ml + s2 * mstep));
+    mstar = warp_max(mstar);
+    auto weight = [&](int s2) {
+        const float m0 = __ldg(ml + s2 * mstep);
+        return (mstar == -INFINITY || m0 == -INFINITY) ? 0.f : expf(m0 - mstar);
+    };
+    float l = 0.f;
+    for (int s2 = lane; s2 < Sq; s2 += 32) l += weight(s2) * __ldg(ml + s2 * mstep + 1);
+    l = warp_sum(l);
+    if (mstar != -INFINITY && sk != -INFINITY) l += expf(sk - mstar);
+    if (tid == 0 && lse) lse[qi * H + h] = l > 0.f ? mstar + logf(l) : -INFINITY;
+    if (!active) return;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    // slot weights in slot order; a slot of weight 0 is not added (its values
+    // are never used, whatever they hold)
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < Sq; s0 += kBatch) {
+        if (s0 > 0) {
+#pragma unroll
+            for (int j = 0; j < kBatch; j++)
+                if (s0 + j < Sq) v[j] = __ldg(po + (s0 + j) * ostep + d4);
         }
-        l = warp_sum(l);
-        if (mstar != -INFINITY && sk != -INFINITY) l += expf(sk - mstar);
-        if (lane == 0) {
-            s_inv = l > 0.f ? 1.f / l : 0.f;
-            if (lse) lse[qi * H + h] = l > 0.f ? mstar + logf(l) : -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kBatch; j++) {
+            if (s0 + j >= Sq) break;
+            const float w = weight(s0 + j);
+            if (w == 0.f) continue;
+            acc.x = fmaf(w, v[j].x, acc.x);
+            acc.y = fmaf(w, v[j].y, acc.y);
+            acc.z = fmaf(w, v[j].z, acc.z);
+            acc.w = fmaf(w, v[j].w, acc.w);
         }
     }
-    __syncthreads();
-    const float inv = s_inv;
-    for (int d4 = tid; d4 < D / 4; d4 += blockDim.x) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        // eight partials in flight at a time; a slot of weight 0 is not added
-        // (its values are never used, whatever they hold)
-        for (int s0 = 0; s0 < Sq; s0 += 8) {
-            float4 v[8];
+    float o[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+    const int d0 = 4 * d4;
+    if (derotate && d0 >= D - kRopeDims) {
 #pragma unroll
-            for (int j = 0; j < 8; j++)
-                if (s0 + j < Sq)
-                    v[j] = __ldg(reinterpret_cast<const float4*>(part_o + ((qi * S + s0 + j) * H + h) * D) + d4);
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                if (s0 + j >= Sq) break;
-                const float w = wts[s0 + j];
-                if (w == 0.f) continue;
-                acc.x = fmaf(w, v[j].x, acc.x);
-                acc.y = fmaf(w, v[j].y, acc.y);
-                acc.z = fmaf(w, v[j].z, acc.z);
-                acc.w = fmaf(w, v[j].w, acc.w);
-            }
+        for (int pr = 0; pr < 2; pr++) {
+            const int j = (d0 + 2 * pr - (D - kRopeDims)) >> 1;
+            float c, sn;
+            rope_cs(-(double)i, theta.t[j], &c, &sn);
+            const float x0 = o[2 * pr], x1 = o[2 * pr + 1];
+            o[2 * pr] = x0 * c - x1 * sn;
+            o[2 * pr + 1] = x0 * sn + x1 * c;
         }
-        float o[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
-        const int d0 = 4 * d4;
-        if (derotate && d0 >= D - kRopeDims) {
-#pragma unroll
-            for (int pr = 0; pr < 2; pr++) {
-                const int j = (d0 + 2 * pr - (D - kRopeDims)) >> 1;
-                const float c = cs[2 * j], sn = cs[2 * j + 1];
-                const float x0 = o[2 * pr], x1 = o[2 * pr + 1];
-                o[2 * pr] = x0 * c - x1 * sn;
-                o[2 * pr + 1] = x0 * sn + x1 * c;
-            }
-        }
-        if (act == CSA_F32) {
-            reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (qi * H + h) * D)[d4] =
-                make_float4(o[0], o[1], o[2], o[3]);
-        } else {
-            uint2 pk;
-            pk.x = (uint32_t)f32_to_bf16_rn(o[0]) | ((uint32_t)f32_to_bf16_rn(o[1]) << 16);
-            pk.y = (uint32_t)f32_to_bf16_rn(o[2]) | ((uint32_t)f32_to_bf16_rn(o[3]) << 16);
-            reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(out) + (qi * H + h) * D)[d4] = pk;
-        }
+    }
+    if (act == CSA_F32) {
+        reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (qi * H + h) * D)[d4] =
+            make_float4(o[0], o[1], o[2], o[3]);
+    } else {
+        uint2 pk;
+        pk.x = (uint32_t)f32_to_bf16_rn(o[0]) | ((uint32_t)f32_to_bf16_rn(o[1]) << 16);
+        pk.y = (uint32_t)f32_to_bf16_rn(o[2]) | ((uint32_t)f32_to_bf16_rn(o[3]) << 16);
+        reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(out) + (qi * H + h) * D)[d4] = pk;
     }
 }
 
@@ -391,7 +394,7 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
     const int by_query = ranges && Q <= pl.tc_grid - 1;
     const int64_t blocks = (!ranges || by_query) ? (int64_t)Q * H : (int64_t)(pl.tc_grid - 1) * H;
     if (blocks == 0) return cudaSuccess;  // every query was finished by its only CTA
-    attend_combine_kernel<<<(unsigned)blocks, 128, (size_t)pl.splits * sizeof(float), st>>>(
+    attend_combine_kernel<<<(unsigned)blocks, 128, 0, st>>>(
         part_o, part_ml, pl.splits, H, g.D, sink, q_pos, g.derotate, out, g.act, lse,
         ranges ? (int64_t)pl.tc_T : 0, pl.tc_total, pl.tc_grid, by_query, rope_theta(g));
     note_launch();
