@@ -51,13 +51,13 @@ L2_DRAIN_BYTES = 256 << 20
 # captured build (sha256 prefix of the listed files); otherwise it is null.
 CAPTURED_TRAFFIC = {
     "csa_decode_bf16_b32_128k": (
-        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "a2ad93cc9701906e", 274861056),
+        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "9e56bce23e6c0021", 274861056),
     "csa_decode_fp8cache_b8_1m": (
-        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "a2ad93cc9701906e", 546892032),
+        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "9e56bce23e6c0021", 546892032),
     "csa_decode_fp8idx_b32_128k": (
-        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "a2ad93cc9701906e", 143112448),
+        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "9e56bce23e6c0021", 143112448),
     "csa_chunked_prefill_bf16_64k_8k": (
-        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "a2ad93cc9701906e", 712416256),
+        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "9e56bce23e6c0021", 712416256),
     "hca_decode_bf16_b32_1m": (
         ["k_attend_tc.cu", "tc_util.cuh", "common.cuh"], "d3971cf40a8a59e9", 284304512),
 }

@@ -1,5 +1,6 @@
 // k_indexer_tc.cu -- lightning-indexer scoring on the 5th-generation tensor
-// cores (tcgen05 + TMEM + TMA), for bf16 keys of 128 dims and 64 heads.
+// cores (tcgen05 + TMEM + TMA), for keys of 128 dims and 64 heads, in bf16
+// or in E4M3 with one float32 scale per key (kind::f8f6f4 MMAs).
 //
 // "DeepSeek-V4百万上下文时代的开源宣言" §三.2, CSA "Step 2: Lightning Indexer
 // Top-K 选择": score_b = sum_h w_h * relu(q_h . k_b) over causally complete
@@ -12,11 +13,14 @@
 // reuses every key tile for four queries per MMA.
 //
 // Persistent CTAs walk a contiguous range of (query group, key tile) units.
-// Warp 0 issues TMA loads, warp 1 issues the MMAs, the other warps are the
-// epilogue: four (one per TMEM lane quarter) for NQ = 1, sixteen for NQ = 4,
-// where four warps share a quarter and take one of the four queries each (the
-// epilogue, 256 values per key, would otherwise hold the tensor pipe back).  Every wait is bounded: on a timeout the kernel flags
-// CSA_DEV_TIMEOUT, all roles leave their loops and TMEM is freed.
+// Warp 0 issues TMA loads; the MMAs are issued by warp 1, or for NQ = 1 by
+// warps 1 and 2 on alternate tiles; the other warps are the epilogue: for
+// NQ = 1 two groups of four (one per TMEM lane quarter) on alternate
+// accumulators, for NQ = 4 sixteen, where four warps share a quarter and take
+// one of the four queries each (the epilogue, 256 values per key, would
+// otherwise hold the tensor pipe back).  Every wait is bounded: on a timeout
+// the kernel flags CSA_DEV_TIMEOUT, all roles leave their loops and TMEM is
+// freed.
 #include "common.cuh"
 #include "internal.h"
 #include "tc_util.cuh"

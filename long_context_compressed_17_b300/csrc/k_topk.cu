@@ -22,6 +22,12 @@
 // start of its own chunk of the score row -- the scores are consumed -- and
 // one CTA per query selects the final k from the concatenated candidates
 // (still in ascending index order).
+//
+// When few queries each hold one chunk (decode), a cluster of four CTAs
+// selects each query instead: every CTA holds a quarter of the row, the radix
+// passes sum the four histograms over distributed shared memory (each CTA
+// then takes the same decisions), and each CTA lists its kept blocks after
+// those of the CTAs before it.
 #include <cstddef>
 
 #include "common.cuh"
