@@ -460,7 +460,7 @@ def run_gpu(args, rank, world):
            "head_dim": w.D, "heads": w.H, "ratio": w.m, "topk": w.topk, "window": w.W,
            "idx_heads": w.H_I, "idx_dim": w.d_I, "kv_format": w.kv_fmt, "seed": w.seed,
            "l2": "flushed before every timed step: 512 MiB write, then a 256 MiB read of another buffer",
-           "timing": "CUDA events around each step; step captured as 3 CUDA graphs",
+           "timing": "CUDA events around each step; the step captured as CUDA graphs split around the dominant kernel",
            "parallelism": "replicas" if world > 1 else "single GPU",
            "batch_invariant": bool(args.batch_invariant)}
     cfg.update(step_info)
@@ -619,13 +619,20 @@ def cpu_baseline(w, inp, budget_s=15.0):
     # as many queries as fit the budget with the cores busy, capped at the batch
     n_q = int(max(1, min(w.Q, (budget_s / max(t1, 1e-3)) * min(cores, w.Q) * 0.8)))
     s = _oracle_sample(w, inp, n_q)
+    # a sample that is the whole batch is run again until about half the
+    # budget is spent, so that the figure rests on several seconds of work
+    passes = 0
     t0 = time.perf_counter()
-    oracle_step(w, s, raw_pos0)
-    t = time.perf_counter() - t0
-    return {"value": round(n_q / t, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": "%d of the workload's %d queries (%s), %.1f s" % (
+    while True:
+        oracle_step(w, s, raw_pos0)
+        passes += 1
+        t = time.perf_counter() - t0
+        if n_q < w.Q or t >= 0.5 * budget_s or passes >= 64:
+            break
+    return {"value": round(n_q * passes / t, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%d of the workload's %d queries (%s), %d pass%s, %.1f s" % (
                 n_q, w.Q, "sequences 0..%d" % (n_q - 1) if w.kind != "csa_prefill"
-                else "the last %d new tokens" % n_q, t)}
+                else "the last %d new tokens" % n_q, passes, "" if passes == 1 else "es", t)}
 
 
 def run_reference(args, rank, world):
