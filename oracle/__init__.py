@@ -82,6 +82,14 @@ def _declare(L):
     L.oracle_pack_idx_keys_fp8.restype = None
     L.oracle_index_scores_fp8.argtypes = [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _i64, _vp]
     L.oracle_index_scores_fp8.restype = None
+    L.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+    L.oracle_e2m1_decode.restype = _dbl
+    L.oracle_e2m1_encode.argtypes = [_dbl]
+    L.oracle_e2m1_encode.restype = ctypes.c_uint8
+    L.oracle_pack_idx_keys_fp4.argtypes = [_vp, _i64, _i32, _vp, _vp]
+    L.oracle_pack_idx_keys_fp4.restype = None
+    L.oracle_index_scores_fp4.argtypes = [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _i64, _vp]
+    L.oracle_index_scores_fp4.restype = None
     L.oracle_topk.argtypes = [_vp, _i64, _i32, _vp, _vp]
     L.oracle_topk.restype = _i64
     L.oracle_attend_rows.argtypes = [_vp, _i32, _i32, _i32, _i64, _vp, _i64, _vp, _dbl, _i32,
@@ -265,6 +273,58 @@ def index_scores_fp8(q: np.ndarray, w, codes: np.ndarray, scales: np.ndarray) ->
     n = codes.shape[0]
     out = np.empty(n, dtype=np.float64)
     lib().oracle_index_scores_fp8(_ptr(q), fmt_of(q), _ptr(w), HI, dI, _ptr(codes), _ptr(scales), n,
+                                  _ptr(out))
+    return out
+
+
+def e2m1_decode(code: int) -> float:
+    """E2M1 (FP4) code 0..15 -> value."""
+    return float(lib().oracle_e2m1_decode(int(code)))
+
+
+def e2m1_encode(x: float) -> int:
+    """value -> E2M1 code (nearest, ties to the even code, saturating at 6)."""
+    return int(lib().oracle_e2m1_encode(float(x)))
+
+
+def pack_idx_keys_fp4(x: np.ndarray):
+    """float32 keys [n, dI] (dI a multiple of 32) -> (E2M1 codes uint8
+    [n, dI/2], two dims a byte, the even dim in the low nibble; scale bytes
+    uint8 [n, dI/32], block scale 2^(byte - 127))."""
+    x = _c(x, np.float32)
+    n, dI = x.shape
+    assert dI % 32 == 0
+    codes = np.empty((n, dI // 2), dtype=np.uint8)
+    scales = np.empty((n, dI // 32), dtype=np.uint8)
+    lib().oracle_pack_idx_keys_fp4(_ptr(x), n, dI, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def decode_idx_keys_fp4(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """FP4 keys -> float64 values [n, dI] (the oracle's decoder, element by element)."""
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    n, half = codes.shape
+    out = np.empty((n, 2 * half), dtype=np.float64)
+    for b in range(n):
+        for d in range(2 * half):
+            byte = int(codes[b, d // 2])
+            c = (byte >> 4) if d & 1 else (byte & 15)
+            out[b, d] = e2m1_decode(c) * 2.0 ** (int(scales[b, d // 32]) - 127)
+    return out
+
+
+def index_scores_fp4(q: np.ndarray, w, codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """q stored [HI, dI] (its heads quantised to E4M3 inside), w [HI], FP4 keys
+    (codes [n, dI/2], scale bytes [n, dI/32]) -> float64 scores [n]."""
+    q = _c(q)
+    HI, dI = q.shape
+    w = _c(w, np.float64)
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    n = codes.shape[0]
+    out = np.empty(n, dtype=np.float64)
+    lib().oracle_index_scores_fp4(_ptr(q), fmt_of(q), _ptr(w), HI, dI, _ptr(codes), _ptr(scales), n,
                                   _ptr(out))
     return out
 

@@ -346,6 +346,121 @@ void oracle_index_scores_fp8(const void* q, int q_fmt, const double* w, int HI, 
     free(qc);
 }
 
+/* ------------------------------------------------------------------------ */
+/* FP4 indexer keys                                                          */
+/* ------------------------------------------------------------------------ */
+
+/* [gitcode] §2.1.1 and §3.2: the indexer's QK path is quantised to FP4 in
+ * 1 x 32 sub-blocks, which convert to E4M3 without loss when the sub-block
+ * scales of a row stay within the range E4M3's two extra exponent bits
+ * cover.  This oracle's reading of that format: every 32 consecutive dims of
+ * a key share one power-of-two scale 2^e (stored as the byte e + 127), set
+ * by the block's largest magnitude a as e = floor(log2 a) - 2 (so a / 2^e
+ * lies in [4, 8): the E2M1 grid tops out at 6 = 1.5 * 2^2), e = 0 for an
+ * all-zero block; each dim is the E2M1 code of x / 2^e, round to nearest,
+ * ties to the even code, saturating at +-6. */
+
+/* E2M1 code (4 bits: sign, two exponent bits with bias 1, one mantissa bit)
+ * -> value.  Exponent field 0 holds the subnormals 0 and 0.5. */
+double oracle_e2m1_decode(uint8_t code) {
+    const int sign = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+    const double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -v : v;
+}
+
+/* value -> E2M1 code: the nearest of the fifteen values, ties to the even
+ * code, magnitudes beyond 6 saturating (a plain search over the codes). */
+uint8_t oracle_e2m1_encode(double x) {
+    const int neg = x < 0.0 || (x == 0.0 && signbit(x));
+    const double a = fabs(x);
+    int best = 0;
+    double bd = fabs(a - oracle_e2m1_decode(0));
+    for (int c = 1; c < 8; c++) {
+        const double d = fabs(a - oracle_e2m1_decode((uint8_t)c));
+        if (d < bd || (d == bd && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            bd = d;
+        }
+    }
+    return (uint8_t)(best | (neg && best != 0 ? 8 : 0));
+}
+
+/* Keys x [n, dI] (dI a multiple of 32) -> codes [n, dI/2] (dim 2j in the low
+ * nibble of byte j, dim 2j+1 in the high nibble) and scale bytes [n, dI/32]
+ * (block scale 2^(byte - 127)). */
+void oracle_pack_idx_keys_fp4(const float* x, int64_t n, int dI, uint8_t* codes, uint8_t* scales) {
+    const int nb = dI / 32;
+    for (int64_t b = 0; b < n; b++) {
+        const float* row = x + b * dI;
+        for (int j = 0; j < nb; j++) {
+            double amax = 0.0;
+            for (int d = 0; d < 32; d++) {
+                const double a = fabs((double)row[j * 32 + d]);
+                if (a > amax) amax = a;
+            }
+            int e = 0;
+            if (amax > 0.0) {
+                int ex;
+                frexp(amax, &ex); /* amax = f * 2^ex, f in [0.5, 1): floor(log2 amax) = ex - 1 */
+                e = ex - 1 - 2;
+                if (e < -127) e = -127;
+                if (e > 127) e = 127;
+            }
+            scales[b * nb + j] = (uint8_t)(e + 127);
+            for (int d = 0; d < 32; d++) {
+                const int dim = j * 32 + d;
+                const uint8_t c = oracle_e2m1_encode(ldexp((double)row[dim], -e)); /* exact: a power of two */
+                uint8_t* byte = codes + b * (dI / 2) + dim / 2;
+                if ((dim & 1) == 0)
+                    *byte = c;
+                else
+                    *byte = (uint8_t)(*byte | (c << 4));
+            }
+        }
+    }
+}
+
+/* Indexer score with FP4 keys (above) and each query head quantised to E4M3
+ * with one float32 scale per head, as for FP8 keys:
+ *   score_b = sum_h w_h * relu(sum_d (q8_hd * sq_h) * (k4_bd * 2^e_b,d/32)),  b < n
+ * every dequantised value and the sums in double. */
+void oracle_index_scores_fp4(const void* q, int q_fmt, const double* w, int HI, int dI,
+                             const uint8_t* key_codes, const uint8_t* key_scales, int64_t n,
+                             double* scores) {
+    double* qq = (double*)malloc(sizeof(double) * (size_t)HI * (size_t)dI);
+    double* kk = (double*)malloc(sizeof(double) * (size_t)dI);
+    double* row = (double*)malloc(sizeof(double) * (size_t)dI);
+    float* rowf = (float*)malloc(sizeof(float) * (size_t)dI);
+    uint8_t* qc = (uint8_t*)malloc((size_t)dI);
+    for (int h = 0; h < HI; h++) {
+        oracle_read_row(q, q_fmt, dI, h, row);
+        for (int d = 0; d < dI; d++) rowf[d] = (float)row[d];
+        float sq = orc_fp8_row_quant(rowf, dI, qc);
+        for (int d = 0; d < dI; d++) qq[(size_t)h * dI + d] = oracle_e4m3_decode(qc[d]) * (double)sq;
+    }
+    const int nb = dI / 32;
+    for (int64_t b = 0; b < n; b++) {
+        for (int d = 0; d < dI; d++) {
+            const uint8_t byte = key_codes[b * (dI / 2) + d / 2];
+            const uint8_t c = (d & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+            kk[d] = ldexp(oracle_e2m1_decode(c), (int)key_scales[b * nb + d / 32] - 127);
+        }
+        double s = 0.0;
+        for (int h = 0; h < HI; h++) {
+            double dot = 0.0;
+            for (int d = 0; d < dI; d++) dot += qq[(size_t)h * dI + d] * kk[d];
+            double relu = dot > 0.0 ? dot : 0.0;
+            s += w[h] * relu;
+        }
+        scores[b] = s;
+    }
+    free(qq);
+    free(kk);
+    free(row);
+    free(rowf);
+    free(qc);
+}
+
 typedef struct {
     double s;
     int64_t i;
