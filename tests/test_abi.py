@@ -230,3 +230,16 @@ def test_index_topk_fp8_validation(L):
     a = L.csa_workspace_bytes(p, L.OP_INDEX_TOPK, 2, 8, 64, 64, 4096, 128)
     b = L.csa_workspace_bytes(p, L.OP_INDEX_TOPK_FP8, 2, 8, 64, 64, 4096, 128)
     assert b >= a + 8 * 64 * 128 + 8 * 64 * 4
+
+
+def test_batch_invariant_attend_needs_its_own_workspace(L):
+    """A workspace sized for the balanced splits is too small for the fixed
+    ones at the decode shape (32 queries of 18 tiles: at most a few CTAs meet a
+    query, 9 fixed splits each): the call is refused before any launch."""
+    base = L.params(512, 4, topk=1024)
+    inv = L.params(512, 4, topk=1024, batch_invariant=True)
+    n_def = L.csa_workspace_bytes(base, L.OP_ATTEND, 32, 32, 64, 0, 32768, 128)
+    n_inv = L.csa_workspace_bytes(inv, L.OP_ATTEND, 32, 32, 64, 0, 32768, 128)
+    assert n_inv > n_def
+    kw = _attend_args(L, inv, B=32, Q=32, n_cap=32768, ws_bytes=n_def)
+    assert _status_of(L.csa_attend, **kw) == 4  # CSA_ERR_WORKSPACE
