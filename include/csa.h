@@ -216,9 +216,12 @@ csa_status csa_index_topk_fp8(const csa_params* p, const void* q_idx, const floa
  * scratch until the process exits.
  *   - Q * ceil(n_cap / 128) * 128 must not exceed CSA_NOALLOC_MAX_SCORES;
  *     larger requests return CSA_ERR_INVALID_ARG and launch nothing.
- *   - The first call on a device looks up the scratch's device address on
- *     that device (with that device current); make that first call before
- *     any stream capture.
+ *   - Every call looks up the scratch's device address on the current
+ *     device (a host-side query, no allocation).  The first call on a device
+ *     loads the library's device code there if nothing has yet; make that
+ *     first call before any stream capture.  Sizes the top-k selection cannot
+ *     hold (as for csa_index_topk) return CSA_ERR_UNSUPPORTED, launching
+ *     nothing.
  *   - All calls share the one scratch array, which keeps the last call's
  *     contents.  Calls whose work overlaps on the GPU (different streams or
  *     threads without ordering between them) race and give wrong results:

@@ -4,6 +4,8 @@
 #include <math.h>
 
 #include <atomic>
+#include <mutex>
+#include <unordered_map>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -33,15 +35,40 @@ static csa_status cuda_fail(cudaError_t e, const char* what) {
     return fail(CSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// Per-device host caches: the SM count and the largest dynamic shared memory
+// set on each kernel.  A process may drive several devices (each call works
+// on the current one), so nothing is cached process-wide.
+constexpr int kMaxDev = 64;
+static std::atomic<int> g_sms[kMaxDev];
+static std::mutex g_attr_mu;
+static std::unordered_map<const void*, size_t> g_attr[kMaxDev];
+
+static int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    return dev;
+}
+
 int num_sms() {
-    static int n = 0;
+    const int dev = current_device();
+    int n = (dev >= 0 && dev < kMaxDev) ? g_sms[dev].load(std::memory_order_relaxed) : 0;
     if (n == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 148;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        if (dev >= 0 && dev < kMaxDev) g_sms[dev].store(n, std::memory_order_relaxed);
     }
     return n;
+}
+
+cudaError_t set_smem_attr(const void* kernel, size_t bytes) {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDev)
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    std::lock_guard<std::mutex> lock(g_attr_mu);
+    size_t& have = g_attr[dev][kernel];
+    if (bytes <= have) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) have = bytes;
+    return e;
 }
 
 Geometry resolve(const csa_params* p) {

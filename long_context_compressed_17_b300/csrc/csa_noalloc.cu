@@ -12,8 +12,6 @@
 // scores are fully rewritten before they are read.
 #include <stdio.h>
 
-#include <mutex>
-
 #include "common.cuh"
 #include "internal.h"
 
@@ -23,38 +21,23 @@ constexpr size_t kNoallocHeader = kStatusWordBytes;
 constexpr size_t kNoallocScratchBytes = kNoallocHeader + (size_t)CSA_NOALLOC_MAX_SCORES * sizeof(float);
 
 // Host code must not use this name as an address: it is a host-side stand-in.
-// The device address comes from cudaGetSymbolAddress, per device.
+// The device address comes from cudaGetSymbolAddress on the current device.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-static std::mutex g_scratch_mu;
-static void* g_scratch_addr[kMaxDevices];
-
-// Device address of the scratch on the current device; looked up once per
-// device, with that device current.
+// Device address of the scratch on the current device.  It is looked up on
+// every call rather than cached: the lookup is a host-side table read once
+// the library's module is loaded on the device, and a cached address would go
+// stale if the device's primary context were reset and the module reloaded
+// elsewhere.
 static csa_status scratch_address(void** out) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
         char msg[160];
-        snprintf(msg, sizeof(msg), "csa_index_topk_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
+        snprintf(msg, sizeof(msg), "csa_index_topk_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
         return set_error(CSA_ERR_CUDA, msg);
     }
-    if (dev < 0 || dev >= kMaxDevices)
-        return set_error(CSA_ERR_UNSUPPORTED, "csa_index_topk_noalloc: device ordinal above 63");
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || p == nullptr) {
-            char msg[160];
-            snprintf(msg, sizeof(msg), "csa_index_topk_noalloc: cudaGetSymbolAddress: %s",
-                     cudaGetErrorString(e));
-            return set_error(CSA_ERR_CUDA, msg);
-        }
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    *out = p;
     return CSA_OK;
 }
 
@@ -80,7 +63,7 @@ extern "C" csa_status csa_index_topk_noalloc(const csa_params* p, const void* q_
     }
     if (status && ((uintptr_t)status & 3u))
         return set_error(CSA_ERR_INVALID_ARG, "csa_index_topk_noalloc: status is not 4-byte aligned");
-    // the checks csa_index_score / csa_topk_select apply, made before anything is launched
+    // every check csa_index_score / csa_topk_select apply, made before anything is launched
     if (!p || csa_workspace_bytes(p, CSA_OP_INDEX_TOPK, B > 0 ? B : 1, Q, 1, n_idx_heads, n_cap, 0) == 0)
         return set_error(CSA_ERR_INVALID_ARG, "csa_index_topk_noalloc: invalid params or sizes");
     if (p->topk < 1 || p->topk > 4096)
@@ -90,6 +73,9 @@ extern "C" csa_status csa_index_topk_noalloc(const csa_params* p, const void* q_
     if (B < 1 || Q % B != 0)
         return set_error(CSA_ERR_INVALID_ARG, "csa_index_topk_noalloc: Q must be a multiple of B");
     if (Q == 0) return CSA_OK;
+    if (topk_chunk(n_cap, Q, p->topk) == 0)
+        return set_error(CSA_ERR_UNSUPPORTED,
+                         "csa_index_topk_noalloc: the top-k selection of these sizes does not fit in shared memory");
     const void* ptrs[] = {q_idx, w_idx, q_pos, topk_idx};
     for (const void* ptr : ptrs)
         if (!ptr || ((uintptr_t)ptr & 15u))

@@ -103,7 +103,12 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
                           int64_t n_win, const int64_t* win_pos0, const float* sink, void* out,
                           float* lse, uint8_t* ws, uint32_t* status, cudaStream_t st);
 
+// SM count of the current device (cached per device).
 int num_sms();
+
+// Raise a kernel's dynamic shared memory limit to at least `bytes` on the
+// current device (cached per device and kernel; thread-safe).
+cudaError_t set_smem_attr(const void* kernel, size_t bytes);
 
 // Kernel launch accounting (csa_launch_count).
 void note_launch(int n = 1);

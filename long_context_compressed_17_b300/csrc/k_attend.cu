@@ -327,8 +327,7 @@ template <int D, int HG>
 static cudaError_t run_generic(const AttendArgs& a, int Q, int H, cudaStream_t st) {
     size_t smem = (size_t)(HG * D + kAttRows * (D + 1) + HG * kAttRows + 3 * HG + 64) * sizeof(float) +
                   kAttRows * sizeof(void*);
-    cudaError_t e = cudaFuncSetAttribute(attend_generic_kernel<D, HG>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(attend_generic_kernel<D, HG>), smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)Q, (unsigned)(H / HG), (unsigned)a.S);
     attend_generic_kernel<D, HG><<<grid, kAttThreads, smem, st>>>(a);

@@ -1126,12 +1126,9 @@ cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool spars
     a.derotate = g.derotate;
     a.status = status;
     a.theta = rope_theta(g);
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmem);
+    {
+        cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(attend_tc_kernel), kSmem);
         if (e != cudaSuccess) return e;
-        attr = true;
     }
     CUtensorMap tm_q;
     {

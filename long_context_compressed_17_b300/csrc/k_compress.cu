@@ -272,12 +272,9 @@ cudaError_t launch_compress(const Geometry& g, const void* kv, int B, int64_t T,
         const size_t slice = ((size_t)mt * act_rb + 15) & ~(size_t)15;
         const size_t smem = slice + (size_t)(((mt + 3) & ~3) + kSplit * (4 + g.D) + 32) * sizeof(float);
         if (slice >= (size_t)g.D * sizeof(float) && smem <= 200 * 1024) {
-            static size_t attr = 0;
-            if (smem > attr) {
-                cudaError_t e = cudaFuncSetAttribute(compress_cluster_kernel,
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            {
+                cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(compress_cluster_kernel), smem);
                 if (e != cudaSuccess) return e;
-                attr = smem;
             }
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3((unsigned)(nb * kSplit), (unsigned)B, 1);
@@ -306,8 +303,7 @@ cudaError_t launch_compress(const Geometry& g, const void* kv, int B, int64_t T,
     const int staged = blk_bytes <= kCompressStageMax ? 1 : 0;
     if (staged) smem += blk_bytes;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(compress_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(compress_kernel), smem);
         if (e != cudaSuccess) return e;
     }
     dim3 grid((unsigned)nb, (unsigned)B);

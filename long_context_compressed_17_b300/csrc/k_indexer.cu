@@ -88,8 +88,7 @@ cudaError_t launch_indexer(const Geometry& g, const void* q_idx, const float* w_
     size_t smem = (size_t)(HI * dI + HI) * sizeof(float);
     auto run = [&](auto kern) -> cudaError_t {
         if (smem > 48 * 1024) {
-            cudaError_t a = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)smem);
+            cudaError_t a = set_smem_attr(reinterpret_cast<const void*>(kern), smem);
             if (a != cudaSuccess) return a;
         }
         kern<<<grid, kIdxTile, smem, st>>>(reinterpret_cast<const uint8_t*>(q_idx), w_idx, HI,

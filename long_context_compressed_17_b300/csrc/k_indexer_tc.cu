@@ -377,12 +377,9 @@ template <int NQ, bool F8>
 static cudaError_t run_indexer(const CUtensorMap& tm_keys, const CUtensorMap& tm_q, const IdxArgs& a, int grid,
                                cudaStream_t st) {
     using C = Cfg<NQ, F8>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<NQ, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)C::kSmem);
+    {
+        cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(indexer_tc_kernel<NQ, F8>), C::kSmem);
         if (e != cudaSuccess) return e;
-        attr = true;
     }
     indexer_tc_kernel<NQ, F8><<<grid, C::kThreads, C::kSmem, st>>>(tm_keys, tm_q, a);
     note_launch();

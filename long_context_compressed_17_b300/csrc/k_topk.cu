@@ -577,12 +577,9 @@ cudaError_t launch_topk(const Geometry& g, float* scores, int64_t ld, int64_t n_
     if (n_cap <= kChunk && n_cap >= kClusterMinKeys && (int64_t)Q * kClusterCS <= 2LL * num_sms()) {
         // few queries of one chunk each (decode): kClusterCS CTAs a query
         const size_t smem = ((size_t)(n_cap / kClusterCS + 4) * sizeof(uint32_t) + 15) & ~(size_t)15;
-        static size_t attr = 0;
-        if (smem > attr) {
-            cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel<kClusterCS>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        {
+            cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(topk_cluster_kernel<kClusterCS>), smem);
             if (e != cudaSuccess) return e;
-            attr = smem;
         }
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)kClusterCS, (unsigned)Q, 1);
@@ -606,14 +603,10 @@ cudaError_t launch_topk(const Geometry& g, float* scores, int64_t ld, int64_t n_
     const size_t smem1 = ((size_t)(n_cap < kChunk ? (n_cap > 0 ? n_cap : 1) : kChunk) * sizeof(uint32_t) + 15) & ~(size_t)15;
     // two CTAs an SM when both fit in its 228 KiB of shared memory
     const bool two = smem1 + sizeof(Scratch) + 1024 <= 114 * 1024;
-    static int attr1[2] = {0, 0};
-    if ((int)smem1 > attr1[two]) {
-        cudaError_t e = two ? cudaFuncSetAttribute(topk_chunk_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)smem1)
-                            : cudaFuncSetAttribute(topk_chunk_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)smem1);
+    {
+        cudaError_t e = two ? set_smem_attr(reinterpret_cast<const void*>(topk_chunk_kernel<2>), smem1)
+                            : set_smem_attr(reinterpret_cast<const void*>(topk_chunk_kernel<1>), smem1);
         if (e != cudaSuccess) return e;
-        attr1[two] = (int)smem1;
     }
     dim3 grid1((unsigned)max_chunks, (unsigned)Q);
     if (two)
@@ -624,12 +617,8 @@ cudaError_t launch_topk(const Geometry& g, float* scores, int64_t ld, int64_t n_
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || max_chunks <= 1) return e;
     const size_t smem2 = ((size_t)max_chunks * k * sizeof(uint32_t) + 15) & ~(size_t)15;
-    static int attr2 = 0;
-    if ((int)smem2 > attr2) {
-        e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
-        if (e != cudaSuccess) return e;
-        attr2 = (int)smem2;
-    }
+    e = set_smem_attr(reinterpret_cast<const void*>(topk_merge_kernel), smem2);
+    if (e != cudaSuccess) return e;
     topk_merge_kernel<<<(unsigned)Q, kThreads, smem2, st>>>(scores, ld, n_cap, q_pos, g.m, k, idx, sel);
     note_launch();
     return cudaGetLastError();

@@ -243,3 +243,14 @@ def test_batch_invariant_attend_needs_its_own_workspace(L):
     assert n_inv > n_def
     kw = _attend_args(L, inv, B=32, Q=32, n_cap=32768, ws_bytes=n_def)
     assert _status_of(L.csa_attend, **kw) == 4  # CSA_ERR_WORKSPACE
+
+
+def test_noalloc_refuses_an_oversized_selection_before_any_launch(L):
+    # fits the static scratch (1 x 4194304 scores) but not the top-k merge's shared
+    # memory (128 chunks x 1024 candidates): refused before the status word is cleared
+    p = L.params(512, 4, topk=1024)
+    n0 = L.csa_launch_count()
+    with pytest.raises(L.CsaError) as ei:
+        L.csa_index_topk_noalloc(p, FAKE, FAKE, 64, 128, FAKE, 4194304, 1, 1, FAKE, FAKE, None, None)
+    assert ei.value.status == 2 and "shared memory" in L.csa_last_error()
+    assert L.csa_launch_count() == n0

@@ -3,7 +3,8 @@ allocate device memory (a plug-in whose host framework owns every device
 allocation, or a latency-critical path that cannot risk the synchronisation an
 allocation may cause).  Its scores live in a scratch array inside the library,
 so the checks here are: it agrees with csa_index_topk (which uses a caller
-workspace) on two calls in a row with different shapes, it rejects requests
+workspace) on three calls in a row with different shapes (the last one large
+enough for the chunked selection), it rejects requests
 larger than the scratch, and it reports device status through its own output.
 
 This file is named to be collected last.
@@ -59,11 +60,15 @@ CALLS = [
                                       topk=100),
     workloads.CSA_DECODE_128K.replace(name="noalloc_b", seed=7, B=2, L_per_seq=(3001, 777),
                                       topk=50, H_I=32),
+    # more than 32768 blocks: the selection runs in chunks whose candidates are
+    # written over the scores (here the shared scratch) and merged
+    workloads.CSA_DECODE_128K.replace(name="noalloc_c", seed=8, B=2, L_per_seq=(160000, 140001),
+                                      topk=1024),
 ]
 
 
-def test_noalloc_matches_workspace_entry_point_on_two_calls(L):
-    for w in CALLS:  # two calls in a row, the second smaller than the first
+def test_noalloc_matches_workspace_entry_point_on_calls_in_a_row(L):
+    for w in CALLS:  # calls in a row: the second smaller than the first, the third chunked
         p = L.params(w.D, w.m, topk=w.topk, window=w.W, act=w.act, kv=w.kv_fmt)
         inp = _inputs(w)
         ref_idx, ref_sc = _with_workspace(L, w, p, inp)
