@@ -51,22 +51,22 @@ L2_DRAIN_BYTES = 256 << 20
 # A figure holds only while the kernel's sources are byte-identical to the
 # captured build (sha256 prefix of the listed files); otherwise it is null.
 CAPTURED_TRAFFIC = {
-    "csa_decode_bf16_b32_128k": (
+    ("csa_decode_bf16_b32_128k", "indexer"): (
         ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "9e56bce23e6c0021", 274861056),
-    "csa_decode_fp8cache_b8_1m": (
+    ("csa_decode_fp8cache_b8_1m", "indexer"): (
         ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "9e56bce23e6c0021", 546892032),
-    "csa_decode_fp8idx_b32_128k": (
+    ("csa_decode_fp8idx_b32_128k", "indexer"): (
         ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "9e56bce23e6c0021", 143112448),
-    "csa_chunked_prefill_bf16_64k_8k": (
+    ("csa_chunked_prefill_bf16_64k_8k", "indexer"): (
         ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "9e56bce23e6c0021", 712416256),
-    "hca_decode_bf16_b32_1m": (
+    ("hca_decode_bf16_b32_1m", "attention"): (
         ["k_attend_tc.cu", "tc_util.cuh", "common.cuh"], "d3971cf40a8a59e9", 284304512),
 }
 
 
-def captured_traffic(workload: str):
+def captured_traffic(workload: str, kernel: str):
     import hashlib
-    entry = CAPTURED_TRAFFIC.get(workload)
+    entry = CAPTURED_TRAFFIC.get((workload, kernel))
     if entry is None:
         return None
     files, digest, nbytes = entry
@@ -214,27 +214,54 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ work units
 def algorithmic(w: workloads.Workload, row_bytes: int):
-    """Algorithmic bytes / flops per step: the dominant kernel and the whole step."""
+    """Algorithmic work of every kernel segment of a step (bytes for the
+    HBM-bound ones, flops for the tensor- or ALU-bound ones) and of the step.
+    The per-unit figures are the ones the design notes tabulate: decode
+    indexer n*(d_I*2) + queries and weights per query (E4M3 keys: n*(d_I+4));
+    attention (k + W) or (n + W) stored rows + q and out per query; prefill
+    indexer 2*H_I*d_I*n(i) and attention 4*H*D*(k + W) flops per query."""
     act_es = 4 if w.act == "f32" else 2
+    seg = {}
     if w.kind in ("csa_decode", "hca_decode"):
         n_av = [L // w.m for L in w.lengths]
         q_out = w.H * w.D * act_es * 2
+        act_rb = w.D * act_es
+        # append: the newest raw token and its raw-ring slot, the window row and,
+        # where a block completes, the block's earlier raw tokens and its entry
+        app = sum(2 * act_rb + row_bytes + ((w.m - 1) * act_rb + row_bytes if L % w.m == 0 else 0)
+                  for L in w.lengths)
         if w.kind == "csa_decode":
             if w.idx_fmt == "fp8":  # E4M3 codes and a float32 scale per key; bf16 queries quantised in the step
                 idx_bytes = sum(n * (w.d_I + 4) + w.H_I * w.d_I * act_es + w.H_I * 4 for n in n_av)
+            elif w.idx_fmt == "fp4":  # E2M1 codes and four scale bytes per key (68 bytes)
+                idx_bytes = sum(n * (w.d_I // 2 + w.d_I // 32) + w.H_I * w.d_I * act_es + w.H_I * 4 for n in n_av)
             else:
                 idx_bytes = sum(n * w.d_I * act_es + w.H_I * w.d_I * act_es + w.H_I * 4 for n in n_av)
-            rows = w.B * (min(w.topk, max(n_av)) + w.W)
-            step = idx_bytes + rows * row_bytes + w.B * q_out
-            return {"kernel": "indexer", "bound": "hbm", "bytes": idx_bytes, "step_bytes": step}
+            att = sum((min(w.topk, n) + w.W) * row_bytes for n in n_av) + w.B * q_out
+            topk = sum(n * 4 for n in n_av)  # the score rows the selection reads
+            seg["indexer"] = {"bound": "hbm", "bytes": idx_bytes}
+            seg["topk"] = {"bound": "hbm", "bytes": topk,
+                           "note": "latency-bound selection; bytes are the score rows read"}
+            seg["attention"] = {"bound": "hbm", "bytes": att}
+            return seg, idx_bytes + att + app
         att = sum((n + w.W) * row_bytes for n in n_av) + w.B * q_out
-        return {"kernel": "hca_attend", "bound": "hbm", "bytes": att, "step_bytes": att}
-    # prefill: indexer flops over causally complete blocks
+        seg["append"] = {"bound": "hbm", "bytes": app}
+        seg["attention"] = {"bound": "hbm", "bytes": att}
+        return seg, att + app
+    # prefill: indexer flops over causally complete blocks, attention over k + W rows
     fl = 0
     for t in range(w.T_new):
         fl += 2 * w.H_I * w.d_I * ((w.T_cached + t + 1) // w.m)
+    att = 0
+    for t in range(w.T_new):
+        i = w.T_cached + t
+        att += 4 * w.H * w.D * (min(w.topk, (i + 1) // w.m) + min(w.W, i + 1))
     bound = "alu" if w.act == "f32" else "tensor"
-    return {"kernel": "indexer", "bound": bound, "flops": fl, "step_flops": fl}
+    seg["indexer"] = {"bound": bound, "flops": fl}
+    seg["topk"] = {"bound": "hbm", "bytes": sum(4 * ((w.T_cached + t + 1) // w.m) for t in range(w.T_new)),
+                   "note": "latency-bound selection; bytes are the score rows read"}
+    seg["attention"] = {"bound": bound, "flops": att}
+    return seg, None
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -243,7 +270,7 @@ class GpuStep:
 
     def __init__(self, w: workloads.Workload, batch_invariant: bool = False):
         import long_context_compressed_17_b300 as L
-        from long_context_compressed_17_b300.pipeline import DecodeLayer, LayerConfig, PrefillLayer
+        from long_context_compressed_17_b300.pipeline import DecodeLayer, LayerConfig, PrefillLayer, ring_order
         self.L, self.w = L, w
         self.inp = workloads.generate(w, device="cuda")
         inp = self.inp
@@ -265,11 +292,17 @@ class GpuStep:
                     self.rows[key] = x.clone()
             torch.cuda.synchronize()
         if w.kind in ("csa_decode", "hca_decode"):
-            assert len(set(w.lengths)) == 1, "the benchmark runs uniform lengths"
+            # decode state: cache, window ring (position p at row p mod W) and the
+            # raw tokens of each sequence's current block (slot p mod m); every
+            # step appends each sequence's newest token at its own position
             self.layer = DecodeLayer(cfg, w.B, w.n_cap, w.W)
-            Lb = w.lengths[0]
-            self.pos_first = Lb - w.m
-            self.win_row = (Lb - 1) - int(inp["win_pos0"][0])
+            lens = torch.tensor(w.lengths, dtype=torch.int64)
+            self.rows["window"] = ring_order(self.rows["window"], inp["win_pos0"].cpu(), w.W)
+            self.raw_ring = ring_order(inp["kv_new"], (lens - w.m).tolist(), w.m)
+            self.kv_tok = inp["kv_new"][:, w.m - 1].contiguous()
+            self.step_inputs = {"q": inp["q"], "kv_tok": self.kv_tok, "q_pos": inp["q_pos"]}
+            if w.kind == "csa_decode":
+                self.step_inputs.update(q_idx=inp["q_idx"], w_idx=inp["w_idx"])
             if w.kind == "csa_decode":
                 # the append feeds only the attention: it runs on a side stream
                 # beside the indexer's top-k (one CTA per query leaves most SMs free)
@@ -286,7 +319,16 @@ class GpuStep:
                     self.idx_ws_bytes = 256 + (w.B * 64 * 128 + 255) // 256 * 256 + (w.B * 64 * 4 + 255) // 256 * 256
                     self.idx_ws = L.workspace(self.idx_ws_bytes)
                     torch.cuda.synchronize()
+                if w.idx_fmt == "fp4":  # layer state: the keys in FP4, packed once
+                    keys = inp["keys"]
+                    self.key_pack = torch.empty(w.B, L.csa_index_keys_fp4_bytes(w.n_cap), dtype=torch.uint8,
+                                                device="cuda")
+                    L.csa_index_keys_pack_fp4(cfg.params(), keys, w.B, w.n_cap, w.d_I, self.key_pack)
+                    self.idx_ws_bytes = 256 + (w.B * 64 * 128 + 255) // 256 * 256 + (w.B * 64 * 4 + 255) // 256 * 256
+                    self.idx_ws = L.workspace(self.idx_ws_bytes)
+                    torch.cuda.synchronize()
         else:
+            self.step_inputs = {k: inp[k] for k in ("q", "kv_raw", "q_pos", "q_idx", "w_idx")}
             self.layer = PrefillLayer(cfg, w.T_cached, w.T_new)
             if w.T_cached:
                 old = inp["cache_old"]
@@ -298,56 +340,68 @@ class GpuStep:
             self.ld = (self.layer.n_cap + 127) // 128 * 128
             self.scores = torch.empty(w.T_new, self.ld, dtype=torch.float32, device="cuda")
 
-    # the three segments of a step
-    def has_before(self):
-        return self.w.kind == "csa_prefill" or (self.w.kind == "hca_decode" and self.pos_first >= 0)
-
-    def before(self):
-        w, inp, lay = self.w, self.inp, self.layer
-        if w.kind == "csa_prefill":
-            lay.compress(inp["kv_raw"], inp["w_z"], inp["bias"])
-        elif w.kind == "hca_decode" and self.pos_first >= 0:
-            lay.append(inp["kv_new"], self.pos_first, inp["w_z"], inp["bias"], self.rows["cache"],
-                       self.rows["window"], self.win_row)
-
-    def dominant(self):
-        w, inp, lay, L = self.w, self.inp, self.layer, self.L
+    # ------------------------------------------------------------ segments of a step
+    def segments(self):
+        """The step as named kernel segments, in order; each is captured as its
+        own CUDA graph so that events bracket it."""
+        w = self.w
         if w.kind == "hca_decode":
-            L.hca_attend(lay.p, inp["q"], w.H, w.B, w.B, inp["q_pos"], self.rows["cache"],
-                         w.n_cap, self.rows["window"], w.W, inp["win_pos0"], inp["sink"], lay.out,
-                         lay.lse, lay.ws, lay.ws_bytes)
-            return
+            return [("append", self.append), ("attention", self.attention)]
+        if w.kind == "csa_decode":
+            return [("indexer", self.indexer), ("topk", self.topk), ("attention", self.attention)]
+        return [("compress", self.compress), ("indexer", self.indexer), ("topk", self.topk),
+                ("attention", self.attention)]
+
+    def append(self, stream=None):
+        inp = self.inp
+        self.layer.append(self.kv_tok, inp["q_pos"], inp["w_z"], inp["bias"], self.raw_ring, self.rows["cache"],
+                          self.rows["window"], stream=stream)
+
+    def compress(self):
+        inp = self.inp
+        self.layer.compress(inp["kv_raw"], inp["w_z"], inp["bias"])
+
+    def indexer(self):
+        w, inp, lay, L = self.w, self.inp, self.layer, self.L
         B = w.B if w.kind == "csa_decode" else 1
         n_cap = w.n_cap if w.kind == "csa_decode" else lay.n_cap
-        keys = inp["keys"]
         if w.idx_fmt == "fp8":
             L.csa_index_score_fp8(lay.p, inp["q_idx"], inp["w_idx"], w.H_I, w.d_I, self.key_codes,
                                   self.key_scales, n_cap, B, w.Q, inp["q_pos"], self.scores, self.ld,
                                   self.idx_ws, self.idx_ws_bytes)
-            return
-        L.csa_index_score(lay.p, inp["q_idx"], inp["w_idx"], w.H_I, w.d_I, keys, n_cap, B, w.Q,
-                          inp["q_pos"], self.scores, self.ld, lay.ws, lay.ws_bytes)
+        elif w.idx_fmt == "fp4":
+            L.csa_index_score_fp4(lay.p, inp["q_idx"], inp["w_idx"], w.H_I, w.d_I, self.key_pack, n_cap, B, w.Q,
+                                  inp["q_pos"], self.scores, self.ld, self.idx_ws, self.idx_ws_bytes)
+        else:
+            L.csa_index_score(lay.p, inp["q_idx"], inp["w_idx"], w.H_I, w.d_I, inp["keys"], n_cap, B, w.Q,
+                              inp["q_pos"], self.scores, self.ld, lay.ws, lay.ws_bytes)
 
-    def after(self):
+    def topk(self):
+        """The selection; for decode the append runs beside it on a side stream
+        (it feeds only the attention) and joins before the segment ends."""
         w, inp, lay, L = self.w, self.inp, self.layer, self.L
-        if w.kind == "hca_decode":
-            return
         n_cap = w.n_cap if w.kind == "csa_decode" else lay.n_cap
-        forked = w.kind == "csa_decode" and self.pos_first >= 0
+        forked = w.kind == "csa_decode"
         if forked:
             main = torch.cuda.current_stream()
             self.ev_fork.record(main)
             self.side.wait_event(self.ev_fork)
-            lay.append(inp["kv_new"], self.pos_first, inp["w_z"], inp["bias"], self.rows["cache"],
-                       self.rows["window"], self.win_row, stream=self.side)
+            self.append(stream=self.side)
             self.ev_join.record(self.side)
         L.csa_topk_select(lay.p, self.scores, self.ld, n_cap, w.Q, inp["q_pos"], lay.topk_idx,
                           lay.topk_score)
         if forked:
             main.wait_event(self.ev_join)
-        if w.kind == "csa_decode":
+
+    def attention(self):
+        w, inp, lay, L = self.w, self.inp, self.layer, self.L
+        if w.kind == "hca_decode":
+            L.hca_attend(lay.p, inp["q"], w.H, w.B, w.B, inp["q_pos"], self.rows["cache"],
+                         w.n_cap, self.rows["window"], w.W, None, inp["sink"], lay.out,
+                         lay.lse, lay.ws, lay.ws_bytes)
+        elif w.kind == "csa_decode":
             L.csa_attend(lay.p, inp["q"], w.H, w.B, w.B, inp["q_pos"], self.rows["cache"],
-                         w.n_cap, lay.topk_idx, self.rows["window"], w.W, inp["win_pos0"],
+                         w.n_cap, lay.topk_idx, self.rows["window"], w.W, None,
                          inp["sink"], lay.out, lay.lse, lay.ws, lay.ws_bytes)
         else:
             L.csa_attend(lay.p, inp["q"], w.H, 1, w.Q, inp["q_pos"], lay.cache, lay.n_cap,
@@ -355,22 +409,64 @@ class GpuStep:
                          lay.lse, lay.ws, lay.ws_bytes)
 
     def run_eager(self):
-        self.before()
-        self.dominant()
-        self.after()
+        for _, fn in self.segments():
+            fn()
 
     def capture(self):
-        self.graphs = []
-        for seg in (self.before, self.dominant, self.after):
-            if seg == self.before and not self.has_before():
-                self.graphs.append(None)
-                continue
+        """The whole step as one CUDA graph (what a serving loop replays), with
+        timing events recorded between its segments inside the graph; where
+        the runtime cannot record events inside a graph, one graph a segment."""
+        segs = self.segments()
+        try:
+            self.inner = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(segs) - 1)]
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                seg()
-            self.graphs.append(g)
-        torch.cuda.synchronize()
-        self.launches_per_step = None
+                for j, (_, fn) in enumerate(segs):
+                    fn()
+                    if j < len(segs) - 1:
+                        self.inner[j].record()
+            torch.cuda.synchronize()
+            self.graphs = [("step", g)]
+            self.one_graph = True
+        except (TypeError, RuntimeError):
+            torch.cuda.synchronize()
+            self.one_graph = False
+            self.graphs = []
+            for name, fn in segs:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    fn()
+                self.graphs.append((name, g))
+            torch.cuda.synchronize()
+        self.seg_names = [n for n, _ in segs]
+
+
+def _roofline(kernel, work, ms, peaks, traffic):
+    """One kernel's roofline entry: algorithmic work per launch / CUDA-event time."""
+    if work["bound"] == "hbm":
+        achieved = work["bytes"] / (ms * 1e-3) / 1e9
+        r = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+             "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic, "kernel": kernel,
+             "kernel_ms": round(ms, 5), "bytes_per_launch": work["bytes"],
+             "peak_source": peaks["source"] + " copy bandwidth (burst)",
+             # the same against the nominal ~8 TB/s the layer is specified against
+             "nominal_peak": NOMINAL_HBM_GBS, "nominal_frac": round(achieved / NOMINAL_HBM_GBS, 4)}
+    elif work["bound"] == "tensor":
+        achieved = work["flops"] / (ms * 1e-3) / 1e12
+        r = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+             "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic, "kernel": kernel,
+             "kernel_ms": round(ms, 5), "flops_per_launch": work["flops"],
+             "peak_source": peaks["source"] + " bf16 dense (burst)"}
+    else:
+        # fp32 FMA peak: 148 SMs x 128 lanes x 2 flop x max SM clock
+        peak = 148 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+        achieved = work["flops"] / (ms * 1e-3) / 1e12
+        r = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+             "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel, "kernel_ms": round(ms, 5),
+             "flops_per_launch": work["flops"], "peak_source": "fp32 FMA units x max clock"}
+    if "note" in work:
+        r["note"] = work["note"]
+    return r
 
 
 def run_gpu(args, rank, world):
@@ -378,7 +474,7 @@ def run_gpu(args, rank, world):
     w = workloads.BY_NAME[args.workload]
     peaks = measured_peaks()
     st = GpuStep(w, batch_invariant=args.batch_invariant)
-    alg = algorithmic(w, st.row_bytes)
+    segs, step_bytes = algorithmic(w, st.row_bytes)
     for _ in range(2):  # untimed eager passes: kernel attributes, first-launch costs
         st.run_eager()
     torch.cuda.synchronize()
@@ -392,37 +488,48 @@ def run_gpu(args, rank, world):
         flush.zero_()
         torch.sum(drain, dim=None, out=drain_out)
 
-    g0, g1, g2 = st.graphs
     for _ in range(args.warmup):
         flush_l2()
-        if g0 is not None:
-            g0.replay()
-        g1.replay()
-        g2.replay()
+        for _, g in st.graphs:
+            g.replay()
     torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    nseg = len(st.seg_names)
+    step_ms, seg_ms = [], {n: [] for n in st.seg_names}
     _barrier(world)
     torch.cuda.synchronize()
-    n0 = L.csa_launch_count()
     with ClockSampler(torch.cuda.current_device()) as clk:
-        for k in range(args.steps):
-            flush_l2()                    # L2 flushed before every timed step
-            e = ev[k]
-            e[0].record()
-            if g0 is not None:
-                g0.replay()
-            e[1].record()
-            g1.replay()
-            e[2].record()
-            g2.replay()
-            e[3].record()
+        if st.one_graph:
+            # one replay a step; the events inside the graph are re-recorded by
+            # every replay, so each step's times are read before the next
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g = st.graphs[0][1]
+            for k in range(args.steps):
+                flush_l2()                # L2 flushed before every timed step
+                e0.record()
+                g.replay()
+                e1.record()
+                e1.synchronize()
+                marks = [e0] + st.inner + [e1]
+                step_ms.append(e0.elapsed_time(e1))
+                for j, n in enumerate(st.seg_names):
+                    seg_ms[n].append(marks[j].elapsed_time(marks[j + 1]))
+        else:
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nseg + 1)] for _ in range(args.steps)]
+            for k in range(args.steps):
+                flush_l2()
+                e = ev[k]
+                e[0].record()
+                for j, (_, g) in enumerate(st.graphs):
+                    g.replay()
+                    e[j + 1].record()
+            torch.cuda.synchronize()
+            step_ms = [ev[k][0].elapsed_time(ev[k][nseg]) for k in range(args.steps)]
+            seg_ms = {name: [ev[k][j].elapsed_time(ev[k][j + 1]) for k in range(args.steps)]
+                      for j, name in enumerate(st.seg_names)}
         torch.cuda.synchronize()
     _barrier(world)
-    step_ms = [ev[k][0].elapsed_time(ev[k][3]) for k in range(args.steps)]
-    dom_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
-    ms = statistics.mean(step_ms)
+    ms = statistics.median(step_ms)
     ms = _max_over_ranks(ms, world)
-    dom = statistics.mean(dom_ms)
     # kernels per step, counted on an eager pass (graph replays do not go through the library)
     n1 = L.csa_launch_count()
     st.run_eager()
@@ -432,48 +539,37 @@ def run_gpu(args, rank, world):
     e2e = run_e2e(st, args)
 
     value = world * w.Q / (ms * 1e-3)
-    if alg["bound"] == "hbm":
-        achieved = alg["bytes"] / (dom * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": captured_traffic(w.name), "kernel": alg["kernel"], "kernel_ms": round(dom, 5),
-                "bytes_per_launch": alg["bytes"], "peak_source": peaks["source"] + " (burst)",
-                # the same against the nominal ~8 TB/s the layer is specified against
-                "nominal_peak": NOMINAL_HBM_GBS, "nominal_frac": round(achieved / NOMINAL_HBM_GBS, 4)}
-    elif alg["bound"] == "tensor":
-        achieved = alg["flops"] / (dom * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "traffic": captured_traffic(w.name), "kernel": alg["kernel"], "kernel_ms": round(dom, 5),
-                "flops_per_launch": alg["flops"], "peak_source": peaks["source"] + " bf16 (burst)"}
-    else:
-        # fp32 FMA peak: 148 SMs x 128 lanes x 2 flop x max SM clock
-        peak = 148 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
-        achieved = alg["flops"] / (dom * 1e-3) / 1e12
-        roof = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(peak, 1),
-                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
-                "kernel": alg["kernel"], "kernel_ms": round(dom, 5),
-                "flops_per_launch": alg["flops"], "peak_source": "fp32 FMA units x max clock"}
-    step_info = {}
-    if "step_bytes" in alg:
-        step_info = {"step_gbs": round(alg["step_bytes"] / (ms * 1e-3) / 1e9, 1),
-                     "step_hbm_frac": round(alg["step_bytes"] / (ms * 1e-3) / 1e9 /
-                                            peaks["hbm_gbs"], 4)}
+    rooflines = {}
+    for name, work in segs.items():
+        rooflines[name] = _roofline(name, work, statistics.median(seg_ms[name]), peaks,
+                                    captured_traffic(w.name, name))
+    # the dominant kernel: the segment that takes the most time
+    dom = max(segs, key=lambda n: statistics.median(seg_ms[n]))
+    roof = rooflines[dom]
+    step_info = {"segments_ms": {n: round(statistics.median(v), 5) for n, v in seg_ms.items()}}
+    if step_bytes is not None:
+        step_info.update({"step_gbs": round(step_bytes / (ms * 1e-3) / 1e9, 1),
+                          "step_hbm_frac": round(step_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)})
     cfg = {"workload": w.name, "kind": w.kind, "batch": w.B, "context": max(w.lengths),
            "head_dim": w.D, "heads": w.H, "ratio": w.m, "topk": w.topk, "window": w.W,
-           "idx_heads": w.H_I, "idx_dim": w.d_I, "kv_format": w.kv_fmt, "seed": w.seed,
+           "idx_heads": w.H_I, "idx_dim": w.d_I, "kv_format": w.kv_fmt, "idx_format": w.idx_fmt, "seed": w.seed,
            "l2": "flushed before every timed step: 512 MiB write, then a 256 MiB read of another buffer",
-           "timing": "CUDA events around each step; the step captured as CUDA graphs split around the dominant kernel",
+           "timing": ("the step captured as one CUDA graph, replayed once a step; CUDA events before and "
+                      "after the replay and between its kernel segments (recorded inside the graph); "
+                      "ms_per_step is the median over the timed steps") if st.one_graph else
+                     ("each kernel segment captured as a CUDA graph, CUDA events between the replays; "
+                      "ms_per_step is the median over the timed steps"),
            "parallelism": "replicas" if world > 1 else "single GPU",
            "batch_invariant": bool(args.batch_invariant)}
     cfg.update(step_info)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "ms_per_step_mean": round(statistics.mean(step_ms), 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.act, "data": "synthetic (seeded; shapes of the pages' 1M-context workloads)",
-        "config": cfg, "roofline": roof, "e2e": e2e, "gpu_launches": per_step * args.steps,
-        "clocks": clk.summary(),
+        "config": cfg, "roofline": roof, "rooflines": rooflines, "e2e": e2e,
+        "gpu_launches": per_step * args.steps, "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, st.inp, budget_s=args.cpu_seconds)
@@ -484,12 +580,8 @@ def run_e2e(st: GpuStep, args):
     """Same metric through the public API with host buffers: per step, copy the
     new token's inputs from pinned host memory, run the step's calls, read the
     outputs back; wall time with a synchronize per step."""
-    w, inp = st.w, st.inp
-    names = ["q", "kv_new", "q_pos", "win_pos0"] if w.kind != "csa_prefill" else \
-        ["q", "kv_raw", "q_pos"]
-    if w.kind != "hca_decode":
-        names += ["q_idx", "w_idx"]
-    host = {n: inp[n].cpu().pin_memory() for n in names}
+    w, dev_in = st.w, st.step_inputs
+    host = {n: t.cpu().pin_memory() for n, t in dev_in.items()}
     out = st.layer.out
     lse = st.layer.lse
     h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
@@ -500,7 +592,7 @@ def run_e2e(st: GpuStep, args):
 
     def one_step():
         for nm, t in host.items():
-            inp[nm].copy_(t, non_blocking=True)
+            dev_in[nm].copy_(t, non_blocking=True)
         st.run_eager()
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
@@ -525,9 +617,10 @@ def run_e2e(st: GpuStep, args):
     t = statistics.mean(times)
     return {"value": round(w.Q / t, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(t * 1e3, 4),
-            "note": "per step one CUDA graph replay: copies of the new token's inputs from pinned "
-                    "host memory, the library calls, copies of the outputs to pinned host memory; "
-                    "cache, window and indexer keys stay resident in HBM (layer state)"}
+            "note": "per step one CUDA graph replay: copies of the step's inputs from pinned host memory "
+                    "(decode: each sequence's newest raw token, its position, q, indexer q and weights), "
+                    "the library calls, copies of the outputs to pinned host memory; cache, window ring, "
+                    "raw-token ring and indexer keys stay resident in HBM (layer state)"}
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -579,13 +672,17 @@ def oracle_step(w, s, raw_pos0=0):
             window[b, Lb - 1 - int(s["win_pos0"][b])] = oracle.store_rows(r, fmt)[0]
         seq = np.arange(n_q, dtype=np.int32)
         idx = None
-        if w.kind == "csa_decode" and w.idx_fmt == "fp8":
+        if w.kind == "csa_decode" and w.idx_fmt in ("fp8", "fp4"):
             idx = np.empty((n_q, w.topk), np.int32)
             for b in range(n_q):
                 n_av = (int(s["q_pos"][b]) + 1) // w.m
                 keys = (s["keys"][b, :n_av].astype(np.uint32) << 16).view(np.float32)  # bf16 bits
-                codes, scales = oracle.pack_idx_keys_fp8(keys)
-                sc = oracle.index_scores_fp8(s["q_idx"][b], s["w_idx"][b], codes, scales)
+                if w.idx_fmt == "fp8":
+                    codes, scales = oracle.pack_idx_keys_fp8(keys)
+                    sc = oracle.index_scores_fp8(s["q_idx"][b], s["w_idx"][b], codes, scales)
+                else:
+                    codes, scales = oracle.pack_idx_keys_fp4(keys)
+                    sc = oracle.index_scores_fp4(s["q_idx"][b], s["w_idx"][b], codes, scales)
                 idx[b], _ = oracle.topk(sc, w.topk)
         elif w.kind == "csa_decode":
             idx, _ = oracle.index_topk_batch(s["q_idx"], s["w_idx"], s["keys"], seq, s["q_pos"],

@@ -132,6 +132,36 @@ csa_status csa_append(const csa_params* p, const void* kv_new, int32_t B, int64_
                       int64_t out_seq_stride, void* win_out, int64_t win_seq_stride,
                       csa_stream_t stream);
 
+/* One decode step's cache maintenance for a ragged batch, in one launch
+ * [peacm §三.2 CSA "Step 1: KV 压缩" (every m tokens pooled into one entry),
+ * HCA (m' = 128); 四项关键 Trick "Sliding Window" (the most recent W raw
+ * tokens)].  This entry point has no counterpart on the pages: it keeps the
+ * decode state current one token at a time.  Sequence s's newest token is at
+ * position t = pos[s]; every sequence has its own length.  The call
+ *   - stores the token's raw row in slot t mod m of the sequence's raw ring
+ *     (the raw tokens of its current block: position p sits in slot p mod m);
+ *   - writes its window row RoPE(RMSNorm(kv_t), t) at row t mod n_win of the
+ *     sequence's window ring (read by csa_attend / hca_attend with
+ *     win_pos0 = NULL);
+ *   - when t + 1 is a multiple of m, pools the completed block (positions
+ *     t-m+1 .. t: ring slots 0 .. m-2 and the new token) into cache entry
+ *     (t + 1)/m - 1, with the arithmetic of csa_compress.
+ *   kv_tok:   [B, D] the newest raw token of each sequence, p->act_format
+ *   pos:      [B] int64 (device)
+ *   raw_ring: [B, m, D] in p->act_format: state kept by the caller between
+ *             calls (zero-initialise it); may be NULL when m = 1
+ *   cache:    [B, n_cap] rows in p->kv_format
+ *   window:   [B, n_win] rows in p->kv_format, a ring; ignored (may be NULL)
+ *             when p->window = 0 or n_win = 0
+ *   ws:       at least 256 bytes; its status word receives
+ *             CSA_DEV_BAD_POSITION for a negative position or an entry at or
+ *             beyond n_cap, and that sequence's write is skipped.
+ * Blocks that do not fit the compressor's shared-memory staging return
+ * CSA_ERR_UNSUPPORTED. */
+csa_status csa_decode_append(const csa_params* p, const void* kv_tok, int32_t B, const int64_t* pos,
+                             void* raw_ring, const float* w_z, const float* bias, void* cache, int64_t n_cap,
+                             void* window, int64_t n_win, void* ws, size_t ws_bytes, csa_stream_t stream);
+
 /* Lightning indexer + top-k [peacm §三.2 CSA "Step 2: Lightning Indexer Top-K
  * 选择"; gitcode §2.1.1].  For query q at position i = q_pos[q] in sequence
  * s = q / (Q/B), over the complete blocks b < floor((i+1)/m):
@@ -201,6 +231,42 @@ csa_status csa_index_topk_fp8(const csa_params* p, const void* q_idx, const floa
                               const float* key_scales, int64_t n_cap, int32_t B, int32_t Q,
                               const int64_t* q_pos, int32_t* topk_idx, float* topk_score, void* ws,
                               size_t ws_bytes, csa_stream_t stream);
+
+/* The lightning indexer with FP4 keys [gitcode §2.1.1: the indexer's QK path
+ * in FP4; §3.2: FP4 with 1x32 sub-block scales, converted to FP8 (E4M3)
+ * without loss for computation].  A key of 128 dims is stored as E2M1 codes
+ * (dim 2i in the low nibble of byte i, dim 2i+1 in the high one) and four
+ * block exponent bytes, block j (dims 32j .. 32j+31) scaled by
+ * 2^(byte - 127): e_j = floor(log2 amax_j) - 2 (the block's largest value in
+ * [4, 8); 0 for an all-zero block), a nonzero block more than 14 binades below
+ * the key's largest raised to that largest minus 14 (the key then converts to
+ * E4M3 codes with one power-of-two scale per key without loss), code = E2M1 of
+ * x / 2^e_j, nearest with ties to the even code, saturating at 6.  68 bytes a
+ * key (bf16 keys take 256, E4M3 keys 132).
+ * Storage: per sequence, ceil(n_cap / 128) tiles of csa_index_keys_fp4_bytes(128)
+ * = 8704 bytes, tile t holding keys 128t .. 128t+127: their 64-byte code rows,
+ * then their 4 exponent bytes each (key slots past n_cap are zero).
+ * csa_index_keys_pack_fp4 writes that form from keys [B, n_cap, 128] in
+ * p->act_format; pack: B * csa_index_keys_fp4_bytes(n_cap) bytes (device).
+ * csa_index_topk_fp4 / csa_index_score_fp4 are csa_index_topk_fp8 /
+ * csa_index_score_fp8 over such keys: the query heads are quantised to E4M3
+ * inside the call as for E4M3 keys, every key is expanded to E4M3 codes with
+ * one power-of-two scale in shared memory, and
+ *   score_b = sum_h w_idx[q,h] * relu((q8_h * sq_h) . k4_b)
+ * with the products accumulated in float32 on the tensor cores.  Requires
+ * n_idx_heads = 64, idx_dim = 128, n_cap >= 128 (or 0), and the workspace
+ * of CSA_OP_INDEX_TOPK_FP4 (the scoring half: as csa_index_score_fp8's). */
+int64_t csa_index_keys_fp4_bytes(int64_t n_cap);
+csa_status csa_index_keys_pack_fp4(const csa_params* p, const void* keys, int32_t B, int64_t n_cap,
+                                   int32_t idx_dim, uint8_t* pack, csa_stream_t stream);
+csa_status csa_index_score_fp4(const csa_params* p, const void* q_idx, const float* w_idx,
+                               int32_t n_idx_heads, int32_t idx_dim, const uint8_t* key_pack, int64_t n_cap,
+                               int32_t B, int32_t Q, const int64_t* q_pos, float* scores, int64_t ld_scores,
+                               void* ws, size_t ws_bytes, csa_stream_t stream);
+csa_status csa_index_topk_fp4(const csa_params* p, const void* q_idx, const float* w_idx,
+                              int32_t n_idx_heads, int32_t idx_dim, const uint8_t* key_pack, int64_t n_cap,
+                              int32_t B, int32_t Q, const int64_t* q_pos, int32_t* topk_idx, float* topk_score,
+                              void* ws, size_t ws_bytes, csa_stream_t stream);
 
 /* csa_index_topk for callers that cannot allocate device memory.  The pages
  * have no counterpart to this entry point; it exists for integration only.
@@ -289,7 +355,8 @@ typedef enum {
     CSA_OP_INDEX_TOPK = 1,
     CSA_OP_ATTEND = 2,
     CSA_OP_HCA_ATTEND = 3,
-    CSA_OP_INDEX_TOPK_FP8 = 4
+    CSA_OP_INDEX_TOPK_FP8 = 4,
+    CSA_OP_INDEX_TOPK_FP4 = 5
 } csa_op;
 
 /* Bytes of workspace an operation needs for these sizes (0 on invalid input).
@@ -311,6 +378,17 @@ uint32_t csa_last_device_bits(void);
 /* Number of kernels this library has launched in this process (all
  * threads), for launch accounting in benchmarks. */
 uint64_t csa_launch_count(void);
+
+/* Test hook for failure detection (the pages have no counterpart; off by
+ * default, process-wide).  While on, every launch of the tensor-core lightning
+ * indexer (csa_index_score / csa_index_topk with bf16 keys of 128 dims, 64
+ * heads, n_cap >= 128) has its TMA producer issue no copy at all, so the MMA
+ * warps' bounded waits for the query and key tiles expire after 2 s of wall
+ * time: the kernel sets CSA_DEV_TIMEOUT in the caller's status word, every
+ * role leaves its loop (nothing is in flight), TMEM is freed, and the
+ * context stays usable.  csa_check_status then reports CSA_ERR_DEVICE.  Scores
+ * written under the hook are meaningless.  Pass 0 to turn it off. */
+csa_status csa_test_withhold_indexer_loads(int32_t on);
 
 const char* csa_status_string(csa_status s);
 const char* csa_last_error(void);

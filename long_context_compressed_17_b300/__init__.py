@@ -15,9 +15,10 @@ import os
 import torch
 
 __all__ = [
-    "CsaError", "CsaParams", "F32", "BF16", "FP8_MIXED", "OP_INDEX_TOPK", "OP_INDEX_TOPK_FP8", "OP_ATTEND",
-    "OP_HCA_ATTEND", "params", "lib", "csa_row_bytes", "csa_cache_pack", "csa_compress", "csa_append", "csa_index_keys_pack", "csa_index_score_fp8", "csa_index_topk_fp8",
-    "csa_index_topk", "csa_index_score", "csa_topk_select", "csa_launch_count", "csa_index_topk_noalloc", "csa_attend", "hca_attend", "csa_workspace_bytes", "csa_workspace_init",
+    "CsaError", "CsaParams", "F32", "BF16", "FP8_MIXED", "OP_INDEX_TOPK", "OP_INDEX_TOPK_FP8", "OP_INDEX_TOPK_FP4", "OP_ATTEND",
+    "OP_HCA_ATTEND", "params", "lib", "csa_row_bytes", "csa_cache_pack", "csa_compress", "csa_append", "csa_decode_append", "csa_index_keys_pack", "csa_index_score_fp8", "csa_index_topk_fp8",
+    "csa_index_keys_fp4_bytes", "csa_index_keys_pack_fp4", "csa_index_score_fp4", "csa_index_topk_fp4",
+    "csa_index_topk", "csa_index_score", "csa_topk_select", "csa_launch_count", "csa_test_withhold_indexer_loads", "csa_index_topk_noalloc", "csa_attend", "hca_attend", "csa_workspace_bytes", "csa_workspace_init",
     "csa_check_status", "csa_last_device_bits", "csa_status_string", "csa_last_error",
     "workspace", "LIB_PATH",
 ]
@@ -25,7 +26,7 @@ __all__ = [
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcsa.so")
 
 F32, BF16, FP8_MIXED = 0, 1, 2
-OP_INDEX_TOPK, OP_ATTEND, OP_HCA_ATTEND, OP_INDEX_TOPK_FP8 = 1, 2, 3, 4
+OP_INDEX_TOPK, OP_ATTEND, OP_HCA_ATTEND, OP_INDEX_TOPK_FP8, OP_INDEX_TOPK_FP4 = 1, 2, 3, 4, 5
 _FMT = {"f32": F32, "bf16": BF16, "fp8m": FP8_MIXED}
 
 
@@ -78,11 +79,19 @@ def lib() -> ctypes.CDLL:
             "csa_cache_pack": (_i32, [P, _vp, _i64, _vp, _vp]),
             "csa_compress": (_i32, [P, _vp, _i32, _i64, _i64, _i64, _vp, _vp, _vp, _i64, _vp]),
             "csa_append": (_i32, [P, _vp, _i32, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _vp]),
+            "csa_decode_append": (_i32, [P, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _i64, _vp, _sz,
+                                         _vp]),
             "csa_index_keys_pack": (_i32, [P, _vp, _i64, _i32, _vp, _vp, _vp]),
             "csa_index_score_fp8": (_i32, [P, _vp, _vp, _i32, _i32, _vp, _vp, _i64, _i32, _i32, _vp,
                                            _vp, _i64, _vp, _sz, _vp]),
             "csa_index_topk_fp8": (_i32, [P, _vp, _vp, _i32, _i32, _vp, _vp, _i64, _i32, _i32, _vp,
                                           _vp, _vp, _vp, _sz, _vp]),
+            "csa_index_keys_fp4_bytes": (_i64, [_i64]),
+            "csa_index_keys_pack_fp4": (_i32, [P, _vp, _i32, _i64, _i32, _vp, _vp]),
+            "csa_index_score_fp4": (_i32, [P, _vp, _vp, _i32, _i32, _vp, _i64, _i32, _i32, _vp, _vp, _i64, _vp,
+                                           _sz, _vp]),
+            "csa_index_topk_fp4": (_i32, [P, _vp, _vp, _i32, _i32, _vp, _i64, _i32, _i32, _vp, _vp, _vp, _vp,
+                                          _sz, _vp]),
             "csa_index_topk": (_i32, [P, _vp, _vp, _i32, _i32, _vp, _i64, _i32, _i32, _vp, _vp,
                                       _vp, _vp, _sz, _vp]),
             "csa_attend": (_i32, [P, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _vp, _i64, _vp,
@@ -93,6 +102,7 @@ def lib() -> ctypes.CDLL:
                                        _i64, _vp, _sz, _vp]),
             "csa_topk_select": (_i32, [P, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp]),
             "csa_launch_count": (ctypes.c_uint64, []),
+            "csa_test_withhold_indexer_loads": (_i32, [_i32]),
             "csa_index_topk_noalloc": (_i32, [P, _vp, _vp, _i32, _i32, _vp, _i64, _i32, _i32, _vp,
                                               _vp, _vp, _vp, _vp]),
             "csa_workspace_bytes": (_sz, [P, _i32, _i32, _i32, _i32, _i32, _i64, _i64]),
@@ -157,6 +167,13 @@ def csa_append(p, kv_new, B, kv_seq_stride, pos0, w_z, bias, entry_out, out_seq_
                             win_seq_stride, _stream(stream)), "csa_append")
 
 
+def csa_decode_append(p, kv_tok, B, pos, raw_ring, w_z, bias, cache, n_cap, window, n_win, ws, ws_bytes,
+                      stream=None):
+    _check(lib().csa_decode_append(ctypes.byref(p), _ptr(kv_tok), B, _ptr(pos), _ptr(raw_ring), _ptr(w_z),
+                                   _ptr(bias), _ptr(cache), n_cap, _ptr(window), n_win, _ptr(ws), ws_bytes,
+                                   _stream(stream)), "csa_decode_append")
+
+
 def csa_compress(p, kv_raw, B, T, kv_seq_stride, pos0, w_z, bias, out, out_seq_stride,
                  stream=None):
     _check(lib().csa_compress(ctypes.byref(p), _ptr(kv_raw), B, T, kv_seq_stride, pos0,
@@ -193,6 +210,29 @@ def csa_index_topk_fp8(p, q_idx, w_idx, n_idx_heads, idx_dim, key_codes, key_sca
                                     _stream(stream)), "csa_index_topk_fp8")
 
 
+def csa_index_keys_fp4_bytes(n_cap: int) -> int:
+    return int(lib().csa_index_keys_fp4_bytes(n_cap))
+
+
+def csa_index_keys_pack_fp4(p, keys, B, n_cap, idx_dim, pack, stream=None):
+    _check(lib().csa_index_keys_pack_fp4(ctypes.byref(p), _ptr(keys), B, n_cap, idx_dim, _ptr(pack),
+                                         _stream(stream)), "csa_index_keys_pack_fp4")
+
+
+def csa_index_score_fp4(p, q_idx, w_idx, n_idx_heads, idx_dim, key_pack, n_cap, B, Q, q_pos, scores, ld_scores,
+                        ws, ws_bytes, stream=None):
+    _check(lib().csa_index_score_fp4(ctypes.byref(p), _ptr(q_idx), _ptr(w_idx), n_idx_heads, idx_dim,
+                                     _ptr(key_pack), n_cap, B, Q, _ptr(q_pos), _ptr(scores), ld_scores, _ptr(ws),
+                                     ws_bytes, _stream(stream)), "csa_index_score_fp4")
+
+
+def csa_index_topk_fp4(p, q_idx, w_idx, n_idx_heads, idx_dim, key_pack, n_cap, B, Q, q_pos, topk_idx, topk_score,
+                       ws, ws_bytes, stream=None):
+    _check(lib().csa_index_topk_fp4(ctypes.byref(p), _ptr(q_idx), _ptr(w_idx), n_idx_heads, idx_dim,
+                                    _ptr(key_pack), n_cap, B, Q, _ptr(q_pos), _ptr(topk_idx), _ptr(topk_score),
+                                    _ptr(ws), ws_bytes, _stream(stream)), "csa_index_topk_fp4")
+
+
 def csa_index_score(p, q_idx, w_idx, n_idx_heads, idx_dim, keys, n_cap, B, Q, q_pos, scores,
                     ld_scores, ws, ws_bytes, stream=None):
     _check(lib().csa_index_score(ctypes.byref(p), _ptr(q_idx), _ptr(w_idx), n_idx_heads, idx_dim,
@@ -221,6 +261,10 @@ def csa_index_topk_noalloc(p, q_idx, w_idx, n_idx_heads, idx_dim, keys, n_cap, B
 
 def csa_launch_count() -> int:
     return int(lib().csa_launch_count())
+
+
+def csa_test_withhold_indexer_loads(on: bool):
+    _check(lib().csa_test_withhold_indexer_loads(int(bool(on))), "csa_test_withhold_indexer_loads")
 
 
 def csa_attend(p, q, H, B, Q, q_pos, cache, n_cap, topk_idx, window, n_win, win_pos0, sink, out,

@@ -116,12 +116,13 @@ IndexTopkPlan plan_index_topk(const Geometry& g, int B, int Q, int HI, int64_t n
 }
 
 bool attend_tc_supported(const Geometry& g, bool sparse, int H, int64_t n_cap, int64_t n_win);
-void plan_attend_tc(const Geometry& g, bool sparse, int Q, int64_t n_cap, AttendPlan* pl);
+void plan_attend_tc(const Geometry& g, bool sparse, int Q, int64_t n_cap, int64_t n_win, bool ring, AttendPlan* pl);
 
 AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int64_t n_cap,
-                       int64_t n_win) {
+                       int64_t n_win, bool ring) {
     (void)B;
     AttendPlan pl;
+    pl.ring = ring ? 1 : 0;
     pl.list_len = (sparse ? (int64_t)g.k : n_cap) + g.W;
     pl.use_tc = attend_tc_supported(g, sparse, H, n_cap, n_win) ? 1 : 0;
     pl.tc_T_sel = pl.tc_T = pl.tc_grid = pl.tc_deq = pl.tc_seg = pl.tc_nseg = 0;
@@ -129,7 +130,7 @@ AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int6
     if (pl.use_tc) {
         pl.head_group = H;
         pl.rows_per_split = 0;
-        plan_attend_tc(g, sparse, Q, n_cap, &pl);
+        plan_attend_tc(g, sparse, Q, n_cap, n_win, ring, &pl);
     } else {
         pl.head_group = (H % 16 == 0) ? 16 : 8;
         const int hgs = H / pl.head_group;
@@ -288,14 +289,49 @@ csa_status csa_append(const csa_params* p, const void* kv_new, int32_t B, int64_
     return e == cudaSuccess ? CSA_OK : cuda_fail(e, "csa_append");
 }
 
+csa_status csa_decode_append(const csa_params* p, const void* kv_tok, int32_t B, const int64_t* pos,
+                             void* raw_ring, const float* w_z, const float* bias, void* cache, int64_t n_cap,
+                             void* window, int64_t n_win, void* ws, size_t ws_bytes, csa_stream_t stream) {
+    CHECK(check_params(p));
+    if (B < 0 || B > 65535) return fail(CSA_ERR_INVALID_ARG, "B %d out of range", B);
+    if (n_cap < 0 || n_cap > (1LL << 30) || n_win < 0 || n_win > (1LL << 30))
+        return fail(CSA_ERR_INVALID_ARG, "n_cap / n_win out of range");
+    if (B == 0) return CSA_OK;
+    Geometry g = resolve(p);
+    if (!decode_append_supported(g))
+        return fail(CSA_ERR_UNSUPPORTED, "csa_decode_append: a block of %d tokens of %d dims does not fit the compressor",
+                    p->ratio, p->head_dim);
+    CHECK(check_ptr(kv_tok, "kv_tok"));
+    CHECK(check_ptr(pos, "pos"));
+    CHECK(check_ptr(raw_ring, "raw_ring", p->ratio == 1));
+    CHECK(check_ptr(w_z, "w_z"));
+    if (!bias) return fail(CSA_ERR_INVALID_ARG, "bias is NULL");
+    CHECK(check_ptr(cache, "cache", n_cap == 0));
+    const bool win = p->window > 0 && n_win > 0;
+    CHECK(check_ptr(window, "window", !win));
+    CHECK(check_ptr(ws, "ws"));
+    if (ws_bytes < kStatusWordBytes) return fail(CSA_ERR_WORKSPACE, "workspace smaller than 256 bytes");
+    cudaError_t e = launch_decode_append(g, kv_tok, B, pos, raw_ring, w_z, bias, cache, n_cap,
+                                         win ? window : nullptr, n_win, reinterpret_cast<uint32_t*>(ws),
+                                         (cudaStream_t)stream);
+    return e == cudaSuccess ? CSA_OK : cuda_fail(e, "csa_decode_append");
+}
+
 size_t csa_workspace_bytes(const csa_params* p, int32_t op, int32_t B, int32_t Q, int32_t H,
                            int32_t n_idx_heads, int64_t n_cap, int64_t n_win) {
     if (check_params(p) != CSA_OK || B <= 0 || Q < 0 || n_cap < 0 || n_win < 0) return 0;
     Geometry g = resolve(p);
     if (op == CSA_OP_INDEX_TOPK) return plan_index_topk(g, B, Q, n_idx_heads, n_cap).total;
-    if (op == CSA_OP_INDEX_TOPK_FP8) return plan_index_topk(g, B, Q, n_idx_heads, n_cap, true).total;
-    if (op == CSA_OP_ATTEND) return H > 0 ? plan_attend(g, true, B, Q, H, n_cap, n_win).total : 0;
-    if (op == CSA_OP_HCA_ATTEND) return H > 0 ? plan_attend(g, false, B, Q, H, n_cap, n_win).total : 0;
+    if (op == CSA_OP_INDEX_TOPK_FP8 || op == CSA_OP_INDEX_TOPK_FP4)
+        return plan_index_topk(g, B, Q, n_idx_heads, n_cap, true).total;
+    // one size serves both window layouts (linear or ring)
+    if (op == CSA_OP_ATTEND || op == CSA_OP_HCA_ATTEND) {
+        if (H <= 0) return 0;
+        const bool sparse = op == CSA_OP_ATTEND;
+        const size_t a = plan_attend(g, sparse, B, Q, H, n_cap, n_win, false).total;
+        const size_t b = plan_attend(g, sparse, B, Q, H, n_cap, n_win, true).total;
+        return a > b ? a : b;
+    }
     return 0;
 }
 
@@ -408,6 +444,11 @@ csa_status csa_topk_select(const csa_params* p, float* scores, int64_t ld_scores
 
 uint64_t csa_launch_count(void) { return (uint64_t)g_launches.load(); }
 
+csa_status csa_test_withhold_indexer_loads(int32_t on) {
+    set_indexer_withhold(on);
+    return CSA_OK;
+}
+
 static csa_status attend_common(const csa_params* p, bool sparse, const void* q, int32_t H,
                                 int32_t B, int32_t Q, const int64_t* q_pos, const void* cache,
                                 int64_t n_cap, const int32_t* topk_idx, const void* window,
@@ -428,13 +469,17 @@ static csa_status attend_common(const csa_params* p, bool sparse, const void* q,
     CHECK(check_ptr(cache, "cache", n_cap == 0));
     if (sparse) CHECK(check_ptr(topk_idx, "topk_idx"));
     CHECK(check_ptr(window, "window", n_win == 0 || p->window == 0));
-    CHECK(check_ptr(win_pos0, "win_pos0", p->window == 0));
+    CHECK(check_ptr(win_pos0, "win_pos0", true));  // NULL: the window is a ring
+    const bool ring = win_pos0 == nullptr;
+    if (ring && p->window > 0 && n_win < p->window)
+        return fail(CSA_ERR_INVALID_ARG, "%s: a ring window needs n_win (%lld) >= W (%d)", name, (long long)n_win,
+                    p->window);
     CHECK(check_ptr(sink, "sink"));
     CHECK(check_ptr(out, "out"));
     CHECK(check_ptr(lse, "lse", true));
     CHECK(check_ptr(ws, "ws"));
     Geometry g = resolve(p);
-    AttendPlan pl = plan_attend(g, sparse, B, Q, H, n_cap, n_win);
+    AttendPlan pl = plan_attend(g, sparse, B, Q, H, n_cap, n_win, ring);
     if (ws_bytes < pl.total) return fail(CSA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", name, ws_bytes, pl.total);
     uint8_t* w = reinterpret_cast<uint8_t*>(ws);
     cudaError_t e = launch_attend(g, pl, sparse, q, H, B, Q, q_pos, cache, n_cap, topk_idx, window,
@@ -527,6 +572,91 @@ csa_status csa_index_topk_fp8(const csa_params* p, const void* q_idx, const floa
     if (e != cudaSuccess) return cuda_fail(e, "csa_index_topk_fp8: indexer");
     e = launch_topk(g, scores, pl.n_cap_pad, n_cap, Q, q_pos, topk_idx, topk_score, st);
     return e == cudaSuccess ? CSA_OK : cuda_fail(e, "csa_index_topk_fp8: top-k");
+}
+
+int64_t csa_index_keys_fp4_bytes(int64_t n_cap) {
+    if (n_cap < 0) return -1;
+    return (n_cap + 127) / 128 * kFp4KeyTileBytes;
+}
+
+csa_status csa_index_keys_pack_fp4(const csa_params* p, const void* keys, int32_t B, int64_t n_cap,
+                                   int32_t idx_dim, uint8_t* pack, csa_stream_t stream) {
+    CHECK(check_params(p));
+    if (idx_dim != 128) return fail(CSA_ERR_UNSUPPORTED, "idx_dim %d: FP4 keys take 128", idx_dim);
+    if (B < 0 || n_cap < 0 || n_cap > (1LL << 30)) return fail(CSA_ERR_INVALID_ARG, "B / n_cap out of range");
+    if (B == 0 || n_cap == 0) return CSA_OK;
+    CHECK(check_ptr(keys, "keys"));
+    CHECK(check_ptr(pack, "pack"));
+    Geometry g = resolve(p);
+    cudaError_t e = launch_pack_idx_keys_fp4(g, keys, B, n_cap, pack, (cudaStream_t)stream);
+    return e == cudaSuccess ? CSA_OK : cuda_fail(e, "csa_index_keys_pack_fp4");
+}
+
+// The checks shared by the FP4 scoring calls.
+static csa_status check_fp4_index(const csa_params* p, int32_t n_idx_heads, int32_t idx_dim, const uint8_t* key_pack,
+                                  int64_t n_cap, int32_t B, int32_t Q, const void* q_idx, const float* w_idx,
+                                  const int64_t* q_pos) {
+    CHECK(check_params(p));
+    if (idx_dim != 128 || n_idx_heads != 64)
+        return fail(CSA_ERR_UNSUPPORTED, "FP4 keys take 64 heads of 128 dims (got %d x %d)", n_idx_heads, idx_dim);
+    if (B < 1 || Q < 0 || Q % B != 0) return fail(CSA_ERR_INVALID_ARG, "Q %d must be a multiple of B %d", Q, B);
+    if (n_cap < 0 || n_cap > (1LL << 30)) return fail(CSA_ERR_INVALID_ARG, "n_cap out of range");
+    if (Q == 0) return CSA_OK;
+    if (n_cap > 0 && n_cap < 128) return fail(CSA_ERR_UNSUPPORTED, "FP4 keys need n_cap >= 128");
+    CHECK(check_ptr(q_idx, "q_idx"));
+    CHECK(check_ptr(w_idx, "w_idx"));
+    CHECK(check_ptr(key_pack, "key_pack", n_cap == 0));
+    CHECK(check_ptr(q_pos, "q_pos"));
+    return CSA_OK;
+}
+
+csa_status csa_index_score_fp4(const csa_params* p, const void* q_idx, const float* w_idx,
+                               int32_t n_idx_heads, int32_t idx_dim, const uint8_t* key_pack, int64_t n_cap,
+                               int32_t B, int32_t Q, const int64_t* q_pos, float* scores, int64_t ld_scores,
+                               void* ws, size_t ws_bytes, csa_stream_t stream) {
+    CHECK(check_fp4_index(p, n_idx_heads, idx_dim, key_pack, n_cap, B, Q, q_idx, w_idx, q_pos));
+    if (ld_scores < n_cap || ld_scores % 4 != 0)
+        return fail(CSA_ERR_INVALID_ARG, "ld_scores %lld must be >= n_cap and a multiple of 4", (long long)ld_scores);
+    if (Q == 0) return CSA_OK;
+    CHECK(check_ptr(scores, "scores"));
+    CHECK(check_ptr(ws, "ws"));
+    const size_t q8_off = kStatusWordBytes;
+    const size_t weff_off = q8_off + align256((size_t)Q * 64 * 128);
+    const size_t need = weff_off + align256((size_t)Q * 64 * sizeof(float));
+    if (ws_bytes < need) return fail(CSA_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+    Geometry g = resolve(p);
+    uint8_t* w = reinterpret_cast<uint8_t*>(ws);
+    cudaError_t e = launch_indexer_fp4(g, q_idx, w_idx, key_pack, n_cap, B, Q, q_pos, reinterpret_cast<uint32_t*>(w),
+                                       scores, ld_scores, w + q8_off, reinterpret_cast<float*>(w + weff_off),
+                                       (cudaStream_t)stream);
+    return e == cudaSuccess ? CSA_OK : cuda_fail(e, "csa_index_score_fp4");
+}
+
+csa_status csa_index_topk_fp4(const csa_params* p, const void* q_idx, const float* w_idx,
+                              int32_t n_idx_heads, int32_t idx_dim, const uint8_t* key_pack, int64_t n_cap,
+                              int32_t B, int32_t Q, const int64_t* q_pos, int32_t* topk_idx, float* topk_score,
+                              void* ws, size_t ws_bytes, csa_stream_t stream) {
+    CHECK(check_fp4_index(p, n_idx_heads, idx_dim, key_pack, n_cap, B, Q, q_idx, w_idx, q_pos));
+    if (p->topk < 1 || p->topk > 4096) return fail(CSA_ERR_INVALID_ARG, "topk %d not in [1, 4096]", p->topk);
+    if (Q == 0) return CSA_OK;
+    CHECK(check_ptr(topk_idx, "topk_idx"));
+    CHECK(check_ptr(topk_score, "topk_score", true));
+    CHECK(check_ptr(ws, "ws"));
+    if (topk_chunk(n_cap, Q, p->topk) == 0)
+        return fail(CSA_ERR_UNSUPPORTED, "top-%d of %lld blocks does not fit the selection's shared memory",
+                    p->topk, (long long)n_cap);
+    Geometry g = resolve(p);
+    IndexTopkPlan pl = plan_index_topk(g, B, Q, n_idx_heads, n_cap, true);
+    if (ws_bytes < pl.total) return fail(CSA_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, pl.total);
+    uint8_t* w = reinterpret_cast<uint8_t*>(ws);
+    float* scores = reinterpret_cast<float*>(w + pl.scores_off);
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = launch_indexer_fp4(g, q_idx, w_idx, key_pack, n_cap, B, Q, q_pos, reinterpret_cast<uint32_t*>(w),
+                                       scores, pl.n_cap_pad, w + pl.q8_off, reinterpret_cast<float*>(w + pl.weff_off),
+                                       st);
+    if (e != cudaSuccess) return cuda_fail(e, "csa_index_topk_fp4: indexer");
+    e = launch_topk(g, scores, pl.n_cap_pad, n_cap, Q, q_pos, topk_idx, topk_score, st);
+    return e == cudaSuccess ? CSA_OK : cuda_fail(e, "csa_index_topk_fp4: top-k");
 }
 
 csa_status csa_attend(const csa_params* p, const void* q, int32_t H, int32_t B, int32_t Q,

@@ -59,6 +59,10 @@ struct AttendPlan {
     // tensor-core kernel: tiles of 64 rows per query (selected / cache part
     // and all), Q * tc_T tiles dealt to tc_grid persistent CTAs
     int tc_T_sel, tc_T, tc_grid;
+    // window tiles: ceil(W / 64) tiles of positions (linear window), or
+    // ceil(n_win / 64) tiles of ring rows (ring window: position p at row
+    // p mod n_win, every row whose position is in the window valid)
+    int ring;
     int64_t tc_total;
     // batch-invariant splits: tc_seg tiles each (0: balanced ranges), tc_nseg
     // per query
@@ -73,7 +77,7 @@ struct AttendPlan {
     size_t total;
 };
 AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int64_t n_cap,
-                       int64_t n_win);
+                       int64_t n_win, bool ring);
 
 cudaError_t launch_cache_pack(const Geometry& g, const float* src, int64_t n, void* dst,
                               cudaStream_t st);
@@ -83,6 +87,12 @@ cudaError_t launch_compress(const Geometry& g, const void* kv, int B, int64_t T,
                             int64_t kv_stride, int64_t pos0, const float* w_z, const float* bias,
                             void* out, int64_t out_stride, void* win_out, int64_t win_stride,
                             cudaStream_t st);
+// Ragged decode append (csa_decode_append): raw ring slot, window ring row
+// and, for sequences whose newest token completes a block, the block's entry.
+bool decode_append_supported(const Geometry& g);
+cudaError_t launch_decode_append(const Geometry& g, const void* tok, int B, const int64_t* pos, void* ring,
+                                 const float* w_z, const float* bias, void* cache, int64_t n_cap, void* window,
+                                 int64_t n_win, uint32_t* status, cudaStream_t st);
 cudaError_t launch_indexer(const Geometry& g, const void* q_idx, const float* w_idx, int HI,
                            int dI, const void* keys, int64_t n_cap, int B, int Q,
                            const int64_t* q_pos, uint32_t* status, float* scores, int64_t ld,
@@ -91,12 +101,22 @@ cudaError_t launch_indexer_fp8(const Geometry& g, const void* q_idx, const float
                                const float* key_scales, int64_t n_cap, int B, int Q, const int64_t* q_pos,
                                uint32_t* status, float* scores, int64_t ld, uint8_t* q8, float* w_eff,
                                cudaStream_t st);
+// FP4 indexer keys: packed tiles of 8704 bytes (128 keys' E2M1 codes, then
+// their block-exponent bytes), ceil(n_cap / 128) tiles a sequence.
+constexpr int64_t kFp4KeyTileBytes = 8704;
+cudaError_t launch_pack_idx_keys_fp4(const Geometry& g, const void* keys, int B, int64_t n_cap, uint8_t* pack,
+                                     cudaStream_t st);
+cudaError_t launch_indexer_fp4(const Geometry& g, const void* q_idx, const float* w_idx, const uint8_t* key_pack,
+                               int64_t n_cap, int B, int Q, const int64_t* q_pos, uint32_t* status, float* scores,
+                               int64_t ld, uint8_t* q8, float* w_eff, cudaStream_t st);
 cudaError_t launch_pack_idx_keys(const Geometry& g, const void* rows, int64_t n, uint8_t* codes, float* scales,
                                  cudaStream_t st);
 cudaError_t launch_topk(const Geometry& g, float* scores, int64_t ld, int64_t n_cap, int Q,
                         const int64_t* q_pos, int32_t* idx, float* sel, cudaStream_t st);
 // Chunk size of the top-k selection for these sizes; 0: does not fit.
 int64_t topk_chunk(int64_t n_cap, int Q, int k);
+// Test hook of csa_test_withhold_indexer_loads.
+void set_indexer_withhold(int on);
 cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, const void* q,
                           int H, int B, int Q, const int64_t* q_pos, const void* cache,
                           int64_t n_cap, const int32_t* topk_idx, const void* window,

@@ -35,7 +35,7 @@ struct AttendArgs {
     int k;
     const uint8_t* window;
     int64_t n_win;
-    const int64_t* win_pos0;
+    const int64_t* win_pos0;  // nullptr: the window is a ring (position p at row p mod n_win)
     int W, m, R;
     RopeTheta theta;
     float eps, scale;
@@ -68,6 +68,8 @@ __device__ __forceinline__ const uint8_t* resolve_row(const AttendArgs& a, int64
     }
     int64_t wpos = i - a.W + 1 + (p - a.list_base);
     if (wpos < 0) return nullptr;
+    if (a.win_pos0 == nullptr)  // ring window: position p at row p mod n_win (n_win >= W)
+        return a.window + ((int64_t)seq * a.n_win + wpos % a.n_win) * a.rb;
     int64_t wr = wpos - a.win_pos0[seq];
     if (wr < 0 || wr >= a.n_win) {
         atomicOr(a.status, CSA_DEV_BAD_WINDOW);

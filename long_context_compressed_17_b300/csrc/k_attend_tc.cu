@@ -89,7 +89,7 @@ struct AttTcArgs {
     int pre;                  // tm_sel maps [Q, T * 64, 512]: each query's rows in tile order
     const uint8_t* cache;     // [B, n_cap, 512] bf16 rows the gather warps copy
     int64_t n_cap, n_win;
-    const int64_t* win_pos0;  // [B]
+    const int64_t* win_pos0;  // [B]; nullptr: ring window (position p at row p mod n_win)
     int W, m, qps;
     float eps, scale_log2;
     int T_sel, T;             // tiles per query: selected / cache part, all
@@ -154,9 +154,16 @@ __device__ __forceinline__ bool tile_live(const AttTcArgs& a, const QueryInfo& q
         return (int64_t)lt * kRows < qi.n_av;
     }
     const int r0 = (lt - a.T_sel) * kRows;
+    if (a.win_pos0 == nullptr) return r0 < a.n_win && r0 <= qi.i;  // ring rows r0 ..: some hold positions <= i
     if (r0 >= a.W) return false;
     const int rlast = min(a.W, r0 + kRows) - 1;
     return qi.i - a.W + 1 + rlast >= 0;
+}
+
+// Ring window: the position row r holds for a query at position i, the
+// latest p <= i with p = r mod n_win (negative: not written yet).
+__device__ __forceinline__ int64_t ring_pos(int64_t i, int64_t r, int64_t n_win) {
+    return i - (((i - r) % n_win) + n_win) % n_win;
 }
 
 // Boxes of a gathered tile fetched by the producer warp; the gather warps
@@ -344,7 +351,7 @@ struct DeqGatherArgs {
     const uint8_t* window;    // [B, n_win, rb]
     int64_t rb, n_cap, n_win;
     const int64_t* q_pos;     // [Q]
-    const int64_t* win_pos0;  // [B]
+    const int64_t* win_pos0;  // [B]; nullptr: ring window
     const int32_t* topk_idx;  // [Q, k]; nullptr: every cache row in order
     int k, W, m, qps, T_sel, T;
     int64_t rows;             // Q * T * 64
@@ -370,9 +377,14 @@ __global__ void __launch_bounds__(kDeqThreads) dequant_gather_kernel(const DeqGa
         if (e >= 0 && e < n_av) src = a.cache + ((int64_t)seq * a.n_cap + e) * a.rb;
     } else {
         const int rw = p - a.T_sel * kRows;
-        const int64_t wr = i - a.W + 1 + rw - a.win_pos0[seq];
-        if (rw < a.W && i - a.W + 1 + rw >= 0 && wr >= 0 && wr < a.n_win)
-            src = a.window + ((int64_t)seq * a.n_win + wr) * a.rb;
+        if (a.win_pos0 == nullptr) {  // ring rows in buffer order
+            const int64_t wpos = rw < a.n_win ? ring_pos(i, rw, a.n_win) : -1;
+            if (wpos >= 0 && wpos >= i - a.W + 1) src = a.window + ((int64_t)seq * a.n_win + rw) * a.rb;
+        } else {
+            const int64_t wr = i - a.W + 1 + rw - a.win_pos0[seq];
+            if (rw < a.W && i - a.W + 1 + rw >= 0 && wr >= 0 && wr < a.n_win)
+                src = a.window + ((int64_t)seq * a.n_win + wr) * a.rb;
+        }
     }
     warp_dequant_row(src, a.out + r * kD, threadIdx.x & 31);
 }
@@ -447,8 +459,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t tcount = 0;
         uint32_t fills[kStages] = {0, 0};  // fills of each stage (by any warp)
         auto box_row0 = [&](const QueryInfo& inf, int lt) {
-            return lt < a.T_sel ? lt * kRows
-                                : (int)(inf.i - a.W + 1 + (int64_t)(lt - a.T_sel) * kRows - a.win_pos0[inf.seq]);
+            if (lt < a.T_sel) return lt * kRows;
+            if (a.win_pos0 == nullptr) return (lt - a.T_sel) * kRows;  // ring rows in buffer order
+            return (int)(inf.i - a.W + 1 + (int64_t)(lt - a.T_sel) * kRows - a.win_pos0[inf.seq]);
         };
         // The next live TMA-tile (not gathered) after global tile g within this
         // CTA's range is prefetched into L2 while the current one is loaded.
@@ -752,11 +765,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     } else {
                         const int r = (lt - a.T_sel) * kRows + row;
-                        const int64_t wpos = inf.i - a.W + 1 + r;
-                        if (r < a.W && wpos >= 0) {
-                            const int64_t wr = wpos - a.win_pos0[inf.seq];
-                            if (wr >= 0 && wr < a.n_win) valid = true;
-                            else if (report) atomicOr(a.status, CSA_DEV_BAD_WINDOW);
+                        if (a.win_pos0 == nullptr) {  // ring row r: valid when its position is in the window
+                            const int64_t wpos = r < a.n_win ? ring_pos(inf.i, r, a.n_win) : -1;
+                            valid = wpos >= 0 && wpos >= inf.i - a.W + 1;
+                        } else {
+                            const int64_t wpos = inf.i - a.W + 1 + r;
+                            if (r < a.W && wpos >= 0) {
+                                const int64_t wr = wpos - a.win_pos0[inf.seq];
+                                if (wr >= 0 && wr < a.n_win) valid = true;
+                                else if (report) atomicOr(a.status, CSA_DEV_BAD_WINDOW);
+                            }
                         }
                     }
                 }
@@ -999,9 +1017,10 @@ bool attend_tc_supported(const Geometry& g, bool sparse, int H, int64_t n_cap, i
     return true;
 }
 
-void plan_attend_tc(const Geometry& g, bool sparse, int Q, int64_t n_cap, AttendPlan* pl) {
+void plan_attend_tc(const Geometry& g, bool sparse, int Q, int64_t n_cap, int64_t n_win, bool ring, AttendPlan* pl) {
     pl->tc_T_sel = sparse ? (g.k + kRows - 1) / kRows : (int)((n_cap + kRows - 1) / kRows);
-    pl->tc_T = pl->tc_T_sel + (g.W + kRows - 1) / kRows;
+    const int64_t win_rows = g.W > 0 ? (ring ? n_win : (int64_t)g.W) : 0;
+    pl->tc_T = pl->tc_T_sel + (int)((win_rows + kRows - 1) / kRows);
     pl->tc_total = (int64_t)Q * pl->tc_T;
     const int64_t sms = num_sms();
     if (g.inv) {  // fixed splits of tc_seg tiles, whole splits per CTA

@@ -65,40 +65,23 @@ __device__ void window_row(const uint8_t* tok, int act, float* row, float* red, 
     norm_rope_store(row, ss, red, D, eps, pos, theta, kvfmt, dst);
 }
 
-// grid (n_blocks_out, B).  Dynamic smem: (m + D + 32) floats, rounded up to
-// 16 bytes, then (when `staged`) the block's m raw rows.
-__global__ void __launch_bounds__(kCompressThreads)
-    compress_kernel(const uint8_t* __restrict__ kv, int act, int64_t act_row_bytes,
-                    int64_t kv_seq_bytes, int D, int m, int64_t pos0,
-                    const float* __restrict__ w_z, const float* __restrict__ bias,
-                    uint8_t* __restrict__ out, int kvfmt, int64_t kv_row_bytes,
-                    int64_t out_seq_bytes, float eps, RopeTheta theta, int staged,
-                    uint8_t* __restrict__ win_out, int64_t win_seq_bytes) {
-    extern __shared__ __align__(16) float sm[];
-    float* z = sm;            // [m] scores, then pooling weights
-    float* row = sm + m;      // [D]
-    float* red = row + D;     // [32]
-    uint8_t* stage = reinterpret_cast<uint8_t*>(sm + ((m + D + 32 + 3) & ~3));
+// The block of m raw rows at src (shared memory or global) pooled into one
+// entry and stored at dst: pooling scores z_t = kv_t . w_z + bias[t], softmax
+// over the block, the weighted sum, RMSNorm and RoPE at `pos` (whole CTA; z:
+// m floats, row: D floats, red: 32 floats of shared scratch).  m = 1 is a
+// window row: its single weight is exactly 1.
+__device__ __forceinline__ void pool_block_store(const uint8_t* src, int act, int64_t act_row_bytes, int D, int m,
+                                                 const float* __restrict__ w_z, const float* __restrict__ bias,
+                                                 float* z, float* row, float* red, float eps, double pos,
+                                                 const RopeTheta& theta, int kvfmt, uint8_t* dst) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int nwarps = kCompressThreads / 32;
-    const int64_t b = blockIdx.x;
-    const uint8_t* blk = kv + blockIdx.y * kv_seq_bytes + b * m * act_row_bytes;
-    const uint8_t* src = blk;
-    if (staged) {  // one coalesced pass over HBM; both sweeps below read smem
-        const int64_t n16 = (int64_t)m * act_row_bytes / 16;
-        const uint4* g = reinterpret_cast<const uint4*>(blk);
-        uint4* s = reinterpret_cast<uint4*>(stage);
-        for (int64_t i = tid; i < n16; i += kCompressThreads) s[i] = __ldg(g + i);
-        __syncthreads();
-        src = stage;
-    }
-
     if (m == 1) {
         // a single token: its pooling weight is exactly 1 (window rows)
         if (tid == 0) z[0] = 1.f;
         __syncthreads();
     } else {
-        // pooling scores z_t = kv_t . w_z + bias[t mod m]   (pos0 is a multiple of m)
+        // pooling scores z_t = kv_t . w_z + bias[t mod m]   (blocks start at multiples of m)
         for (int t = warp; t < m; t += nwarps) {
             const uint8_t* r = src + t * act_row_bytes;
             float acc = 0.f;
@@ -120,7 +103,6 @@ __global__ void __launch_bounds__(kCompressThreads)
         }
         __syncthreads();
     }
-
     // pooled vector and its sum of squares
     float ss = 0.f;
     for (int d = tid; d < D; d += kCompressThreads) {
@@ -130,8 +112,38 @@ __global__ void __launch_bounds__(kCompressThreads)
         ss = fmaf(c, c, ss);
     }
     // RMSNorm, partial RoPE at the block's last position, store
+    norm_rope_store(row, ss, red, D, eps, pos, theta, kvfmt, dst);
+}
+
+// grid (n_blocks_out, B).  Dynamic smem: (m + D + 32) floats, rounded up to
+// 16 bytes, then (when `staged`) the block's m raw rows.
+__global__ void __launch_bounds__(kCompressThreads)
+    compress_kernel(const uint8_t* __restrict__ kv, int act, int64_t act_row_bytes,
+                    int64_t kv_seq_bytes, int D, int m, int64_t pos0,
+                    const float* __restrict__ w_z, const float* __restrict__ bias,
+                    uint8_t* __restrict__ out, int kvfmt, int64_t kv_row_bytes,
+                    int64_t out_seq_bytes, float eps, RopeTheta theta, int staged,
+                    uint8_t* __restrict__ win_out, int64_t win_seq_bytes) {
+    extern __shared__ __align__(16) float sm[];
+    float* z = sm;            // [m] scores, then pooling weights
+    float* row = sm + m;      // [D]
+    float* red = row + D;     // [32]
+    uint8_t* stage = reinterpret_cast<uint8_t*>(sm + ((m + D + 32 + 3) & ~3));
+    const int tid = threadIdx.x;
+    const int64_t b = blockIdx.x;
+    const uint8_t* blk = kv + blockIdx.y * kv_seq_bytes + b * m * act_row_bytes;
+    const uint8_t* src = blk;
+    if (staged) {  // one coalesced pass over HBM; both sweeps below read smem
+        const int64_t n16 = (int64_t)m * act_row_bytes / 16;
+        const uint4* g = reinterpret_cast<const uint4*>(blk);
+        uint4* s = reinterpret_cast<uint4*>(stage);
+        for (int64_t i = tid; i < n16; i += kCompressThreads) s[i] = __ldg(g + i);
+        __syncthreads();
+        src = stage;
+    }
     const double pos = (double)(pos0 + b * m + m - 1);
-    norm_rope_store(row, ss, red, D, eps, pos, theta, kvfmt, out + blockIdx.y * out_seq_bytes + b * kv_row_bytes);
+    pool_block_store(src, act, act_row_bytes, D, m, w_z, bias, z, row, red, eps, pos, theta, kvfmt,
+                     out + blockIdx.y * out_seq_bytes + b * kv_row_bytes);
     if (win_out != nullptr) {  // the window row of the block's last token
         __syncthreads();       // `row` is free again
         window_row(src + (m - 1) * act_row_bytes, act, row, red, D, eps, pos, theta, kvfmt,
@@ -151,33 +163,38 @@ __global__ void __launch_bounds__(kCompressThreads)
 // m / kSplit scores, then kSplit slots of (4 + D) floats, then 32 floats.
 constexpr int kSplit = 8;
 
-__global__ void __launch_bounds__(kCompressThreads)
-    compress_cluster_kernel(const uint8_t* __restrict__ kv, int act, int64_t act_row_bytes,
-                            int64_t kv_seq_bytes, int D, int m, int64_t pos0,
-                            const float* __restrict__ w_z, const float* __restrict__ bias,
-                            uint8_t* __restrict__ out, int kvfmt, int64_t kv_row_bytes,
-                            int64_t out_seq_bytes, float eps, RopeTheta theta,
-                            uint8_t* __restrict__ win_out, int64_t win_seq_bytes) {
-    extern __shared__ __align__(16) float sm[];
-    const int mt = m / kSplit;                          // tokens of this CTA
-    const int rank = (int)tc::cluster_ctarank();        // == blockIdx.x % kSplit
-    const int64_t b = blockIdx.x / kSplit;              // output entry
-    const size_t slice_bytes = (size_t)mt * act_row_bytes;
-    uint8_t* stage = reinterpret_cast<uint8_t*>(sm);
-    float* z = reinterpret_cast<float*>(stage + ((slice_bytes + 15) & ~(size_t)15));
-    float* slots = z + ((mt + 3) & ~3);                 // [kSplit][4 + D]
-    float* red = slots + kSplit * (4 + D);              // [32]
+// Shared memory of a cluster CTA: the slice's raw rows (at least D floats),
+// then m / kSplit scores, then kSplit slots of (4 + D) floats, then 32 floats.
+struct ClusterSmem {
+    uint8_t* stage;
+    float *z, *slots, *red;
+    __device__ ClusterSmem(float* sm, int mt, int64_t act_row_bytes, int D) {
+        const size_t slice_bytes = (size_t)mt * act_row_bytes;
+        stage = reinterpret_cast<uint8_t*>(sm);
+        z = reinterpret_cast<float*>(stage + ((slice_bytes + 15) & ~(size_t)15));
+        slots = z + ((mt + 3) & ~3);  // [kSplit][4 + D]
+        red = slots + kSplit * (4 + D);
+    }
+};
+
+// The pooling of one block by a cluster of kSplit CTAs, CTA `rank` holding
+// raw tokens rank*mt .. rank*mt+mt-1 of the block in c.stage (visible to the
+// CTA).  CTA 0 stores the entry at entry_dst; CTA kSplit-1 stores the window
+// row of the block's last token at win_dst (when not null).  Every CTA of the
+// cluster must call this (one cluster barrier).
+__device__ __forceinline__ void cluster_pool_store(const ClusterSmem& c, int rank, int act, int64_t act_row_bytes,
+                                                   int D, int m, const float* __restrict__ w_z,
+                                                   const float* __restrict__ bias, float eps, double pos,
+                                                   const RopeTheta& theta, int kvfmt, uint8_t* entry_dst,
+                                                   uint8_t* win_dst) {
+    const int mt = m / kSplit;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int nwarps = kCompressThreads / 32;
-    const int t0 = rank * mt;                           // first token of the slice within the block
-    {
-        const uint4* g = reinterpret_cast<const uint4*>(kv + blockIdx.y * kv_seq_bytes +
-                                                        (b * m + t0) * act_row_bytes);
-        uint4* s = reinterpret_cast<uint4*>(stage);
-        const int64_t n16 = (int64_t)slice_bytes / 16;
-        for (int64_t i = tid; i < n16; i += kCompressThreads) s[i] = __ldg(g + i);
-    }
-    __syncthreads();
+    const int t0 = rank * mt;  // first token of the slice within the block
+    uint8_t* stage = c.stage;
+    float* z = c.z;
+    float* slots = c.slots;
+    float* red = c.red;
     for (int t = warp; t < mt; t += nwarps) {
         const uint8_t* r = stage + t * act_row_bytes;
         float acc = 0.f;
@@ -199,9 +216,9 @@ __global__ void __launch_bounds__(kCompressThreads)
         float p[4];
 #pragma unroll
         for (int e = 0; e < 4; e++) {
-            float c = 0.f;
-            for (int t = 0; t < mt; t++) c = fmaf(z[t], load_act(stage + t * act_row_bytes, act, 4 * d4 + e), c);
-            p[e] = c;
+            float cc = 0.f;
+            for (int t = 0; t < mt; t++) cc = fmaf(z[t], load_act(stage + t * act_row_bytes, act, 4 * d4 + e), cc);
+            p[e] = cc;
         }
         tc::st_cluster_v4(slot0 + 16u * (1 + d4), make_uint4(__float_as_uint(p[0]), __float_as_uint(p[1]),
                                                                __float_as_uint(p[2]), __float_as_uint(p[3])));
@@ -209,12 +226,10 @@ __global__ void __launch_bounds__(kCompressThreads)
     if (tid == 0)
         tc::st_cluster_v4(slot0, make_uint4(__float_as_uint(zmax), __float_as_uint(zsum), 0u, 0u));
     tc::cluster_sync();  // every slot of CTA 0 is written and visible
-    const double pos = (double)(pos0 + b * m + m - 1);
-    if (rank == kSplit - 1 && win_out != nullptr) {
+    if (rank == kSplit - 1 && win_dst != nullptr) {
         // the window row of the block's last token, the last row of this slice;
         // this CTA's own slots are unused and hold the row
-        window_row(stage + (mt - 1) * act_row_bytes, act, slots, red, D, eps, pos, theta, kvfmt,
-                   win_out + blockIdx.y * win_seq_bytes + b * kv_row_bytes);
+        window_row(stage + (mt - 1) * act_row_bytes, act, slots, red, D, eps, pos, theta, kvfmt, win_dst);
         return;
     }
     if (rank != 0) return;
@@ -227,13 +242,165 @@ __global__ void __launch_bounds__(kCompressThreads)
     // merged pooled vector and its sum of squares
     float ss = 0.f;
     for (int d = tid; d < D; d += kCompressThreads) {
-        float c = 0.f;
-        for (int r = 0; r < kSplit; r++) c = fmaf(slots[r * (4 + D) + 4 + d], expf(slots[r * (4 + D)] - M), c);
-        c *= invS;
-        row[d] = c;
-        ss = fmaf(c, c, ss);
+        float cc = 0.f;
+        for (int r = 0; r < kSplit; r++) cc = fmaf(slots[r * (4 + D) + 4 + d], expf(slots[r * (4 + D)] - M), cc);
+        cc *= invS;
+        row[d] = cc;
+        ss = fmaf(cc, cc, ss);
     }
-    norm_rope_store(row, ss, red, D, eps, pos, theta, kvfmt, out + blockIdx.y * out_seq_bytes + b * kv_row_bytes);
+    norm_rope_store(row, ss, red, D, eps, pos, theta, kvfmt, entry_dst);
+}
+
+__global__ void __launch_bounds__(kCompressThreads)
+    compress_cluster_kernel(const uint8_t* __restrict__ kv, int act, int64_t act_row_bytes,
+                            int64_t kv_seq_bytes, int D, int m, int64_t pos0,
+                            const float* __restrict__ w_z, const float* __restrict__ bias,
+                            uint8_t* __restrict__ out, int kvfmt, int64_t kv_row_bytes,
+                            int64_t out_seq_bytes, float eps, RopeTheta theta,
+                            uint8_t* __restrict__ win_out, int64_t win_seq_bytes) {
+    extern __shared__ __align__(16) float sm[];
+    const int mt = m / kSplit;                          // tokens of this CTA
+    const int rank = (int)tc::cluster_ctarank();        // == blockIdx.x % kSplit
+    const int64_t b = blockIdx.x / kSplit;              // output entry
+    const ClusterSmem c(sm, mt, act_row_bytes, D);
+    {
+        const uint4* g = reinterpret_cast<const uint4*>(kv + blockIdx.y * kv_seq_bytes +
+                                                        (b * m + rank * mt) * act_row_bytes);
+        uint4* st = reinterpret_cast<uint4*>(c.stage);
+        const int64_t n16 = (int64_t)mt * act_row_bytes / 16;
+        for (int64_t i = threadIdx.x; i < n16; i += kCompressThreads) st[i] = __ldg(g + i);
+    }
+    __syncthreads();
+    cluster_pool_store(c, rank, act, act_row_bytes, D, m, w_z, bias, eps, (double)(pos0 + b * m + m - 1), theta,
+                       kvfmt, out + blockIdx.y * out_seq_bytes + b * kv_row_bytes,
+                       win_out != nullptr ? win_out + blockIdx.y * win_seq_bytes + b * kv_row_bytes : nullptr);
+}
+
+// ---------------------------------------------------------------- decode append
+// One decode step's cache maintenance for a ragged batch: sequence s's newest
+// token sits at position t = pos[s].  Its raw row goes to slot t mod m of the
+// sequence's raw ring (the tokens of its current block, position p at slot
+// p mod m), its window row RoPE(RMSNorm(kv_t), t) to row t mod n_win of the
+// window ring, and when it completes a block (t + 1 a multiple of m) the
+// block -- ring slots 0 .. m-2 and the new token -- is pooled into cache
+// entry (t + 1)/m - 1.  The pooling and the window row are the compressor's
+// own code (pool_block_store / cluster_pool_store, window_row).
+struct DecodeAppend {
+    const int64_t* pos;     // [B]
+    const uint8_t* tok;     // [B] raw rows of the newest tokens (act format)
+    uint8_t* ring;          // [B, m] raw rows (act format); nullptr when m == 1
+    uint8_t* cache;         // [B, n_cap] stored rows
+    int64_t n_cap;
+    uint8_t* window;        // [B, n_win] stored rows; nullptr: no window
+    int64_t n_win;
+    uint32_t* status;
+};
+
+// Position checks of the step: the token's slot in its block and whether it
+// completes a block whose entry fits in the cache (flagged otherwise).
+__device__ __forceinline__ bool append_completes(const DecodeAppend& d, int64_t t, int m, bool report) {
+    if ((t + 1) % m != 0) return false;
+    if ((t + 1) / m > d.n_cap) {
+        if (report) atomicOr(d.status, CSA_DEV_BAD_POSITION);
+        return false;
+    }
+    return true;
+}
+
+// grid (B); dynamic smem: (m + D + 32) floats rounded up to 16 bytes, then m raw rows.
+__global__ void __launch_bounds__(kCompressThreads)
+    append_step_kernel(const DecodeAppend d, int act, int64_t act_row_bytes, int D, int m,
+                       const float* __restrict__ w_z, const float* __restrict__ bias, int kvfmt,
+                       int64_t kv_row_bytes, float eps, RopeTheta theta) {
+    extern __shared__ __align__(16) float sm[];
+    float* z = sm;
+    float* row = sm + m;
+    float* red = row + D;
+    uint8_t* stage = reinterpret_cast<uint8_t*>(sm + ((m + D + 32 + 3) & ~3));
+    const int tid = threadIdx.x;
+    const int64_t s = blockIdx.x;
+    const int64_t t = d.pos[s];
+    if (t < 0) {
+        if (tid == 0) atomicOr(d.status, CSA_DEV_BAD_POSITION);
+        return;
+    }
+    const bool complete = append_completes(d, t, m, tid == 0);
+    const int64_t n16 = act_row_bytes / 16;
+    uint4* last = reinterpret_cast<uint4*>(stage + (m - 1) * act_row_bytes);
+    {
+        const uint4* g = reinterpret_cast<const uint4*>(d.tok + s * act_row_bytes);
+        for (int64_t i = tid; i < n16; i += kCompressThreads) last[i] = __ldg(g + i);
+    }
+    if (complete && m > 1) {  // the block's earlier tokens, written by earlier steps
+        const uint4* g = reinterpret_cast<const uint4*>(d.ring + s * m * act_row_bytes);
+        uint4* st = reinterpret_cast<uint4*>(stage);
+        for (int64_t i = tid; i < (int64_t)(m - 1) * n16; i += kCompressThreads) st[i] = __ldg(g + i);
+    }
+    __syncthreads();
+    if (m > 1) {  // the new token into its slot of the raw ring
+        uint4* g = reinterpret_cast<uint4*>(d.ring + (s * m + t % m) * act_row_bytes);
+        for (int64_t i = tid; i < n16; i += kCompressThreads) g[i] = last[i];
+    }
+    if (complete) {
+        pool_block_store(stage, act, act_row_bytes, D, m, w_z, bias, z, row, red, eps, (double)t, theta, kvfmt,
+                         d.cache + (s * d.n_cap + (t + 1) / m - 1) * kv_row_bytes);
+        __syncthreads();  // `row` is free again
+    }
+    if (d.window != nullptr)
+        window_row(stage + (m - 1) * act_row_bytes, act, row, red, D, eps, (double)t, theta, kvfmt,
+                   d.window + (s * d.n_win + t % d.n_win) * kv_row_bytes);
+}
+
+// The same for blocks split over a cluster of kSplit CTAs: grid (kSplit, B),
+// clusters of (kSplit, 1, 1).  A step that completes no block is done by the
+// last CTA alone (ring slot and window row); the others leave at once.  Every
+// branch before the cluster barrier depends on the sequence only, so all CTAs
+// of a cluster take it together.
+__global__ void __launch_bounds__(kCompressThreads)
+    append_cluster_kernel(const DecodeAppend d, int act, int64_t act_row_bytes, int D, int m,
+                          const float* __restrict__ w_z, const float* __restrict__ bias, int kvfmt,
+                          int64_t kv_row_bytes, float eps, RopeTheta theta) {
+    extern __shared__ __align__(16) float sm[];
+    const int mt = m / kSplit;
+    const int rank = (int)tc::cluster_ctarank();
+    const int64_t s = blockIdx.y;
+    const int64_t t = d.pos[s];
+    const int tid = threadIdx.x;
+    if (t < 0) {
+        if (rank == 0 && tid == 0) atomicOr(d.status, CSA_DEV_BAD_POSITION);
+        return;
+    }
+    const bool complete = append_completes(d, t, m, rank == 0 && tid == 0);
+    const ClusterSmem c(sm, mt, act_row_bytes, D);
+    const int64_t n16 = act_row_bytes / 16;
+    const uint4* tok = reinterpret_cast<const uint4*>(d.tok + s * act_row_bytes);
+    uint4* slot = reinterpret_cast<uint4*>(d.ring + (s * m + t % m) * act_row_bytes);
+    uint8_t* win_dst = d.window != nullptr ? d.window + (s * d.n_win + t % d.n_win) * kv_row_bytes : nullptr;
+    if (!complete) {
+        if (rank != kSplit - 1) return;
+        uint4* st = reinterpret_cast<uint4*>(c.stage);
+        for (int64_t i = tid; i < n16; i += kCompressThreads) st[i] = __ldg(tok + i);
+        __syncthreads();
+        for (int64_t i = tid; i < n16; i += kCompressThreads) slot[i] = st[i];
+        if (win_dst != nullptr)
+            window_row(c.stage, act, c.slots, c.red, D, eps, (double)t, theta, kvfmt, win_dst);
+        return;
+    }
+    {  // slice rank of the block: ring slots rank*mt .. ; the last is the new token
+        const uint4* g = reinterpret_cast<const uint4*>(d.ring + (s * m + rank * mt) * act_row_bytes);
+        uint4* st = reinterpret_cast<uint4*>(c.stage);
+        const int64_t n_ring = (int64_t)(rank == kSplit - 1 ? mt - 1 : mt) * n16;
+        for (int64_t i = tid; i < n_ring; i += kCompressThreads) st[i] = __ldg(g + i);
+        if (rank == kSplit - 1)
+            for (int64_t i = tid; i < n16; i += kCompressThreads) st[n_ring + i] = __ldg(tok + i);
+    }
+    __syncthreads();
+    if (rank == kSplit - 1) {
+        const uint4* st = reinterpret_cast<const uint4*>(c.stage + (mt - 1) * act_row_bytes);
+        for (int64_t i = tid; i < n16; i += kCompressThreads) slot[i] = st[i];
+    }
+    cluster_pool_store(c, rank, act, act_row_bytes, D, m, w_z, bias, eps, (double)t, theta, kvfmt,
+                       d.cache + (s * d.n_cap + (t + 1) / m - 1) * kv_row_bytes, win_dst);
 }
 
 // one warp per row; dynamic smem: 4 warps x D floats
@@ -256,6 +423,73 @@ cudaError_t launch_cache_pack(const Geometry& g, const float* src, int64_t n, vo
     int64_t blocks = (n + 3) / 4;
     pack_kernel<<<(unsigned)blocks, 128, 4 * g.D * sizeof(float), st>>>(
         src, n, g.D, g.kv, g.kv_row_bytes, reinterpret_cast<uint8_t*>(dst));
+    note_launch();
+    return cudaGetLastError();
+}
+
+// Shared memory of the decode append: the cluster form for blocks of 64+
+// tokens that split into kSplit slices of at least D floats, else one CTA per
+// sequence staging the whole block (0: the block does not fit).
+static size_t append_cluster_smem(const Geometry& g) {
+    const int64_t act_rb = row_bytes(g.act, g.D);
+    if (g.m < 64 || g.m % kSplit != 0) return 0;
+    const int mt = g.m / kSplit;
+    const size_t slice = ((size_t)mt * act_rb + 15) & ~(size_t)15;
+    const size_t smem = slice + (size_t)(((mt + 3) & ~3) + kSplit * (4 + g.D) + 32) * sizeof(float);
+    return (slice >= (size_t)g.D * sizeof(float) && smem <= 200 * 1024) ? smem : 0;
+}
+
+static size_t append_single_smem(const Geometry& g) {
+    const size_t smem = (size_t)((g.m + g.D + 32 + 3) & ~3) * sizeof(float) + (size_t)g.m * row_bytes(g.act, g.D);
+    return smem <= 200 * 1024 ? smem : 0;
+}
+
+bool decode_append_supported(const Geometry& g) { return append_cluster_smem(g) > 0 || append_single_smem(g) > 0; }
+
+cudaError_t launch_decode_append(const Geometry& g, const void* tok, int B, const int64_t* pos, void* ring,
+                                 const float* w_z, const float* bias, void* cache, int64_t n_cap, void* window,
+                                 int64_t n_win, uint32_t* status, cudaStream_t st) {
+    if (B == 0) return cudaSuccess;
+    DecodeAppend d;
+    d.pos = pos;
+    d.tok = reinterpret_cast<const uint8_t*>(tok);
+    d.ring = reinterpret_cast<uint8_t*>(ring);
+    d.cache = reinterpret_cast<uint8_t*>(cache);
+    d.n_cap = n_cap;
+    d.window = (g.W > 0 && n_win > 0) ? reinterpret_cast<uint8_t*>(window) : nullptr;
+    d.n_win = n_win;
+    d.status = status;
+    const int64_t act_rb = row_bytes(g.act, g.D);
+    const size_t csm = append_cluster_smem(g);
+    if (csm > 0) {
+        cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(append_cluster_kernel), csm);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)kSplit, (unsigned)B, 1);
+        cfg.blockDim = dim3(kCompressThreads, 1, 1);
+        cfg.dynamicSmemBytes = csm;
+        cfg.stream = st;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = kSplit;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, append_cluster_kernel, d, (int)g.act, act_rb, g.D, g.m, w_z, bias,
+                               (int)g.kv, g.kv_row_bytes, g.eps, rope_theta(g));
+        note_launch();
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
+    const size_t smem = append_single_smem(g);
+    if (smem == 0) return cudaErrorInvalidValue;  // refused earlier by the C ABI
+    if (smem > 48 * 1024) {
+        cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(append_step_kernel), smem);
+        if (e != cudaSuccess) return e;
+    }
+    append_step_kernel<<<(unsigned)B, kCompressThreads, smem, st>>>(d, g.act, act_rb, g.D, g.m, w_z, bias, g.kv,
+                                                                    g.kv_row_bytes, g.eps, rope_theta(g));
     note_launch();
     return cudaGetLastError();
 }

@@ -7,6 +7,7 @@
 //
 // This path serves every shape (fp32 and bf16, idx_dim 64 or 128).  The
 // tensor-core path for bf16 / idx_dim 128 lives in k_indexer_tc.cu.
+#include <limits.h>
 #include "common.cuh"
 #include "internal.h"
 
@@ -157,6 +158,107 @@ cudaError_t launch_pack_idx_keys(const Geometry& g, const void* rows, int64_t n,
                                                                    n, codes, scales);
     note_launch();
     return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ FP4 indexer keys
+// floor(log2 a) of a positive float32, exactly (subnormals included).
+__device__ __forceinline__ int floor_log2_pos(float a) {
+    const uint32_t b = __float_as_uint(a);
+    const int ex = (int)(b >> 23);
+    if (ex != 0) return ex - 127;
+    return (31 - __clz((int)(b & 0x7FFFFFu))) - 149;
+}
+
+// E2M1 code of q: the nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6, ties to the even
+// code, saturating at 6; sign in bit 3 (never on a zero code).
+__device__ __forceinline__ uint32_t e2m1_code(float q) {
+    const float a = fabsf(q);
+    uint32_t c;
+    if (a <= 0.25f) c = 0;        // tie 0.25 -> 0 (even)
+    else if (a < 0.75f) c = 1;    // tie 0.75 -> 1.0 (even)
+    else if (a <= 1.25f) c = 2;   // tie 1.25 -> 1.0
+    else if (a < 1.75f) c = 3;    // tie 1.75 -> 2
+    else if (a <= 2.5f) c = 4;    // tie 2.5 -> 2
+    else if (a < 3.5f) c = 5;     // tie 3.5 -> 4
+    else if (a <= 5.f) c = 6;     // tie 5 -> 4
+    else c = 7;
+    return (c != 0 && q < 0.f) ? (c | 8u) : c;
+}
+
+// keys [B, n_cap, 128] (act format) -> packed tiles [B, n_tiles] of 8704
+// bytes: tile t holds keys 128t .. 128t+127, first their codes (64 bytes a
+// key: dim 2i in the low nibble of byte i, dim 2i+1 in the high one), then
+// their exponent bytes (4 a key, block j's scale 2^(byte - 127)); key slots
+// past n_cap are zero.  Block j: e_j = floor(log2 amax) - 2 (its largest value
+// in [4, 8)), 0 for an all-zero block; a nonzero block more than 14 binades
+// below the key's largest is raised to it minus 14 (the key then converts to
+// E4M3 with one scale without loss); codes = E2M1 of x / 2^e_j.  One warp a
+// key slot, lane l holding dims 4l .. 4l+3 (block l / 8).
+__global__ void __launch_bounds__(256)
+    pack_idx_keys_fp4_kernel(const uint8_t* __restrict__ keys, int act, int64_t n_cap, int n_tiles,
+                             int64_t total_slots, uint8_t* __restrict__ pack) {
+    const int64_t slot = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (slot >= total_slots) return;
+    const int64_t per_seq = (int64_t)n_tiles * 128;
+    const int64_t seq = slot / per_seq, r = slot - seq * per_seq;
+    const int64_t t = r >> 7;
+    const int k = (int)(r & 127);
+    uint8_t* tile = pack + (seq * n_tiles + t) * 8704;
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+    if (r < n_cap) {
+        const uint8_t* row = keys + (seq * n_cap + r) * (int64_t)(act == CSA_F32 ? 512 : 256);
+#pragma unroll
+        for (int e = 0; e < 4; e++) x[e] = load_act(row, act, 4 * lane + e);
+    }
+    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const bool nz = amax > 0.f;
+    int e = nz ? floor_log2_pos(amax) - 2 : 0;
+    int E = nz ? e : INT_MIN;
+    E = max(E, __shfl_xor_sync(0xffffffffu, E, 8));
+    E = max(E, __shfl_xor_sync(0xffffffffu, E, 16));
+    if (nz && e < E - 14) e = E - 14;
+    e = min(127, max(-127, e));
+    uint32_t c = 0;
+#pragma unroll
+    for (int i = 0; i < 4; i++) c |= e2m1_code(ldexpf(x[i], -e)) << (4 * i);
+    *reinterpret_cast<uint16_t*>(tile + k * 64 + 2 * lane) = (uint16_t)c;
+    if ((lane & 7) == 0) tile[128 * 64 + k * 4 + (lane >> 3)] = (uint8_t)(e + 127);
+}
+
+cudaError_t launch_pack_idx_keys_fp4(const Geometry& g, const void* keys, int B, int64_t n_cap, uint8_t* pack,
+                                     cudaStream_t st) {
+    if (B == 0 || n_cap == 0) return cudaSuccess;
+    const int n_tiles = (int)((n_cap + 127) / 128);
+    const int64_t slots = (int64_t)B * n_tiles * 128;
+    pack_idx_keys_fp4_kernel<<<(unsigned)((slots + 7) / 8), 256, 0, st>>>(reinterpret_cast<const uint8_t*>(keys),
+                                                                          g.act, n_cap, n_tiles, slots, pack);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_indexer_tc_fp4(const Geometry& g, const uint8_t* q8, const float* w_eff, const uint8_t* key_pack,
+                                  int64_t n_cap, int B, int Q, const int64_t* q_pos, uint32_t* status,
+                                  float* scores, int64_t ld, cudaStream_t st, bool* launched);
+
+// FP4 indexer: the queries are quantised as for E4M3 keys, then the tcgen05
+// kernel expands the packed keys to E4M3 in shared memory and scores them.
+cudaError_t launch_indexer_fp4(const Geometry& g, const void* q_idx, const float* w_idx, const uint8_t* key_pack,
+                               int64_t n_cap, int B, int Q, const int64_t* q_pos, uint32_t* status, float* scores,
+                               int64_t ld, uint8_t* q8, float* w_eff, cudaStream_t st) {
+    if (Q == 0 || n_cap == 0) return cudaSuccess;
+    const int64_t rows = (int64_t)Q * 64;
+    quant_idx_queries_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(reinterpret_cast<const uint8_t*>(q_idx),
+                                                                          g.act, w_idx, rows, q8, w_eff);
+    note_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bool launched = false;
+    e = launch_indexer_tc_fp4(g, q8, w_eff, key_pack, n_cap, B, Q, q_pos, status, scores, ld, st, &launched);
+    if (e == cudaSuccess && !launched) return cudaErrorInvalidValue;  // shapes checked by the C ABI
+    return e;
 }
 
 // E4M3 indexer: the queries are quantised into q8 / w_eff (workspace), then

@@ -21,6 +21,8 @@
 // otherwise hold the tensor pipe back).  Every wait is bounded: on a timeout
 // the kernel flags CSA_DEV_TIMEOUT, all roles leave their loops and TMEM is
 // freed.
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc_util.cuh"
@@ -38,11 +40,21 @@ constexpr int kHI = 64;            // indexer heads (per query)
 constexpr int kDI = 128;           // indexer dim
 constexpr int kTileKeys = 128;     // MMA M
 
-// F8: keys and queries in E4M3 (kind::f8f6f4 MMAs, K = 32 per MMA), one
-// float32 scale per key row and per query head (folded into the head
-// weights); otherwise bf16 (kind::f16, K = 16).
-template <int NQ, bool F8>
+// Key formats: bf16 (kind::f16 MMAs, K = 16), E4M3 with one float32 scale
+// per key (kind::f8f6f4 MMAs, K = 32; query heads in E4M3 with their scales
+// folded into the head weights), or FP4: E2M1 codes with one power-of-two
+// scale per 32 dims, expanded in shared memory to E4M3 codes with one
+// power-of-two scale per key (exact: the packer keeps a key's block scales
+// within 14 binades of its largest), then scored as E4M3 keys.
+enum { kKeyBf16 = 0, kKeyE4m3 = 1, kKeyFp4 = 2 };
+// A packed FP4 key tile: 128 keys x 64 code bytes, then 128 x 4 exponent bytes.
+constexpr uint32_t kFp4TileBytes = kTileKeys * (kDI / 2) + kTileKeys * (kDI / 32);
+static_assert(kFp4TileBytes == 8704 && kFp4TileBytes % 128 == 0, "FP4 tile layout");
+
+template <int NQ, int KF>
 struct Cfg {
+    static constexpr bool F8 = KF != kKeyBf16;          // E4M3 MMAs
+    static constexpr bool F4 = KF == kKeyFp4;
     static constexpr int kEB = F8 ? 1 : 2;              // bytes per element
     static constexpr uint32_t kStageBytes = kTileKeys * kDI * kEB;  // 32 KiB bf16 (two boxes), 16 KiB E4M3 (one)
     static constexpr int kKSteps = kDI * kEB / 32;      // MMAs per key tile: 32 bytes of K each
@@ -65,18 +77,26 @@ struct Cfg {
     static constexpr int kIssuers = NQ == 1 ? 2 : 1;
     static_assert(kStages % kIssuers == 0 && kAcc % kIssuers == 0, "issuers own whole stages");
     static constexpr int kEpi0 = 1 + kIssuers;          // first epilogue warp
-    static constexpr int kThreads = 32 * kEpi0 + 32 * kEpiWarps;
+    static constexpr int kConvWarps = F4 ? 4 : 0;       // FP4 -> E4M3 converters, one key a thread
+    static constexpr int kConv0 = kEpi0 + kEpiWarps;
+    static constexpr int kThreads = 32 * (kConv0 + kConvWarps);
     static constexpr uint32_t kQBytes = (uint32_t)N * kDI * kEB;
     static constexpr uint32_t kTmemCols = kAcc * N;     // 256 or 512
-    static constexpr size_t kBarBytes = 512;
-    static_assert((2 * kStages + 2 * kQBufs + 2 * kAcc) * 8 + 8 <= kBarBytes, "barrier area too small");
-    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kQBufs * kQBytes + kBarBytes;
+    static constexpr int kRawStages = F4 ? 4 : 0;       // packed FP4 tiles in flight
+    static constexpr int kScaleSlots = F4 ? kStages + kAcc : 0;  // per-key scales of the tiles in flight
+    static constexpr size_t kBarBytes = 1024;
+    static_assert((2 * kStages + 2 * kQBufs + 2 * kAcc + 2 * kRawStages + kScaleSlots) * 8 + 8 <= kBarBytes,
+                  "barrier area too small");
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kQBufs * kQBytes +
+                                    (size_t)kRawStages * kFp4TileBytes + (size_t)kScaleSlots * kTileKeys * 4 +
+                                    kBarBytes;
     static constexpr uint32_t idesc = F8 ? tc::idesc_e4m3_f32(kTileKeys, N) : tc::idesc_bf16_f32(kTileKeys, N);
 };
 
 struct IdxArgs {
     const float* w_idx;    // [Q, 64] (F8: the head weights times the query head scales)
-    const float* key_scales;  // F8: [B, n_cap] per key row; else nullptr
+    const float* key_scales;  // E4M3 keys: [B, n_cap] per key row; else nullptr
+    const uint8_t* key_pack;  // FP4 keys: [B, n_tiles] packed tiles of kFp4TileBytes; else nullptr
     const int64_t* q_pos;  // [Q]
     float* scores;         // [Q, ld]
     int64_t ld;
@@ -86,6 +106,7 @@ struct IdxArgs {
     int n_tiles;           // key tiles per query group
     int64_t total_units;   // groups * n_tiles
     uint32_t* status;
+    int withhold;          // test hook: the producer issues nothing (see csa_test_withhold_indexer_loads)
 };
 
 // Blocks a query group sees: the largest floor((i+1)/m) of its queries, capped.
@@ -102,31 +123,43 @@ __device__ __forceinline__ int64_t group_avail(const IdxArgs& a, int64_t g) {
 
 }  // namespace
 
-template <int NQ, bool F8>
-__global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
+template <int NQ, int KF>
+__global__ void __launch_bounds__(Cfg<NQ, KF>::kThreads, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                       const __grid_constant__ CUtensorMap tm_q, IdxArgs a) {
-    using C = Cfg<NQ, F8>;
+    using C = Cfg<NQ, KF>;
+    constexpr bool F8 = C::F8;
+    constexpr bool F4 = C::F4;
     constexpr uint32_t kStageBytes = C::kStageBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = sm;
     uint8_t* sB = sA + C::kStages * kStageBytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::kQBufs * C::kQBytes);
+    uint8_t* sRaw = sB + C::kQBufs * C::kQBytes;                                   // FP4 packed tiles
+    float* sKs = reinterpret_cast<float*>(sRaw + (size_t)C::kRawStages * kFp4TileBytes);  // FP4 key scales
+    uint64_t* full = reinterpret_cast<uint64_t*>(sKs + C::kScaleSlots * kTileKeys);
     uint64_t* empty = full + C::kStages;
     uint64_t* qfull = empty + C::kStages;
     uint64_t* qempty = qfull + C::kQBufs;
     uint64_t* tfull = qempty + C::kQBufs;
     uint64_t* tempty = tfull + C::kAcc;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + C::kAcc);
+    uint64_t* rfull = tempty + C::kAcc;        // FP4: packed tile landed
+    uint64_t* rempty = rfull + C::kRawStages;  // FP4: packed tile read by the converters
+    uint64_t* sfull = rempty + C::kRawStages;  // FP4: key scales of a tile written
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfull + C::kScaleSlots);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; s++) {
-            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&full[s], F4 ? C::kConvWarps : 1);  // FP4: every converter warp
             tc::mbar_init(&empty[s], 1);
         }
+        for (int s = 0; s < C::kRawStages; s++) {
+            tc::mbar_init(&rfull[s], 1);
+            tc::mbar_init(&rempty[s], C::kConvWarps);
+        }
+        for (int s = 0; s < C::kScaleSlots; s++) tc::mbar_init(&sfull[s], C::kConvWarps);
         for (int b = 0; b < C::kQBufs; b++) {
             tc::mbar_init(&qfull[b], 1);
             tc::mbar_init(&qempty[b], C::kIssuers);  // every issuer releases the queries
@@ -155,12 +188,15 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
     const int64_t g0 = u0 / a.n_tiles;
     const int64_t t0 = u0 - g0 * a.n_tiles;
 
-    if (warp == 0 && lane == 0) {
+    if (warp == 0 && lane == 0 && !a.withhold) {
         // ------------------------------------------------ TMA producer
+        // (under the test hook it issues nothing: no copy is ever in flight, the
+        // issuers' bounded waits on the query and key tiles expire)
         tc::tma_prefetch_map(&tm_keys);
         tc::tma_prefetch_map(&tm_q);
         int stage = 0;
         uint32_t phase = 0;
+        uint32_t nraw = 0;  // FP4: packed tiles loaded
         int64_t cur_g = -1, last_loaded = -1, gnav = 0;
         int qloads = 0, seq = 0;
         const float* ksrow = nullptr;  // F8: the sequence's key scales
@@ -174,7 +210,7 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
                 cur_g = g;
                 gnav = group_avail<NQ>(a, g);
                 seq = (int)((g * NQ) / a.qps);
-                if (F8) ksrow = a.key_scales + (int64_t)seq * a.n_cap;
+                if (KF == kKeyE4m3) ksrow = a.key_scales + (int64_t)seq * a.n_cap;
             }
             if ((int64_t)t * kTileKeys >= gnav) continue;  // no complete block in this tile
             if (g != last_loaded) {
@@ -188,12 +224,27 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
                 last_loaded = g;
                 qloads++;
             }
+            if constexpr (F4) {
+                // the packed tile, one bulk copy into the raw ring; the converter
+                // warps expand it into a stage
+                const int rs = (int)(nraw % C::kRawStages);
+                if (!tc::mbar_wait(&rempty[rs], ((nraw / C::kRawStages) & 1u) ^ 1u, abort_flag, a.status)) break;
+                tc::mbar_arrive_expect_tx(&rfull[rs], kFp4TileBytes);
+                const uint8_t* src = a.key_pack + ((int64_t)seq * a.n_tiles + t) * (int64_t)kFp4TileBytes;
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                        tc::smem_u32(sRaw + rs * kFp4TileBytes)),
+                    "l"(src), "r"(kFp4TileBytes), "r"(tc::smem_u32(&rfull[rs]))
+                    : "memory");
+                ++nraw;
+                continue;
+            }
             if (!tc::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status)) break;
             tc::mbar_arrive_expect_tx(&full[stage], kStageBytes);
             uint8_t* dst = sA + stage * kStageBytes;
             tc::tma_load_3d(dst, &tm_keys, &full[stage], 0, (int)(t * kTileKeys), seq);
             if (!F8) tc::tma_load_3d(dst + kStageBytes / 2, &tm_keys, &full[stage], 64, (int)(t * kTileKeys), seq);
-            if (F8) {  // the tile's key scales head for L2 now: the epilogue reads them thousands of cycles later
+            if (KF == kKeyE4m3) {  // the tile's key scales head for L2 now: the epilogue reads them thousands of cycles later
                 const int64_t k0 = t * kTileKeys, kn = min((int64_t)kTileKeys, a.n_cap - k0);
                 for (int64_t o = 0; o < kn; o += 32) tc::prefetch_l2_line(ksrow + k0 + o);
                 tc::prefetch_l2_line(ksrow + k0 + kn - 1);
@@ -256,7 +307,7 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
             tc::mma_commit(&empty[stage]);  // key tile free when these MMAs finish
             tc::mma_commit(&tfull[acc]);    // accumulator ready for the epilogue
         }
-    } else if (warp >= C::kEpi0) {
+    } else if (warp >= C::kEpi0 && warp < C::kConv0) {
         // ------------------------------------------------ epilogue: one key per thread
         const int quarter = warp & 3;          // TMEM lanes this warp may read
         const int row = quarter * 32 + lane;   // key within the tile
@@ -266,6 +317,7 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
         const int q0 = C::kEpiGroups > 1 ? 0 : wq;   // this warp's query within the query group
         int acc = 0;
         uint32_t aphase = 0;
+        uint32_t jl = 0;  // live units so far (FP4: the key-scale slot is jl % kScaleSlots)
         int64_t cur_g = -1, gnav = 0;
         int64_t nav[NQ];
         float* srow = a.scores;            // this warp's query's score row
@@ -309,6 +361,7 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
                 if (key < a.n_cap && grp == 0) srow[key] = -INFINITY;
                 continue;
             }
+            const uint32_t jj = jl++;
             if ((acc % C::kEpiGroups) != grp) {  // the other group's accumulator
                 if (++acc == C::kAcc) {
                     acc = 0;
@@ -318,9 +371,16 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
             }
             // E4M3 keys: this key's scale is on its way while the accumulator is awaited
             // (prefill keeps no row pointer: its sixteen warps are short of registers)
-            const float ksc = (F8 && key < a.n_cap)
-                                  ? __ldg((NQ == 1 ? krow : a.key_scales + (g * NQ / a.qps) * a.n_cap) + key)
-                                  : 1.f;
+            float ksc = (KF == kKeyE4m3 && key < a.n_cap)
+                            ? __ldg((NQ == 1 ? krow : a.key_scales + (g * NQ / a.qps) * a.n_cap) + key)
+                            : 1.f;
+            if constexpr (F4) {  // the power-of-two scale the converters chose for this key
+                // every lane waits (each acquires the converters' writes it reads)
+                const int slot = (int)(jj % C::kScaleSlots);
+                const int oks = tc::mbar_wait(&sfull[slot], (jj / C::kScaleSlots) & 1u, abort_flag, a.status) ? 1 : 0;
+                if (!__all_sync(0xffffffffu, oks)) break;
+                ksc = sKs[slot * kTileKeys + row];
+            }
             // one lane waits, the whole warp follows its verdict (tcgen05.ld is warp-wide)
             int ok = 1;
             if (lane == 0) ok = tc::mbar_wait(&tfull[acc], aphase, abort_flag, a.status) ? 1 : 0;
@@ -351,7 +411,7 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
                     }
                 }
                 float s = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
-                if (F8) s *= ksc;
+                if (F8) s *= ksc;  // E4M3: the stored per-key scale; FP4: the converted key's 2^E
                 if (key < a.n_cap) srow[key] = key < nav[q0] ? s : -INFINITY;
             }
             tc::fence_before_sync();
@@ -360,6 +420,89 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
             if (++acc == C::kAcc) {
                 acc = 0;
                 aphase ^= 1u;
+            }
+        }
+    }
+    if constexpr (F4) {
+        if (warp >= C::kConv0) {
+            // ------------------------------------------------ FP4 -> E4M3 converters
+            // Thread k of the four converter warps expands key k of every tile:
+            // E = the largest exponent of its blocks with a nonzero code, the
+            // key's scale 2^(E - 6) (its largest value 6 * 2^E lands on
+            // 384 <= 448), and block j's codes become the E4M3 codes of
+            // e2m1 * 2^(e_j - E + 6): an 8-entry magnitude table per block
+            // (exact conversions), looked up four codes at a time with byte
+            // permutes, the signs moved from bit 3 of each nibble to bit 7 of
+            // each byte with the permute's sign-replicate selectors.  The row
+            // is written with the 128-byte swizzle of a TMA tile load.
+            const int k = (warp - C::kConv0) * 32 + lane;
+            uint32_t j = 0;
+            int64_t cur_g = -1, gnav = 0;
+            int64_t g = g0;
+            const float kMag[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+            for (int64_t u = u0, t = t0; u < u1; ++u, ++t) {
+                if (t == a.n_tiles) {
+                    t = 0;
+                    ++g;
+                }
+                if (g != cur_g) {
+                    cur_g = g;
+                    gnav = group_avail<NQ>(a, g);
+                }
+                if ((int64_t)t * kTileKeys >= gnav) continue;
+                const uint32_t jj = j++;
+                const int stage = (int)(jj % C::kStages), rs = (int)(jj % C::kRawStages);
+                const int slot = (int)(jj % C::kScaleSlots);
+                if (!tc::mbar_wait(&rfull[rs], (jj / C::kRawStages) & 1u, abort_flag, a.status)) break;
+                if (!tc::mbar_wait(&empty[stage], ((jj / C::kStages) & 1u) ^ 1u, abort_flag, a.status)) break;
+                const uint8_t* raw = sRaw + rs * kFp4TileBytes;
+                uint4 cw[4];
+#pragma unroll
+                for (int c = 0; c < 4; c++) {  // chunk c = block c (32 codes); rotated to spread the banks
+                    const int cc = (c + k) & 3;
+                    cw[cc] = *reinterpret_cast<const uint4*>(raw + k * 64 + cc * 16);
+                }
+                const uint32_t ex = *reinterpret_cast<const uint32_t*>(raw + kTileKeys * 64 + k * 4);
+                int E = -1000;
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    const uint32_t nzm = (cw[c].x | cw[c].y | cw[c].z | cw[c].w) & 0x77777777u;
+                    const int ej = (int)((ex >> (8 * c)) & 0xFFu) - 127;
+                    if (nzm != 0u && ej > E) E = ej;
+                }
+                if (E == -1000) E = 0;  // no nonzero code: any scale
+                const int Ek = E - 6;
+                uint8_t* row = sA + stage * kStageBytes + k * 128;
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    const int sh = (int)((ex >> (8 * c)) & 0xFFu) - 127 - Ek;
+                    uint32_t lut[2] = {0u, 0u};
+#pragma unroll
+                    for (int m = 1; m < 8; m++)
+                        lut[m >> 2] |= (uint32_t)f32_to_e4m3_sat(ldexpf(kMag[m], sh)) << (8 * (m & 3));
+                    const uint32_t w[4] = {cw[c].x, cw[c].y, cw[c].z, cw[c].w};
+                    uint32_t o[8];
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const uint32_t wl = w[i] << 4;
+                        uint32_t sg0, sg1;
+                        asm("prmt.b32 %0, %1, %2, 0xD9C8;" : "=r"(sg0) : "r"(wl), "r"(w[i]));
+                        asm("prmt.b32 %0, %1, %2, 0xFBEA;" : "=r"(sg1) : "r"(wl), "r"(w[i]));
+                        o[2 * i] = __byte_perm(lut[0], lut[1], w[i] & 0x7777u) | (sg0 & 0x80808080u);
+                        o[2 * i + 1] = __byte_perm(lut[0], lut[1], (w[i] >> 16) & 0x7777u) | (sg1 & 0x80808080u);
+                    }
+                    // dims 32c .. 32c+15 are chunk 2c of the row, 32c+16 .. chunk 2c+1
+                    *reinterpret_cast<uint4*>(row + (((2 * c) ^ (k & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ (k & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+                sKs[slot * kTileKeys + k] = ldexpf(1.f, Ek);
+                tc::fence_proxy_async_smem();  // the rows are read by the MMAs (async proxy)
+                __syncwarp();
+                if (lane == 0) {
+                    tc::mbar_arrive(&full[stage]);
+                    tc::mbar_arrive(&sfull[slot]);
+                    tc::mbar_arrive(&rempty[rs]);
+                }
             }
         }
     }
@@ -373,25 +516,33 @@ __global__ void __launch_bounds__(Cfg<NQ, F8>::kThreads, 1)
     }
 }
 
-template <int NQ, bool F8>
+template <int NQ, int KF>
 static cudaError_t run_indexer(const CUtensorMap& tm_keys, const CUtensorMap& tm_q, const IdxArgs& a, int grid,
                                cudaStream_t st) {
-    using C = Cfg<NQ, F8>;
+    using C = Cfg<NQ, KF>;
     {
-        cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(indexer_tc_kernel<NQ, F8>), C::kSmem);
+        cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(indexer_tc_kernel<NQ, KF>), C::kSmem);
         if (e != cudaSuccess) return e;
     }
-    indexer_tc_kernel<NQ, F8><<<grid, C::kThreads, C::kSmem, st>>>(tm_keys, tm_q, a);
+    indexer_tc_kernel<NQ, KF><<<grid, C::kThreads, C::kSmem, st>>>(tm_keys, tm_q, a);
     note_launch();
     return cudaGetLastError();
 }
 
-cudaError_t launch_indexer_tc(const Geometry& g, const void* q_idx, const float* w_idx, int HI,
-                              int dI, const void* keys, const float* key_scales, int64_t n_cap, int B,
-                              int Q, const int64_t* q_pos, uint32_t* status, float* scores, int64_t ld,
-                              cudaStream_t st, bool* launched) {
+static std::atomic<int> g_withhold{0};
+
+void set_indexer_withhold(int on) { g_withhold.store(on ? 1 : 0, std::memory_order_relaxed); }
+
+// kf: kKeyBf16 (keys bf16 [B, n_cap, 128]), kKeyE4m3 (key codes [B, n_cap, 128]
+// + key_scales), kKeyFp4 (keys: packed tiles [B, ceil(n_cap/128)]).  For the
+// 8-bit formats q_idx holds the query codes and w_idx the head weights times
+// the query head scales.
+static cudaError_t launch_indexer_tc_kf(const Geometry& g, int kf, const void* q_idx, const float* w_idx, int HI,
+                                        int dI, const void* keys, const float* key_scales, int64_t n_cap, int B,
+                                        int Q, const int64_t* q_pos, uint32_t* status, float* scores, int64_t ld,
+                                        cudaStream_t st, bool* launched) {
     *launched = false;
-    const bool f8 = key_scales != nullptr;  // q_idx: E4M3 codes, w_idx: weights x head scales
+    const bool f8 = kf != kKeyBf16;
     if ((!f8 && g.act != CSA_BF16) || HI != kHI || dI != kDI || n_cap < kTileKeys || Q < 1) return cudaSuccess;
     if (((uintptr_t)w_idx & 15u) || (ld % 4) != 0) return cudaSuccess;
     const int qps = Q / B;
@@ -404,13 +555,20 @@ cudaError_t launch_indexer_tc(const Geometry& g, const void* q_idx, const float*
     const uint64_t qd[2] = {(uint64_t)kDI, (uint64_t)Q * kHI};
     const uint64_t qs[1] = {(uint64_t)kDI * eb};
     const uint32_t qbox[2] = {(uint32_t)(128 / eb), (uint32_t)(NQ * kHI)};
-    const bool maps = f8 ? (make_tmap_u8(&tm_keys, keys, 3, kd, ks, kb) && make_tmap_u8(&tm_q, q_idx, 2, qd, qs, qbox))
-                         : (make_tmap_bf16(&tm_keys, keys, 3, kd, ks, kb) &&
-                            make_tmap_bf16(&tm_q, q_idx, 2, qd, qs, qbox));
+    bool maps;
+    if (kf == kKeyFp4) {  // no key map: packed tiles come by bulk copy
+        maps = make_tmap_u8(&tm_q, q_idx, 2, qd, qs, qbox);
+        tm_keys = tm_q;
+    } else if (f8) {
+        maps = make_tmap_u8(&tm_keys, keys, 3, kd, ks, kb) && make_tmap_u8(&tm_q, q_idx, 2, qd, qs, qbox);
+    } else {
+        maps = make_tmap_bf16(&tm_keys, keys, 3, kd, ks, kb) && make_tmap_bf16(&tm_q, q_idx, 2, qd, qs, qbox);
+    }
     if (!maps) return f8 ? cudaErrorInvalidValue : cudaSuccess;  // bf16: the CUDA-core path runs instead
     IdxArgs a;
     a.w_idx = w_idx;
-    a.key_scales = key_scales;
+    a.key_scales = kf == kKeyE4m3 ? key_scales : nullptr;
+    a.key_pack = kf == kKeyFp4 ? reinterpret_cast<const uint8_t*>(keys) : nullptr;
     a.q_pos = q_pos;
     a.scores = scores;
     a.ld = ld;
@@ -420,15 +578,33 @@ cudaError_t launch_indexer_tc(const Geometry& g, const void* q_idx, const float*
     a.n_tiles = (int)((n_cap + kTileKeys - 1) / kTileKeys);
     a.total_units = (int64_t)(Q / NQ) * a.n_tiles;
     a.status = status;
+    a.withhold = g_withhold.load(std::memory_order_relaxed);
     const int64_t sms = num_sms();
     const int grid = (int)(a.total_units < sms ? a.total_units : sms);
     cudaError_t e;
-    if (NQ == 1)
-        e = f8 ? run_indexer<1, true>(tm_keys, tm_q, a, grid, st) : run_indexer<1, false>(tm_keys, tm_q, a, grid, st);
+    if (kf == kKeyFp4)
+        e = NQ == 1 ? run_indexer<1, kKeyFp4>(tm_keys, tm_q, a, grid, st) : run_indexer<4, kKeyFp4>(tm_keys, tm_q, a, grid, st);
+    else if (kf == kKeyE4m3)
+        e = NQ == 1 ? run_indexer<1, kKeyE4m3>(tm_keys, tm_q, a, grid, st) : run_indexer<4, kKeyE4m3>(tm_keys, tm_q, a, grid, st);
     else
-        e = f8 ? run_indexer<4, true>(tm_keys, tm_q, a, grid, st) : run_indexer<4, false>(tm_keys, tm_q, a, grid, st);
+        e = NQ == 1 ? run_indexer<1, kKeyBf16>(tm_keys, tm_q, a, grid, st) : run_indexer<4, kKeyBf16>(tm_keys, tm_q, a, grid, st);
     if (e == cudaSuccess) *launched = true;
     return e;
+}
+
+cudaError_t launch_indexer_tc(const Geometry& g, const void* q_idx, const float* w_idx, int HI,
+                              int dI, const void* keys, const float* key_scales, int64_t n_cap, int B,
+                              int Q, const int64_t* q_pos, uint32_t* status, float* scores, int64_t ld,
+                              cudaStream_t st, bool* launched) {
+    return launch_indexer_tc_kf(g, key_scales != nullptr ? kKeyE4m3 : kKeyBf16, q_idx, w_idx, HI, dI, keys,
+                                key_scales, n_cap, B, Q, q_pos, status, scores, ld, st, launched);
+}
+
+cudaError_t launch_indexer_tc_fp4(const Geometry& g, const uint8_t* q8, const float* w_eff, const uint8_t* key_pack,
+                                  int64_t n_cap, int B, int Q, const int64_t* q_pos, uint32_t* status,
+                                  float* scores, int64_t ld, cudaStream_t st, bool* launched) {
+    return launch_indexer_tc_kf(g, kKeyFp4, q8, w_eff, kHI, kDI, key_pack, nullptr, n_cap, B, Q, q_pos, status,
+                                scores, ld, st, launched);
 }
 
 }  // namespace csa

@@ -3,15 +3,20 @@
 These helpers own no arithmetic: they allocate device buffers with torch and
 issue the C-ABI calls in the order the layer needs them.
 
-Decode step (one new token per sequence, every sequence at the same length L):
-  1. append: when the new token completes a block, csa_append pools the newest
-     m raw tokens into cache entry L/m - 1 and writes the new token's
-     normalised, rotated window row (one launch; the same as csa_compress with
-     ratio m, then with ratio 1).
-  2. CSA: csa_index_topk then csa_attend.  HCA: hca_attend.
+Decode step (one new token per sequence; every sequence has its own length).
+The decode state of B sequences is three caller-owned device buffers:
+  raw_ring [B, m, D]   raw tokens of each sequence's current block (position p
+                       in slot p mod m)
+  cache    [B, n_cap]  compressed entries in the cache row format
+  window   [B, n_win]  window rows, a ring (position p at row p mod n_win)
+  1. append: csa_decode_append stores the newest token kv_tok [B, D] (at
+     positions pos [B]) in its raw-ring slot, writes its window row and, for
+     every sequence whose token completes a block, pools the block into its
+     cache entry (one launch).
+  2. CSA: csa_index_topk then csa_attend; HCA: hca_attend (ring window).
 Prefill (one sequence, a chunk of new tokens after `T_cached` cached ones):
   csa_compress over the chunk (ratio=m) and over the window tokens (ratio=1),
-  then csa_index_topk and csa_attend for every new token.
+  then csa_index_topk and csa_attend for every new token (linear window).
 """
 from __future__ import annotations
 
@@ -19,8 +24,8 @@ from dataclasses import dataclass
 
 import torch
 
-from . import (BF16, F32, FP8_MIXED, OP_ATTEND, OP_HCA_ATTEND, OP_INDEX_TOPK, csa_append,
-               csa_attend, csa_compress, csa_index_topk, csa_row_bytes, csa_workspace_bytes,
+from . import (BF16, F32, FP8_MIXED, OP_ATTEND, OP_HCA_ATTEND, OP_INDEX_TOPK, csa_attend,
+               csa_compress, csa_decode_append, csa_index_topk, csa_row_bytes, csa_workspace_bytes,
                hca_attend, params, workspace)
 
 _ACT_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
@@ -69,58 +74,70 @@ class LayerConfig:
         return torch.zeros(*shape, self.D, dtype=dt, device=device)
 
 
-class DecodeLayer:
-    """Buffers and calls of one decode step for B sequences."""
+def ring_order(rows: torch.Tensor, first_pos, n: int) -> torch.Tensor:
+    """Rows [B, n, ...] holding positions first_pos[b] + r (r = 0 .. n-1) laid out
+    as a ring of n rows: position p at row p mod n (a permutation per sequence)."""
+    out = torch.empty_like(rows)
+    for b in range(rows.shape[0]):
+        shift = int(first_pos[b]) % n
+        out[b] = torch.roll(rows[b], shifts=shift, dims=0)
+    return out
 
-    def __init__(self, cfg: LayerConfig, B: int, n_cap: int, n_win: int, device="cuda"):
-        self.cfg, self.B, self.n_cap, self.n_win = cfg, B, n_cap, n_win
+
+class DecodeLayer:
+    """Buffers and calls of one decode step for B sequences of any lengths."""
+
+    def __init__(self, cfg: LayerConfig, B: int, n_cap: int, n_win: int = 0, device="cuda"):
+        self.cfg, self.B, self.n_cap = cfg, B, n_cap
+        self.n_win = n_win if n_win > 0 else cfg.W
         self.p = cfg.params()
-        self.p1 = cfg.params(ratio=1)
         act = _ACT_DTYPE[_fmt(cfg.act)]
+        self.act_dtype = act
         self.out = torch.empty(B, cfg.H, cfg.D, dtype=act, device=device)
         self.lse = torch.empty(B, cfg.H, dtype=torch.float32, device=device)
         nb = 0
         if cfg.sparse:
             self.topk_idx = torch.empty(B, cfg.topk, dtype=torch.int32, device=device)
             self.topk_score = torch.empty(B, cfg.topk, dtype=torch.float32, device=device)
-            nb = csa_workspace_bytes(self.p, OP_INDEX_TOPK, B, B, cfg.H, cfg.H_I, n_cap, n_win)
-            nb = max(nb, csa_workspace_bytes(self.p, OP_ATTEND, B, B, cfg.H, cfg.H_I, n_cap, n_win))
+            nb = csa_workspace_bytes(self.p, OP_INDEX_TOPK, B, B, cfg.H, cfg.H_I, n_cap, self.n_win)
+            nb = max(nb, csa_workspace_bytes(self.p, OP_ATTEND, B, B, cfg.H, cfg.H_I, n_cap, self.n_win))
         else:
-            nb = csa_workspace_bytes(self.p, OP_HCA_ATTEND, B, B, cfg.H, 0, n_cap, n_win)
+            nb = csa_workspace_bytes(self.p, OP_HCA_ATTEND, B, B, cfg.H, 0, n_cap, self.n_win)
         self.ws = workspace(nb, device)
         self.ws_bytes = self.ws.numel()
         self._side = torch.cuda.Stream(device=device) if cfg.sparse else None
         self._fork, self._join = torch.cuda.Event(), torch.cuda.Event()
 
-    def append(self, kv_new, pos_first, w_z, bias, cache, window, win_row, stream=None):
-        """kv_new [B, m, D] raw tokens at positions pos_first .. pos_first+m-1 (a
-        complete block): pool it into cache entry pos_first/m and write the last
-        token's window row into window row `win_row`."""
+    def new_state(self, device="cuda"):
+        """Zeroed decode state: (raw_ring [B, m, D], cache [B, n_cap], window [B, n_win])."""
         cfg = self.cfg
-        rb = cache.element_size() * (cache.shape[-1])
-        e = pos_first // cfg.m
-        # one launch: the entry and the last token's window row
-        csa_append(self.p, kv_new, self.B, cfg.m, pos_first, w_z, bias, cache.data_ptr() + e * rb,
-                   self.n_cap, window.data_ptr() + win_row * rb, self.n_win, stream)
+        raw_ring = torch.zeros(self.B, cfg.m, cfg.D, dtype=self.act_dtype, device=device)
+        return raw_ring, cfg.empty_rows(self.B, self.n_cap, device=device), \
+            cfg.empty_rows(self.B, self.n_win, device=device)
 
-    def step(self, kv_new, pos_first, w_z, bias, q, cache, window, win_row, q_pos, win_pos0, sink,
-             q_idx=None, w_idx=None, keys=None):
-        """One decode step on the current stream: append the newest block's entry
-        and window row, then attend.  For CSA the append feeds only the
+    def append(self, kv_tok, pos, w_z, bias, raw_ring, cache, window, stream=None):
+        """kv_tok [B, D]: each sequence's newest raw token, at positions pos [B]."""
+        csa_decode_append(self.p, kv_tok, self.B, pos, raw_ring, w_z, bias, cache, self.n_cap, window,
+                          self.n_win, self.ws, self.ws_bytes, stream)
+
+    def step(self, kv_tok, pos, w_z, bias, raw_ring, q, cache, window, sink, q_idx=None, w_idx=None,
+             keys=None):
+        """One decode step on the current stream: append the newest tokens,
+        then attend at their positions.  For CSA the append feeds only the
         attention, so it runs on a side stream beside the indexer and top-k
-        (whose one CTA per query leaves most SMs free) and the attention waits
-        for both; HCA attends to the new entry, so it appends first."""
+        (whose few CTAs leave most SMs free) and the attention waits for both;
+        HCA attends to the new entries, so it appends first."""
         if not self.cfg.sparse:
-            self.append(kv_new, pos_first, w_z, bias, cache, window, win_row)
-            return self.attend(q, cache, window, q_pos, win_pos0, sink)
+            self.append(kv_tok, pos, w_z, bias, raw_ring, cache, window)
+            return self.attend(q, cache, window, pos, None, sink)
         main = torch.cuda.current_stream()
         self._fork.record(main)
         self._side.wait_event(self._fork)
-        self.append(kv_new, pos_first, w_z, bias, cache, window, win_row, stream=self._side)
+        self.append(kv_tok, pos, w_z, bias, raw_ring, cache, window, stream=self._side)
         self._join.record(self._side)
-        self.index_topk(q_idx, w_idx, keys, q_pos, stream=main)
+        self.index_topk(q_idx, w_idx, keys, pos, stream=main)
         main.wait_event(self._join)
-        return self.attend(q, cache, window, q_pos, win_pos0, sink, stream=main, selected=True)
+        return self.attend(q, cache, window, pos, None, sink, stream=main, selected=True)
 
     def index_topk(self, q_idx, w_idx, keys, q_pos, stream=None):
         cfg = self.cfg
@@ -130,7 +147,8 @@ class DecodeLayer:
     def attend(self, q, cache, window, q_pos, win_pos0, sink, q_idx=None, w_idx=None, keys=None,
                stream=None, selected=False):
         """CSA: index and select (unless `selected`: topk_idx holds this step's
-        selection), then attend; HCA: attend to every complete block."""
+        selection), then attend; HCA: attend to every complete block.
+        win_pos0 None: the window is a ring (position p at row p mod n_win)."""
         cfg = self.cfg
         if cfg.sparse:
             if not selected:

@@ -27,6 +27,7 @@
  *
  * Parity pins for every function live in tests/test_oracle_*.py.
  */
+#include <limits.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -387,11 +388,25 @@ uint8_t oracle_e2m1_encode(double x) {
 
 /* Keys x [n, dI] (dI a multiple of 32) -> codes [n, dI/2] (dim 2j in the low
  * nibble of byte j, dim 2j+1 in the high nibble) and scale bytes [n, dI/32]
- * (block scale 2^(byte - 127)). */
+ * (block scale 2^(byte - 127)).
+ * Block j of a key: amax = its largest magnitude; exponent e_j =
+ * floor(log2 amax) - 2 (the block's largest value lands in [4, 8)), 0 for an
+ * all-zero block.  The pages convert FP4 keys to FP8 (E4M3) without loss as
+ * long as the ratio of a key's largest to smallest sub-block scale stays
+ * within a threshold [gitcode §3.2]; with one E4M3 scale per key, set six
+ * binades below the key's largest block scale E (its largest value 6 then
+ * lands on 6 * 2^6 = 384 <= 448), a block converts exactly when its smallest
+ * step 0.5 * 2^(e_j - E + 6) is still an E4M3 value (>= 2^-9), i.e.
+ * e_j >= E - 14.  The format keeps every key within that ratio: a nonzero
+ * block's exponent below E - 14 is raised to E - 14 (its values then round
+ * on that coarser grid). */
 void oracle_pack_idx_keys_fp4(const float* x, int64_t n, int dI, uint8_t* codes, uint8_t* scales) {
     const int nb = dI / 32;
+    int* ex = (int*)malloc(sizeof(int) * (size_t)nb);
+    int* nz = (int*)malloc(sizeof(int) * (size_t)nb);
     for (int64_t b = 0; b < n; b++) {
         const float* row = x + b * dI;
+        int emax = INT_MIN;
         for (int j = 0; j < nb; j++) {
             double amax = 0.0;
             for (int d = 0; d < 32; d++) {
@@ -399,13 +414,20 @@ void oracle_pack_idx_keys_fp4(const float* x, int64_t n, int dI, uint8_t* codes,
                 if (a > amax) amax = a;
             }
             int e = 0;
-            if (amax > 0.0) {
-                int ex;
-                frexp(amax, &ex); /* amax = f * 2^ex, f in [0.5, 1): floor(log2 amax) = ex - 1 */
-                e = ex - 1 - 2;
-                if (e < -127) e = -127;
-                if (e > 127) e = 127;
+            nz[j] = amax > 0.0;
+            if (nz[j]) {
+                int ef;
+                frexp(amax, &ef); /* amax = f * 2^ef, f in [0.5, 1): floor(log2 amax) = ef - 1 */
+                e = ef - 1 - 2;
+                if (e > emax) emax = e;
             }
+            ex[j] = e;
+        }
+        for (int j = 0; j < nb; j++) {
+            int e = ex[j];
+            if (nz[j] && e < emax - 14) e = emax - 14; /* the conversion threshold */
+            if (e < -127) e = -127;
+            if (e > 127) e = 127;
             scales[b * nb + j] = (uint8_t)(e + 127);
             for (int d = 0; d < 32; d++) {
                 const int dim = j * 32 + d;
@@ -418,6 +440,8 @@ void oracle_pack_idx_keys_fp4(const float* x, int64_t n, int dI, uint8_t* codes,
             }
         }
     }
+    free(ex);
+    free(nz);
 }
 
 /* Indexer score with FP4 keys (above) and each query head quantised to E4M3

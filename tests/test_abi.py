@@ -254,3 +254,37 @@ def test_noalloc_refuses_an_oversized_selection_before_any_launch(L):
         L.csa_index_topk_noalloc(p, FAKE, FAKE, 64, 128, FAKE, 4194304, 1, 1, FAKE, FAKE, None, None)
     assert ei.value.status == 2 and "shared memory" in L.csa_last_error()
     assert L.csa_launch_count() == n0
+
+
+def test_ring_window_needs_room_for_the_window(L):
+    # win_pos0 NULL: the window buffer is a ring and must hold W rows
+    p = L.params(512, 4, topk=64, window=128)
+    n0 = L.csa_launch_count()
+    assert _status_of(L.csa_attend, **_attend_args(L, p, win_pos0=None, n_win=100)) == 1
+    assert "ring" in L.csa_last_error()
+    assert L.csa_launch_count() == n0
+
+
+def test_workspace_covers_both_window_layouts(L):
+    # one workspace size serves the linear and the ring window (a ring of more
+    # than W rows is read in more tiles)
+    p = L.params(512, 4, topk=1024, window=128)
+    a = L.csa_workspace_bytes(p, L.OP_ATTEND, 2, 2, 64, 64, 4096, 128)
+    b = L.csa_workspace_bytes(p, L.OP_ATTEND, 2, 2, 64, 64, 4096, 512)
+    assert b >= a > 0
+
+
+def test_decode_append_validation(L):
+    p = L.params(512, 4)
+    base = dict(p=p, kv_tok=FAKE, B=2, pos=FAKE, raw_ring=FAKE, w_z=FAKE, bias=FAKE, cache=FAKE,
+                n_cap=100, window=FAKE, n_win=128, ws=FAKE, ws_bytes=256)
+    n0 = L.csa_launch_count()
+    assert _status_of(L.csa_decode_append, **dict(base, pos=None)) == 1
+    assert _status_of(L.csa_decode_append, **dict(base, raw_ring=None)) == 1   # m > 1 needs the ring
+    assert _status_of(L.csa_decode_append, **dict(base, kv_tok=FAKE + 4)) == 1
+    assert _status_of(L.csa_decode_append, **dict(base, ws_bytes=100)) == 4
+    assert _status_of(L.csa_decode_append, **dict(base, B=-1)) == 1
+    # a block too large to stage: 1024 fp32 tokens of 512 dims
+    big = L.params(512, 1024, act="f32", kv="f32")
+    assert _status_of(L.csa_decode_append, **dict(base, p=big)) == 2
+    assert L.csa_launch_count() == n0

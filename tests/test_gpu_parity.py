@@ -221,29 +221,92 @@ def test_append_matches_two_compress_calls(m, kv):
     assert outs[0][0][:, e].abs().sum() > 0 and outs[0][1][:, wr].abs().sum() > 0
 
 
+@pytest.mark.parametrize("m,kv", [(4, "bf16"), (128, "bf16"), (4, "fp8m"), (128, "fp8m")])
+def test_decode_append_matches_the_fused_append(m, kv):
+    """csa_decode_append over a ragged batch: sequences whose newest token
+    completes a block get the same entry and window row bits as csa_append
+    over that block; the others get only their window row (and raw-ring slot),
+    their cache entries untouched."""
+    import long_context_compressed_17_b300 as L
+    from long_context_compressed_17_b300.pipeline import DecodeLayer, LayerConfig
+    B, D, n_cap, n_win = 4, 512, 40, 128
+    cfg = LayerConfig(D=D, H=64, m=m, kv=kv)
+    g = torch.Generator(device="cpu").manual_seed(31 + m)
+    blk = (torch.randn(B, m, D, generator=g) * 2).to(torch.bfloat16).cuda()
+    w_z = (torch.randn(D, generator=g) * 0.02).cuda()
+    bias = (torch.randn(m, generator=g) * 0.1).cuda()
+    # sequences 0 and 2 complete block 11 / 30; 1 and 3 stop inside a block
+    pos = torch.tensor([12 * m - 1, 7 * m + 2, 31 * m - 1, 3 * m], dtype=torch.int64)
+    layer = DecodeLayer(cfg, B, n_cap, n_win)
+    raw_ring, cache, window = layer.new_state()
+    for b in range(B):  # the block's tokens before the newest one, in their ring slots
+        p0 = int(pos[b]) - int(pos[b]) % m
+        for t in range(p0, int(pos[b])):
+            raw_ring[b, t % m] = blk[b, t - p0]
+    kv_tok = torch.stack([blk[b, int(pos[b]) % m] for b in range(B)]).contiguous()
+    layer.append(kv_tok, pos.cuda(), w_z, bias, raw_ring, cache, window)
+    torch.cuda.synchronize()
+    L.csa_check_status(layer.ws)
+    rb = cache.shape[-1] * cache.element_size()
+    for b in range(B):
+        t = int(pos[b])
+        assert torch.equal(raw_ring[b, t % m], blk[b, t % m]), "raw ring slot"
+        win_ref = cfg.empty_rows(1, 1)
+        if (t + 1) % m == 0:
+            ent_ref = cfg.empty_rows(1, 1)
+            L.csa_append(cfg.params(), blk[b:b + 1], 1, m, t + 1 - m, w_z, bias, ent_ref, 1, win_ref, 1)
+            torch.cuda.synchronize()
+            assert torch.equal(cache[b, (t + 1) // m - 1].cpu(), ent_ref[0, 0].cpu()), "entry seq %d" % b
+            assert int((cache[b].view(torch.uint8) != 0).any(dim=-1).sum()) == 1
+        else:
+            L.csa_compress(cfg.params(ratio=1), kv_tok[b:b + 1], 1, 1, 1, t, w_z, bias, win_ref, 1)
+            torch.cuda.synchronize()
+            assert not bool((cache[b].view(torch.uint8) != 0).any()), "no entry for an incomplete block"
+        assert torch.equal(window[b, t % n_win].cpu(), win_ref[0, 0].cpu()), "window row seq %d" % b
+    assert rb > 0
+
+
+def test_decode_append_flags_a_position_beyond_the_cache():
+    import long_context_compressed_17_b300 as L
+    from long_context_compressed_17_b300.pipeline import DecodeLayer, LayerConfig
+    cfg = LayerConfig(D=512, H=64, m=4)
+    layer = DecodeLayer(cfg, 2, 8, 128)
+    raw_ring, cache, window = layer.new_state()
+    tok = torch.randn(2, 512, device="cuda").to(torch.bfloat16)
+    pos = torch.tensor([8 * 4 + 3, 5], dtype=torch.int64, device="cuda")  # entry 8 of an 8-entry cache
+    layer.append(tok, pos, torch.zeros(512, device="cuda"), torch.zeros(4, device="cuda"), raw_ring, cache,
+                 window)
+    with pytest.raises(L.CsaError):
+        L.csa_check_status(layer.ws)
+    assert L.csa_last_device_bits() & 0x4
+    assert not bool((cache.view(torch.uint8) != 0).any())
+    assert bool((window[1, 5].view(torch.uint8) != 0).any())  # the other sequence proceeds
+
+
 @pytest.mark.parametrize("kv", ["bf16", "fp8m"])
 def test_decode_step_with_side_stream_append_matches_sequential(kv):
     """DecodeLayer.step runs the CSA append on a side stream beside the
     indexer and top-k; outputs, cache and window rows equal those of the
-    sequential append-then-attend, bit for bit."""
-    from long_context_compressed_17_b300.pipeline import DecodeLayer
-    w = SMALL_CSA.replace(name="csa_step_overlap", B=4, L_per_seq=(8192,) * 4, kv_fmt=kv)
+    sequential append-then-attend, bit for bit (a ragged batch, two of whose
+    sequences complete a block)."""
+    from long_context_compressed_17_b300.pipeline import DecodeLayer, ring_order
+    w = SMALL_CSA.replace(name="csa_step_overlap", B=4, L_per_seq=(8192, 8191, 4096, 3001), kv_fmt=kv)
     inp = _to_cuda(workloads.generate(w))
     cfg = H.cfg_of(w)
-    Lb = w.lengths[0]
-    win_row = (Lb - 1) - int(inp["win_pos0"][0])
+    lens = torch.tensor(w.lengths, dtype=torch.int64)
+    kv_tok = inp["kv_new"][:, w.m - 1].contiguous()
     res = []
     for overlapped in (False, True):
         cache = H.gpu_pack(w, inp["cache"])
-        window = H.gpu_pack(w, inp["window"])
+        window = ring_order(H.gpu_pack(w, inp["window"]), inp["win_pos0"].cpu(), w.W)
+        raw_ring = ring_order(inp["kv_new"], (lens - w.m).tolist(), w.m)
         layer = DecodeLayer(cfg, w.B, w.n_cap, w.W)
-        args = (inp["kv_new"], Lb - w.m, inp["w_z"], inp["bias"])
         if overlapped:
-            out, lse = layer.step(*args, inp["q"], cache, window, win_row, inp["q_pos"], inp["win_pos0"],
-                                  inp["sink"], q_idx=inp["q_idx"], w_idx=inp["w_idx"], keys=inp["keys"])
+            out, lse = layer.step(kv_tok, inp["q_pos"], inp["w_z"], inp["bias"], raw_ring, inp["q"], cache,
+                                  window, inp["sink"], q_idx=inp["q_idx"], w_idx=inp["w_idx"], keys=inp["keys"])
         else:
-            layer.append(*args, cache, window, win_row)
-            out, lse = layer.attend(inp["q"], cache, window, inp["q_pos"], inp["win_pos0"], inp["sink"],
+            layer.append(kv_tok, inp["q_pos"], inp["w_z"], inp["bias"], raw_ring, cache, window)
+            out, lse = layer.attend(inp["q"], cache, window, inp["q_pos"], None, inp["sink"],
                                     q_idx=inp["q_idx"], w_idx=inp["w_idx"], keys=inp["keys"])
         torch.cuda.synchronize()
         import long_context_compressed_17_b300 as L

@@ -166,3 +166,80 @@ def test_fp4_to_e4m3_is_lossless_while_block_scales_stay_within_eight_binades():
     y[:, 96:] *= 2.0 ** -14
     c4, sc4 = oracle.pack_idx_keys_fp4(y)
     assert not _to_e4m3_per_key(oracle.decode_idx_keys_fp4(c4, sc4))[2]
+
+
+def _block_exponents(x, dI=128):
+    """floor(log2 amax) - 2 per 32-dim block (None for an all-zero block)."""
+    out = []
+    for j in range(dI // 32):
+        amax = float(np.abs(x[j * 32:(j + 1) * 32]).max())
+        out.append(None if amax == 0.0 else math.floor(math.log2(amax)) - 2)
+    return out
+
+
+def test_packer_keeps_block_scales_within_fourteen_binades_of_the_largest():
+    """A block far below the key's largest gets the exponent E - 14, and its
+    codes are the half-even roundings of its values on that coarser grid."""
+    rng = np.random.default_rng(66)
+    n, dI = 30, 128
+    x = rng.standard_normal((n, dI)).astype(np.float32)
+    drop = rng.integers(15, 30, size=n)           # binades block 3 sits below the others
+    x[:, 96:] *= np.exp2(-drop)[:, None].astype(np.float32)
+    x[5, 64:96] = 0.0                              # an all-zero block keeps exponent 0
+    codes, scales = oracle.pack_idx_keys_fp4(x)
+    for b in range(n):
+        ref = _block_exponents(x[b])
+        E = max(e for e in ref if e is not None)
+        es = scales[b].astype(int) - 127
+        for j, e in enumerate(ref):
+            want = 0 if e is None else max(e, E - 14)
+            assert es[j] == want, (b, j, es[j], want)
+        assert es[3] == E - 14  # the dropped block was raised
+        for d in range(96, 128):
+            c = (int(codes[b, d // 2]) >> 4) if d & 1 else (int(codes[b, d // 2]) & 15)
+            got = oracle.e2m1_decode(c)
+            want = _half_even_reference(float(x[b, d]) / 2.0 ** es[3])
+            assert got == want or (got == 0.0 and want == 0.0), (b, d)
+
+
+def _to_e4m3_centred(codes4, scales4):
+    """The conversion the FP4 indexer kernel makes: every key's FP4 values to
+    E4M3 codes with one power-of-two scale per key, 2^(E - 6) for E the
+    largest exponent of its nonzero blocks (through torch's cast); returns
+    codes, scales and whether every value survived."""
+    dec = oracle.decode_idx_keys_fp4(codes4, scales4)
+    n, dI = dec.shape
+    codes = np.empty((n, dI), dtype=np.uint8)
+    scales = np.empty(n, dtype=np.float32)
+    exact = True
+    es = scales4.astype(np.int64) - 127
+    for b in range(n):
+        nz = [j for j in range(dI // 32) if np.any(dec[b, j * 32:(j + 1) * 32] != 0.0)]
+        E = max(es[b, j] for j in nz) if nz else 6
+        S = 2.0 ** (E - 6)
+        c = torch.from_numpy((dec[b] / S).astype(np.float32)).to(torch.float8_e4m3fn)
+        codes[b] = c.view(torch.uint8).numpy()
+        scales[b] = S
+        exact &= bool(np.array_equal(c.to(torch.float32).numpy().astype(np.float64) * S, dec[b]))
+    return codes, scales, exact
+
+
+def test_every_packed_key_converts_to_e4m3_without_loss():
+    """Keys with sub-block scale spreads from 0 to 30 binades (the packer
+    keeps them within 14): the centred per-key E4M3 conversion is exact, and
+    the FP8 oracle over the converted keys gives the FP4 oracle's scores bit
+    for bit."""
+    rng = np.random.default_rng(67)
+    HI, dI, n = 8, 128, 60
+    spread = rng.integers(0, 31, size=(n, dI // 32))
+    x = (rng.standard_normal((n, dI)) * np.repeat(np.exp2(-spread.astype(np.float64)), 32, axis=1)).astype(np.float32)
+    x[7, :32] = 0.0
+    codes4, scales4 = oracle.pack_idx_keys_fp4(x)
+    es = scales4.astype(np.int64) - 127
+    assert np.all(es.max(axis=1) - es.min(axis=1) <= 14 + 127)  # zero blocks keep exponent 0
+    codes8, scales8, exact = _to_e4m3_centred(codes4, scales4)
+    assert exact
+    q = rng.standard_normal((HI, dI)).astype(np.float32)
+    w = rng.uniform(0, 1, size=HI)
+    assert np.array_equal(oracle.index_scores_fp4(q, w, codes4, scales4),
+                          oracle.index_scores_fp8(q, w, codes8, scales8))

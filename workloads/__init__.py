@@ -48,7 +48,7 @@ class Workload:
     rope_base: float = 10000.0
     eps: float = 1e-6
     softmax_scale: float = 0.0  # <= 0: 1/sqrt(D)
-    idx_fmt: str = "bf16"  # "bf16" | "fp8": indexer keys stored as E4M3 codes + a scale per row
+    idx_fmt: str = "bf16"  # "bf16" | "fp8": E4M3 codes + a scale per key | "fp4": E2M1 codes + 4 block exponents
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -92,7 +92,9 @@ FULL = [CSA_PREFILL_F32, CSA_DECODE_128K, HCA_DECODE_1M, CSA_CHUNKED_PREFILL, CS
 # The headline decode shape with the indexer keys in E4M3 (the keys are the
 # same N(0,1) draws; each side quantises them itself).
 CSA_DECODE_128K_FP8IDX = CSA_DECODE_128K.replace(name="csa_decode_fp8idx_b32_128k", idx_fmt="fp8")
-EXTRA = [CSA_DECODE_128K_FP8IDX]
+# ... and with FP4 indexer keys (E2M1 codes, one power-of-two scale per 32 dims).
+CSA_DECODE_128K_FP4IDX = CSA_DECODE_128K.replace(name="csa_decode_fp4idx_b32_128k", idx_fmt="fp4")
+EXTRA = [CSA_DECODE_128K_FP8IDX, CSA_DECODE_128K_FP4IDX]
 BY_NAME = {w.name: w for w in FULL + EXTRA}
 
 
