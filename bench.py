@@ -213,6 +213,15 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ work units
+def out_proj_work(w: workloads.Workload, G: int, d_g: int):
+    """The grouped projection: decode streams its weights (HBM), prefill is a
+    dense contraction (2 * Q * G * d_g * K flops)."""
+    K = w.H // G * w.D
+    if w.kind in ("csa_decode", "hca_decode"):
+        return {"bound": "hbm", "bytes": G * d_g * K * 2 + w.Q * w.H * w.D * 2 + w.Q * G * d_g * 2}
+    return {"bound": "tensor", "flops": 2 * w.Q * G * d_g * K}
+
+
 def algorithmic(w: workloads.Workload, row_bytes: int):
     """Algorithmic work of every kernel segment of a step (bytes for the
     HBM-bound ones, flops for the tensor- or ALU-bound ones) and of the step.
@@ -268,7 +277,10 @@ def algorithmic(w: workloads.Workload, row_bytes: int):
 class GpuStep:
     """Buffers and CUDA graphs of one step, split as [before | dominant | after]."""
 
-    def __init__(self, w: workloads.Workload, batch_invariant: bool = False):
+    # grouped output projection (when timed): G groups of H/G heads, d_g outputs a group
+    PROJ_G, PROJ_DG = 8, 512
+
+    def __init__(self, w: workloads.Workload, batch_invariant: bool = False, out_proj: bool = False):
         import long_context_compressed_17_b300 as L
         from long_context_compressed_17_b300.pipeline import DecodeLayer, LayerConfig, PrefillLayer, ring_order
         self.L, self.w = L, w
@@ -327,7 +339,15 @@ class GpuStep:
                     self.idx_ws_bytes = 256 + (w.B * 64 * 128 + 255) // 256 * 256 + (w.B * 64 * 4 + 255) // 256 * 256
                     self.idx_ws = L.workspace(self.idx_ws_bytes)
                     torch.cuda.synchronize()
-        else:
+        self.out_proj = out_proj
+        if out_proj:  # synthetic weights, N(0, 1/K) so that the outputs are of order 1
+            K = w.H // self.PROJ_G * w.D
+            gen = torch.Generator(device="cuda").manual_seed(1000 + w.seed)
+            self.proj_w = (torch.randn(self.PROJ_G, self.PROJ_DG, K, device="cuda", generator=gen) /
+                           K ** 0.5).to(torch.bfloat16)
+            self.proj_out = torch.empty(w.Q, self.PROJ_G * self.PROJ_DG, dtype=torch.bfloat16, device="cuda")
+            self.proj_ws = L.workspace(256)
+        if w.kind == "csa_prefill":
             self.step_inputs = {k: inp[k] for k in ("q", "kv_raw", "q_pos", "q_idx", "w_idx")}
             self.layer = PrefillLayer(cfg, w.T_cached, w.T_new)
             if w.T_cached:
@@ -346,11 +366,20 @@ class GpuStep:
         own CUDA graph so that events bracket it."""
         w = self.w
         if w.kind == "hca_decode":
-            return [("append", self.append), ("attention", self.attention)]
-        if w.kind == "csa_decode":
-            return [("indexer", self.indexer), ("topk", self.topk), ("attention", self.attention)]
-        return [("compress", self.compress), ("indexer", self.indexer), ("topk", self.topk),
-                ("attention", self.attention)]
+            segs = [("append", self.append), ("attention", self.attention)]
+        elif w.kind == "csa_decode":
+            segs = [("indexer", self.indexer), ("topk", self.topk), ("attention", self.attention)]
+        else:
+            segs = [("compress", self.compress), ("indexer", self.indexer), ("topk", self.topk),
+                    ("attention", self.attention)]
+        if self.out_proj:
+            segs.append(("out_proj", self.project))
+        return segs
+
+    def project(self):
+        w, lay = self.w, self.layer
+        self.L.csa_grouped_out_proj(lay.out, w.Q, w.H, w.D, self.PROJ_G, self.proj_w, self.PROJ_DG, self.proj_out,
+                                    self.proj_ws, self.proj_ws.numel())
 
     def append(self, stream=None):
         inp = self.inp
@@ -473,8 +502,12 @@ def run_gpu(args, rank, world):
     import long_context_compressed_17_b300 as L
     w = workloads.BY_NAME[args.workload]
     peaks = measured_peaks()
-    st = GpuStep(w, batch_invariant=args.batch_invariant)
+    st = GpuStep(w, batch_invariant=args.batch_invariant, out_proj=args.with_out_proj)
     segs, step_bytes = algorithmic(w, st.row_bytes)
+    if args.with_out_proj:
+        segs["out_proj"] = out_proj_work(w, st.PROJ_G, st.PROJ_DG)
+        if step_bytes is not None and segs["out_proj"]["bound"] == "hbm":
+            step_bytes += segs["out_proj"]["bytes"]
     for _ in range(2):  # untimed eager passes: kernel attributes, first-launch costs
         st.run_eager()
     torch.cuda.synchronize()
@@ -560,7 +593,8 @@ def run_gpu(args, rank, world):
                      ("each kernel segment captured as a CUDA graph, CUDA events between the replays; "
                       "ms_per_step is the median over the timed steps"),
            "parallelism": "replicas" if world > 1 else "single GPU",
-           "batch_invariant": bool(args.batch_invariant)}
+           "batch_invariant": bool(args.batch_invariant),
+           "out_proj": ({"groups": st.PROJ_G, "outputs_per_group": st.PROJ_DG} if args.with_out_proj else None)}
     cfg.update(step_info)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -809,6 +843,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch-invariant", action="store_true",
                     help="attention with fixed splits: each query's result independent of the batch")
+    ap.add_argument("--with-out-proj", action="store_true",
+                    help="append the grouped output projection (8 groups of 8 heads, 512 outputs each) to the step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

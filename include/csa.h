@@ -245,7 +245,8 @@ csa_status csa_index_topk_fp8(const csa_params* p, const void* q_idx, const floa
  * key (bf16 keys take 256, E4M3 keys 132).
  * Storage: per sequence, ceil(n_cap / 128) tiles of csa_index_keys_fp4_bytes(128)
  * = 8704 bytes, tile t holding keys 128t .. 128t+127: their 64-byte code rows,
- * then their 4 exponent bytes each (key slots past n_cap are zero).
+ * then their 4 exponent bytes each (key slots past n_cap hold an all-zero
+ * key: codes 0, exponent bytes 127).
  * csa_index_keys_pack_fp4 writes that form from keys [B, n_cap, 128] in
  * p->act_format; pack: B * csa_index_keys_fp4_bytes(n_cap) bytes (device).
  * csa_index_topk_fp4 / csa_index_score_fp4 are csa_index_topk_fp8 /
@@ -349,6 +350,24 @@ csa_status hca_attend(const csa_params* p, const void* q, int32_t H, int32_t B, 
                       const int64_t* q_pos, const void* cache, int64_t n_cap, const void* window,
                       int64_t n_win, const int64_t* win_pos0, const float* sink, void* out,
                       float* lse, void* ws, size_t ws_bytes, csa_stream_t stream);
+
+/* Grouped output projection [peacm §三.2 CSA "Step 4: Grouped Output
+ * Projection" (the heads of dim 512 are projected in groups, cutting the
+ * cost)].  The H heads form G consecutive groups of H/G; group g's
+ * concatenated head outputs x_g (K = H/G * D values a query) are projected by
+ * its own matrix W_g [d_g, K]:
+ *   out[q, g*d_g + n] = sum_k x_g[q, k] * W_g[n, k]
+ * (block-diagonal: G times cheaper than one dense projection of the same
+ * width), in bf16 on the tensor cores with float32 accumulation, rounded to
+ * bf16 once.
+ *   o:   [Q, H, D] bf16 (e.g. csa_attend's out)
+ *   w:   [G, d_g, K] bf16 (row n of W_g: output n's weights over K)
+ *   out: [Q, G * d_g] bf16
+ *   ws:  at least 256 bytes (status word: CSA_DEV_TIMEOUT on an expired wait)
+ * Requires H % G == 0, K a multiple of 64, d_g a positive multiple of 64;
+ * other shapes return CSA_ERR_UNSUPPORTED. */
+csa_status csa_grouped_out_proj(const void* o, int32_t Q, int32_t H, int32_t D, int32_t G, const void* w,
+                                int32_t d_g, void* out, void* ws, size_t ws_bytes, csa_stream_t stream);
 
 /* Workspace */
 typedef enum {

@@ -442,6 +442,22 @@ csa_status csa_topk_select(const csa_params* p, float* scores, int64_t ld_scores
     return e == cudaSuccess ? CSA_OK : cuda_fail(e, "csa_topk_select");
 }
 
+csa_status csa_grouped_out_proj(const void* o, int32_t Q, int32_t H, int32_t D, int32_t G, const void* w,
+                                int32_t d_g, void* out, void* ws, size_t ws_bytes, csa_stream_t stream) {
+    if (Q < 0 || Q > (1 << 24) || H < 1 || D < 1 || G < 1 || d_g < 1)
+        return fail(CSA_ERR_INVALID_ARG, "csa_grouped_out_proj: bad sizes");
+    if (!out_proj_supported(H, D, G, d_g))
+        return fail(CSA_ERR_UNSUPPORTED, "csa_grouped_out_proj: needs H %% G == 0, H/G*D and d_g multiples of 64");
+    if (Q == 0) return CSA_OK;
+    CHECK(check_ptr(o, "o"));
+    CHECK(check_ptr(w, "w"));
+    CHECK(check_ptr(out, "out"));
+    CHECK(check_ptr(ws, "ws"));
+    if (ws_bytes < kStatusWordBytes) return fail(CSA_ERR_WORKSPACE, "workspace smaller than 256 bytes");
+    cudaError_t e = launch_out_proj(o, Q, H, D, G, w, d_g, out, reinterpret_cast<uint32_t*>(ws), (cudaStream_t)stream);
+    return e == cudaSuccess ? CSA_OK : cuda_fail(e, "csa_grouped_out_proj");
+}
+
 uint64_t csa_launch_count(void) { return (uint64_t)g_launches.load(); }
 
 csa_status csa_test_withhold_indexer_loads(int32_t on) {

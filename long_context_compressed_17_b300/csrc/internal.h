@@ -124,6 +124,11 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
                           float* lse, uint8_t* ws, uint32_t* status, cudaStream_t st);
 
 // SM count of the current device (cached per device).
+// Grouped output projection (k_out_proj.cu).
+bool out_proj_supported(int H, int D, int G, int d_g);
+cudaError_t launch_out_proj(const void* o, int Q, int H, int D, int G, const void* w, int d_g, void* out,
+                            uint32_t* status, cudaStream_t st);
+
 int num_sms();
 
 // Raise a kernel's dynamic shared memory limit to at least `bytes` on the

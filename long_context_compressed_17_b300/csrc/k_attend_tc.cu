@@ -32,12 +32,16 @@
 // by more than 2^8; O^T (in TMEM) and the partial sums are then rescaled in
 // place.
 //
-// Warp roles (20 warps): warp 0 orders every use of a stage, loads TMA tiles
-// (consecutive rows) and hands gathered tiles to warps 18..19, which fetch the
-// selected rows with TMA gather4 (two warps issue them twice as fast as one);
-// warp 1 issues the MMAs in a dynamic order (PV of a tile as soon as its P is
-// written, QK of the next as soon as its stage has landed); warps 2..17
-// prepare q', run the softmax and the epilogue.  FP8 rows are first
+// Warp roles (at most 20 warps, five per scheduler, so that each thread
+// keeps 96 registers): warp 0 orders every use of a stage and loads TMA
+// tiles (consecutive rows); warps 2..17 prepare q', run the softmax and the
+// epilogue.  Where every tile is a TMA tile (dense lists, pre-gathered rows)
+// warp 1 issues the QK products (a tile's as soon as its stage has landed
+// and its S^T buffer is free) and warp 18 the PV products (a tile's as soon
+// as its P is written), so that neither waits behind the other's issue.
+// Where selected rows are gathered, warp 1 issues both products and warps
+// 18..19 fetch the rows with TMA gather4 (gather issue, not MMA issue,
+// bounds those tiles).  FP8 rows are first
 // dequantised to bf16 in the workspace (dequant_gather_kernel or
 // dequant_rows_kernel).  Every wait is bounded; on a timeout the kernel sets
 // CSA_DEV_TIMEOUT, every role leaves its loop, outstanding copies and MMAs are
@@ -69,8 +73,6 @@ constexpr uint32_t kPBytes = kRows * kH * 2;        // 64 rows x 64 heads
 constexpr size_t kSmem = 1024 + kStages * kStageBytes + kQBytes + 2 * kPBytes;
 constexpr int kSoftWarps = 16;                      // 4 TMEM lane quarters x 4 head quarters
 constexpr int kSoftThreads = kSoftWarps * 32;
-constexpr int kLoadWarps = 2;                       // warps issuing TMA gathers (and warp 0)
-constexpr int kThreads = 64 + kSoftThreads + 32 * kLoadWarps;
 constexpr int kHW = kH / 4;                         // heads per softmax warp
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // S^T buffers: 2 x 64 columns
@@ -166,12 +168,19 @@ __device__ __forceinline__ int64_t ring_pos(int64_t i, int64_t r, int64_t n_win)
     return i - (((i - r) % n_win) + n_win) % n_win;
 }
 
-// Boxes of a gathered tile fetched by the producer warp; the gather warps
-// share the others.  TMA gathers issued from several warps proceed in
-// parallel, so the 128 gather4 copies of a tile are spread over warps (two
-// gather warps saturate it: a third, the producer, gains nothing).
-constexpr int kProducerBoxes = 0;
-constexpr int kLoaderBoxes = (8 - kProducerBoxes) / kLoadWarps;
+// Warp roles of the two layouts.  Split (tiles loaded by TMA only): warp 1
+// issues the QK products and warp 18 the PV products.  Otherwise (gathered
+// tiles): warp 1 issues both and warps 18..19 fetch the selected rows with
+// TMA gather4, each four of the eight 64-dim boxes of every row (TMA gathers
+// issued from several warps proceed in parallel; two warps issue them twice
+// as fast as one).
+template <bool kSplit>
+struct Roles {
+    static constexpr int kLoadWarps = kSplit ? 0 : 2;
+    static constexpr int kPvWarp = kSplit ? 2 + kSoftWarps : 1;
+    static constexpr int kThreads = 32 * (2 + kSoftWarps + kLoadWarps + (kSplit ? 1 : 0));
+    static constexpr int kLoaderBoxes = kLoadWarps > 0 ? 8 / kLoadWarps : 0;
+};
 
 // Whether tile lt is copied row by row from the selected cache rows (by
 // gather4) rather than loaded as a TMA tile.
@@ -391,7 +400,8 @@ __global__ void __launch_bounds__(kDeqThreads) dequant_gather_kernel(const DeqGa
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kSplit>
+__global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tm_sel, const __grid_constant__ CUtensorMap tm_win,
                      const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ AttTcArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -402,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages], go[kStages];
     __shared__ __align__(8) uint64_t s_full[2], p_full[2];
-    __shared__ __align__(8) uint64_t o_full, o_seg, q_full, q_raw, mma_done;
+    __shared__ __align__(8) uint64_t o_full, o_seg, q_full, q_raw, mma_done, pv_done;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_sh;
     __shared__ float red[4][kH];
@@ -410,7 +420,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ float rot_cs[64];
     volatile int* abort_flag = &abort_sh;
 
+    constexpr int kLoadWarps = Roles<kSplit>::kLoadWarps;
+    constexpr int kPvWarp = Roles<kSplit>::kPvWarp;
+    constexpr int kLoaderBoxes = Roles<kSplit>::kLoaderBoxes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 0) {
+        // the first position and row indices this CTA reads head for L2
+        // during the setup (the loads that wait for them come next)
+        const int64_t g0 = range_begin(a, blockIdx.x);
+        if (g0 < range_begin(a, blockIdx.x + 1)) {
+            const int64_t q0 = g0 / a.T;
+            const int lt0 = (int)(g0 - q0 * a.T);
+            if (lane == 0) prefetch_l2(a.q_pos + q0);
+            const int64_t p = (int64_t)lt0 * kRows + (lane - 1) * 32;  // lanes 1..4: two tiles' indices
+            if (a.topk_idx != nullptr && !a.pre && lane >= 1 && lane <= 4 && lt0 < a.T_sel && p < a.k)
+                prefetch_l2(a.topk_idx + q0 * a.k + p);
+        }
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; s++) {
             tc::mbar_init(&full[s], 1);
@@ -426,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_init(&q_full, 1);
         tc::mbar_init(&q_raw, 1);   // raw q of the CTA's first segment landed in sQ
         tc::mbar_init(&mma_done, 1);
+        tc::mbar_init(&pv_done, 1);
         abort_sh = 0;
         tc::fence_barrier_init();
         tc::fence_proxy_async_smem();
@@ -493,11 +520,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) tc::mbar_arrive_expect_tx(&full[st], kStageBytes);
             if (is_gathered(a, lt)) {
                 if (lane == 0) tc::mbar_arrive(&go[st]);  // the gather warps join in
-                if (kProducerBoxes > 0) {
-                    int rows[4];
-                    gather_rows(a, qi, inf, lt, lane, rows);
-                    gather_boxes(&tm_sel, &full[st], sE + st * kStageBytes, rows, 0, kProducerBoxes, lane);
-                }
             } else {
                 uint8_t* dst = sE + st * kStageBytes;
                 __syncwarp();
@@ -520,111 +542,207 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!tc::mbar_drain(&full[st], (fills[st] - 1u) & 1u)) atomicOr(a.status, CSA_DEV_TIMEOUT);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issue
-        // Issue order is dynamic: the PV product of tile t as soon as its P is
-        // written, the QK product of tile t+1 as soon as its stage has landed
-        // and the S^T buffer it reuses is free (PV of tile t-1 issued).
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kRows, kH, 0, 0);
-            constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, kH, 1, 1);
-            const uint32_t sE0 = tc::smem_u32(sE), sQ0 = tc::smem_u32(sQ), sP0 = tc::smem_u32(sP);
-            uint32_t t_qk = 0, t_pv = 0, nq = 0;
-            bool first_of[4], last_of[4];  // segment flags of tiles t_pv .. t_qk-1 (at most 2)
-            // QK cursor over this CTA's live tiles
-            int64_t g = g_begin;
-            int64_t cur_q = -1, cur_end = g_begin, q_in = -1;  // q_in: query whose q' is in sQ
-            QueryInfo inf{};
-            int lt_last = -1;
-            bool at_seg_start = true;
-            auto advance = [&]() -> bool {  // move g to the next live tile; false at the end
-                for (; g < g_end; ++g) {
-                    const int64_t qi = g / a.T;
-                    if (g >= cur_end) {
-                        cur_q = qi;
-                        inf = query_info(a, qi);
-                        cur_end = seg_end_of(a, g, g_end);
-                        lt_last = last_live(a, inf, (int)(g - qi * a.T), (int)(cur_end - qi * a.T));
-                        at_seg_start = true;
-                    }
-                    if (tile_live(a, inf, (int)(g - qi * a.T))) return true;
-                }
-                return false;
-            };
-            bool more = advance();
-            uint64_t idle_since = 0;
-            while (more || t_pv < t_qk) {
-                bool progress = false;
-                if (t_pv < t_qk) {
-                    const int b = t_pv & 1;
-                    if (tc::mbar_test_wait(&p_full[b], (t_pv >> 1) & 1u)) {
-                        tc::fence_after_sync();
-                        const uint32_t stage = sE0 + b * kStageBytes;
-                        const uint32_t pb = sP0 + b * kPBytes;
-                        const bool first = first_of[t_pv & 3];
-#pragma unroll
-                        for (int c = 0; c < 4; c++) {
-#pragma unroll
-                            for (int kk = 0; kk < kRows / 16; kk++) {
-                                const uint64_t ad = tc::sdesc_sw128(stage + 2 * c * kBoxBytes + kk * 2048, kBoxBytes, 1024);
-                                const uint64_t bd = tc::sdesc_sw128(pb + kk * 2048, kBoxBytes, 1024);
-                                tc::mma_bf16_ss(tmem + kColO + 64 * c, ad, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
-                            }
+    } else if (warp == 1 || warp == kPvWarp) {
+        if constexpr (kSplit) {
+            // ------------------------------------------------------------ MMA issue
+            // Two issuing threads, so that a PV product never waits behind the
+            // issue of a QK product (one thread issues an MMA every ~85 cycles while
+            // the softmax warps share its scheduler): warp 1 issues the QK product
+            // of every tile as soon as its stage has landed and the S^T buffer it
+            // reuses is free (the softmax of the tile two before has read it);
+            // warp kPvWarp issues the PV product of every tile as soon as its P is
+            // written.  The QK product of tile t+2 cannot start before the PV
+            // product of tile t has freed its stage, so neither thread can see a
+            // barrier phase of the other's overtaken.  Descriptors are built once
+            // per operand and advanced by constant offsets of the 128-byte-swizzled
+            // boxes (the start-address field never carries: shared addresses stay
+            // below 2^18).
+            if (lane == 0) {
+                const bool qk_role = warp == 1;
+                constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kRows, kH, 0, 0);
+                constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, kH, 1, 1);
+                const uint32_t sE0 = tc::smem_u32(sE), sQ0 = tc::smem_u32(sQ), sP0 = tc::smem_u32(sP);
+                const uint64_t dq0 = tc::sdesc_sw128(sQ0, 16, 1024);
+                uint32_t t = 0, nq = 0;
+                // cursor over this CTA's live tiles
+                int64_t g = g_begin;
+                int64_t cur_q = -1, cur_end = g_begin, q_in = -1;  // q_in: query whose q' is in sQ
+                QueryInfo inf{};
+                int lt_last = -1;
+                bool at_seg_start = true;
+                auto advance = [&]() -> bool {  // move g to the next live tile; false at the end
+                    for (; g < g_end; ++g) {
+                        const int64_t qi = g / a.T;
+                        if (g >= cur_end) {
+                            cur_q = qi;
+                            inf = query_info(a, qi);
+                            cur_end = seg_end_of(a, g, g_end);
+                            lt_last = last_live(a, inf, (int)(g - qi * a.T), (int)(cur_end - qi * a.T));
+                            at_seg_start = true;
                         }
-                        tc::mma_commit(&empty[b]);
-                        tc::mma_commit(&o_full);
-                        if (last_of[t_pv & 3]) tc::mma_commit(&o_seg);
-                        ++t_pv;
-                        progress = true;
+                        if (tile_live(a, inf, (int)(g - qi * a.T))) return true;
                     }
-                }
-                if (more && t_pv + 1 >= t_qk) {  // S^T buffer of tile t_qk is free
-                    const int b = t_qk & 1;
-                    // q' is prepared once per query: a later split of the same
-                    // query in this CTA reuses it
-                    const bool need_q = at_seg_start && cur_q != q_in;
-                    bool ready = !need_q || tc::mbar_test_wait(&q_full, nq & 1u);
-                    if (ready) ready = tc::mbar_test_wait(&full[b], (t_qk >> 1) & 1u);
-                    if (ready) {
+                    return false;
+                };
+                while (advance()) {
+                    const int b = t & 1;
+                    const uint32_t stage = sE0 + b * kStageBytes;
+                    if (qk_role) {
+                        // the S^T buffer of tile t: the softmax of tile t - 2 has read it
+                        if (t >= 2 && !tc::mbar_wait(&p_full[b], ((t - 2) >> 1) & 1u, abort_flag, a.status)) break;
+                        // q' is prepared once per query: a later split of the same query in
+                        // this CTA reuses it
+                        const bool need_q = at_seg_start && cur_q != q_in;
+                        if (need_q && !tc::mbar_wait(&q_full, nq & 1u, abort_flag, a.status)) break;
+                        if (!tc::mbar_wait(&full[b], (t >> 1) & 1u, abort_flag, a.status)) break;
                         tc::fence_after_sync();
-                        const uint32_t stage = sE0 + b * kStageBytes;
-#pragma unroll 8
+                        const uint64_t da0 = tc::sdesc_sw128(stage, 16, 1024);
+    #pragma unroll
                         for (int kg = 0; kg < kD / 16; kg++) {
-                            const uint64_t ad = tc::sdesc_sw128(stage + (kg >> 2) * kBoxBytes + (kg & 3) * 32, 16, 1024);
-                            const uint64_t bd = tc::sdesc_sw128(sQ0 + (kg >> 2) * kQBoxBytes + (kg & 3) * 32, 16, 1024);
-                            tc::mma_bf16_ss(tmem + kColS + 64 * b, ad, bd, idesc_qk, kg != 0 ? 1u : 0u);
+                            const uint32_t off = ((kg >> 2) * kBoxBytes + (kg & 3) * 32) >> 4;
+                            const uint32_t offq = ((kg >> 2) * kQBoxBytes + (kg & 3) * 32) >> 4;
+                            tc::mma_bf16_ss(tmem + kColS + 64 * b, da0 + off, dq0 + offq, idesc_qk, kg != 0 ? 1u : 0u);
                         }
                         tc::mma_commit(&s_full[b]);
                         if (need_q) {
                             ++nq;
                             q_in = cur_q;
                         }
-                        first_of[t_qk & 3] = at_seg_start;
-                        last_of[t_qk & 3] = (int)(g - cur_q * a.T) == lt_last;
-                        at_seg_start = false;
-                        ++t_qk;
-                        ++g;
-                        more = advance();
-                        progress = true;
+                    } else {
+                        const bool first = at_seg_start;
+                        const bool last = (int)(g - cur_q * a.T) == lt_last;
+                        if (!tc::mbar_wait(&p_full[b], (t >> 1) & 1u, abort_flag, a.status)) break;
+                        tc::fence_after_sync();
+                        const uint64_t da0 = tc::sdesc_sw128(stage, kBoxBytes, 1024);
+                        const uint64_t db0 = tc::sdesc_sw128(sP0 + b * kPBytes, kBoxBytes, 1024);
+    #pragma unroll
+                        for (int c = 0; c < 4; c++) {
+    #pragma unroll
+                            for (int kk = 0; kk < kRows / 16; kk++) {
+                                const uint32_t off = (2 * c * kBoxBytes + kk * 2048) >> 4;
+                                tc::mma_bf16_ss(tmem + kColO + 64 * c, da0 + off, db0 + ((kk * 2048) >> 4), idesc_pv,
+                                                (first && kk == 0) ? 0u : 1u);
+                            }
+                        }
+                        tc::mma_commit(&empty[b]);
+                        tc::mma_commit(&o_full);
+                        if (last) tc::mma_commit(&o_seg);
                     }
+                    at_seg_start = false;
+                    ++t;
+                    ++g;
                 }
-                if (progress) {
-                    idle_since = 0;
-                } else {
-                    if (*abort_flag) break;
-                    const uint64_t now = tc::globaltimer_ns();
-                    if (idle_since == 0) {
-                        idle_since = now;
-                    } else if (now - idle_since > tc::kWaitLimitNs) {
-                        atomicOr(a.status, CSA_DEV_TIMEOUT);
-                        *abort_flag = 1;
-                        break;
-                    }
-                }
+                // every MMA this thread issued must be complete before TMEM is freed
+                uint64_t* done = qk_role ? &mma_done : &pv_done;
+                tc::mma_commit(done);
+                if (!tc::mbar_drain(done, 0)) atomicOr(a.status, CSA_DEV_TIMEOUT);
             }
-            // every MMA issued so far must be complete before TMEM is freed
-            tc::mma_commit(&mma_done);
-            if (!tc::mbar_drain(&mma_done, 0)) atomicOr(a.status, CSA_DEV_TIMEOUT);
+        } else {
+            // ------------------------------------------------------------ MMA issue
+            // Issue order is dynamic: the PV product of tile t as soon as its P is
+            // written, the QK product of tile t+1 as soon as its stage has landed
+            // and the S^T buffer it reuses is free (PV of tile t-1 issued).
+            if (lane == 0) {
+                constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kRows, kH, 0, 0);
+                constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, kH, 1, 1);
+                const uint32_t sE0 = tc::smem_u32(sE), sQ0 = tc::smem_u32(sQ), sP0 = tc::smem_u32(sP);
+                uint32_t t_qk = 0, t_pv = 0, nq = 0;
+                bool first_of[4], last_of[4];  // segment flags of tiles t_pv .. t_qk-1 (at most 2)
+                // QK cursor over this CTA's live tiles
+                int64_t g = g_begin;
+                int64_t cur_q = -1, cur_end = g_begin, q_in = -1;  // q_in: query whose q' is in sQ
+                QueryInfo inf{};
+                int lt_last = -1;
+                bool at_seg_start = true;
+                auto advance = [&]() -> bool {  // move g to the next live tile; false at the end
+                    for (; g < g_end; ++g) {
+                        const int64_t qi = g / a.T;
+                        if (g >= cur_end) {
+                            cur_q = qi;
+                            inf = query_info(a, qi);
+                            cur_end = seg_end_of(a, g, g_end);
+                            lt_last = last_live(a, inf, (int)(g - qi * a.T), (int)(cur_end - qi * a.T));
+                            at_seg_start = true;
+                        }
+                        if (tile_live(a, inf, (int)(g - qi * a.T))) return true;
+                    }
+                    return false;
+                };
+                bool more = advance();
+                uint64_t idle_since = 0;
+                while (more || t_pv < t_qk) {
+                    bool progress = false;
+                    if (t_pv < t_qk) {
+                        const int b = t_pv & 1;
+                        if (tc::mbar_test_wait(&p_full[b], (t_pv >> 1) & 1u)) {
+                            tc::fence_after_sync();
+                            const uint32_t stage = sE0 + b * kStageBytes;
+                            const uint32_t pb = sP0 + b * kPBytes;
+                            const bool first = first_of[t_pv & 3];
+    #pragma unroll
+                            for (int c = 0; c < 4; c++) {
+    #pragma unroll
+                                for (int kk = 0; kk < kRows / 16; kk++) {
+                                    const uint64_t ad = tc::sdesc_sw128(stage + 2 * c * kBoxBytes + kk * 2048, kBoxBytes, 1024);
+                                    const uint64_t bd = tc::sdesc_sw128(pb + kk * 2048, kBoxBytes, 1024);
+                                    tc::mma_bf16_ss(tmem + kColO + 64 * c, ad, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
+                                }
+                            }
+                            tc::mma_commit(&empty[b]);
+                            tc::mma_commit(&o_full);
+                            if (last_of[t_pv & 3]) tc::mma_commit(&o_seg);
+                            ++t_pv;
+                            progress = true;
+                        }
+                    }
+                    if (more && t_pv + 1 >= t_qk) {  // S^T buffer of tile t_qk is free
+                        const int b = t_qk & 1;
+                        // q' is prepared once per query: a later split of the same
+                        // query in this CTA reuses it
+                        const bool need_q = at_seg_start && cur_q != q_in;
+                        bool ready = !need_q || tc::mbar_test_wait(&q_full, nq & 1u);
+                        if (ready) ready = tc::mbar_test_wait(&full[b], (t_qk >> 1) & 1u);
+                        if (ready) {
+                            tc::fence_after_sync();
+                            const uint32_t stage = sE0 + b * kStageBytes;
+    #pragma unroll 8
+                            for (int kg = 0; kg < kD / 16; kg++) {
+                                const uint64_t ad = tc::sdesc_sw128(stage + (kg >> 2) * kBoxBytes + (kg & 3) * 32, 16, 1024);
+                                const uint64_t bd = tc::sdesc_sw128(sQ0 + (kg >> 2) * kQBoxBytes + (kg & 3) * 32, 16, 1024);
+                                tc::mma_bf16_ss(tmem + kColS + 64 * b, ad, bd, idesc_qk, kg != 0 ? 1u : 0u);
+                            }
+                            tc::mma_commit(&s_full[b]);
+                            if (need_q) {
+                                ++nq;
+                                q_in = cur_q;
+                            }
+                            first_of[t_qk & 3] = at_seg_start;
+                            last_of[t_qk & 3] = (int)(g - cur_q * a.T) == lt_last;
+                            at_seg_start = false;
+                            ++t_qk;
+                            ++g;
+                            more = advance();
+                            progress = true;
+                        }
+                    }
+                    if (progress) {
+                        idle_since = 0;
+                    } else {
+                        if (*abort_flag) break;
+                        const uint64_t now = tc::globaltimer_ns();
+                        if (idle_since == 0) {
+                            idle_since = now;
+                        } else if (now - idle_since > tc::kWaitLimitNs) {
+                            atomicOr(a.status, CSA_DEV_TIMEOUT);
+                            *abort_flag = 1;
+                            break;
+                        }
+                    }
+                }
+                // every MMA issued so far must be complete before TMEM is freed
+                tc::mma_commit(&mma_done);
+                if (!tc::mbar_drain(&mma_done, 0)) atomicOr(a.status, CSA_DEV_TIMEOUT);
+            }
         }
     } else if (warp < 2 + kSoftWarps) {
         // ------------------------------------------------------------ softmax + epilogue
@@ -641,48 +759,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
 
         // q' = RoPE(RMSNorm(q), i) of query qi into sQ (bf16, 128-byte
-        // swizzle).  staged: the raw rows were loaded into sQ by TMA (the
-        // CTA's first segment) and are normalised in place; otherwise they are
-        // read from global memory (L2: prefetched when the segment before
-        // started).  Lane l of a warp holds dims 16l .. 16l+15 of a head: two
-        // 16-byte chunks of box l/4 of that head's 128-byte row.
-        auto prep_q = [&](int64_t qi, auto staged_c) {
-            constexpr bool staged = decltype(staged_c)::value;
+        // swizzle).  The raw rows are loaded into sQ by TMA (q_raw): by warp 0
+        // for the CTA's first query, by this role for every later one as soon
+        // as the QK products of the query before are done (its rows were
+        // prefetched into L2 when that query's segment started); they are
+        // normalised and rotated in place.  Lane l of a warp holds dims
+        // 16l .. 16l+15 of a head: two 16-byte chunks of box l/4 of that
+        // head's 128-byte row.
+        uint32_t qraw_issued = next_live_query(a, g_begin, g_end) >= 0 ? 1u : 0u, qraw_done = 0;
+        auto load_q = [&](int64_t qi) {  // by one thread
+            tc::mbar_arrive_expect_tx(&q_raw, kQBytes);
+            for (int bx = 0; bx < 8; bx++)
+                tc::tma_load_3d(sQ + bx * kQBoxBytes, &tm_q, &q_raw, bx * 64, 0, (int)qi);
+        };
+        auto prep_q = [&](int64_t qi) {
             constexpr int kHq = kH / kSoftWarps;  // heads of this warp
             const int64_t i = a.q_pos[qi];
-            if constexpr (!staged)
-                for (int hh = 1; hh < kHq; hh++)  // on their way into L2 meanwhile
-                    prefetch_l2(a.q + (qi * kH + sw * kHq + hh) * kD + lane * 16);
             const int ch = (lane & 3) * 2;
             // this lane's chunk c (0, 1) of head h in sQ
             uint8_t* const qbase = sQ + (lane >> 2) * kQBoxBytes;
 #define QCHUNK(h, c) reinterpret_cast<uint4*>(qbase + (h) * 128 + (((ch + (c)) ^ ((h) & 7)) << 4))
-            const uint4* gsrc = reinterpret_cast<const uint4*>(a.q + (qi * kH + sw * kHq) * kD) + lane * 2;
-            uint4 u0 = make_uint4(0u, 0u, 0u, 0u), u1 = u0;
-            if constexpr (!staged) {
-                u0 = __ldg(gsrc);
-                u1 = __ldg(gsrc + 1);
-            }
             if (tid < 32) {
                 float c, s;
                 rope_cs((double)i, a.theta.t[tid], &c, &s);
                 rot_cs[2 * tid] = c;
                 rot_cs[2 * tid + 1] = s;
             }
-            bool ok = true;
-            if constexpr (staged) ok = warp_wait(&q_raw, 0, abort_flag, a.status, lane);
+            const bool ok = warp_wait(&q_raw, qraw_done & 1u, abort_flag, a.status, lane);
+            if (ok) ++qraw_done;
             softmax_barrier();
             if (ok) {
 #pragma unroll 1
                 for (int hh = 0; hh < kHq; hh++) {
                     const int h = sw * kHq + hh;
-                    if constexpr (staged) {
-                        u0 = *QCHUNK(h, 0);
-                        u1 = *QCHUNK(h, 1);
-                    } else if (hh > 0) {
-                        u0 = __ldg(gsrc + hh * (kD / 8));
-                        u1 = __ldg(gsrc + hh * (kD / 8) + 1);
-                    }
+                    const uint4 u0 = *QCHUNK(h, 0), u1 = *QCHUNK(h, 1);
                     const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
                     float x[16];
 #pragma unroll
@@ -722,7 +832,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         {
             const int64_t q0 = next_live_query(a, g_begin, g_end);
-            if (q0 >= 0) prep_q(q0, std::true_type{});
+            if (q0 >= 0) prep_q(q0);
         }
         uint32_t tcount = 0, nseg = 0;
         bool stop = false;
@@ -735,10 +845,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int lt0 = (int)(g - qi * a.T), lt1 = (int)(seg_end - qi * a.T);
             const int lt_last = last_live(a, inf, lt0, lt1);
             if (tid == 0 && (inf.i + 1) / a.m > a.n_cap) atomicOr(a.status, CSA_DEV_BAD_POSITION);
-            {  // the next segment's q rows head for L2 while this one runs
-                const int64_t qn = next_live_query(a, seg_end, g_end);
-                if (qn >= 0) prefetch_l2(a.q + (qn * kH + sw * (kH / kSoftWarps) + (lane >> 3)) * kD + (lane & 7) * 64);
-            }
+            // the next query's q rows head for L2 while this segment runs
+            const int64_t qn = next_live_query(a, seg_end, g_end);
+            const bool q_next = qn >= 0 && qn != qi;  // a further split of this query keeps q'
+            if (q_next) prefetch_l2(a.q + (qn * kH + sw * (kH / kSoftWarps) + (lane >> 3)) * kD + (lane & 7) * 64);
 #pragma unroll
             for (int h = 0; h < kHW; h++) l_part[h] = 0.f;
             int seg_tiles = 0;
@@ -780,6 +890,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float mask = valid ? 0.f : -INFINITY;  // x = s * scale + mask
                 const bool ok = warp_wait(&s_full[b], (tcount >> 1) & 1u, abort_flag, a.status, lane);
+                // the segment's QK products are all done: the next query's raw
+                // rows may replace q' in sQ while this tile's softmax runs
+                if (ok && lt == lt_last && q_next && tid == 0) {
+                    load_q(qn);
+                    ++qraw_issued;
+                }
                 float x[kHW];
                 bool need = false;
                 if (ok) {
@@ -859,12 +975,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) tc::mbar_arrive(&p_full[b]);
                 ++seg_tiles;
                 ++tcount;
-                if (lt == lt_last) {
-                    // every QK product of this segment is done: q' of the next
-                    // query may go in (a further split of this one keeps it)
-                    const int64_t qn = next_live_query(a, seg_end, g_end);
-                    if (qn >= 0 && qn != qi) prep_q(qn, std::false_type{});
-                }
+                if (lt == lt_last && q_next) prep_q(qn);
             }
             if (stop) break;
             // ---------------------------------------------------- segment epilogue
@@ -948,13 +1059,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             softmax_barrier();  // red[], fac_s[], rot_cs[] are free again
             g = seg_end;
         }
-    } else {
+        // leave no copy of q rows in flight (a wait that gave up left one)
+        if (tid == 0 && qraw_issued > qraw_done && !tc::mbar_drain(&q_raw, (qraw_issued - 1u) & 1u))
+            atomicOr(a.status, CSA_DEV_TIMEOUT);
+    } else if (warp < 2 + kSoftWarps + kLoadWarps) {
         // ------------------------------------------------------------ gathers
         // The gathered tiles (selected rows) are fetched with TMA gather4 by
-        // the producer warp and the gather warps together, each its own boxes
-        // of every row; the producer warp, which waits for every use of a
-        // stage in order, arms the stage's full barrier with the tile's bytes
-        // and hands it over through go[stage].
+        // the gather warps, each its own boxes of every row; the producer
+        // warp, which waits for every use of a stage in order, arms the
+        // stage's full barrier with the tile's bytes and hands it over
+        // through go[stage].
         const int lw = warp - 2 - kSoftWarps;
         // Cursor over this CTA's gathered tiles; the indices of the next one
         // are read while the current one waits for its stage.
@@ -987,8 +1101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool have_n = next_gathered(qi_n, lt_n, st_n);
             if (have_n) gather_rows(a, qi_n, query_info(a, qi_n), lt_n, lane, rows_n);
             if (!warp_wait(&go[st], (ngo[st]++) & 1u, abort_flag, a.status, lane)) break;
-            gather_boxes(&tm_sel, &full[st], sE + st * kStageBytes, rows, kProducerBoxes + lw * kLoaderBoxes,
-                         kLoaderBoxes, lane);
+            gather_boxes(&tm_sel, &full[st], sE + st * kStageBytes, rows, lw * kLoaderBoxes, kLoaderBoxes, lane);
             have = have_n;
             qi = qi_n;
             lt = lt_n;
@@ -1146,7 +1259,8 @@ cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool spars
     a.status = status;
     a.theta = rope_theta(g);
     {
-        cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(attend_tc_kernel), kSmem);
+        cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(attend_tc_kernel<true>), kSmem);
+        if (e == cudaSuccess) e = set_smem_attr(reinterpret_cast<const void*>(attend_tc_kernel<false>), kSmem);
         if (e != cudaSuccess) return e;
     }
     CUtensorMap tm_q;
@@ -1156,7 +1270,11 @@ cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool spars
         const uint32_t box[3] = {64, (uint32_t)kH, 1};
         if (!make_tmap_bf16(&tm_q, q, 3, d, sd, box)) return cudaErrorInvalidValue;
     }
-    attend_tc_kernel<<<pl.tc_grid, kThreads, kSmem, st>>>(tm_sel, tm_win, tm_q, a);
+    // the split issue layout where no tile is gathered
+    if (a.pre || a.topk_idx == nullptr)
+        attend_tc_kernel<true><<<pl.tc_grid, Roles<true>::kThreads, kSmem, st>>>(tm_sel, tm_win, tm_q, a);
+    else
+        attend_tc_kernel<false><<<pl.tc_grid, Roles<false>::kThreads, kSmem, st>>>(tm_sel, tm_win, tm_q, a);
     note_launch();
     return cudaGetLastError();
 }

@@ -189,7 +189,7 @@ __device__ __forceinline__ uint32_t e2m1_code(float q) {
 // bytes: tile t holds keys 128t .. 128t+127, first their codes (64 bytes a
 // key: dim 2i in the low nibble of byte i, dim 2i+1 in the high one), then
 // their exponent bytes (4 a key, block j's scale 2^(byte - 127)); key slots
-// past n_cap are zero.  Block j: e_j = floor(log2 amax) - 2 (its largest value
+// past n_cap hold an all-zero key (codes 0, exponent bytes 127).  Block j: e_j = floor(log2 amax) - 2 (its largest value
 // in [4, 8)), 0 for an all-zero block; a nonzero block more than 14 binades
 // below the key's largest is raised to it minus 14 (the key then converts to
 // E4M3 with one scale without loss); codes = E2M1 of x / 2^e_j.  One warp a

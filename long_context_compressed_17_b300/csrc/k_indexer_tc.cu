@@ -60,8 +60,10 @@ struct Cfg {
     static constexpr int kKSteps = kDI * kEB / 32;      // MMAs per key tile: 32 bytes of K each
     static constexpr int N = NQ * kHI;                  // MMA N
     // key tiles and TMEM accumulators in flight: E4M3 tiles are half the bytes,
-    // so twice as many are in flight for the same shared memory
-    static constexpr int kStages = F8 ? 8 : 4;
+    // so twice as many are in flight for the same shared memory; FP4 tiles
+    // land in the raw ring (the HBM stream's depth) and spend only the
+    // conversion-to-MMA span in a stage
+    static constexpr int kStages = F4 ? 4 : (F8 ? 8 : 4);
     static constexpr int kAcc = NQ == 1 ? (F8 ? 8 : 4) : 2;
     static constexpr int kQBufs = NQ == 1 ? 2 : 1;
     // Epilogue warps: for NQ = 4, sixteen (four per TMEM lane quarter, one
@@ -82,7 +84,7 @@ struct Cfg {
     static constexpr int kThreads = 32 * (kConv0 + kConvWarps);
     static constexpr uint32_t kQBytes = (uint32_t)N * kDI * kEB;
     static constexpr uint32_t kTmemCols = kAcc * N;     // 256 or 512
-    static constexpr int kRawStages = F4 ? 4 : 0;       // packed FP4 tiles in flight
+    static constexpr int kRawStages = F4 ? 12 : 0;      // packed FP4 tiles in flight (~104 KiB)
     static constexpr int kScaleSlots = F4 ? kStages + kAcc : 0;  // per-key scales of the tiles in flight
     static constexpr size_t kBarBytes = 1024;
     static_assert((2 * kStages + 2 * kQBufs + 2 * kAcc + 2 * kRawStages + kScaleSlots) * 8 + 8 <= kBarBytes,
@@ -150,6 +152,18 @@ __global__ void __launch_bounds__(Cfg<NQ, KF>::kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // FP4: E4M3 codes of the E2M1 magnitudes 0..7 times 2^sh for every shift
+    // sh = -8 .. 6 a nonzero block can have (eight bytes per shift)
+    __shared__ uint2 fp4_lut[15];
+    if constexpr (F4) {
+        if (threadIdx.x < 15) {
+            const float kMag[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+            uint32_t w[2] = {0u, 0u};
+            for (int m = 1; m < 8; m++)
+                w[m >> 2] |= (uint32_t)f32_to_e4m3_sat(ldexpf(kMag[m], (int)threadIdx.x - 8)) << (8 * (m & 3));
+            fp4_lut[threadIdx.x] = make_uint2(w[0], w[1]);
+        }
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; s++) {
             tc::mbar_init(&full[s], F4 ? C::kConvWarps : 1);  // FP4: every converter warp
@@ -434,12 +448,13 @@ __global__ void __launch_bounds__(Cfg<NQ, KF>::kThreads, 1)
             // (exact conversions), looked up four codes at a time with byte
             // permutes, the signs moved from bit 3 of each nibble to bit 7 of
             // each byte with the permute's sign-replicate selectors.  The row
-            // is written with the 128-byte swizzle of a TMA tile load.
+            // is written with the 128-byte swizzle of a TMA tile load.  A block
+            // whose codes are all zero may have any shift: its table is never
+            // read beyond entry 0, so the shift is clamped into the table.
             const int k = (warp - C::kConv0) * 32 + lane;
             uint32_t j = 0;
             int64_t cur_g = -1, gnav = 0;
             int64_t g = g0;
-            const float kMag[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
             for (int64_t u = u0, t = t0; u < u1; ++u, ++t) {
                 if (t == a.n_tiles) {
                     t = 0;
@@ -475,11 +490,9 @@ __global__ void __launch_bounds__(Cfg<NQ, KF>::kThreads, 1)
                 uint8_t* row = sA + stage * kStageBytes + k * 128;
 #pragma unroll
                 for (int c = 0; c < 4; c++) {
-                    const int sh = (int)((ex >> (8 * c)) & 0xFFu) - 127 - Ek;
-                    uint32_t lut[2] = {0u, 0u};
-#pragma unroll
-                    for (int m = 1; m < 8; m++)
-                        lut[m >> 2] |= (uint32_t)f32_to_e4m3_sat(ldexpf(kMag[m], sh)) << (8 * (m & 3));
+                    const int sh = min(6, max(-8, (int)((ex >> (8 * c)) & 0xFFu) - 127 - Ek));
+                    const uint2 lt = fp4_lut[sh + 8];
+                    const uint32_t lut[2] = {lt.x, lt.y};
                     const uint32_t w[4] = {cw[c].x, cw[c].y, cw[c].z, cw[c].w};
                     uint32_t o[8];
 #pragma unroll

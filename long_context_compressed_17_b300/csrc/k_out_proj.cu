@@ -1,0 +1,207 @@
+// k_out_proj.cu -- grouped output projection on the 5th-generation tensor
+// cores (tcgen05 + TMEM + TMA).
+//
+// "DeepSeek-V4百万上下文时代的开源宣言" §三.2, CSA "Step 4: Grouped Output
+// Projection": the 512-dim heads are projected in groups to cut the cost.  The
+// H heads form G consecutive groups; group g's concatenated head outputs x_g
+// (K = H/G * D values a query) are projected by its own matrix W_g [d_g, K]:
+//   out[q, g*d_g + n] = sum_k x_g[q, k] * W_g[n, k]
+// a block-diagonal projection, G times cheaper than a dense one of the same
+// output width.  Each group is a dense bf16 GEMM with fp32 accumulation:
+// tiles of 128 queries x BN outputs, K in stages of 64 (128-byte rows, the
+// 128-byte swizzle) loaded by TMA into a four-stage ring, M = 128 x N = BN
+// MMAs issued by one thread into a TMEM accumulator, and four epilogue warps
+// (one per TMEM lane quarter) converting a row's outputs to bf16.  Decode
+// (a few dozen queries) streams the weights with narrow tiles (BN = 64) so
+// that more CTAs share the stream; prefill uses BN = 256.  Query rows past Q
+// read as zeros (TMA fill) and are not stored.  Every wait is bounded: on a
+// timeout the kernel flags CSA_DEV_TIMEOUT, every role leaves, outstanding
+// MMAs are waited for and TMEM is freed.
+#include "common.cuh"
+#include "internal.h"
+#include "tc_util.cuh"
+
+namespace csa {
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box);
+
+namespace {
+
+constexpr int kBM = 128;  // queries per tile (MMA M)
+constexpr int kBK = 64;   // K per stage: one 128-byte row of bf16
+constexpr int kOpStages = 4;
+constexpr int kOpThreads = 64 + 128;
+
+template <int BN>
+struct OpCfg {
+    static constexpr uint32_t kABytes = kBM * kBK * 2;
+    static constexpr uint32_t kBBytes = BN * kBK * 2;
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    static constexpr size_t kSmem = 1024 + (size_t)kOpStages * kStageBytes;
+    static constexpr uint32_t kTmemCols = BN;  // a power of two >= 32
+    static constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, BN);
+};
+
+struct OpArgs {
+    uint16_t* out;  // [Q, G * d_g] bf16
+    int Q, d_g, K;  // K = H/G * D
+    int64_t ldo;    // G * d_g
+    uint32_t* status;
+};
+
+}  // namespace
+
+template <int BN>
+__global__ void __launch_bounds__(kOpThreads, 1)
+    out_proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                    const __grid_constant__ OpArgs a) {
+    using C = OpCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t full[kOpStages], empty[kOpStages], acc_full, mma_done;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_sh;
+    volatile int* abort_flag = &abort_sh;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * BN, g = blockIdx.z;
+    const int nk = a.K / kBK;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kOpStages; s++) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        tc::mbar_init(&acc_full, 1);
+        tc::mbar_init(&mma_done, 1);
+        abort_sh = 0;
+        tc::fence_barrier_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&tmem_slot, C::kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        tc::tma_prefetch_map(&tm_x);
+        tc::tma_prefetch_map(&tm_w);
+        uint32_t issued = 0;
+        for (int kt = 0; kt < nk; kt++) {
+            const int s = kt % kOpStages;
+            if (!tc::mbar_wait(&empty[s], ((kt / kOpStages) & 1u) ^ 1u, abort_flag, a.status)) break;
+            tc::mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+            uint8_t* st = sm + s * C::kStageBytes;
+            tc::tma_load_2d(st, &tm_x, &full[s], g * a.K + kt * kBK, m0);
+            tc::tma_load_3d(st + C::kABytes, &tm_w, &full[s], kt * kBK, n0, g);
+            ++issued;
+        }
+        // leave no copy in flight: every stage's newest fill has landed
+        for (uint32_t kt = issued > kOpStages ? issued - kOpStages : 0; kt < issued; kt++)
+            if (!tc::mbar_drain(&full[kt % kOpStages], (kt / kOpStages) & 1u)) atomicOr(a.status, CSA_DEV_TIMEOUT);
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issue
+        for (int kt = 0; kt < nk; kt++) {
+            const int s = kt % kOpStages;
+            if (!tc::mbar_wait(&full[s], (kt / kOpStages) & 1u, abort_flag, a.status)) break;
+            tc::fence_after_sync();
+            const uint32_t sa = tc::smem_u32(sm + s * C::kStageBytes);
+            const uint32_t sb = sa + C::kABytes;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; kk++)
+                tc::mma_bf16_ss(tmem, tc::sdesc_kmajor_sw128(sa + kk * 32), tc::sdesc_kmajor_sw128(sb + kk * 32),
+                                C::idesc, (kt | kk) != 0 ? 1u : 0u);
+            tc::mma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+        }
+        tc::mma_commit(&acc_full);
+        // every MMA issued must be complete before TMEM is freed
+        tc::mma_commit(&mma_done);
+        if (!tc::mbar_drain(&mma_done, 0)) atomicOr(a.status, CSA_DEV_TIMEOUT);
+    } else if (warp >= 2) {
+        // ------------------------------------------------ epilogue: one query row per thread
+        const int quarter = warp & 3;
+        const int row = m0 + quarter * 32 + lane;
+        int ok = 1;
+        if (lane == 0) ok = tc::mbar_wait(&acc_full, 0, abort_flag, a.status) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok && !*abort_flag) {
+            tc::fence_after_sync();
+            uint16_t* dst = a.out + (int64_t)row * a.ldo + (int64_t)g * a.d_g + n0;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                float v[32];
+                tc::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+                tc::tmem_ld_wait();
+                if (row < a.Q && n0 + c0 < a.d_g) {
+                    uint32_t p[16];
+#pragma unroll
+                    for (int j = 0; j < 16; j++)
+                        p[j] = (uint32_t)f32_to_bf16_rn(v[2 * j]) | ((uint32_t)f32_to_bf16_rn(v[2 * j + 1]) << 16);
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+                    for (int j = 0; j < 4; j++) d4[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+                }
+            }
+        }
+    }
+    // ---------------------------------------------------- teardown
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+bool out_proj_supported(int H, int D, int G, int d_g) {
+    if (G < 1 || H % G != 0) return false;
+    const int K = H / G * D;
+    return K % kBK == 0 && d_g >= 64 && d_g % 64 == 0;
+}
+
+cudaError_t launch_out_proj(const void* o, int Q, int H, int D, int G, const void* w, int d_g, void* out,
+                            uint32_t* status, cudaStream_t st) {
+    if (Q == 0) return cudaSuccess;
+    const int K = H / G * D;
+    // narrow tiles for a few queries (more CTAs stream the weights), wide ones otherwise
+    const bool narrow = Q <= kBM || d_g % 256 != 0;
+    CUtensorMap tm_x, tm_w;
+    {
+        const uint64_t d[2] = {(uint64_t)H * D, (uint64_t)Q};
+        const uint64_t s[1] = {(uint64_t)H * D * 2};
+        const uint32_t box[2] = {(uint32_t)kBK, (uint32_t)kBM};
+        if (!make_tmap_bf16(&tm_x, o, 2, d, s, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const uint64_t d[3] = {(uint64_t)K, (uint64_t)d_g, (uint64_t)G};
+        const uint64_t s[2] = {(uint64_t)K * 2, (uint64_t)d_g * K * 2};
+        const uint32_t box[3] = {(uint32_t)kBK, narrow ? 64u : 256u, 1};
+        if (!make_tmap_bf16(&tm_w, w, 3, d, s, box)) return cudaErrorInvalidValue;
+    }
+    OpArgs a;
+    a.out = reinterpret_cast<uint16_t*>(out);
+    a.Q = Q;
+    a.d_g = d_g;
+    a.K = K;
+    a.ldo = (int64_t)G * d_g;
+    a.status = status;
+    const dim3 grid((unsigned)((Q + kBM - 1) / kBM), (unsigned)(d_g / (narrow ? 64 : 256)), (unsigned)G);
+    cudaError_t e;
+    if (narrow) {
+        e = set_smem_attr(reinterpret_cast<const void*>(out_proj_kernel<64>), OpCfg<64>::kSmem);
+        if (e != cudaSuccess) return e;
+        out_proj_kernel<64><<<grid, kOpThreads, OpCfg<64>::kSmem, st>>>(tm_x, tm_w, a);
+    } else {
+        e = set_smem_attr(reinterpret_cast<const void*>(out_proj_kernel<256>), OpCfg<256>::kSmem);
+        if (e != cudaSuccess) return e;
+        out_proj_kernel<256><<<grid, kOpThreads, OpCfg<256>::kSmem, st>>>(tm_x, tm_w, a);
+    }
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace csa

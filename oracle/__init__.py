@@ -433,3 +433,35 @@ def attend_batch(q, seq, pos, m, cache, D, idx, window, win_pos0, W, sink, scale
     if st != OK:
         raise ValueError("oracle_attend_batch: status %d" % st)
     return out, lse
+
+
+# --------------------------------------------------------------------------
+# grouped output projection
+# --------------------------------------------------------------------------
+def grouped_out_proj(o: np.ndarray, w: np.ndarray, G: int) -> np.ndarray:
+    """Grouped output projection ["DeepSeek-V4百万上下文时代的开源宣言" §三.2 CSA
+    "Step 4: Grouped Output Projection" (the 512-dim heads are projected in
+    groups, which cuts the cost)]: the H heads form G consecutive groups of
+    H/G; group g's concatenated head outputs x_g (H/G * D values) are
+    projected by its own matrix, out[:, g*d_g:(g+1)*d_g] = x_g . W_g^T.
+    o: stored attention outputs [Q, H, D]; w: stored weights [G, d_g, H/G*D]
+    (row n of W_g is output n's weights).  Returns float64 [Q, G*d_g]."""
+    x = read_act(o)
+    Q, H, D = x.shape
+    assert H % G == 0
+    wt = read_act(w)
+    Gw, d_g, K = wt.shape
+    assert Gw == G and K == H // G * D
+    xg = x.reshape(Q, G, K)
+    out = np.empty((Q, G * d_g), dtype=np.float64)
+    for g in range(G):
+        out[:, g * d_g:(g + 1) * d_g] = xg[:, g, :] @ wt[g].T
+    return out
+
+
+def read_act(a: np.ndarray) -> np.ndarray:
+    """Stored activations (bf16 bits as uint16, float32 or float64) -> float64."""
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)

@@ -288,3 +288,13 @@ def test_decode_append_validation(L):
     big = L.params(512, 1024, act="f32", kv="f32")
     assert _status_of(L.csa_decode_append, **dict(base, p=big)) == 2
     assert L.csa_launch_count() == n0
+
+
+def test_grouped_out_proj_validation(L):
+    n0 = L.csa_launch_count()
+    base = dict(o=FAKE, Q=4, H=64, D=512, G=8, w=FAKE, d_g=512, out=FAKE, ws=FAKE, ws_bytes=256)
+    assert _status_of(L.csa_grouped_out_proj, **dict(base, G=7)) == 2      # H % G
+    assert _status_of(L.csa_grouped_out_proj, **dict(base, d_g=100)) == 2  # d_g % 64
+    assert _status_of(L.csa_grouped_out_proj, **dict(base, o=FAKE + 8)) == 1
+    assert _status_of(L.csa_grouped_out_proj, **dict(base, ws_bytes=16)) == 4
+    assert L.csa_launch_count() == n0

@@ -1,6 +1,6 @@
 """GPU parity of the FP4 lightning indexer ["DeepSeek-V4 技术报告深度解析"
 §2.1.1, §3.2]: the key packer bit-exact against the oracle (codes, block
-exponents, the 14-binade threshold, the tile layout and its zero padding),
+exponents, the 14-binade threshold, the tile layout and its all-zero padding keys),
 and the scores and top-k sets of csa_index_topk_fp4 / csa_index_score_fp4
 against the oracle's FP4 scores (its exact top-k), in decode (one query per
 sequence) and prefill-like (four queries per MMA) shapes, ragged and at the
@@ -69,7 +69,7 @@ def test_key_pack_is_bit_exact(L):
         rc, rs = oracle.pack_idx_keys_fp4(keys[b].float().numpy())
         assert np.array_equal(codes[b], rc), "codes of sequence %d" % b
         assert np.array_equal(exps[b], rs), "exponents of sequence %d" % b
-    assert np.all(pad_c == 0) and np.all(pad_e == 0)
+    assert np.all(pad_c == 0) and np.all(pad_e == 127)  # all-zero keys (scale 1)
     # the threshold was exercised
     es = exps[1, 10].astype(int) - 127
     assert es[3] == es[:3].max() - 14
