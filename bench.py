@@ -442,10 +442,18 @@ class GpuStep:
             fn()
 
     def capture(self):
-        """The whole step as one CUDA graph (what a serving loop replays), with
-        timing events recorded between its segments inside the graph; where
-        the runtime cannot record events inside a graph, one graph a segment."""
+        """The whole step as one CUDA graph (what a serving loop replays), and
+        a second copy with timing events recorded between its segments inside
+        the graph (an event between two kernels makes the second wait for the
+        first to finish, where the plain graph lets it be scheduled while the
+        first finishes); where the runtime cannot record events inside a
+        graph, one graph a segment."""
         segs = self.segments()
+        self.plain = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.plain):
+            for _, fn in segs:
+                fn()
+        torch.cuda.synchronize()
         try:
             self.inner = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(segs) - 1)]
             g = torch.cuda.CUDAGraph()
@@ -523,6 +531,8 @@ def run_gpu(args, rank, world):
 
     for _ in range(args.warmup):
         flush_l2()
+        st.plain.replay()
+        flush_l2()
         for _, g in st.graphs:
             g.replay()
     torch.cuda.synchronize()
@@ -539,11 +549,16 @@ def run_gpu(args, rank, world):
             for k in range(args.steps):
                 flush_l2()                # L2 flushed before every timed step
                 e0.record()
+                st.plain.replay()
+                e1.record()
+                e1.synchronize()
+                step_ms.append(e0.elapsed_time(e1))
+                flush_l2()                # the segment times, from the copy with events inside
+                e0.record()
                 g.replay()
                 e1.record()
                 e1.synchronize()
                 marks = [e0] + st.inner + [e1]
-                step_ms.append(e0.elapsed_time(e1))
                 for j, n in enumerate(st.seg_names):
                     seg_ms[n].append(marks[j].elapsed_time(marks[j + 1]))
         else:
@@ -587,9 +602,10 @@ def run_gpu(args, rank, world):
            "head_dim": w.D, "heads": w.H, "ratio": w.m, "topk": w.topk, "window": w.W,
            "idx_heads": w.H_I, "idx_dim": w.d_I, "kv_format": w.kv_fmt, "idx_format": w.idx_fmt, "seed": w.seed,
            "l2": "flushed before every timed step: 512 MiB write, then a 256 MiB read of another buffer",
-           "timing": ("the step captured as one CUDA graph, replayed once a step; CUDA events before and "
-                      "after the replay and between its kernel segments (recorded inside the graph); "
-                      "ms_per_step is the median over the timed steps") if st.one_graph else
+           "timing": ("the step captured as one CUDA graph, replayed once a step between CUDA events "
+                      "(ms_per_step: the median over the timed steps); the segment times come from a copy "
+                      "of the graph with events recorded between its kernel segments, replayed after each "
+                      "timed step (L2 flushed again)") if st.one_graph else
                      ("each kernel segment captured as a CUDA graph, CUDA events between the replays; "
                       "ms_per_step is the median over the timed steps"),
            "parallelism": "replicas" if world > 1 else "single GPU",

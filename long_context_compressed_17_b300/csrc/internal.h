@@ -123,13 +123,32 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
                           int64_t n_win, const int64_t* win_pos0, const float* sink, void* out,
                           float* lse, uint8_t* ws, uint32_t* status, cudaStream_t st);
 
-// SM count of the current device (cached per device).
 // Grouped output projection (k_out_proj.cu).
 bool out_proj_supported(int H, int D, int G, int d_g);
 cudaError_t launch_out_proj(const void* o, int Q, int H, int D, int G, const void* w, int d_g, void* out,
                             uint32_t* status, cudaStream_t st);
 
+// SM count of the current device (cached per device).
 int num_sms();
+
+// Launch `kernel` as a programmatic dependent of the grid before it in the
+// stream: its CTAs may be scheduled while that grid finishes, and every read
+// of that grid's results comes after grid_dep_wait() in the kernel.
+template <class... KArgs, class... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // Raise a kernel's dynamic shared memory limit to at least `bytes` on the
 // current device (cached per device and kernel; thread-safe).

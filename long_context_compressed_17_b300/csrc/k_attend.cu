@@ -16,6 +16,7 @@
 // composition of a single query.
 #include "common.cuh"
 #include "internal.h"
+#include "tc_util.cuh"
 
 namespace csa {
 
@@ -220,6 +221,7 @@ __global__ void __launch_bounds__(128)
                           const int64_t* __restrict__ q_pos, int derotate, void* __restrict__ out,
                           int act, float* __restrict__ lse, int64_t tiles, int64_t total, int grid,
                           int by_query, RopeTheta theta) {
+    tc::grid_dep_wait();  // the partials of the attention kernel before (a programmatic dependent launch)
     const int tid = threadIdx.x, lane = tid & 31;
     const int h = (int)(blockIdx.x % H);
     int64_t qi;
@@ -395,10 +397,12 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
     const int by_query = ranges && Q <= pl.tc_grid - 1;
     const int64_t blocks = (!ranges || by_query) ? (int64_t)Q * H : (int64_t)(pl.tc_grid - 1) * H;
     if (blocks == 0) return cudaSuccess;  // every query was finished by its only CTA
-    attend_combine_kernel<<<(unsigned)blocks, 128, 0, st>>>(
-        part_o, part_ml, pl.splits, H, g.D, sink, q_pos, g.derotate, out, g.act, lse,
-        ranges ? (int64_t)pl.tc_T : 0, pl.tc_total, pl.tc_grid, by_query, rope_theta(g));
+    const cudaError_t ec = launch_dependent(
+        attend_combine_kernel, dim3((unsigned)blocks), dim3(128), 0, st, part_o, part_ml, pl.splits, H, g.D, sink,
+        q_pos, g.derotate, out, g.act, lse, ranges ? (int64_t)pl.tc_T : 0, pl.tc_total, pl.tc_grid, by_query,
+        rope_theta(g));
     note_launch();
+    if (ec != cudaSuccess) return ec;
     return cudaGetLastError();
 }
 

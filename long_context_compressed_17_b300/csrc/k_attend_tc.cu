@@ -424,19 +424,7 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
     constexpr int kPvWarp = Roles<kSplit>::kPvWarp;
     constexpr int kLoaderBoxes = Roles<kSplit>::kLoaderBoxes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp == 0) {
-        // the first position and row indices this CTA reads head for L2
-        // during the setup (the loads that wait for them come next)
-        const int64_t g0 = range_begin(a, blockIdx.x);
-        if (g0 < range_begin(a, blockIdx.x + 1)) {
-            const int64_t q0 = g0 / a.T;
-            const int lt0 = (int)(g0 - q0 * a.T);
-            if (lane == 0) prefetch_l2(a.q_pos + q0);
-            const int64_t p = (int64_t)lt0 * kRows + (lane - 1) * 32;  // lanes 1..4: two tiles' indices
-            if (a.topk_idx != nullptr && !a.pre && lane >= 1 && lane <= 4 && lt0 < a.T_sel && p < a.k)
-                prefetch_l2(a.topk_idx + q0 * a.k + p);
-        }
-    }
+    tc::grid_dep_launch();  // the combine after this kernel may be scheduled now
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; s++) {
             tc::mbar_init(&full[s], 1);
@@ -465,6 +453,9 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = tmem_slot;
+    // Launched as a programmatic dependent: the setup above overlapped the
+    // kernel before; every global read comes after it has completed.
+    tc::grid_dep_wait();
 
     const int64_t g_begin = range_begin(a, blockIdx.x);
     const int64_t g_end = range_begin(a, blockIdx.x + 1);
@@ -1271,11 +1262,13 @@ cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool spars
         if (!make_tmap_bf16(&tm_q, q, 3, d, sd, box)) return cudaErrorInvalidValue;
     }
     // the split issue layout where no tile is gathered
-    if (a.pre || a.topk_idx == nullptr)
-        attend_tc_kernel<true><<<pl.tc_grid, Roles<true>::kThreads, kSmem, st>>>(tm_sel, tm_win, tm_q, a);
-    else
-        attend_tc_kernel<false><<<pl.tc_grid, Roles<false>::kThreads, kSmem, st>>>(tm_sel, tm_win, tm_q, a);
+    const cudaError_t e = (a.pre || a.topk_idx == nullptr)
+        ? launch_dependent(attend_tc_kernel<true>, dim3(pl.tc_grid), dim3(Roles<true>::kThreads), kSmem, st,
+                           tm_sel, tm_win, tm_q, a)
+        : launch_dependent(attend_tc_kernel<false>, dim3(pl.tc_grid), dim3(Roles<false>::kThreads), kSmem, st,
+                           tm_sel, tm_win, tm_q, a);
     note_launch();
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -79,7 +79,11 @@ struct Cfg {
     static constexpr int kIssuers = NQ == 1 ? 2 : 1;
     static_assert(kStages % kIssuers == 0 && kAcc % kIssuers == 0, "issuers own whole stages");
     static constexpr int kEpi0 = 1 + kIssuers;          // first epilogue warp
-    static constexpr int kConvWarps = F4 ? 4 : 0;       // FP4 -> E4M3 converters, one key a thread
+    // FP4 -> E4M3 converters, one key a thread: groups of four warps on
+    // alternate tiles (decode: two groups, or the conversion would fall
+    // behind the HBM stream)
+    static constexpr int kConvWarps = F4 ? (NQ == 1 ? 8 : 4) : 0;
+    static constexpr int kConvGroups = kConvWarps / 4;
     static constexpr int kConv0 = kEpi0 + kEpiWarps;
     static constexpr int kThreads = 32 * (kConv0 + kConvWarps);
     static constexpr uint32_t kQBytes = (uint32_t)N * kDI * kEB;
@@ -130,6 +134,7 @@ __global__ void __launch_bounds__(Cfg<NQ, KF>::kThreads, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                       const __grid_constant__ CUtensorMap tm_q, IdxArgs a) {
     using C = Cfg<NQ, KF>;
+    tc::grid_dep_launch();  // the selection after this kernel may be scheduled now
     constexpr bool F8 = C::F8;
     constexpr bool F4 = C::F4;
     constexpr uint32_t kStageBytes = C::kStageBytes;
@@ -166,14 +171,14 @@ __global__ void __launch_bounds__(Cfg<NQ, KF>::kThreads, 1)
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; s++) {
-            tc::mbar_init(&full[s], F4 ? C::kConvWarps : 1);  // FP4: every converter warp
+            tc::mbar_init(&full[s], F4 ? 4 : 1);  // FP4: every warp of a converter group
             tc::mbar_init(&empty[s], 1);
         }
         for (int s = 0; s < C::kRawStages; s++) {
             tc::mbar_init(&rfull[s], 1);
-            tc::mbar_init(&rempty[s], C::kConvWarps);
+            tc::mbar_init(&rempty[s], 4);
         }
-        for (int s = 0; s < C::kScaleSlots; s++) tc::mbar_init(&sfull[s], C::kConvWarps);
+        for (int s = 0; s < C::kScaleSlots; s++) tc::mbar_init(&sfull[s], 4);
         for (int b = 0; b < C::kQBufs; b++) {
             tc::mbar_init(&qfull[b], 1);
             tc::mbar_init(&qempty[b], C::kIssuers);  // every issuer releases the queries
@@ -451,7 +456,8 @@ __global__ void __launch_bounds__(Cfg<NQ, KF>::kThreads, 1)
             // is written with the 128-byte swizzle of a TMA tile load.  A block
             // whose codes are all zero may have any shift: its table is never
             // read beyond entry 0, so the shift is clamped into the table.
-            const int k = (warp - C::kConv0) * 32 + lane;
+            const int k = ((warp - C::kConv0) & 3) * 32 + lane;
+            const uint32_t grp = (uint32_t)((warp - C::kConv0) >> 2);  // takes tiles jj = grp mod kConvGroups
             uint32_t j = 0;
             int64_t cur_g = -1, gnav = 0;
             int64_t g = g0;
@@ -466,6 +472,7 @@ __global__ void __launch_bounds__(Cfg<NQ, KF>::kThreads, 1)
                 }
                 if ((int64_t)t * kTileKeys >= gnav) continue;
                 const uint32_t jj = j++;
+                if (jj % C::kConvGroups != grp) continue;
                 const int stage = (int)(jj % C::kStages), rs = (int)(jj % C::kRawStages);
                 const int slot = (int)(jj % C::kScaleSlots);
                 if (!tc::mbar_wait(&rfull[rs], (jj / C::kRawStages) & 1u, abort_flag, a.status)) break;

@@ -526,6 +526,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         int32_t* __restrict__ idx, float* __restrict__ sel) {
     extern __shared__ __align__(16) uint32_t keys[];  // [<= kChunk / CS + 4], 16-byte aligned
     __shared__ TopkScratch<CS> s;
+    tc::grid_dep_wait();    // the scores of the kernel before (a programmatic dependent launch)
+    tc::grid_dep_launch();  // ... and the attention after may be scheduled now
     const int rank = (int)tc::cluster_ctarank();
     const int64_t q = blockIdx.y;
     const int n = (int)n_complete(q_pos, q, m, n_cap);
@@ -586,13 +588,15 @@ cudaError_t launch_topk(const Geometry& g, float* scores, int64_t ld, int64_t n_
         cfg.blockDim = dim3(kThreads, 1, 1);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = st;
-        cudaLaunchAttribute at[1];
+        cudaLaunchAttribute at[2];
         at[0].id = cudaLaunchAttributeClusterDimension;
         at[0].val.clusterDim.x = kClusterCS;
         at[0].val.clusterDim.y = 1;
         at[0].val.clusterDim.z = 1;
+        at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see grid_dep_wait
+        at[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = at;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 2;
         cudaError_t e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel<kClusterCS>, (const float*)scores, ld, n_cap,
                                            q_pos, g.m, k, idx, sel);
         note_launch();

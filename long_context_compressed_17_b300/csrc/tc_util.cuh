@@ -168,6 +168,16 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     return false;
 }
 
+// Programmatic dependent launch.  grid_dep_wait: this thread waits until
+// the grid launched before this one in the stream has completed and its
+// memory operations are visible (a no-op when this grid was not launched as
+// a programmatic dependent).  grid_dep_launch: this CTA lets the next grid in
+// the stream, if launched as a programmatic dependent, be scheduled once
+// every CTA of this grid has done so or exited (so a waiting dependent never
+// holds an SM that a CTA of this grid has yet to start on).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // All threads of all CTAs of the cluster.
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
