@@ -117,6 +117,7 @@ IndexTopkPlan plan_index_topk(const Geometry& g, int B, int Q, int HI, int64_t n
 
 bool attend_tc_supported(const Geometry& g, bool sparse, int H, int64_t n_cap, int64_t n_win);
 void plan_attend_tc(const Geometry& g, bool sparse, int Q, int64_t n_cap, int64_t n_win, bool ring, AttendPlan* pl);
+void plan_attend_tc_aligned(int Q, AttendPlan* pl);
 
 AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int64_t n_cap,
                        int64_t n_win, bool ring) {
@@ -125,7 +126,7 @@ AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int6
     pl.ring = ring ? 1 : 0;
     pl.list_len = (sparse ? (int64_t)g.k : n_cap) + g.W;
     pl.use_tc = attend_tc_supported(g, sparse, H, n_cap, n_win) ? 1 : 0;
-    pl.tc_T_sel = pl.tc_T = pl.tc_grid = pl.tc_deq = pl.tc_seg = pl.tc_nseg = 0;
+    pl.tc_T_sel = pl.tc_T = pl.tc_grid = pl.tc_deq = pl.tc_seg = pl.tc_nseg = pl.tc_qcta = pl.tc_qrem = 0;
     pl.tc_total = 0;
     if (pl.use_tc) {
         pl.head_group = H;
@@ -148,19 +149,21 @@ AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int6
         pl.splits = (int)((pl.list_len + pl.rows_per_split - 1) / pl.rows_per_split);
         if (pl.splits < 1) pl.splits = 1;
     }
-    pl.part_o_off = kStatusWordBytes;
-    size_t o_bytes = align256((size_t)Q * pl.splits * H * g.D * sizeof(float));
-    pl.part_ml_off = pl.part_o_off + o_bytes;
-    size_t ml_bytes = align256((size_t)Q * pl.splits * H * 2 * sizeof(float));
-    pl.deq_off = pl.part_ml_off + ml_bytes;
-    size_t deq_bytes = 0;
+    size_t deq_rows = 0;
     if (pl.use_tc && g.kv == CSA_FP8_MIXED) {
         // dequantise whichever is fewer rows: the ones the queries read or all
         const size_t per_query = (size_t)Q * pl.tc_T * 64;
         const size_t stored = (size_t)B * (size_t)(n_cap + (g.W > 0 ? n_win : 0));
         pl.tc_deq = per_query <= stored ? 1 : 2;
-        deq_bytes = align256((pl.tc_deq == 1 ? per_query : stored) * g.D * 2);
+        deq_rows = pl.tc_deq == 1 ? per_query : stored;
     }
+    if (pl.use_tc && sparse && pl.tc_deq != 1) plan_attend_tc_aligned(Q, &pl);  // the rows are gathered
+    pl.part_o_off = kStatusWordBytes;
+    size_t o_bytes = align256((size_t)Q * pl.splits * H * g.D * sizeof(float));
+    pl.part_ml_off = pl.part_o_off + o_bytes;
+    size_t ml_bytes = align256((size_t)Q * pl.splits * H * 2 * sizeof(float));
+    pl.deq_off = pl.part_ml_off + ml_bytes;
+    const size_t deq_bytes = align256(deq_rows * g.D * 2);
     pl.total = pl.deq_off + deq_bytes;
     return pl;
 }

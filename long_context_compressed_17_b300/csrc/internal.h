@@ -67,6 +67,9 @@ struct AttendPlan {
     // batch-invariant splits: tc_seg tiles each (0: balanced ranges), tc_nseg
     // per query
     int tc_seg, tc_nseg;
+    // query-aligned ranges (see TileDeal): CTAs per query, and how many
+    // queries get one more (tc_qcta 0: balanced over all tiles)
+    int tc_qcta, tc_qrem;
     // FP8 rows reach the tensor-core kernel dequantised to bf16 in the
     // workspace: 1 = the rows each query reads, [Q, tc_T * 64, D] in tile
     // order; 2 = every stored row, [B, n_cap, D] then [B, n_win, D]; 0 = the

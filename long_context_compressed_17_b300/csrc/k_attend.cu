@@ -208,33 +208,34 @@ __global__ void __launch_bounds__(kAttThreads) attend_generic_kernel(AttendArgs 
 // block barrier, and the partial rows are requested before the weights.
 //   CUDA-core kernel, or fixed splits (tiles == 0): grid Q*H, query q has
 //   S_alloc partials.
-//   Tensor-core kernel (tiles > 0): CTA c of `grid` owns the tiles
-//   [c*total/grid, (c+1)*total/grid) of all queries' tile lists (tiles per
-//   query); only a query cut by a CTA boundary has partials (one per CTA
-//   meeting it), every other query was finished by its only CTA.  With
-//   by_query the grid is Q*H and block (q, h) takes query q if it was cut;
-//   otherwise the grid is (grid-1)*H and block (b-1, h) handles the query cut
-//   by boundary b, if b is the first boundary inside it.
+//   Tensor-core kernel (tiles > 0): the CTAs own contiguous ranges of all
+//   queries' tile lists (tiles per query) as TileDeal{total, tiles, grid,
+//   qcta, qrem} deals them; only a query cut by a CTA boundary has partials
+//   (one per CTA meeting it), every other query was finished by its only
+//   CTA.  With by_query the grid is Q*H and block (q, h) takes query q if it
+//   was cut; otherwise the grid is (grid-1)*H and block (b-1, h) handles the
+//   query cut by boundary b, if b is the first boundary inside it.
 __global__ void __launch_bounds__(128)
     attend_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                           int S_alloc, int H, int D, const float* __restrict__ sink,
                           const int64_t* __restrict__ q_pos, int derotate, void* __restrict__ out,
                           int act, float* __restrict__ lse, int64_t tiles, int64_t total, int grid,
-                          int by_query, RopeTheta theta) {
+                          int qcta, int qrem, int by_query, RopeTheta theta) {
     tc::grid_dep_wait();  // the partials of the attention kernel before (a programmatic dependent launch)
     const int tid = threadIdx.x, lane = tid & 31;
     const int h = (int)(blockIdx.x % H);
     int64_t qi;
     int Sq;
     if (tiles > 0) {
-        auto cta_of = [&](int64_t g) { return ((g + 1) * grid - 1) / total; };
+        const TileDeal deal{total, tiles, grid, qcta, qrem};
+        auto cta_of = [&](int64_t g) { return deal.cta_of(g); };
         int64_t c0;
         if (by_query) {
             qi = blockIdx.x / H;
             c0 = cta_of(qi * tiles);
         } else {
             const int64_t b = blockIdx.x / H + 1;
-            const int64_t g = b * total / grid;  // first tile of CTA b
+            const int64_t g = deal.begin(b);     // first tile of CTA b
             if (g % tiles == 0) return;          // the boundary falls between queries
             qi = g / tiles;
             c0 = cta_of(qi * tiles);
@@ -394,12 +395,13 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
     // Fixed splits (and the CUDA-core kernel): every query has pl.splits
     // partials, merged in split order by a block per query.
     const bool ranges = pl.use_tc && pl.tc_seg == 0;
-    const int by_query = ranges && Q <= pl.tc_grid - 1;
+    const int by_query = ranges && (Q <= pl.tc_grid - 1 || pl.tc_qcta > 0);
     const int64_t blocks = (!ranges || by_query) ? (int64_t)Q * H : (int64_t)(pl.tc_grid - 1) * H;
     if (blocks == 0) return cudaSuccess;  // every query was finished by its only CTA
     const cudaError_t ec = launch_dependent(
         attend_combine_kernel, dim3((unsigned)blocks), dim3(128), 0, st, part_o, part_ml, pl.splits, H, g.D, sink,
-        q_pos, g.derotate, out, g.act, lse, ranges ? (int64_t)pl.tc_T : 0, pl.tc_total, pl.tc_grid, by_query,
+        q_pos, g.derotate, out, g.act, lse, ranges ? (int64_t)pl.tc_T : 0, pl.tc_total, pl.tc_grid, pl.tc_qcta,
+        pl.tc_qrem, by_query,
         rope_theta(g));
     note_launch();
     if (ec != cudaSuccess) return ec;

@@ -98,6 +98,7 @@ struct AttTcArgs {
     int64_t total;            // Q * T
     int grid;
     int seg, nseg;            // batch-invariant splits of seg tiles, nseg per query (seg 0: off)
+    int qcta, qrem;           // query-aligned ranges (TileDeal; qcta 0: balanced over all tiles)
     int S;                    // partial slots per query
     float* part_o;            // [Q, S, 64, 512]
     float* part_ml;           // [Q, S, 64, 2]
@@ -109,16 +110,18 @@ struct AttTcArgs {
     RopeTheta theta;
 };
 
-// CTA that owns global tile g (CTA c owns [c*total/grid, (c+1)*total/grid)).
-__device__ __forceinline__ int64_t cta_of(const AttTcArgs& a, int64_t g) {
-    return ((g + 1) * a.grid - 1) / a.total;
+__device__ __forceinline__ TileDeal deal_of(const AttTcArgs& a) {
+    return TileDeal{a.total, (int64_t)a.T, a.grid, a.qcta, a.qrem};
 }
 
-// First global tile of CTA c's range: balanced over tiles, or, with fixed
-// splits, over whole splits (CTA c takes splits [c*n/grid, (c+1)*n/grid) of
-// the n = Q * nseg in query order).
+// CTA that owns global tile g (ranges without fixed splits).
+__device__ __forceinline__ int64_t cta_of(const AttTcArgs& a, int64_t g) { return deal_of(a).cta_of(g); }
+
+// First global tile of CTA c's range: balanced over tiles or query-aligned
+// (TileDeal), or, with fixed splits, over whole splits (CTA c takes splits
+// [c*n/grid, (c+1)*n/grid) of the n = Q * nseg in query order).
 __device__ __forceinline__ int64_t range_begin(const AttTcArgs& a, int64_t c) {
-    if (a.seg == 0) return c * a.total / a.grid;
+    if (a.seg == 0) return deal_of(a).begin(c);
     const int64_t sp = c * (a.total / a.T * a.nseg) / a.grid;
     const int64_t qi = sp / a.nseg;
     return qi * a.T + min((int64_t)a.T, (sp % a.nseg) * a.seg);
@@ -1136,6 +1139,7 @@ void plan_attend_tc(const Geometry& g, bool sparse, int Q, int64_t n_cap, int64_
         return;
     }
     pl->tc_grid = (int)(pl->tc_total < sms ? pl->tc_total : sms);
+    pl->tc_qcta = pl->tc_qrem = 0;
     int smax = 1;
     if (pl->tc_total > 0) {
         auto cta = [&](int64_t t) { return ((t + 1) * pl->tc_grid - 1) / pl->tc_total; };
@@ -1145,6 +1149,21 @@ void plan_attend_tc(const Geometry& g, bool sparse, int Q, int64_t n_cap, int64_
         }
     }
     pl->splits = smax;
+}
+
+// Query-aligned ranges (TileDeal) for gathered tiles when there are no more
+// queries than SMs: a CTA that met two queries would load the second q
+// behind the first one's gathers in its TMA queue (~8 us at 128K context),
+// and the slowest CTA sets the kernel's time.  Lists of TMA tiles keep the
+// balanced ranges (measured: HCA decode 120.8 -> 123.9 us aligned).
+void plan_attend_tc_aligned(int Q, AttendPlan* pl) {
+    const int64_t sms = num_sms();
+    if (pl->tc_seg != 0 || Q < 1 || Q > sms || pl->tc_T < 2) return;
+    const int64_t per = sms / Q;
+    pl->tc_qcta = (int)(per < pl->tc_T ? per : pl->tc_T);
+    pl->tc_qrem = pl->tc_qcta < pl->tc_T ? (int)(sms - (int64_t)Q * pl->tc_qcta) : 0;
+    pl->tc_grid = Q * pl->tc_qcta + pl->tc_qrem;
+    pl->splits = pl->tc_qcta + (pl->tc_qrem > 0 ? 1 : 0);
 }
 
 cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool sparse, const void* q,
@@ -1238,6 +1257,8 @@ cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool spars
     a.T = pl.tc_T;
     a.total = pl.tc_total;
     a.grid = pl.tc_grid;
+    a.qcta = pl.tc_qcta;
+    a.qrem = pl.tc_qrem;
     a.seg = pl.tc_seg;
     a.nseg = pl.tc_nseg;
     a.S = pl.splits;

@@ -84,6 +84,7 @@ struct Cfg {
     // behind the HBM stream)
     static constexpr int kConvWarps = F4 ? (NQ == 1 ? 8 : 4) : 0;
     static constexpr int kConvGroups = kConvWarps / 4;
+    static_assert(kConvGroups * 4 == kConvWarps, "whole converter groups");
     static constexpr int kConv0 = kEpi0 + kEpiWarps;
     static constexpr int kThreads = 32 * (kConv0 + kConvWarps);
     static constexpr uint32_t kQBytes = (uint32_t)N * kDI * kEB;
