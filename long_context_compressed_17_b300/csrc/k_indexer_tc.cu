@@ -33,6 +33,8 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t
                     const uint64_t* strides_bytes, const uint32_t* box);
 bool make_tmap_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                   const uint64_t* strides_bytes, const uint32_t* box);
+bool make_tmap_u8_linear(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                         const uint64_t* strides_bytes, const uint32_t* box);
 
 namespace {
 
@@ -50,6 +52,7 @@ enum { kKeyBf16 = 0, kKeyE4m3 = 1, kKeyFp4 = 2 };
 // A packed FP4 key tile: 128 keys x 64 code bytes, then 128 x 4 exponent bytes.
 constexpr uint32_t kFp4TileBytes = kTileKeys * (kDI / 2) + kTileKeys * (kDI / 32);
 static_assert(kFp4TileBytes == 8704 && kFp4TileBytes % 128 == 0, "FP4 tile layout");
+constexpr int kFp4Rows = kFp4TileBytes / 128;  // 68 rows of 128 bytes
 
 template <int NQ, int KF>
 struct Cfg {
@@ -245,17 +248,13 @@ __global__ void __launch_bounds__(Cfg<NQ, KF>::kThreads, 1)
                 qloads++;
             }
             if constexpr (F4) {
-                // the packed tile, one bulk copy into the raw ring; the converter
-                // warps expand it into a stage
+                // the packed tile, one TMA box of 68 rows of 128 bytes into the
+                // raw ring; the converter warps expand it into a stage
                 const int rs = (int)(nraw % C::kRawStages);
                 if (!tc::mbar_wait(&rempty[rs], ((nraw / C::kRawStages) & 1u) ^ 1u, abort_flag, a.status)) break;
                 tc::mbar_arrive_expect_tx(&rfull[rs], kFp4TileBytes);
-                const uint8_t* src = a.key_pack + ((int64_t)seq * a.n_tiles + t) * (int64_t)kFp4TileBytes;
-                asm volatile(
-                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                        tc::smem_u32(sRaw + rs * kFp4TileBytes)),
-                    "l"(src), "r"(kFp4TileBytes), "r"(tc::smem_u32(&rfull[rs]))
-                    : "memory");
+                tc::tma_load_2d(sRaw + rs * kFp4TileBytes, &tm_keys, &rfull[rs], 0,
+                                (int)(((int64_t)seq * a.n_tiles + t) * kFp4Rows));
                 ++nraw;
                 continue;
             }
@@ -345,7 +344,7 @@ __global__ void __launch_bounds__(Cfg<NQ, KF>::kThreads, 1)
         // the query's head weights: in registers for decode (loaded once per query
         // group), read through L1 per tile in prefill (the registers go to the
         // sixteen epilogue warps there)
-        constexpr bool kWRegs = NQ == 1;
+        constexpr bool kWRegs = NQ == 1 && !F4;  // FP4: the converter warps leave 96 registers
         float wr[kWRegs ? kHI : 1];
         int64_t g = g0;
         for (int64_t u = u0, t = t0; u < u1; ++u, ++t) {
@@ -410,6 +409,25 @@ __global__ void __launch_bounds__(Cfg<NQ, KF>::kThreads, 1)
             const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::N);
             {
                 float acc4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
+                if constexpr (F4) {
+                    // sixteen heads a load, their weights through L1 (the
+                    // converter warps leave the epilogue 96 registers a thread)
+                    const float4* w4 = reinterpret_cast<const float4*>(a.w_idx + (g * NQ + q0) * kHI);
+#pragma unroll
+                    for (int qt = 0; qt < 4; qt++) {
+                        float v[16];
+                        tc::tmem_ld16(tbase + (uint32_t)(q0 * kHI + qt * 16), v);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int j4 = 0; j4 < 4; j4++) {
+                            const float4 w = __ldg(w4 + qt * 4 + j4);
+                            acc4[0] = fmaf(w.x, fmaxf(v[4 * j4 + 0], 0.f), acc4[0]);
+                            acc4[1] = fmaf(w.y, fmaxf(v[4 * j4 + 1], 0.f), acc4[1]);
+                            acc4[2] = fmaf(w.z, fmaxf(v[4 * j4 + 2], 0.f), acc4[2]);
+                            acc4[3] = fmaf(w.w, fmaxf(v[4 * j4 + 3], 0.f), acc4[3]);
+                        }
+                    }
+                } else
 #pragma unroll
                 for (int half = 0; half < 2; half++) {
                     float v[32];
@@ -479,12 +497,11 @@ __global__ void __launch_bounds__(Cfg<NQ, KF>::kThreads, 1)
                 if (!tc::mbar_wait(&rfull[rs], (jj / C::kRawStages) & 1u, abort_flag, a.status)) break;
                 if (!tc::mbar_wait(&empty[stage], ((jj / C::kStages) & 1u) ^ 1u, abort_flag, a.status)) break;
                 const uint8_t* raw = sRaw + rs * kFp4TileBytes;
+                // chunk c = block c (32 codes); static indices keep cw in
+                // registers (a lane-dependent index would put it in local memory)
                 uint4 cw[4];
 #pragma unroll
-                for (int c = 0; c < 4; c++) {  // chunk c = block c (32 codes); rotated to spread the banks
-                    const int cc = (c + k) & 3;
-                    cw[cc] = *reinterpret_cast<const uint4*>(raw + k * 64 + cc * 16);
-                }
+                for (int c = 0; c < 4; c++) cw[c] = *reinterpret_cast<const uint4*>(raw + k * 64 + c * 16);
                 const uint32_t ex = *reinterpret_cast<const uint32_t*>(raw + kTileKeys * 64 + k * 4);
                 int E = -1000;
 #pragma unroll
@@ -577,9 +594,14 @@ static cudaError_t launch_indexer_tc_kf(const Geometry& g, int kf, const void* q
     const uint64_t qs[1] = {(uint64_t)kDI * eb};
     const uint32_t qbox[2] = {(uint32_t)(128 / eb), (uint32_t)(NQ * kHI)};
     bool maps;
-    if (kf == kKeyFp4) {  // no key map: packed tiles come by bulk copy
-        maps = make_tmap_u8(&tm_q, q_idx, 2, qd, qs, qbox);
-        tm_keys = tm_q;
+    if (kf == kKeyFp4) {
+        // packed tiles as rows of 128 bytes, one box of kFp4Rows rows a tile,
+        // copied linearly (tiled TMA moves them several times faster than
+        // one bulk copy a tile)
+        const uint64_t pd[2] = {128, (uint64_t)B * (uint64_t)((n_cap + kTileKeys - 1) / kTileKeys) * kFp4Rows};
+        const uint64_t ps[1] = {128};
+        const uint32_t pbox[2] = {128, (uint32_t)kFp4Rows};
+        maps = make_tmap_u8_linear(&tm_keys, keys, 2, pd, ps, pbox) && make_tmap_u8(&tm_q, q_idx, 2, qd, qs, qbox);
     } else if (f8) {
         maps = make_tmap_u8(&tm_keys, keys, 3, kd, ks, kb) && make_tmap_u8(&tm_q, q_idx, 2, qd, qs, qbox);
     } else {

@@ -24,10 +24,12 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// bf16 tensor of `rank` dims (dims[0] innermost), 128-byte swizzled boxes,
-// zero fill outside the tensor.  Returns false if the map cannot be built.
+// Tensor of `rank` dims (dims[0] innermost), 128-byte swizzled boxes (or,
+// linear, boxes stored row after row), zero fill outside the tensor.  Returns
+// false if the map cannot be built.
 static bool make_tmap(CUtensorMapDataType dt, CUtensorMap* map, const void* base, int rank,
-                      const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
+                      const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                      bool linear = false) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn || rank < 1 || rank > 5) return false;
     cuuint64_t gd[5];
@@ -40,7 +42,8 @@ static bool make_tmap(CUtensorMapDataType dt, CUtensorMap* map, const void* base
         if (i + 1 < rank) gs[i] = strides_bytes[i];
     }
     CUresult r = fn(map, dt, (cuuint32_t)rank, const_cast<void*>(base), gd,
-                    gs, bd, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    gs, bd, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    linear ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -54,6 +57,12 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t
 bool make_tmap_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                   const uint64_t* strides_bytes, const uint32_t* box) {
     return make_tmap(CU_TENSOR_MAP_DATA_TYPE_UINT8, map, base, rank, dims, strides_bytes, box);
+}
+
+// Bytes, boxes stored linearly (packed FP4 key tiles, copied as they are).
+bool make_tmap_u8_linear(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                         const uint64_t* strides_bytes, const uint32_t* box) {
+    return make_tmap(CU_TENSOR_MAP_DATA_TYPE_UINT8, map, base, rank, dims, strides_bytes, box, true);
 }
 
 }  // namespace csa
