@@ -19,8 +19,8 @@
 // accumulators, for NQ = 4 sixteen, where four warps share a quarter and take
 // one of the four queries each (the epilogue, 256 values per key, would
 // otherwise hold the tensor pipe back).  Every wait is bounded: on a timeout
-// the kernel flags CSA_DEV_TIMEOUT, all roles leave their loops and TMEM is
-// freed.
+// the kernel flags CSA_DEV_TIMEOUT, all roles leave their loops, the copies
+// and MMAs in flight are waited for (bounded too) and TMEM is freed.
 #include <atomic>
 
 #include "common.cuh"
@@ -93,9 +93,10 @@ struct Cfg {
     static constexpr uint32_t kQBytes = (uint32_t)N * kDI * kEB;
     static constexpr uint32_t kTmemCols = kAcc * N;     // 256 or 512
     static constexpr int kRawStages = F4 ? 12 : 0;      // packed FP4 tiles in flight (~104 KiB)
+    static constexpr int kRawSlots = kRawStages / 2;    // ... loaded two consecutive live tiles a slot
     static constexpr int kScaleSlots = F4 ? kStages + kAcc : 0;  // per-key scales of the tiles in flight
     static constexpr size_t kBarBytes = 1024;
-    static_assert((2 * kStages + 2 * kQBufs + 2 * kAcc + 2 * kRawStages + kScaleSlots) * 8 + 8 <= kBarBytes,
+    static_assert((2 * kStages + 2 * kQBufs + 2 * kAcc + 2 * kRawSlots + kScaleSlots + kIssuers) * 8 + 8 <= kBarBytes,
                   "barrier area too small");
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kQBufs * kQBytes +
                                     (size_t)kRawStages * kFp4TileBytes + (size_t)kScaleSlots * kTileKeys * 4 +
@@ -154,10 +155,11 @@ __global__ void __launch_bounds__(Cfg<NQ, KF>::kThreads, 1)
     uint64_t* qempty = qfull + C::kQBufs;
     uint64_t* tfull = qempty + C::kQBufs;
     uint64_t* tempty = tfull + C::kAcc;
-    uint64_t* rfull = tempty + C::kAcc;        // FP4: packed tile landed
-    uint64_t* rempty = rfull + C::kRawStages;  // FP4: packed tile read by the converters
-    uint64_t* sfull = rempty + C::kRawStages;  // FP4: key scales of a tile written
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfull + C::kScaleSlots);
+    uint64_t* rfull = tempty + C::kAcc;       // FP4: the packed tiles of a raw slot landed
+    uint64_t* rempty = rfull + C::kRawSlots;  // FP4: both tiles of a raw slot read by the converters
+    uint64_t* sfull = rempty + C::kRawSlots;  // FP4: key scales of a tile written
+    uint64_t* idone = sfull + C::kScaleSlots;  // every MMA of an issuer done (before TMEM is freed)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(idone + C::kIssuers);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -178,11 +180,12 @@ __global__ void __launch_bounds__(Cfg<NQ, KF>::kThreads, 1)
             tc::mbar_init(&full[s], F4 ? 4 : 1);  // FP4: every warp of a converter group
             tc::mbar_init(&empty[s], 1);
         }
-        for (int s = 0; s < C::kRawStages; s++) {
+        for (int s = 0; s < C::kRawSlots; s++) {
             tc::mbar_init(&rfull[s], 1);
-            tc::mbar_init(&rempty[s], 4);
+            tc::mbar_init(&rempty[s], 8);  // the four warps of each converter group
         }
         for (int s = 0; s < C::kScaleSlots; s++) tc::mbar_init(&sfull[s], 4);
+        for (int i = 0; i < C::kIssuers; i++) tc::mbar_init(&idone[i], 1);
         for (int b = 0; b < C::kQBufs; b++) {
             tc::mbar_init(&qfull[b], 1);
             tc::mbar_init(&qempty[b], C::kIssuers);  // every issuer releases the queries
@@ -220,6 +223,7 @@ __global__ void __launch_bounds__(Cfg<NQ, KF>::kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         uint32_t nraw = 0;  // FP4: packed tiles loaded
+        uint32_t nkey = 0;  // key tiles loaded into the stages
         int64_t cur_g = -1, last_loaded = -1, gnav = 0;
         int qloads = 0, seq = 0;
         const float* ksrow = nullptr;  // F8: the sequence's key scales
@@ -248,18 +252,43 @@ __global__ void __launch_bounds__(Cfg<NQ, KF>::kThreads, 1)
                 qloads++;
             }
             if constexpr (F4) {
-                // the packed tile, one TMA box of 68 rows of 128 bytes into the
-                // raw ring; the converter warps expand it into a stage
-                const int rs = (int)(nraw % C::kRawStages);
-                if (!tc::mbar_wait(&rempty[rs], ((nraw / C::kRawStages) & 1u) ^ 1u, abort_flag, a.status)) break;
-                tc::mbar_arrive_expect_tx(&rfull[rs], kFp4TileBytes);
-                tc::tma_load_2d(sRaw + rs * kFp4TileBytes, &tm_keys, &rfull[rs], 0,
-                                (int)(((int64_t)seq * a.n_tiles + t) * kFp4Rows));
+                // Packed tiles, one TMA box of 68 rows of 128 bytes each, into
+                // the raw ring two live tiles a slot (the second found ahead:
+                // each producer pass costs far more than its copies), where the
+                // converter warps expand them into stages.
+                if ((nraw & 1u) == 0) {
+                    const uint32_t pr = nraw >> 1;
+                    const int rs = (int)(pr % C::kRawSlots);
+                    if (!tc::mbar_wait(&rempty[rs], ((pr / C::kRawSlots) & 1u) ^ 1u, abort_flag, a.status)) break;
+                    // the next live tile in this CTA's range, if any
+                    int seq_n = seq;
+                    int64_t t_n = t, g_n = g, nav_n = gnav;
+                    bool has_next = false;
+                    for (int64_t un = u + 1; un < u1; ++un) {
+                        if (++t_n == a.n_tiles) {
+                            t_n = 0;
+                            ++g_n;
+                            nav_n = group_avail<NQ>(a, g_n);
+                            seq_n = (int)((g_n * NQ) / a.qps);
+                        }
+                        if (t_n * kTileKeys < nav_n) {
+                            has_next = true;
+                            break;
+                        }
+                    }
+                    tc::mbar_arrive_expect_tx(&rfull[rs], kFp4TileBytes * (has_next ? 2u : 1u));
+                    uint8_t* dst = sRaw + (size_t)rs * 2 * kFp4TileBytes;
+                    tc::tma_load_2d(dst, &tm_keys, &rfull[rs], 0, (int)(((int64_t)seq * a.n_tiles + t) * kFp4Rows));
+                    if (has_next)
+                        tc::tma_load_2d(dst + kFp4TileBytes, &tm_keys, &rfull[rs], 0,
+                                        (int)(((int64_t)seq_n * a.n_tiles + t_n) * kFp4Rows));
+                }
                 ++nraw;
                 continue;
             }
             if (!tc::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status)) break;
             tc::mbar_arrive_expect_tx(&full[stage], kStageBytes);
+            ++nkey;
             uint8_t* dst = sA + stage * kStageBytes;
             tc::tma_load_3d(dst, &tm_keys, &full[stage], 0, (int)(t * kTileKeys), seq);
             if (!F8) tc::tma_load_3d(dst + kStageBytes / 2, &tm_keys, &full[stage], 64, (int)(t * kTileKeys), seq);
@@ -273,6 +302,17 @@ __global__ void __launch_bounds__(Cfg<NQ, KF>::kThreads, 1)
                 phase ^= 1u;
             }
         }
+        // Leave no copy in flight (a role that gave up may not have consumed
+        // them): the newest load of every buffer must have landed.
+        auto drain_newest = [&](uint64_t* bars, uint32_t loads, uint32_t n) {
+            for (uint32_t s2 = 0; s2 < n && s2 < loads; s2++) {
+                const uint32_t i = s2 + (loads - 1u - s2) / n * n;  // newest load into buffer s2
+                if (!tc::mbar_drain(&bars[s2], (i / n) & 1u)) atomicOr(a.status, CSA_DEV_TIMEOUT);
+            }
+        };
+        drain_newest(full, nkey, (uint32_t)C::kStages);
+        drain_newest(qfull, (uint32_t)qloads, (uint32_t)C::kQBufs);
+        if constexpr (F4) drain_newest(rfull, (nraw + 1u) >> 1, (uint32_t)C::kRawSlots);
     } else if (warp >= 1 && warp < C::kEpi0 && lane == 0) {
         // ------------------------------------------------ MMA issuers
         // Issuer `me` takes the live units j with j % kIssuers == me; every
@@ -326,6 +366,9 @@ __global__ void __launch_bounds__(Cfg<NQ, KF>::kThreads, 1)
             tc::mma_commit(&empty[stage]);  // key tile free when these MMAs finish
             tc::mma_commit(&tfull[acc]);    // accumulator ready for the epilogue
         }
+        // every MMA this thread issued must be complete before TMEM is freed
+        tc::mma_commit(&idone[me]);
+        if (!tc::mbar_drain(&idone[me], 0)) atomicOr(a.status, CSA_DEV_TIMEOUT);
     } else if (warp >= C::kEpi0 && warp < C::kConv0) {
         // ------------------------------------------------ epilogue: one key per thread
         const int quarter = warp & 3;          // TMEM lanes this warp may read
@@ -492,11 +535,11 @@ __global__ void __launch_bounds__(Cfg<NQ, KF>::kThreads, 1)
                 if ((int64_t)t * kTileKeys >= gnav) continue;
                 const uint32_t jj = j++;
                 if (jj % C::kConvGroups != grp) continue;
-                const int stage = (int)(jj % C::kStages), rs = (int)(jj % C::kRawStages);
+                const int stage = (int)(jj % C::kStages), rs = (int)((jj >> 1) % C::kRawSlots);
                 const int slot = (int)(jj % C::kScaleSlots);
-                if (!tc::mbar_wait(&rfull[rs], (jj / C::kRawStages) & 1u, abort_flag, a.status)) break;
+                if (!tc::mbar_wait(&rfull[rs], ((jj >> 1) / C::kRawSlots) & 1u, abort_flag, a.status)) break;
                 if (!tc::mbar_wait(&empty[stage], ((jj / C::kStages) & 1u) ^ 1u, abort_flag, a.status)) break;
-                const uint8_t* raw = sRaw + rs * kFp4TileBytes;
+                const uint8_t* raw = sRaw + ((size_t)rs * 2 + (jj & 1u)) * kFp4TileBytes;
                 // chunk c = block c (32 codes); static indices keep cw in
                 // registers (a lane-dependent index would put it in local memory)
                 uint4 cw[4];
