@@ -46,21 +46,30 @@ L2_DRAIN_BYTES = 256 << 20
 
 
 # ------------------------------------------------------------------ captured traffic
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of a
-# workload's dominant kernel, from the ncu captures summarised in profiles/.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# a segment's main kernel (attention: attend_tc_kernel, without the combine),
+# from the ncu captures summarised in profiles/.
 # A figure holds only while the kernel's sources are byte-identical to the
 # captured build (sha256 prefix of the listed files); otherwise it is null.
 CAPTURED_TRAFFIC = {
     ("csa_decode_bf16_b32_128k", "indexer"): (
-        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "9e56bce23e6c0021", 274861056),
-    ("csa_decode_fp8cache_b8_1m", "indexer"): (
-        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "9e56bce23e6c0021", 546892032),
+        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "d6f7b9e8baac8a37", 275543808),
+    ("csa_decode_fp4idx_b32_128k", "indexer"): (
+        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "d6f7b9e8baac8a37", 72882432),
     ("csa_decode_fp8idx_b32_128k", "indexer"): (
-        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "9e56bce23e6c0021", 143112448),
+        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "d6f7b9e8baac8a37", 143776000),
+    ("csa_decode_fp8cache_b8_1m", "indexer"): (
+        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "d6f7b9e8baac8a37", 547094272),
     ("csa_chunked_prefill_bf16_64k_8k", "indexer"): (
-        ["k_indexer_tc.cu", "tc_util.cuh", "common.cuh"], "9e56bce23e6c0021", 712416256),
+        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "d6f7b9e8baac8a37", 712484608),
+    ("csa_decode_bf16_b32_128k", "attention"): (
+        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "5b9077c3ddc945a5", 40542976),
     ("hca_decode_bf16_b32_1m", "attention"): (
-        ["k_attend_tc.cu", "tc_util.cuh", "common.cuh"], "d3971cf40a8a59e9", 284304512),
+        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "5b9077c3ddc945a5", 282211584),
+    ("csa_chunked_prefill_bf16_64k_8k", "attention"): (
+        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "5b9077c3ddc945a5", 1182272256),
+    ("csa_decode_bf16_b32_128k", "topk"): (
+        ['k_topk.cu', 'tc_util.cuh', 'common.cuh'], "0fddc9f8cadd4be9", 4233984),
 }
 
 
