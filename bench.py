@@ -355,7 +355,7 @@ class GpuStep:
             self.proj_w = (torch.randn(self.PROJ_G, self.PROJ_DG, K, device="cuda", generator=gen) /
                            K ** 0.5).to(torch.bfloat16)
             self.proj_out = torch.empty(w.Q, self.PROJ_G * self.PROJ_DG, dtype=torch.bfloat16, device="cuda")
-            self.proj_ws = L.workspace(256)
+            self.proj_ws = L.workspace(L.csa_grouped_out_proj_ws_bytes(w.Q, self.PROJ_G, self.PROJ_DG))
         if w.kind == "csa_prefill":
             self.step_inputs = {k: inp[k] for k in ("q", "kv_raw", "q_pos", "q_idx", "w_idx")}
             self.layer = PrefillLayer(cfg, w.T_cached, w.T_new)

@@ -363,11 +363,20 @@ csa_status hca_attend(const csa_params* p, const void* q, int32_t H, int32_t B, 
  *   o:   [Q, H, D] bf16 (e.g. csa_attend's out)
  *   w:   [G, d_g, K] bf16 (row n of W_g: output n's weights over K)
  *   out: [Q, G * d_g] bf16
- *   ws:  at least 256 bytes (status word: CSA_DEV_TIMEOUT on an expired wait)
+ *   ws:  at least 256 bytes (status word: CSA_DEV_TIMEOUT on an expired wait).
+ *        With at least csa_grouped_out_proj_ws_bytes(Q, G, d_g) bytes, a
+ *        decode-sized call (Q <= 128) splits K over several CTAs a group and
+ *        sums their float32 products in the workspace (in no fixed order: the
+ *        bits of an output may differ between calls within float32 rounding)
+ *        before the one bf16 rounding; with less it runs unsplit.
  * Requires H % G == 0, K a multiple of 64, d_g a positive multiple of 64;
  * other shapes return CSA_ERR_UNSUPPORTED. */
 csa_status csa_grouped_out_proj(const void* o, int32_t Q, int32_t H, int32_t D, int32_t G, const void* w,
                                 int32_t d_g, void* out, void* ws, size_t ws_bytes, csa_stream_t stream);
+
+/* Workspace bytes csa_grouped_out_proj uses at most for these sizes: 256, plus
+ * 4 * Q * G * d_g when Q <= 128 (the split products' float32 sums). */
+size_t csa_grouped_out_proj_ws_bytes(int32_t Q, int32_t G, int32_t d_g);
 
 /* Workspace */
 typedef enum {

@@ -18,7 +18,7 @@ __all__ = [
     "CsaError", "CsaParams", "F32", "BF16", "FP8_MIXED", "OP_INDEX_TOPK", "OP_INDEX_TOPK_FP8", "OP_INDEX_TOPK_FP4", "OP_ATTEND",
     "OP_HCA_ATTEND", "params", "lib", "csa_row_bytes", "csa_cache_pack", "csa_compress", "csa_append", "csa_decode_append", "csa_index_keys_pack", "csa_index_score_fp8", "csa_index_topk_fp8",
     "csa_index_keys_fp4_bytes", "csa_index_keys_pack_fp4", "csa_index_score_fp4", "csa_index_topk_fp4",
-    "csa_index_topk", "csa_index_score", "csa_topk_select", "csa_launch_count", "csa_test_withhold_indexer_loads", "csa_index_topk_noalloc", "csa_attend", "hca_attend", "csa_grouped_out_proj", "csa_workspace_bytes", "csa_workspace_init",
+    "csa_index_topk", "csa_index_score", "csa_topk_select", "csa_launch_count", "csa_test_withhold_indexer_loads", "csa_index_topk_noalloc", "csa_attend", "hca_attend", "csa_grouped_out_proj", "csa_grouped_out_proj_ws_bytes", "csa_workspace_bytes", "csa_workspace_init",
     "csa_check_status", "csa_last_device_bits", "csa_status_string", "csa_last_error",
     "workspace", "LIB_PATH",
 ]
@@ -106,6 +106,7 @@ def lib() -> ctypes.CDLL:
             "csa_index_topk_noalloc": (_i32, [P, _vp, _vp, _i32, _i32, _vp, _i64, _i32, _i32, _vp,
                                               _vp, _vp, _vp, _vp]),
             "csa_grouped_out_proj": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp, _sz, _vp]),
+            "csa_grouped_out_proj_ws_bytes": (_sz, [_i32, _i32, _i32]),
             "csa_workspace_bytes": (_sz, [P, _i32, _i32, _i32, _i32, _i32, _i64, _i64]),
             "csa_workspace_init": (_i32, [_vp, _sz, _vp]),
             "csa_check_status": (_i32, [_vp, _vp]),
@@ -282,6 +283,10 @@ def hca_attend(p, q, H, B, Q, q_pos, cache, n_cap, window, n_win, win_pos0, sink
                             _ptr(window), n_win, _ptr(win_pos0), _ptr(sink), _ptr(out), _ptr(lse),
                             _ptr(ws), ws_bytes, _stream(stream)),
            "hca_attend")
+
+
+def csa_grouped_out_proj_ws_bytes(Q, G, d_g):
+    return lib().csa_grouped_out_proj_ws_bytes(Q, G, d_g)
 
 
 def csa_grouped_out_proj(o, Q, H, D, G, w, d_g, out, ws, ws_bytes, stream=None):

@@ -457,8 +457,20 @@ csa_status csa_grouped_out_proj(const void* o, int32_t Q, int32_t H, int32_t D, 
     CHECK(check_ptr(out, "out"));
     CHECK(check_ptr(ws, "ws"));
     if (ws_bytes < kStatusWordBytes) return fail(CSA_ERR_WORKSPACE, "workspace smaller than 256 bytes");
-    cudaError_t e = launch_out_proj(o, Q, H, D, G, w, d_g, out, reinterpret_cast<uint32_t*>(ws), (cudaStream_t)stream);
+    // decode-sized calls split K when the workspace holds the float32 sums
+    float* acc = (Q <= 128 && ws_bytes >= csa_grouped_out_proj_ws_bytes(Q, G, d_g))
+                     ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + kStatusWordBytes)
+                     : nullptr;
+    cudaError_t e = launch_out_proj(o, Q, H, D, G, w, d_g, out, acc, reinterpret_cast<uint32_t*>(ws),
+                                    (cudaStream_t)stream);
     return e == cudaSuccess ? CSA_OK : cuda_fail(e, "csa_grouped_out_proj");
+}
+
+size_t csa_grouped_out_proj_ws_bytes(int32_t Q, int32_t G, int32_t d_g) {
+    if (Q < 0 || G < 1 || d_g < 1) return 0;
+    size_t n = kStatusWordBytes;
+    if (Q <= 128) n += (size_t)4 * (size_t)Q * (size_t)G * (size_t)d_g;
+    return n;
 }
 
 uint64_t csa_launch_count(void) { return (uint64_t)g_launches.load(); }

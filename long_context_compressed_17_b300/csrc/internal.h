@@ -128,8 +128,10 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
 
 // Grouped output projection (k_out_proj.cu).
 bool out_proj_supported(int H, int D, int G, int d_g);
+// acc: float32 [Q, G * d_g] scratch for split-K sums (decode-sized Q), or
+// nullptr to run unsplit.
 cudaError_t launch_out_proj(const void* o, int Q, int H, int D, int G, const void* w, int d_g, void* out,
-                            uint32_t* status, cudaStream_t st);
+                            float* acc, uint32_t* status, cudaStream_t st);
 
 // SM count of the current device (cached per device).
 int num_sms();

@@ -297,4 +297,8 @@ def test_grouped_out_proj_validation(L):
     assert _status_of(L.csa_grouped_out_proj, **dict(base, d_g=100)) == 2  # d_g % 64
     assert _status_of(L.csa_grouped_out_proj, **dict(base, o=FAKE + 8)) == 1
     assert _status_of(L.csa_grouped_out_proj, **dict(base, ws_bytes=16)) == 4
+    # decode-sized calls may use float32 sums in the workspace; larger ones need the status word only
+    assert L.csa_grouped_out_proj_ws_bytes(32, 8, 512) == 256 + 4 * 32 * 8 * 512
+    assert L.csa_grouped_out_proj_ws_bytes(129, 8, 512) == 256
+    assert L.csa_grouped_out_proj_ws_bytes(-1, 8, 512) == 0
     assert L.csa_launch_count() == n0

@@ -1,7 +1,9 @@
 """GPU parity of the grouped output projection ["DeepSeek-V4百万上下文时代的开源
 宣言" §三.2 CSA "Step 4: Grouped Output Projection"] against the oracle:
-decode-sized (32 queries, narrow tiles streaming the weights), prefill-sized
-with a ragged last query tile (wide tiles), and a small odd shape.  Every bf16
+decode-sized (32 queries, narrow tiles streaming the weights; unsplit, and
+with K split over four CTAs a group whose float32 products are summed in the
+workspace), prefill-sized with a ragged last query tile (wide tiles), and a
+small odd shape.  Every bf16
 output must be the rounding of a value within float32 accumulation noise of
 the oracle's double result (so it equals the rounded oracle except near a
 rounding midpoint), and the outputs meet the bf16 tolerances."""
@@ -25,13 +27,13 @@ def L():
     return pkg
 
 
-def _case(L, Q, H, D, G, d_g, seed):
+def _case(L, Q, H, D, G, d_g, seed, split=False):
     g = torch.Generator(device="cpu").manual_seed(seed)
     K = H // G * D
     o = torch.randn(Q, H, D, generator=g).to(torch.bfloat16)
     w = (torch.randn(G, d_g, K, generator=g) / K ** 0.5).to(torch.bfloat16)
     out = torch.full((Q, G * d_g), float("nan"), dtype=torch.bfloat16, device="cuda")
-    ws = L.workspace(256)
+    ws = L.workspace(L.csa_grouped_out_proj_ws_bytes(Q, G, d_g) if split else 256)
     L.csa_grouped_out_proj(o.cuda(), Q, H, D, G, w.cuda(), d_g, out, ws, ws.numel())
     torch.cuda.synchronize()
     L.csa_check_status(ws)
@@ -53,6 +55,11 @@ def _case(L, Q, H, D, G, d_g, seed):
 
 def test_decode_sized(L):
     _case(L, Q=32, H=64, D=512, G=8, d_g=512, seed=91)
+
+
+def test_decode_sized_split_k(L):
+    _case(L, Q=32, H=64, D=512, G=8, d_g=512, seed=94, split=True)
+    _case(L, Q=7, H=8, D=128, G=2, d_g=128, seed=95, split=True)  # K = 512: one step a CTA
 
 
 def test_prefill_sized_with_a_ragged_tile(L):
