@@ -42,6 +42,18 @@ def test_csa_decode_small():
     assert len(st) == 4
 
 
+@pytest.mark.parametrize("B", [37, 75, 148, 149])
+def test_csa_decode_tile_deals(B):
+    """Batches around the SM count: with no more queries than SMs each query's
+    tiles are split over its own CTAs (37: four CTAs a query, one tile each;
+    75: one or two CTAs a query; 148: every query whole in one CTA), beyond it
+    (149) the tiles of all queries are dealt in balanced ranges that cut
+    queries; the combine follows either deal.  Sampled sequences."""
+    w = SMALL_CSA.replace(name="csa_decode_deal_%d" % B, B=B,
+                          L_per_seq=tuple(600 + 37 * b for b in range(B)), topk=100)
+    decode_parity(w, seqs=sorted({0, 1, B // 2, B - 2, B - 1}))
+
+
 def test_csa_decode_small_sink_neginf():
     w = SMALL_CSA.replace(sink="neginf", B=2, L_per_seq=(3000, 1024))
     decode_parity(w)
