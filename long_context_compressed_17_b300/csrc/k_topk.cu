@@ -237,7 +237,9 @@ __device__ Select radix_select(const uint32_t* keys, int n, int k, uint32_t lo, 
         prefix |= (uint32_t)d << shift;
         if (shift == 0) return Select{prefix, remaining};
         top = shift - 1;
-        if (cnt <= kCandCap && src != s.cand) {
+        // (a cluster's CTAs hold a quarter of the row each: their later
+        // passes sweep their own keys again, cheaper than copying them out)
+        if (CS == 1 && cnt <= kCandCap && src != s.cand) {
             // the keys of digit d go to the candidate list (their order is
             // irrelevant): each warp counts its range's hits, takes its place
             // in the list with one atomic, then writes them
