@@ -23,10 +23,11 @@ constexpr size_t kCompressStageMax = 160 * 1024;  // raw block staged in smem up
 // row[0, D) holds a pooled vector (shared memory) and ss each thread's partial
 // sum of its squares: RMSNorm it, rotate its last 64 dims at position pos and
 // store it into a cache row at dst (whole CTA; red: 32 floats of scratch).
+template <int NT>
 __device__ void norm_rope_store(float* row, float ss, float* red, int D, float eps, double pos,
                                 const RopeTheta& theta, int kvfmt, uint8_t* dst) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int nwarps = kCompressThreads / 32;
+    constexpr int nwarps = NT / 32;
     ss = warp_sum(ss);
     if (lane == 0) red[warp] = ss;
     __syncthreads();
@@ -37,7 +38,7 @@ __device__ void norm_rope_store(float* row, float ss, float* red, int D, float e
     }
     __syncthreads();
     const float rn = red[31];
-    for (int d = tid; d < D; d += kCompressThreads) row[d] *= rn;
+    for (int d = tid; d < D; d += NT) row[d] *= rn;
     __syncthreads();
     if (tid < kRopeDims / 2) {
         const int j = tid;
@@ -54,15 +55,16 @@ __device__ void norm_rope_store(float* row, float ss, float* red, int D, float e
 
 // The window row of raw token `tok` (RMSNorm, RoPE at pos; what the
 // compressor with m = 1 writes), through row[0, D).
+template <int NT>
 __device__ void window_row(const uint8_t* tok, int act, float* row, float* red, int D, float eps, double pos,
                            const RopeTheta& theta, int kvfmt, uint8_t* dst) {
     float ss = 0.f;
-    for (int d = threadIdx.x; d < D; d += kCompressThreads) {
+    for (int d = threadIdx.x; d < D; d += NT) {
         const float c = load_act(tok, act, d);
         row[d] = c;
         ss = fmaf(c, c, ss);
     }
-    norm_rope_store(row, ss, red, D, eps, pos, theta, kvfmt, dst);
+    norm_rope_store<NT>(row, ss, red, D, eps, pos, theta, kvfmt, dst);
 }
 
 // The block of m raw rows at src (shared memory or global) pooled into one
@@ -70,12 +72,13 @@ __device__ void window_row(const uint8_t* tok, int act, float* row, float* red, 
 // over the block, the weighted sum, RMSNorm and RoPE at `pos` (whole CTA; z:
 // m floats, row: D floats, red: 32 floats of shared scratch).  m = 1 is a
 // window row: its single weight is exactly 1.
+template <int NT>
 __device__ __forceinline__ void pool_block_store(const uint8_t* src, int act, int64_t act_row_bytes, int D, int m,
                                                  const float* __restrict__ w_z, const float* __restrict__ bias,
                                                  float* z, float* row, float* red, float eps, double pos,
                                                  const RopeTheta& theta, int kvfmt, uint8_t* dst) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int nwarps = kCompressThreads / 32;
+    constexpr int nwarps = NT / 32;
     if (m == 1) {
         // a single token: its pooling weight is exactly 1 (window rows)
         if (tid == 0) z[0] = 1.f;
@@ -105,14 +108,14 @@ __device__ __forceinline__ void pool_block_store(const uint8_t* src, int act, in
     }
     // pooled vector and its sum of squares
     float ss = 0.f;
-    for (int d = tid; d < D; d += kCompressThreads) {
+    for (int d = tid; d < D; d += NT) {
         float c = 0.f;
         for (int t = 0; t < m; t++) c = fmaf(z[t], load_act(src + t * act_row_bytes, act, d), c);
         row[d] = c;
         ss = fmaf(c, c, ss);
     }
     // RMSNorm, partial RoPE at the block's last position, store
-    norm_rope_store(row, ss, red, D, eps, pos, theta, kvfmt, dst);
+    norm_rope_store<NT>(row, ss, red, D, eps, pos, theta, kvfmt, dst);
 }
 
 // grid (n_blocks_out, B).  Dynamic smem: (m + D + 32) floats, rounded up to
@@ -142,11 +145,11 @@ __global__ void __launch_bounds__(kCompressThreads)
         src = stage;
     }
     const double pos = (double)(pos0 + b * m + m - 1);
-    pool_block_store(src, act, act_row_bytes, D, m, w_z, bias, z, row, red, eps, pos, theta, kvfmt,
+    pool_block_store<kCompressThreads>(src, act, act_row_bytes, D, m, w_z, bias, z, row, red, eps, pos, theta, kvfmt,
                      out + blockIdx.y * out_seq_bytes + b * kv_row_bytes);
     if (win_out != nullptr) {  // the window row of the block's last token
         __syncthreads();       // `row` is free again
-        window_row(src + (m - 1) * act_row_bytes, act, row, red, D, eps, pos, theta, kvfmt,
+        window_row<kCompressThreads>(src + (m - 1) * act_row_bytes, act, row, red, D, eps, pos, theta, kvfmt,
                    win_out + blockIdx.y * win_seq_bytes + b * kv_row_bytes);
     }
 }
@@ -229,7 +232,8 @@ __device__ __forceinline__ void cluster_pool_store(const ClusterSmem& c, int ran
     if (rank == kSplit - 1 && win_dst != nullptr) {
         // the window row of the block's last token, the last row of this slice;
         // this CTA's own slots are unused and hold the row
-        window_row(stage + (mt - 1) * act_row_bytes, act, slots, red, D, eps, pos, theta, kvfmt, win_dst);
+        window_row<kCompressThreads>(stage + (mt - 1) * act_row_bytes, act, slots, red, D, eps, pos, theta, kvfmt,
+                                     win_dst);
         return;
     }
     if (rank != 0) return;
@@ -248,7 +252,7 @@ __device__ __forceinline__ void cluster_pool_store(const ClusterSmem& c, int ran
         row[d] = cc;
         ss = fmaf(cc, cc, ss);
     }
-    norm_rope_store(row, ss, red, D, eps, pos, theta, kvfmt, entry_dst);
+    norm_rope_store<kCompressThreads>(row, ss, red, D, eps, pos, theta, kvfmt, entry_dst);
 }
 
 __global__ void __launch_bounds__(kCompressThreads)
@@ -308,7 +312,10 @@ __device__ __forceinline__ bool append_completes(const DecodeAppend& d, int64_t 
 }
 
 // grid (B); dynamic smem: (m + D + 32) floats rounded up to 16 bytes, then m raw rows.
-__global__ void __launch_bounds__(kCompressThreads)
+// kAppendThreads threads and at most 48 registers each: a CTA fits on an SM
+// beside one of the indexer or the top-k, which the append runs beside.
+constexpr int kAppendThreads = 128;
+__global__ void __launch_bounds__(kAppendThreads, 10)
     append_step_kernel(const DecodeAppend d, int act, int64_t act_row_bytes, int D, int m,
                        const float* __restrict__ w_z, const float* __restrict__ bias, int kvfmt,
                        int64_t kv_row_bytes, float eps, RopeTheta theta) {
@@ -329,25 +336,25 @@ __global__ void __launch_bounds__(kCompressThreads)
     uint4* last = reinterpret_cast<uint4*>(stage + (m - 1) * act_row_bytes);
     {
         const uint4* g = reinterpret_cast<const uint4*>(d.tok + s * act_row_bytes);
-        for (int64_t i = tid; i < n16; i += kCompressThreads) last[i] = __ldg(g + i);
+        for (int64_t i = tid; i < n16; i += kAppendThreads) last[i] = __ldg(g + i);
     }
     if (complete && m > 1) {  // the block's earlier tokens, written by earlier steps
         const uint4* g = reinterpret_cast<const uint4*>(d.ring + s * m * act_row_bytes);
         uint4* st = reinterpret_cast<uint4*>(stage);
-        for (int64_t i = tid; i < (int64_t)(m - 1) * n16; i += kCompressThreads) st[i] = __ldg(g + i);
+        for (int64_t i = tid; i < (int64_t)(m - 1) * n16; i += kAppendThreads) st[i] = __ldg(g + i);
     }
     __syncthreads();
     if (m > 1) {  // the new token into its slot of the raw ring
         uint4* g = reinterpret_cast<uint4*>(d.ring + (s * m + t % m) * act_row_bytes);
-        for (int64_t i = tid; i < n16; i += kCompressThreads) g[i] = last[i];
+        for (int64_t i = tid; i < n16; i += kAppendThreads) g[i] = last[i];
     }
     if (complete) {
-        pool_block_store(stage, act, act_row_bytes, D, m, w_z, bias, z, row, red, eps, (double)t, theta, kvfmt,
+        pool_block_store<kAppendThreads>(stage, act, act_row_bytes, D, m, w_z, bias, z, row, red, eps, (double)t, theta, kvfmt,
                          d.cache + (s * d.n_cap + (t + 1) / m - 1) * kv_row_bytes);
         __syncthreads();  // `row` is free again
     }
     if (d.window != nullptr)
-        window_row(stage + (m - 1) * act_row_bytes, act, row, red, D, eps, (double)t, theta, kvfmt,
+        window_row<kAppendThreads>(stage + (m - 1) * act_row_bytes, act, row, red, D, eps, (double)t, theta, kvfmt,
                    d.window + (s * d.n_win + t % d.n_win) * kv_row_bytes);
 }
 
@@ -383,7 +390,7 @@ __global__ void __launch_bounds__(kCompressThreads)
         __syncthreads();
         for (int64_t i = tid; i < n16; i += kCompressThreads) slot[i] = st[i];
         if (win_dst != nullptr)
-            window_row(c.stage, act, c.slots, c.red, D, eps, (double)t, theta, kvfmt, win_dst);
+            window_row<kCompressThreads>(c.stage, act, c.slots, c.red, D, eps, (double)t, theta, kvfmt, win_dst);
         return;
     }
     {  // slice rank of the block: ring slots rank*mt .. ; the last is the new token
@@ -488,7 +495,7 @@ cudaError_t launch_decode_append(const Geometry& g, const void* tok, int B, cons
         cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(append_step_kernel), smem);
         if (e != cudaSuccess) return e;
     }
-    append_step_kernel<<<(unsigned)B, kCompressThreads, smem, st>>>(d, g.act, act_rb, g.D, g.m, w_z, bias, g.kv,
+    append_step_kernel<<<(unsigned)B, kAppendThreads, smem, st>>>(d, g.act, act_rb, g.D, g.m, w_z, bias, g.kv,
                                                                     g.kv_row_bytes, g.eps, rope_theta(g));
     note_launch();
     return cudaGetLastError();

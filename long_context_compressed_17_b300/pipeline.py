@@ -24,7 +24,8 @@ from dataclasses import dataclass
 
 import torch
 
-from . import (BF16, F32, FP8_MIXED, OP_ATTEND, OP_HCA_ATTEND, OP_INDEX_TOPK, csa_attend,
+from . import (BF16, F32, FP8_MIXED, OP_ATTEND, OP_HCA_ATTEND, OP_INDEX_TOPK, csa_attend, csa_index_score,
+               csa_topk_select,
                csa_compress, csa_decode_append, csa_index_topk, csa_row_bytes, csa_workspace_bytes,
                hca_attend, params, workspace)
 
@@ -99,6 +100,9 @@ class DecodeLayer:
         if cfg.sparse:
             self.topk_idx = torch.empty(B, cfg.topk, dtype=torch.int32, device=device)
             self.topk_score = torch.empty(B, cfg.topk, dtype=torch.float32, device=device)
+            # a decode step's indexer scores (the step scores and selects in two calls)
+            self.ld = (n_cap + 127) // 128 * 128
+            self.scores = torch.empty(B, self.ld, dtype=torch.float32, device=device)
             nb = csa_workspace_bytes(self.p, OP_INDEX_TOPK, B, B, cfg.H, cfg.H_I, n_cap, self.n_win)
             nb = max(nb, csa_workspace_bytes(self.p, OP_ATTEND, B, B, cfg.H, cfg.H_I, n_cap, self.n_win))
         else:
@@ -124,18 +128,23 @@ class DecodeLayer:
              keys=None):
         """One decode step on the current stream: append the newest tokens,
         then attend at their positions.  For CSA the append feeds only the
-        attention, so it runs on a side stream beside the indexer and top-k
-        (whose few CTAs leave most SMs free) and the attention waits for both;
-        HCA attends to the new entries, so it appends first."""
+        attention, so it runs on a side stream beside the top-k (whose CTAs
+        leave room for it on every SM; beside the indexer it would hold the
+        indexer's CTAs back) and the attention waits for both; HCA attends to
+        the new entries, so it appends first."""
         if not self.cfg.sparse:
             self.append(kv_tok, pos, w_z, bias, raw_ring, cache, window)
             return self.attend(q, cache, window, pos, None, sink)
+        cfg = self.cfg
         main = torch.cuda.current_stream()
+        csa_index_score(self.p, q_idx, w_idx, cfg.H_I, cfg.d_I, keys, self.n_cap, self.B, self.B, pos,
+                        self.scores, self.ld, self.ws, self.ws_bytes, main)
         self._fork.record(main)
         self._side.wait_event(self._fork)
         self.append(kv_tok, pos, w_z, bias, raw_ring, cache, window, stream=self._side)
         self._join.record(self._side)
-        self.index_topk(q_idx, w_idx, keys, pos, stream=main)
+        csa_topk_select(self.p, self.scores, self.ld, self.n_cap, self.B, pos, self.topk_idx, self.topk_score,
+                        main)
         main.wait_event(self._join)
         return self.attend(q, cache, window, pos, None, sink, stream=main, selected=True)
 
