@@ -80,27 +80,39 @@ __device__ __forceinline__ void rope_cs(double pos, double theta, float* c, floa
 }
 
 // Q queries' tile lists (T tiles each, total = Q*T) dealt to `grid` CTAs in
-// contiguous ranges.  qcta == 0: balanced over all tiles (CTA c owns
-// [c*total/grid, (c+1)*total/grid)).  qcta > 0, query-aligned: queries
-// 0 .. qrem-1 get qcta+1 CTAs and the others qcta (grid = Q*qcta + qrem),
-// each query's tiles split evenly over its CTAs, so that no CTA meets two
-// queries (a CTA meeting two prepares two q' and writes two partials, and
-// the slowest CTA sets the kernel's time).
+// contiguous ranges.  qcta == 0: balanced.  Every query counts as qc + T
+// units, qc of them (the cost of preparing its q' and writing its partial,
+// in tiles) before its first tile, and CTA c owns the tiles among units
+// [c*U/grid, (c+1)*U/grid) of U = Q*(qc + T): a CTA that starts a second
+// query takes qc fewer tiles (qc 0: [c*total/grid, (c+1)*total/grid)).
+// qcta > 0, query-aligned: queries 0 .. qrem-1 get qcta+1 CTAs and the
+// others qcta (grid = Q*qcta + qrem), each query's tiles split evenly over
+// its CTAs, so that no CTA meets two queries (a CTA meeting two prepares two
+// q' and writes two partials, and the slowest CTA sets the kernel's time).
 struct TileDeal {
     int64_t total, T;
-    int grid, qcta, qrem;
+    int grid, qcta, qrem, qc;
     __host__ __device__ int64_t first_cta(int64_t qi) const { return qi * qcta + (qi < qrem ? qi : qrem); }
     __host__ __device__ int64_t ctas(int64_t qi) const { return qcta + (qi < qrem ? 1 : 0); }
+    __host__ __device__ int64_t units() const { return total / T * (T + qc); }
     // first tile of CTA c (c = grid: total)
     __host__ __device__ int64_t begin(int64_t c) const {
-        if (qcta == 0) return c * total / grid;
+        if (qcta == 0) {
+            if (qc == 0) return c * total / grid;
+            const int64_t u = c * units() / grid, qi = u / (T + qc), r = u - qi * (T + qc) - qc;
+            return qi * T + (r > 0 ? r : 0);
+        }
         const int64_t big = (int64_t)qrem * (qcta + 1);
         const int64_t qi = c < big ? c / (qcta + 1) : qrem + (c - big) / qcta;
         return qi * T + (c - first_cta(qi)) * T / ctas(qi);
     }
     // CTA that owns tile g
     __host__ __device__ int64_t cta_of(int64_t g) const {
-        if (qcta == 0) return ((g + 1) * grid - 1) / total;
+        if (qcta == 0) {
+            if (qc == 0) return ((g + 1) * grid - 1) / total;
+            const int64_t qi = g / T, u = qi * (T + qc) + qc + (g - qi * T);
+            return ((u + 1) * grid - 1) / units();
+        }
         const int64_t qi = g / T, t = g - qi * T;
         return first_cta(qi) + ((t + 1) * ctas(qi) - 1) / T;
     }

@@ -126,7 +126,7 @@ AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int6
     pl.ring = ring ? 1 : 0;
     pl.list_len = (sparse ? (int64_t)g.k : n_cap) + g.W;
     pl.use_tc = attend_tc_supported(g, sparse, H, n_cap, n_win) ? 1 : 0;
-    pl.tc_T_sel = pl.tc_T = pl.tc_grid = pl.tc_deq = pl.tc_seg = pl.tc_nseg = pl.tc_qcta = pl.tc_qrem = 0;
+    pl.tc_T_sel = pl.tc_T = pl.tc_grid = pl.tc_deq = pl.tc_seg = pl.tc_nseg = pl.tc_qcta = pl.tc_qrem = pl.tc_qc = 0;
     pl.tc_total = 0;
     if (pl.use_tc) {
         pl.head_group = H;
@@ -162,7 +162,13 @@ AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int6
     size_t o_bytes = align256((size_t)Q * pl.splits * H * g.D * sizeof(float));
     pl.part_ml_off = pl.part_o_off + o_bytes;
     size_t ml_bytes = align256((size_t)Q * pl.splits * H * 2 * sizeof(float));
-    pl.deq_off = pl.part_ml_off + ml_bytes;
+    pl.nslots_off = 0;
+    size_t ns_bytes = 0;
+    if (pl.use_tc && pl.tc_seg == 0) {
+        pl.nslots_off = pl.part_ml_off + ml_bytes;
+        ns_bytes = align256((size_t)Q * sizeof(int32_t));
+    }
+    pl.deq_off = pl.part_ml_off + ml_bytes + ns_bytes;
     const size_t deq_bytes = align256(deq_rows * g.D * 2);
     pl.total = pl.deq_off + deq_bytes;
     return pl;

@@ -68,14 +68,18 @@ struct AttendPlan {
     // per query
     int tc_seg, tc_nseg;
     // query-aligned ranges (see TileDeal): CTAs per query, and how many
-    // queries get one more (tc_qcta 0: balanced over all tiles)
-    int tc_qcta, tc_qrem;
+    // queries get one more (tc_qcta 0: balanced over all tiles, each query
+    // counted as tc_qc more tiles than it has)
+    int tc_qcta, tc_qrem, tc_qc;
     // FP8 rows reach the tensor-core kernel dequantised to bf16 in the
     // workspace: 1 = the rows each query reads, [Q, tc_T * 64, D] in tile
     // order; 2 = every stored row, [B, n_cap, D] then [B, n_win, D]; 0 = the
     // stored rows are bf16 already
     int tc_deq;
     size_t part_o_off, part_ml_off;  // [Q, S, H, D] and [Q, S, H, 2] float32
+    // [Q] int32 (tensor-core ranges only, else 0): how many CTAs left a
+    // partial of each query (0: its only CTA finished it)
+    size_t nslots_off;
     size_t deq_off;                  // bf16 rows of tc_deq
     size_t total;
 };

@@ -202,67 +202,74 @@ __global__ void __launch_bounds__(kAttThreads) attend_generic_kernel(AttendArgs 
 }
 
 // Merge split partials, add the sink, normalise, rotate by -i and store.
-// Block (q, h), 128 threads, thread t owning dims 4t .. 4t+3 (D <= 512).
-// Every warp derives the slot weights and the denominator itself (the same
-// expressions over the same values, so the same bits in every warp): no
-// block barrier, and the partial rows are requested before the weights.
-//   CUDA-core kernel, or fixed splits (tiles == 0): grid Q*H, query q has
+// One warp per (query, head) item, four warps a block; lane l owns the
+// float4 chunks l, l+32, l+64, l+96 of the row (dims 4c .. 4c+3 of chunk c,
+// D <= 512), so the item's scalar work (the slot weights, the denominator,
+// the rotation) is done once for the whole row.  The rows of the first
+// kRing slots are requested at once (before the count of slots is known
+// where it is read from memory: slots below S_alloc are inside the
+// allocation), and every later slot's row kRing slots ahead of its use.
+//   CUDA-core kernel, or fixed splits (tiles == 0): Q*H items, query q has
 //   S_alloc partials.
 //   Tensor-core kernel (tiles > 0): the CTAs own contiguous ranges of all
 //   queries' tile lists (tiles per query) as TileDeal{total, tiles, grid,
-//   qcta, qrem} deals them; only a query cut by a CTA boundary has partials
-//   (one per CTA meeting it), every other query was finished by its only
-//   CTA.  With by_query the grid is Q*H and block (q, h) takes query q if it
-//   was cut; otherwise the grid is (grid-1)*H and block (b-1, h) handles the
-//   query cut by boundary b, if b is the first boundary inside it.
-__global__ void __launch_bounds__(128)
+//   qcta, qrem, qc} deals them; only a query cut by a CTA boundary has
+//   partials (one per CTA meeting it, nslots[q] of them, written by the CTA
+//   holding its first tile), every other query was finished by its only CTA
+//   (nslots[q] = 0).  With by_query item (q, h) takes query q if it was cut;
+//   otherwise there are (grid-1)*H items and item (b-1, h) handles the query
+//   cut by boundary b, if b is the first boundary inside it.
+constexpr int kCombineWarps = 4;
+__global__ void __launch_bounds__(32 * kCombineWarps)
     attend_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
-                          int S_alloc, int H, int D, const float* __restrict__ sink,
-                          const int64_t* __restrict__ q_pos, int derotate, void* __restrict__ out,
-                          int act, float* __restrict__ lse, int64_t tiles, int64_t total, int grid,
-                          int qcta, int qrem, int by_query, RopeTheta theta) {
+                          const int32_t* __restrict__ nslots, int S_alloc, int H, int D,
+                          const float* __restrict__ sink, const int64_t* __restrict__ q_pos, int derotate,
+                          void* __restrict__ out, int act, float* __restrict__ lse, int64_t tiles, int64_t total,
+                          int grid, int qcta, int qrem, int qc, int by_query, int64_t items, RopeTheta theta) {
     tc::grid_dep_wait();  // the partials of the attention kernel before (a programmatic dependent launch)
-    const int tid = threadIdx.x, lane = tid & 31;
-    const int h = (int)(blockIdx.x % H);
-    int64_t qi;
-    int Sq;
-    if (tiles > 0) {
-        const TileDeal deal{total, tiles, grid, qcta, qrem};
-        auto cta_of = [&](int64_t g) { return deal.cta_of(g); };
-        int64_t c0;
-        if (by_query) {
-            qi = blockIdx.x / H;
-            c0 = cta_of(qi * tiles);
-        } else {
-            const int64_t b = blockIdx.x / H + 1;
-            const int64_t g = deal.begin(b);     // first tile of CTA b
-            if (g % tiles == 0) return;          // the boundary falls between queries
-            qi = g / tiles;
-            c0 = cta_of(qi * tiles);
-            if (c0 + 1 != b) return;             // handled at the query's first boundary
-        }
-        const int64_t c1 = cta_of((qi + 1) * tiles - 1);
-        if (c1 == c0) return;                    // finished by its only CTA
-        Sq = (int)(c1 - c0 + 1);
-    } else {
-        qi = blockIdx.x / H;
-        Sq = S_alloc;
+    const int lane = threadIdx.x & 31;
+    const int64_t item = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+    if (item >= items) return;
+    const int h = (int)((uint32_t)item % (uint32_t)H);  // items < 2^31
+    const int64_t unit = (int64_t)((uint32_t)item / (uint32_t)H);
+    int64_t qi = unit;
+    int Sq = S_alloc;  // an upper bound until nslots is read
+    if (tiles > 0 && !by_query) {
+        const TileDeal deal{total, tiles, grid, qcta, qrem, qc};
+        const int64_t b = unit + 1;
+        const int64_t g = deal.begin(b);         // first tile of CTA b
+        if (g % tiles == 0) return;              // the boundary falls between queries
+        qi = g / tiles;
+        const int64_t c0 = deal.cta_of(qi * tiles);
+        if (c0 + 1 != b) return;                 // handled at the query's first boundary
+        Sq = (int)(deal.cta_of((qi + 1) * tiles - 1) - c0 + 1);
     }
     const int S = S_alloc;
-    const int64_t i = q_pos[qi];
     const float* ml = part_ml + (qi * S * H + h) * 2;  // slot s: ml[s * 2H], ml[s * 2H + 1]
     const int64_t mstep = (int64_t)H * 2;
     const float4* po = reinterpret_cast<const float4*>(part_o + (qi * S * H + h) * D);  // slot s: po[s * H*D/4]
     const int64_t ostep = (int64_t)H * D / 4;
-    const int d4 = tid;
-    const bool active = d4 < D / 4;
-    // the first eight slots' rows head out first: they do not wait for the weights
-    constexpr int kBatch = 8;
-    float4 v[kBatch];
+    constexpr int kC = 4;     // chunks a lane (D / 4 <= 128)
+    constexpr int kRing = 4;  // slots whose rows are in flight
+    const int nc = D / 4;
+    float4 v[kRing][kC];
+    auto request = [&](int s2, float4* r) {  // slot s2's row into ring entry r
 #pragma unroll
-    for (int j = 0; j < kBatch; j++)
-        if (active && j < Sq) v[j] = __ldg(po + j * ostep + d4);
+        for (int k = 0; k < kC; k++)
+            if (lane + 32 * k < nc) r[k] = __ldg(po + s2 * ostep + lane + 32 * k);
+    };
+#pragma unroll
+    for (int j = 0; j < kRing; j++)
+        if (j < Sq) request(j, v[j]);
+    const int64_t i = q_pos[qi];
     const float sk = sink[h];
+    if (tiles > 0 && by_query) {
+        Sq = nslots[qi];
+        if (Sq == 0) return;                     // finished by its only CTA
+    }
+    // RoPE at -i for pair `lane` of the rotated dims (the same for every head)
+    float rc = 1.f, rs = 0.f;
+    if (derotate) rope_cs(-(double)i, theta.t[lane], &rc, &rs);
     float mstar = sk;
     for (int s2 = lane; s2 < Sq; s2 += 32) mstar = fmaxf(mstar, __ldg(ml + s2 * mstep));
     mstar = warp_max(mstar);
@@ -274,50 +281,57 @@ __global__ void __launch_bounds__(128)
     for (int s2 = lane; s2 < Sq; s2 += 32) l += weight(s2) * __ldg(ml + s2 * mstep + 1);
     l = warp_sum(l);
     if (mstar != -INFINITY && sk != -INFINITY) l += expf(sk - mstar);
-    if (tid == 0 && lse) lse[qi * H + h] = l > 0.f ? mstar + logf(l) : -INFINITY;
-    if (!active) return;
+    if (lane == 0 && lse) lse[qi * H + h] = l > 0.f ? mstar + logf(l) : -INFINITY;
     const float inv = l > 0.f ? 1.f / l : 0.f;
     // slot weights in slot order; a slot of weight 0 is not added (its values
     // are never used, whatever they hold)
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < Sq; s0 += kBatch) {
-        if (s0 > 0) {
+    float4 acc[kC];
 #pragma unroll
-            for (int j = 0; j < kBatch; j++)
-                if (s0 + j < Sq) v[j] = __ldg(po + (s0 + j) * ostep + d4);
-        }
+    for (int k = 0; k < kC; k++) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < Sq; s0 += kRing) {
 #pragma unroll
-        for (int j = 0; j < kBatch; j++) {
-            if (s0 + j >= Sq) break;
-            const float w = weight(s0 + j);
-            if (w == 0.f) continue;
-            acc.x = fmaf(w, v[j].x, acc.x);
-            acc.y = fmaf(w, v[j].y, acc.y);
-            acc.z = fmaf(w, v[j].z, acc.z);
-            acc.w = fmaf(w, v[j].w, acc.w);
-        }
-    }
-    float o[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
-    const int d0 = 4 * d4;
-    if (derotate && d0 >= D - kRopeDims) {
+        for (int j = 0; j < kRing; j++) {
+            const int s2 = s0 + j;
+            if (s2 >= Sq) break;
+            const float w = weight(s2);
+            if (w != 0.f) {
 #pragma unroll
-        for (int pr = 0; pr < 2; pr++) {
-            const int j = (d0 + 2 * pr - (D - kRopeDims)) >> 1;
-            float c, sn;
-            rope_cs(-(double)i, theta.t[j], &c, &sn);
-            const float x0 = o[2 * pr], x1 = o[2 * pr + 1];
-            o[2 * pr] = x0 * c - x1 * sn;
-            o[2 * pr + 1] = x0 * sn + x1 * c;
+                for (int k = 0; k < kC; k++) {
+                    acc[k].x = fmaf(w, v[j][k].x, acc[k].x);
+                    acc[k].y = fmaf(w, v[j][k].y, acc[k].y);
+                    acc[k].z = fmaf(w, v[j][k].z, acc[k].z);
+                    acc[k].w = fmaf(w, v[j][k].w, acc[k].w);
+                }
+            }
+            if (s2 + kRing < Sq) request(s2 + kRing, v[j]);  // slot s2's entry is free again
         }
     }
-    if (act == CSA_F32) {
-        reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (qi * H + h) * D)[d4] =
-            make_float4(o[0], o[1], o[2], o[3]);
-    } else {
-        uint2 pk;
-        pk.x = (uint32_t)f32_to_bf16_rn(o[0]) | ((uint32_t)f32_to_bf16_rn(o[1]) << 16);
-        pk.y = (uint32_t)f32_to_bf16_rn(o[2]) | ((uint32_t)f32_to_bf16_rn(o[3]) << 16);
-        reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(out) + (qi * H + h) * D)[d4] = pk;
+    // the rotated dims D-64 .. D-1 are chunks (D-64)/4 .. D/4-1: lanes 16..31
+    // of one k, whose pairs are 2(lane-16) and 2(lane-16)+1
+    const int p0 = 2 * (lane & 15);
+    const float c0 = __shfl_sync(0xffffffffu, rc, p0), s0 = __shfl_sync(0xffffffffu, rs, p0);
+    const float c1 = __shfl_sync(0xffffffffu, rc, p0 + 1), s1 = __shfl_sync(0xffffffffu, rs, p0 + 1);
+#pragma unroll
+    for (int k = 0; k < kC; k++) {
+        const int c = lane + 32 * k;
+        if (c >= nc) break;
+        float o[4] = {acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv};
+        if (derotate && 4 * c >= D - kRopeDims) {
+            const float x0 = o[0], x1 = o[1], x2 = o[2], x3 = o[3];
+            o[0] = x0 * c0 - x1 * s0;
+            o[1] = x0 * s0 + x1 * c0;
+            o[2] = x2 * c1 - x3 * s1;
+            o[3] = x2 * s1 + x3 * c1;
+        }
+        if (act == CSA_F32) {
+            reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (qi * H + h) * D)[c] =
+                make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+            uint2 pk;
+            pk.x = (uint32_t)f32_to_bf16_rn(o[0]) | ((uint32_t)f32_to_bf16_rn(o[1]) << 16);
+            pk.y = (uint32_t)f32_to_bf16_rn(o[2]) | ((uint32_t)f32_to_bf16_rn(o[3]) << 16);
+            reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(out) + (qi * H + h) * D)[c] = pk;
+        }
     }
 }
 
@@ -325,8 +339,8 @@ cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool spars
                              int H, int B, int Q, const int64_t* q_pos, const void* cache,
                              int64_t n_cap, const int32_t* topk_idx, const void* window,
                              int64_t n_win, const int64_t* win_pos0, const float* sink,
-                             void* out, float* lse, float* part_o, float* part_ml, uint8_t* deq,
-                             uint32_t* status, cudaStream_t st);
+                             void* out, float* lse, float* part_o, float* part_ml, int32_t* nslots,
+                             uint8_t* deq, uint32_t* status, cudaStream_t st);
 
 template <int D, int HG>
 static cudaError_t run_generic(const AttendArgs& a, int Q, int H, cudaStream_t st) {
@@ -348,10 +362,11 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
     if (Q == 0) return cudaSuccess;
     float* part_o = reinterpret_cast<float*>(ws + pl.part_o_off);
     float* part_ml = reinterpret_cast<float*>(ws + pl.part_ml_off);
+    int32_t* nslots = pl.nslots_off ? reinterpret_cast<int32_t*>(ws + pl.nslots_off) : nullptr;
     cudaError_t e;
     if (pl.use_tc) {
         e = launch_attend_tc(g, pl, sparse, q, H, B, Q, q_pos, cache, n_cap, topk_idx, window,
-                             n_win, win_pos0, sink, out, lse, part_o, part_ml, ws + pl.deq_off, status, st);
+                             n_win, win_pos0, sink, out, lse, part_o, part_ml, nslots, ws + pl.deq_off, status, st);
     } else {
         AttendArgs a;
         a.q = reinterpret_cast<const uint8_t*>(q);
@@ -390,19 +405,22 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
         else return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
-    // tensor-core kernel with balanced ranges: a block per query when there
-    // are no more queries than CTA boundaries, else a block per boundary.
-    // Fixed splits (and the CUDA-core kernel): every query has pl.splits
-    // partials, merged in split order by a block per query.
+    // tensor-core kernel with ranges: an item per (query, head) when there
+    // are no more queries than CTA boundaries (or the ranges are
+    // query-aligned), else per (boundary, head).  Fixed splits (and the
+    // CUDA-core kernel): every query has pl.splits partials, merged in split
+    // order by an item per (query, head).
     const bool ranges = pl.use_tc && pl.tc_seg == 0;
     const int by_query = ranges && (Q <= pl.tc_grid - 1 || pl.tc_qcta > 0);
-    const int64_t blocks = (!ranges || by_query) ? (int64_t)Q * H : (int64_t)(pl.tc_grid - 1) * H;
-    if (blocks == 0) return cudaSuccess;  // every query was finished by its only CTA
+    const int64_t items = (!ranges || by_query) ? (int64_t)Q * H : (int64_t)(pl.tc_grid - 1) * H;
+    if (items == 0) return cudaSuccess;  // every query was finished by its only CTA
+    if (g.D % 128 != 0 || g.D > 512) return cudaErrorInvalidValue;  // the combine's lane layout
+    const int64_t blocks = (items + kCombineWarps - 1) / kCombineWarps;
     const cudaError_t ec = launch_dependent(
-        attend_combine_kernel, dim3((unsigned)blocks), dim3(128), 0, st, part_o, part_ml, pl.splits, H, g.D, sink,
-        q_pos, g.derotate, out, g.act, lse, ranges ? (int64_t)pl.tc_T : 0, pl.tc_total, pl.tc_grid, pl.tc_qcta,
-        pl.tc_qrem, by_query,
-        rope_theta(g));
+        attend_combine_kernel, dim3((unsigned)blocks), dim3(32 * kCombineWarps), 0, st, part_o, part_ml,
+        ranges && by_query ? nslots : nullptr, pl.splits, H, g.D, sink, q_pos, g.derotate, out, g.act, lse,
+        ranges ? (int64_t)pl.tc_T : 0, pl.tc_total, pl.tc_grid,
+        pl.tc_qcta, pl.tc_qrem, pl.tc_qc, by_query, items, rope_theta(g));
     note_launch();
     if (ec != cudaSuccess) return ec;
     return cudaGetLastError();

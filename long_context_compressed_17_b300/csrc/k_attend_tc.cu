@@ -65,6 +65,11 @@ constexpr int kD = 512;
 constexpr int kH = 64;
 constexpr int kRows = 64;                           // rows per tile (QK MMA M)
 constexpr int kStages = 2;
+// A CTA's start of a query (preparing its q' and writing its partial) costs
+// about as much as this many tiles (HCA decode timelines: a CTA meeting two
+// queries ended 10-30 us after one meeting one, at ~3.3 us a tile; attention
+// at batch 32, 1M context: 124.9 us with 3, 122.9 us with 5, 7 or 9)
+constexpr int kQueryCostTiles = 5;
 constexpr uint32_t kBoxBytes = kRows * 128;         // 64 rows x 64 dims (bf16)
 constexpr uint32_t kStageBytes = 8 * kBoxBytes;     // 64 rows x 512 dims
 constexpr uint32_t kQBoxBytes = kH * 128;           // 64 heads x 64 dims
@@ -98,10 +103,11 @@ struct AttTcArgs {
     int64_t total;            // Q * T
     int grid;
     int seg, nseg;            // batch-invariant splits of seg tiles, nseg per query (seg 0: off)
-    int qcta, qrem;           // query-aligned ranges (TileDeal; qcta 0: balanced over all tiles)
+    int qcta, qrem, qc;       // the ranges' TileDeal (qcta 0: balanced, a query counted as qc + T tiles)
     int S;                    // partial slots per query
     float* part_o;            // [Q, S, 64, 512]
     float* part_ml;           // [Q, S, 64, 2]
+    int32_t* nslots;          // [Q]: partials of each query, 0 if finished in one CTA (ranges; else nullptr)
     const float* sink;        // [64]
     uint16_t* out;            // [Q, 64, 512] bf16 (queries finished in one CTA)
     float* lse;               // [Q, 64] or nullptr
@@ -111,7 +117,7 @@ struct AttTcArgs {
 };
 
 __device__ __forceinline__ TileDeal deal_of(const AttTcArgs& a) {
-    return TileDeal{a.total, (int64_t)a.T, a.grid, a.qcta, a.qrem};
+    return TileDeal{a.total, (int64_t)a.T, a.grid, a.qcta, a.qrem, a.qc};
 }
 
 // CTA that owns global tile g (ranges without fixed splits).
@@ -977,8 +983,11 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
             // meeting the query; a query no other CTA meets is finished here
             // (never with fixed splits: their merge order is the same in any batch)
             const int64_t c_first = a.seg ? 0 : cta_of(a, qi * a.T);
+            const int64_t c_last = a.seg ? 0 : cta_of(a, (qi + 1) * a.T - 1);
             const int64_t slot = a.seg ? lt0 / a.seg : (int64_t)blockIdx.x - c_first;
-            const bool whole = !a.seg && c_first == cta_of(a, (qi + 1) * a.T - 1);
+            const bool whole = !a.seg && c_first == c_last;
+            // the CTA holding the query's first tile tells the combine how many partials it has
+            if (a.nslots && lt0 == 0 && tid == 0) a.nslots[qi] = whole ? 0 : (int32_t)(c_last - c_first + 1);
             {
                 const float ls = warp_reduce_scatter16<false>(l_part, lane);
                 if (row_lane) red[quarter][h0 + lane] = ls;
@@ -1140,11 +1149,18 @@ void plan_attend_tc(const Geometry& g, bool sparse, int Q, int64_t n_cap, int64_
     }
     pl->tc_grid = (int)(pl->tc_total < sms ? pl->tc_total : sms);
     pl->tc_qcta = pl->tc_qrem = 0;
+    // with no more queries than CTAs, a query's start counts as
+    // kQueryCostTiles more tiles (where every CTA's share still holds a
+    // tile); with more, every CTA starts about as many queries as another
+    pl->tc_qc = 0;
+    if (pl->tc_total > 0 && Q <= pl->tc_grid &&
+        (int64_t)Q * (pl->tc_T + kQueryCostTiles) / pl->tc_grid >= kQueryCostTiles + 1)
+        pl->tc_qc = kQueryCostTiles;
     int smax = 1;
     if (pl->tc_total > 0) {
-        auto cta = [&](int64_t t) { return ((t + 1) * pl->tc_grid - 1) / pl->tc_total; };
+        const TileDeal deal{pl->tc_total, (int64_t)pl->tc_T, pl->tc_grid, 0, 0, pl->tc_qc};
         for (int64_t q = 0; q < Q; q++) {
-            int n = (int)(cta((q + 1) * pl->tc_T - 1) - cta(q * pl->tc_T) + 1);
+            int n = (int)(deal.cta_of((q + 1) * pl->tc_T - 1) - deal.cta_of(q * pl->tc_T) + 1);
             if (n > smax) smax = n;
         }
     }
@@ -1162,6 +1178,7 @@ void plan_attend_tc_aligned(int Q, AttendPlan* pl) {
     const int64_t per = sms / Q;
     pl->tc_qcta = (int)(per < pl->tc_T ? per : pl->tc_T);
     pl->tc_qrem = pl->tc_qcta < pl->tc_T ? (int)(sms - (int64_t)Q * pl->tc_qcta) : 0;
+    pl->tc_qc = 0;
     pl->tc_grid = Q * pl->tc_qcta + pl->tc_qrem;
     pl->splits = pl->tc_qcta + (pl->tc_qrem > 0 ? 1 : 0);
 }
@@ -1170,8 +1187,8 @@ cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool spars
                              int H, int B, int Q, const int64_t* q_pos, const void* cache,
                              int64_t n_cap, const int32_t* topk_idx, const void* window,
                              int64_t n_win, const int64_t* win_pos0, const float* sink,
-                             void* out, float* lse, float* part_o, float* part_ml, uint8_t* deq,
-                             uint32_t* status, cudaStream_t st) {
+                             void* out, float* lse, float* part_o, float* part_ml, int32_t* nslots,
+                             uint8_t* deq, uint32_t* status, cudaStream_t st) {
     (void)H;
     if (pl.tc_total == 0) return cudaSuccess;
     const int64_t rb = g.kv_row_bytes;
@@ -1259,11 +1276,13 @@ cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool spars
     a.grid = pl.tc_grid;
     a.qcta = pl.tc_qcta;
     a.qrem = pl.tc_qrem;
+    a.qc = pl.tc_qc;
     a.seg = pl.tc_seg;
     a.nseg = pl.tc_nseg;
     a.S = pl.splits;
     a.part_o = part_o;
     a.part_ml = part_ml;
+    a.nslots = nslots;
     a.sink = sink;
     a.out = reinterpret_cast<uint16_t*>(out);
     a.lse = lse;

@@ -72,6 +72,17 @@ def test_hca_decode_several_tiles():
     decode_parity(SMALL_HCA_TILES)
 
 
+def test_hca_decode_query_cost_deal():
+    """Six sequences of 100 to 160 cache tiles on the SMs: each query's tiles
+    span several CTAs, and a CTA whose range starts a query takes five tiles
+    fewer than one that does not (a query's start counted as five tiles);
+    ragged lengths leave the shorter queries' last tiles dead.  Every
+    sequence checked."""
+    L = (128 * 64 * 160, 128 * 64 * 150 + 100, 128 * 9000, 128 * 64 * 100 + 7, 128 * 64 * 131 - 1, 128 * 64 * 120)
+    w = workloads.HCA_DECODE_1M.replace(name="hca_decode_cost_deal", B=6, L_per_seq=L)
+    assert len(decode_parity(w)) == 6
+
+
 def _ramp_toward_q(inp, t_max):
     """Every query head is 1 on dims 0..127 and 0 elsewhere (unrotated dims), so
     its normalised form is exactly 2 there -- exact in bf16 as well.  Cache
