@@ -53,23 +53,23 @@ L2_DRAIN_BYTES = 256 << 20
 # captured build (sha256 prefix of the listed files); otherwise it is null.
 CAPTURED_TRAFFIC = {
     ("csa_decode_bf16_b32_128k", "indexer"): (
-        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "d6f7b9e8baac8a37", 275543808),
+        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "0a757cb256b06b07", 275324928),
     ("csa_decode_fp4idx_b32_128k", "indexer"): (
-        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "d6f7b9e8baac8a37", 72882432),
+        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "0a757cb256b06b07", 72782848),
     ("csa_decode_fp8idx_b32_128k", "indexer"): (
-        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "d6f7b9e8baac8a37", 143776000),
+        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "0a757cb256b06b07", 143533056),
     ("csa_decode_fp8cache_b8_1m", "indexer"): (
-        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "d6f7b9e8baac8a37", 547094272),
+        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "0a757cb256b06b07", 546995968),
     ("csa_chunked_prefill_bf16_64k_8k", "indexer"): (
-        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "d6f7b9e8baac8a37", 712484608),
+        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "0a757cb256b06b07", 712592896),
     ("csa_decode_bf16_b32_128k", "attention"): (
-        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "5b9077c3ddc945a5", 40542976),
+        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "e4fb4fd06f750385", 40692224),
     ("hca_decode_bf16_b32_1m", "attention"): (
-        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "5b9077c3ddc945a5", 282211584),
+        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "e4fb4fd06f750385", 282173184),
     ("csa_chunked_prefill_bf16_64k_8k", "attention"): (
-        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "5b9077c3ddc945a5", 1182272256),
+        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "e4fb4fd06f750385", 1182718720),
     ("csa_decode_bf16_b32_128k", "topk"): (
-        ['k_topk.cu', 'tc_util.cuh', 'common.cuh'], "0fddc9f8cadd4be9", 4233984),
+        ['k_topk.cu', 'tc_util.cuh', 'common.cuh'], "093664ab1598c44d", 4229632),
 }
 
 

@@ -433,7 +433,6 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
     constexpr int kPvWarp = Roles<kSplit>::kPvWarp;
     constexpr int kLoaderBoxes = Roles<kSplit>::kLoaderBoxes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    tc::grid_dep_launch();  // the combine after this kernel may be scheduled now
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; s++) {
             tc::mbar_init(&full[s], 1);
