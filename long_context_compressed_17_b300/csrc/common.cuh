@@ -80,41 +80,56 @@ __device__ __forceinline__ void rope_cs(double pos, double theta, float* c, floa
 }
 
 // Q queries' tile lists (T tiles each, total = Q*T) dealt to `grid` CTAs in
-// contiguous ranges.  qcta == 0: balanced.  Every query counts as qc + T
-// units, qc of them (the cost of preparing its q' and writing its partial,
-// in tiles) before its first tile, and CTA c owns the tiles among units
-// [c*U/grid, (c+1)*U/grid) of U = Q*(qc + T): a CTA that starts a second
-// query takes qc fewer tiles (qc 0: [c*total/grid, (c+1)*total/grid)).
-// qcta > 0, query-aligned: queries 0 .. qrem-1 get qcta+1 CTAs and the
-// others qcta (grid = Q*qcta + qrem), each query's tiles split evenly over
-// its CTAs, so that no CTA meets two queries (a CTA meeting two prepares two
-// q' and writes two partials, and the slowest CTA sets the kernel's time).
+// contiguous ranges.  qcta == 0: balanced, n units over grid CTAs with the
+// first n % grid CTAs taking one more (share / owner).  Every query counts
+// as qc + T units, qc of them (the cost of preparing its q' and writing its
+// partial, in tiles) before its first tile, and CTA c owns the tiles among
+// its units of U = Q*(qc + T): a CTA that starts a second query takes qc
+// fewer tiles (qc 0: the tiles themselves are the units).  qcta > 0,
+// query-aligned: queries 0 .. qrem-1 get qcta+1 CTAs and the others qcta
+// (grid = Q*qcta + qrem), each query's tiles split evenly over its CTAs, so
+// that no CTA meets two queries (a CTA meeting two prepares two q' and
+// writes two partials, and the slowest CTA sets the kernel's time).
+// Unit, tile and CTA counts are below 2^31 (the host plans no more), so the
+// divisions run in 32 bits.
 struct TileDeal {
     int64_t total, T;
     int grid, qcta, qrem, qc;
+    // first of n units that CTA c owns (c = grid: n)
+    __host__ __device__ static int64_t share(int64_t c, int64_t n, int grid) {
+        const uint32_t per = (uint32_t)n / (uint32_t)grid, rem = (uint32_t)n - per * (uint32_t)grid;
+        return c * (int64_t)per + (c < (int64_t)rem ? c : (int64_t)rem);
+    }
+    // CTA owning unit u of n (n >= grid)
+    __host__ __device__ static int64_t owner(int64_t u, int64_t n, int grid) {
+        const uint32_t per = (uint32_t)n / (uint32_t)grid, rem = (uint32_t)n - per * (uint32_t)grid;
+        const uint32_t big = rem * (per + 1);
+        return (uint32_t)u < big ? (uint32_t)u / (per + 1) : rem + ((uint32_t)u - big) / per;
+    }
     __host__ __device__ int64_t first_cta(int64_t qi) const { return qi * qcta + (qi < qrem ? qi : qrem); }
     __host__ __device__ int64_t ctas(int64_t qi) const { return qcta + (qi < qrem ? 1 : 0); }
-    __host__ __device__ int64_t units() const { return total / T * (T + qc); }
+    __host__ __device__ int64_t units() const { return (int64_t)((uint32_t)total / (uint32_t)T) * (T + qc); }
     // first tile of CTA c (c = grid: total)
     __host__ __device__ int64_t begin(int64_t c) const {
         if (qcta == 0) {
-            if (qc == 0) return c * total / grid;
-            const int64_t u = c * units() / grid, qi = u / (T + qc), r = u - qi * (T + qc) - qc;
+            if (qc == 0) return share(c, total, grid);
+            const int64_t u = share(c, units(), grid);
+            const int64_t qi = (uint32_t)u / (uint32_t)(T + qc), r = u - qi * (T + qc) - qc;
             return qi * T + (r > 0 ? r : 0);
         }
         const int64_t big = (int64_t)qrem * (qcta + 1);
-        const int64_t qi = c < big ? c / (qcta + 1) : qrem + (c - big) / qcta;
-        return qi * T + (c - first_cta(qi)) * T / ctas(qi);
+        const int64_t qi = c < big ? (int64_t)((uint32_t)c / (uint32_t)(qcta + 1))
+                                   : qrem + (int64_t)((uint32_t)(c - big) / (uint32_t)qcta);
+        return qi * T + (uint32_t)((c - first_cta(qi)) * T) / (uint32_t)ctas(qi);
     }
     // CTA that owns tile g
     __host__ __device__ int64_t cta_of(int64_t g) const {
+        const int64_t qi = (uint32_t)g / (uint32_t)T, t = g - qi * T;
         if (qcta == 0) {
-            if (qc == 0) return ((g + 1) * grid - 1) / total;
-            const int64_t qi = g / T, u = qi * (T + qc) + qc + (g - qi * T);
-            return ((u + 1) * grid - 1) / units();
+            if (qc == 0) return owner(g, total, grid);
+            return owner(qi * (T + qc) + qc + t, units(), grid);
         }
-        const int64_t qi = g / T, t = g - qi * T;
-        return first_cta(qi) + ((t + 1) * ctas(qi) - 1) / T;
+        return first_cta(qi) + (uint32_t)((t + 1) * ctas(qi) - 1) / (uint32_t)T;
     }
 };
 

@@ -116,7 +116,7 @@ IndexTopkPlan plan_index_topk(const Geometry& g, int B, int Q, int HI, int64_t n
 }
 
 bool attend_tc_supported(const Geometry& g, bool sparse, int H, int64_t n_cap, int64_t n_win);
-void plan_attend_tc(const Geometry& g, bool sparse, int Q, int64_t n_cap, int64_t n_win, bool ring, AttendPlan* pl);
+bool plan_attend_tc(const Geometry& g, bool sparse, int Q, int64_t n_cap, int64_t n_win, bool ring, AttendPlan* pl);
 void plan_attend_tc_aligned(int Q, AttendPlan* pl);
 
 AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int64_t n_cap,
@@ -131,8 +131,14 @@ AttendPlan plan_attend(const Geometry& g, bool sparse, int B, int Q, int H, int6
     if (pl.use_tc) {
         pl.head_group = H;
         pl.rows_per_split = 0;
-        plan_attend_tc(g, sparse, Q, n_cap, n_win, ring, &pl);
-    } else {
+        // more than 2^31 tiles go to the CUDA-core kernel
+        if (!plan_attend_tc(g, sparse, Q, n_cap, n_win, ring, &pl)) {
+            pl.use_tc = 0;
+            pl.tc_T_sel = pl.tc_T = pl.tc_grid = pl.tc_seg = pl.tc_nseg = pl.tc_qcta = pl.tc_qrem = pl.tc_qc = 0;
+            pl.tc_total = 0;
+        }
+    }
+    if (!pl.use_tc) {
         pl.head_group = (H % 16 == 0) ? 16 : 8;
         const int hgs = H / pl.head_group;
         if (g.inv) {  // fixed splits: a function of the list length only

@@ -116,6 +116,24 @@ struct AttTcArgs {
     RopeTheta theta;
 };
 
+// Tile, query and split indices stay below 2^31 (the host plans no more
+// tiles, or query-start units, than that), so their divisions run in 32 bits:
+// a 64-bit division is a long inlined sequence, and the kernel's code
+// outgrew the instruction cache (ncu: 57% hits at CSA decode).
+__device__ __forceinline__ int64_t idiv(int64_t x, int64_t y) { return (int64_t)((uint32_t)x / (uint32_t)y); }
+// Positions may exceed 32 bits: their divisions take the 64-bit sequence out
+// of line, where it is never reached below 2^32.
+__device__ __noinline__ int64_t div_wide(int64_t x, int64_t y) { return x / y; }
+__device__ __noinline__ int64_t mod_wide(int64_t x, int64_t y) {  // in [0, y)
+    const int64_t m = x % y;
+    return m < 0 ? m + y : m;
+}
+// floor((i + 1) / m) for a position i
+__device__ __forceinline__ int64_t blocks_of(int64_t i, int m) {
+    const int64_t x = i + 1;
+    return (x >= 0 && x <= 0xffffffffLL) ? (int64_t)((uint32_t)x / (uint32_t)m) : div_wide(x, m);
+}
+
 __device__ __forceinline__ TileDeal deal_of(const AttTcArgs& a) {
     return TileDeal{a.total, (int64_t)a.T, a.grid, a.qcta, a.qrem, a.qc};
 }
@@ -128,17 +146,17 @@ __device__ __forceinline__ int64_t cta_of(const AttTcArgs& a, int64_t g) { retur
 // [c*n/grid, (c+1)*n/grid) of the n = Q * nseg in query order).
 __device__ __forceinline__ int64_t range_begin(const AttTcArgs& a, int64_t c) {
     if (a.seg == 0) return deal_of(a).begin(c);
-    const int64_t sp = c * (a.total / a.T * a.nseg) / a.grid;
-    const int64_t qi = sp / a.nseg;
-    return qi * a.T + min((int64_t)a.T, (sp % a.nseg) * a.seg);
+    const int64_t sp = TileDeal::share(c, idiv(a.total, a.T) * a.nseg, a.grid);
+    const int64_t qi = idiv(sp, a.nseg);
+    return qi * a.T + min((int64_t)a.T, (sp - qi * a.nseg) * a.seg);
 }
 
 // End of the segment that starts at global tile g: the end of the query's
 // tiles, of the fixed split holding g, or of the CTA's range.
 __device__ __forceinline__ int64_t seg_end_of(const AttTcArgs& a, int64_t g, int64_t g_end) {
-    const int64_t qi = g / a.T;
+    const int64_t qi = idiv(g, a.T);
     int64_t e = (qi + 1) * a.T;
-    if (a.seg > 0) e = min(e, qi * a.T + ((g - qi * a.T) / a.seg + 1) * a.seg);
+    if (a.seg > 0) e = min(e, qi * a.T + (idiv(g - qi * a.T, a.seg) + 1) * a.seg);
     return min(g_end, e);
 }
 
@@ -150,8 +168,8 @@ struct QueryInfo {
 __device__ __forceinline__ QueryInfo query_info(const AttTcArgs& a, int64_t qi) {
     QueryInfo r;
     r.i = a.q_pos[qi];
-    r.seq = (int)(qi / a.qps);
-    int64_t n = (r.i + 1) / a.m;
+    r.seq = (int)idiv(qi, a.qps);
+    int64_t n = blocks_of(r.i, a.m);
     if (n < 0) n = 0;
     r.n_av = n < a.n_cap ? n : a.n_cap;  // an overflow is flagged by the softmax warps
     return r;
@@ -174,7 +192,8 @@ __device__ __forceinline__ bool tile_live(const AttTcArgs& a, const QueryInfo& q
 // Ring window: the position row r holds for a query at position i, the
 // latest p <= i with p = r mod n_win (negative: not written yet).
 __device__ __forceinline__ int64_t ring_pos(int64_t i, int64_t r, int64_t n_win) {
-    return i - (((i - r) % n_win) + n_win) % n_win;
+    const int64_t d = i - r;
+    return i - ((d >= 0 && d <= 0xffffffffLL) ? (int64_t)((uint32_t)d % (uint32_t)n_win) : mod_wide(d, n_win));
 }
 
 // Warp roles of the two layouts.  Split (tiles loaded by TMA only): warp 1
@@ -233,7 +252,7 @@ __device__ __forceinline__ int last_live(const AttTcArgs& a, const QueryInfo& qi
 // live tile, or -1.
 __device__ __forceinline__ int64_t next_live_query(const AttTcArgs& a, int64_t g, int64_t g_end) {
     while (g < g_end) {
-        const int64_t qi = g / a.T;
+        const int64_t qi = idiv(g, a.T);
         const int64_t seg_end = seg_end_of(a, g, g_end);
         const QueryInfo inf = query_info(a, qi);
         if (last_live(a, inf, (int)(g - qi * a.T), (int)(seg_end - qi * a.T)) >= 0) return qi;
@@ -386,8 +405,8 @@ __global__ void __launch_bounds__(kDeqThreads) dequant_gather_kernel(const DeqGa
     const int64_t qi = r / per;
     const int p = (int)(r - qi * per);
     const int64_t i = a.q_pos[qi];
-    const int seq = (int)(qi / a.qps);
-    int64_t n_av = (i + 1) / a.m;
+    const int seq = (int)idiv(qi, a.qps);
+    int64_t n_av = blocks_of(i, a.m);
     n_av = n_av < 0 ? 0 : (n_av < a.n_cap ? n_av : a.n_cap);
     const uint8_t* src = nullptr;
     if (p < a.T_sel * kRows) {
@@ -493,7 +512,7 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
         // CTA's range is prefetched into L2 while the current one is loaded.
         auto prefetch_after = [&](int64_t g) {
             for (++g; g < g_end; ++g) {
-                const int64_t qi = g / a.T;
+                const int64_t qi = idiv(g, a.T);
                 const int lt = (int)(g - qi * a.T);
                 const QueryInfo inf = query_info(a, qi);
                 if (!tile_live(a, inf, lt)) continue;
@@ -508,7 +527,7 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
             }
         };
         for (int64_t g = g_begin; g < g_end; ++g) {
-            const int64_t qi = g / a.T;
+            const int64_t qi = idiv(g, a.T);
             const int lt = (int)(g - qi * a.T);
             const QueryInfo inf = query_info(a, qi);
             if (!tile_live(a, inf, lt)) continue;
@@ -571,7 +590,7 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
                 bool at_seg_start = true;
                 auto advance = [&]() -> bool {  // move g to the next live tile; false at the end
                     for (; g < g_end; ++g) {
-                        const int64_t qi = g / a.T;
+                        const int64_t qi = idiv(g, a.T);
                         if (g >= cur_end) {
                             cur_q = qi;
                             inf = query_info(a, qi);
@@ -655,7 +674,7 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
                 bool at_seg_start = true;
                 auto advance = [&]() -> bool {  // move g to the next live tile; false at the end
                     for (; g < g_end; ++g) {
-                        const int64_t qi = g / a.T;
+                        const int64_t qi = idiv(g, a.T);
                         if (g >= cur_end) {
                             cur_q = qi;
                             inf = query_info(a, qi);
@@ -838,12 +857,12 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
         float l_part[kHW];
         const float* mref = mref_s + h0;  // running reference of this warp's heads (valid once ref_set)
         for (int64_t g = g_begin; g < g_end && !stop;) {
-            const int64_t qi = g / a.T;
+            const int64_t qi = idiv(g, a.T);
             const int64_t seg_end = seg_end_of(a, g, g_end);
             const QueryInfo inf = query_info(a, qi);
             const int lt0 = (int)(g - qi * a.T), lt1 = (int)(seg_end - qi * a.T);
             const int lt_last = last_live(a, inf, lt0, lt1);
-            if (tid == 0 && (inf.i + 1) / a.m > a.n_cap) atomicOr(a.status, CSA_DEV_BAD_POSITION);
+            if (tid == 0 && blocks_of(inf.i, a.m) > a.n_cap) atomicOr(a.status, CSA_DEV_BAD_POSITION);
             // the next query's q rows head for L2 while this segment runs
             const int64_t qn = next_live_query(a, seg_end, g_end);
             const bool q_next = qn >= 0 && qn != qi;  // a further split of this query keeps q'
@@ -983,7 +1002,7 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
             // (never with fixed splits: their merge order is the same in any batch)
             const int64_t c_first = a.seg ? 0 : cta_of(a, qi * a.T);
             const int64_t c_last = a.seg ? 0 : cta_of(a, (qi + 1) * a.T - 1);
-            const int64_t slot = a.seg ? lt0 / a.seg : (int64_t)blockIdx.x - c_first;
+            const int64_t slot = a.seg ? idiv(lt0, a.seg) : (int64_t)blockIdx.x - c_first;
             const bool whole = !a.seg && c_first == c_last;
             // the CTA holding the query's first tile tells the combine how many partials it has
             if (a.nslots && lt0 == 0 && tid == 0) a.nslots[qi] = whole ? 0 : (int32_t)(c_last - c_first + 1);
@@ -1078,7 +1097,7 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
         int64_t g = g_begin;
         auto next_gathered = [&](int64_t& qi, int& lt, int& st) -> bool {
             for (; g < g_end; ++g) {
-                qi = g / a.T;
+                qi = idiv(g, a.T);
                 lt = (int)(g - qi * a.T);
                 const QueryInfo inf = query_info(a, qi);
                 if (!tile_live(a, inf, lt)) continue;
@@ -1132,10 +1151,13 @@ bool attend_tc_supported(const Geometry& g, bool sparse, int H, int64_t n_cap, i
     return true;
 }
 
-void plan_attend_tc(const Geometry& g, bool sparse, int Q, int64_t n_cap, int64_t n_win, bool ring, AttendPlan* pl) {
-    pl->tc_T_sel = sparse ? (g.k + kRows - 1) / kRows : (int)((n_cap + kRows - 1) / kRows);
+bool plan_attend_tc(const Geometry& g, bool sparse, int Q, int64_t n_cap, int64_t n_win, bool ring, AttendPlan* pl) {
+    pl->tc_T_sel = sparse ? (g.k + kRows - 1) / kRows : (int)((n_cap + (int64_t)kRows - 1) / kRows);
     const int64_t win_rows = g.W > 0 ? (ring ? n_win : (int64_t)g.W) : 0;
-    pl->tc_T = pl->tc_T_sel + (int)((win_rows + kRows - 1) / kRows);
+    const int64_t T = pl->tc_T_sel + (win_rows + kRows - 1) / kRows;
+    // the kernel's tile, unit and split indices are 32-bit
+    if ((int64_t)Q * (T + kQueryCostTiles) >= (1LL << 31)) return false;
+    pl->tc_T = (int)T;
     pl->tc_total = (int64_t)Q * pl->tc_T;
     const int64_t sms = num_sms();
     if (g.inv) {  // fixed splits of tc_seg tiles, whole splits per CTA
@@ -1144,7 +1166,7 @@ void plan_attend_tc(const Geometry& g, bool sparse, int Q, int64_t n_cap, int64_
         const int64_t segs = (int64_t)Q * pl->tc_nseg;
         pl->tc_grid = (int)(segs < sms ? segs : sms);
         pl->splits = pl->tc_nseg;
-        return;
+        return true;
     }
     pl->tc_grid = (int)(pl->tc_total < sms ? pl->tc_total : sms);
     pl->tc_qcta = pl->tc_qrem = 0;
@@ -1164,6 +1186,7 @@ void plan_attend_tc(const Geometry& g, bool sparse, int Q, int64_t n_cap, int64_
         }
     }
     pl->splits = smax;
+    return true;
 }
 
 // Query-aligned ranges (TileDeal) for gathered tiles when there are no more
