@@ -53,23 +53,23 @@ L2_DRAIN_BYTES = 256 << 20
 # captured build (sha256 prefix of the listed files); otherwise it is null.
 CAPTURED_TRAFFIC = {
     ("csa_decode_bf16_b32_128k", "indexer"): (
-        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "0a757cb256b06b07", 275324928),
+        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "900c56f3bdeb9bb8", 275500800),
     ("csa_decode_fp4idx_b32_128k", "indexer"): (
-        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "0a757cb256b06b07", 72782848),
+        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "900c56f3bdeb9bb8", 72750336),
     ("csa_decode_fp8idx_b32_128k", "indexer"): (
-        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "0a757cb256b06b07", 143533056),
+        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "900c56f3bdeb9bb8", 143350528),
     ("csa_decode_fp8cache_b8_1m", "indexer"): (
-        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "0a757cb256b06b07", 546995968),
+        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "900c56f3bdeb9bb8", 546927616),
     ("csa_chunked_prefill_bf16_64k_8k", "indexer"): (
-        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "0a757cb256b06b07", 712592896),
+        ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "900c56f3bdeb9bb8", 712617216),
     ("csa_decode_bf16_b32_128k", "attention"): (
-        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "e4fb4fd06f750385", 40692224),
+        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "1a03154d05666be7", 40616192),
     ("hca_decode_bf16_b32_1m", "attention"): (
-        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "e4fb4fd06f750385", 282173184),
+        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "1a03154d05666be7", 282105344),
     ("csa_chunked_prefill_bf16_64k_8k", "attention"): (
-        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "e4fb4fd06f750385", 1182718720),
+        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "1a03154d05666be7", 1170758656),
     ("csa_decode_bf16_b32_128k", "topk"): (
-        ['k_topk.cu', 'tc_util.cuh', 'common.cuh'], "093664ab1598c44d", 4229632),
+        ['k_topk.cu', 'tc_util.cuh', 'common.cuh'], "161157467ed6e84f", 4229632),
 }
 
 
