@@ -69,7 +69,7 @@ CAPTURED_TRAFFIC = {
     ("csa_chunked_prefill_bf16_64k_8k", "attention"): (
         ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "1a03154d05666be7", 1170758656),
     ("csa_decode_bf16_b32_128k", "topk"): (
-        ['k_topk.cu', 'tc_util.cuh', 'common.cuh'], "161157467ed6e84f", 4229632),
+        ['k_topk.cu', 'tc_util.cuh', 'common.cuh'], "b4bea44825501b24", 4229376),
 }
 
 

@@ -109,8 +109,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* sw) {
 }
 
 struct Select {
-    uint32_t T;   // key of the k-th largest
-    int take_eq;  // how many keys equal to T are kept (the lowest indices)
+    uint32_t T;   // the k-th largest key, or the least key of the last digit's bin when all of it is kept
+    int take_eq;  // how many keys equal to T are kept (the lowest indices); every key above T is kept
 };
 
 // Warp sweeps over keys in shared memory: warp w owns the contiguous range
@@ -235,7 +235,11 @@ __device__ Select radix_select(const uint32_t* keys, int n, int k, uint32_t lo, 
         const int d = s.digit, cnt = s.dcount;
         remaining -= s.above;
         prefix |= (uint32_t)d << shift;
-        if (shift == 0) return Select{prefix, remaining};
+        // Done at the last digit, or when digit d holds exactly the keys still
+        // needed: then the k-th largest key is the smallest of them, every key
+        // at or above T = prefix (its lower bits zero) is kept, and there are
+        // k of them, so the set is the exact one and has no tie to break.
+        if (shift == 0 || cnt == remaining) return Select{prefix, remaining};
         top = shift - 1;
         // (a cluster's CTAs hold a quarter of the row each: their later
         // passes sweep their own keys again, cheaper than copying them out)
