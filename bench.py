@@ -63,11 +63,11 @@ CAPTURED_TRAFFIC = {
     ("csa_chunked_prefill_bf16_64k_8k", "indexer"): (
         ['k_indexer_tc.cu', 'tc_util.cuh', 'common.cuh'], "900c56f3bdeb9bb8", 712617216),
     ("csa_decode_bf16_b32_128k", "attention"): (
-        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "1a03154d05666be7", 40616192),
+        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "19c4454ffb1084f4", 40584448),
     ("hca_decode_bf16_b32_1m", "attention"): (
-        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "1a03154d05666be7", 282105344),
+        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "19c4454ffb1084f4", 282270208),
     ("csa_chunked_prefill_bf16_64k_8k", "attention"): (
-        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "1a03154d05666be7", 1170758656),
+        ['k_attend_tc.cu', 'tc_util.cuh', 'common.cuh'], "19c4454ffb1084f4", 1172764672),
     ("csa_decode_bf16_b32_128k", "topk"): (
         ['k_topk.cu', 'tc_util.cuh', 'common.cuh'], "b4bea44825501b24", 4229376),
 }

@@ -144,8 +144,9 @@ __device__ __forceinline__ int64_t cta_of(const AttTcArgs& a, int64_t g) { retur
 // First global tile of CTA c's range: balanced over tiles or query-aligned
 // (TileDeal), or, with fixed splits, over whole splits (CTA c takes splits
 // [c*n/grid, (c+1)*n/grid) of the n = Q * nseg in query order).
+template <bool L>
 __device__ __forceinline__ int64_t range_begin(const AttTcArgs& a, int64_t c) {
-    if (a.seg == 0) return deal_of(a).begin(c);
+    if (L || a.seg == 0) return deal_of(a).begin(c);
     const int64_t sp = TileDeal::share(c, idiv(a.total, a.T) * a.nseg, a.grid);
     const int64_t qi = idiv(sp, a.nseg);
     return qi * a.T + min((int64_t)a.T, (sp - qi * a.nseg) * a.seg);
@@ -153,10 +154,11 @@ __device__ __forceinline__ int64_t range_begin(const AttTcArgs& a, int64_t c) {
 
 // End of the segment that starts at global tile g: the end of the query's
 // tiles, of the fixed split holding g, or of the CTA's range.
+template <bool L>
 __device__ __forceinline__ int64_t seg_end_of(const AttTcArgs& a, int64_t g, int64_t g_end) {
     const int64_t qi = idiv(g, a.T);
     int64_t e = (qi + 1) * a.T;
-    if (a.seg > 0) e = min(e, qi * a.T + (idiv(g - qi * a.T, a.seg) + 1) * a.seg);
+    if (!L && a.seg > 0) e = min(e, qi * a.T + (idiv(g - qi * a.T, a.seg) + 1) * a.seg);
     return min(g_end, e);
 }
 
@@ -177,13 +179,14 @@ __device__ __forceinline__ QueryInfo query_info(const AttTcArgs& a, int64_t qi) 
 
 // Whether tile lt of a query has any row that can be valid.  Every role
 // evaluates the same predicate, so skipped tiles cost nothing anywhere.
+template <bool L>
 __device__ __forceinline__ bool tile_live(const AttTcArgs& a, const QueryInfo& qi, int lt) {
     if (lt < a.T_sel) {
         if (a.topk_idx) return qi.n_av > 0;
         return (int64_t)lt * kRows < qi.n_av;
     }
     const int r0 = (lt - a.T_sel) * kRows;
-    if (a.win_pos0 == nullptr) return r0 < a.n_win && r0 <= qi.i;  // ring rows r0 ..: some hold positions <= i
+    if (L || a.win_pos0 == nullptr) return r0 < a.n_win && r0 <= qi.i;  // ring rows r0 ..: some hold positions <= i
     if (r0 >= a.W) return false;
     const int rlast = min(a.W, r0 + kRows) - 1;
     return qi.i - a.W + 1 + rlast >= 0;
@@ -212,8 +215,9 @@ struct Roles {
 
 // Whether tile lt is copied row by row from the selected cache rows (by
 // gather4) rather than loaded as a TMA tile.
+template <bool L>
 __device__ __forceinline__ bool is_gathered(const AttTcArgs& a, int lt) {
-    return !a.pre && a.topk_idx != nullptr && lt < a.T_sel;
+    return (L || !a.pre) && a.topk_idx != nullptr && lt < a.T_sel;
 }
 
 // Cache rows of the selected blocks of gathered tile lt of query qi that
@@ -242,20 +246,22 @@ __device__ __forceinline__ void gather_boxes(const CUtensorMap* tm, uint64_t* ba
 }
 
 // Last live tile of the segment [lt0, lt1) of a query, or -1.
+template <bool L>
 __device__ __forceinline__ int last_live(const AttTcArgs& a, const QueryInfo& qi, int lt0, int lt1) {
     for (int lt = lt1 - 1; lt >= lt0; --lt)
-        if (tile_live(a, qi, lt)) return lt;
+        if (tile_live<L>(a, qi, lt)) return lt;
     return -1;
 }
 
 // The first query from global tile g on (up to g_end) whose segment has a
 // live tile, or -1.
+template <bool L>
 __device__ __forceinline__ int64_t next_live_query(const AttTcArgs& a, int64_t g, int64_t g_end) {
     while (g < g_end) {
         const int64_t qi = idiv(g, a.T);
-        const int64_t seg_end = seg_end_of(a, g, g_end);
+        const int64_t seg_end = seg_end_of<L>(a, g, g_end);
         const QueryInfo inf = query_info(a, qi);
-        if (last_live(a, inf, (int)(g - qi * a.T), (int)(seg_end - qi * a.T)) >= 0) return qi;
+        if (last_live<L>(a, inf, (int)(g - qi * a.T), (int)(seg_end - qi * a.T)) >= 0) return qi;
         g = seg_end;
     }
     return -1;
@@ -428,7 +434,10 @@ __global__ void __launch_bounds__(kDeqThreads) dequant_gather_kernel(const DeqGa
 
 }  // namespace
 
-template <bool kSplit>
+// kLean: no fixed splits, no pre-gathered rows and a ring window (the
+// decode step's form); the instantiation leaves out the code of the others,
+// which keeps the kernel's instruction footprint down.
+template <bool kSplit, bool kLean>
 __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tm_sel, const __grid_constant__ CUtensorMap tm_win,
                      const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ AttTcArgs a) {
@@ -484,14 +493,14 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
     // kernel before; every global read comes after it has completed.
     tc::grid_dep_wait();
 
-    const int64_t g_begin = range_begin(a, blockIdx.x);
-    const int64_t g_end = range_begin(a, blockIdx.x + 1);
+    const int64_t g_begin = range_begin<kLean>(a, blockIdx.x);
+    const int64_t g_end = range_begin<kLean>(a, blockIdx.x + 1);
 
     if (warp == 0) {
         // ------------------------------------------------------------ loads
         // The raw q rows of the first segment go into sQ ahead of any tile:
         // the softmax warps normalise and rotate them in place.
-        const int64_t q_first = next_live_query(a, g_begin, g_end);
+        const int64_t q_first = next_live_query<kLean>(a, g_begin, g_end);
         if (q_first >= 0) {
             if (lane == 0) tc::mbar_arrive_expect_tx(&q_raw, kQBytes);
             __syncwarp();
@@ -505,7 +514,7 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
         uint32_t fills[kStages] = {0, 0};  // fills of each stage (by any warp)
         auto box_row0 = [&](const QueryInfo& inf, int lt) {
             if (lt < a.T_sel) return lt * kRows;
-            if (a.win_pos0 == nullptr) return (lt - a.T_sel) * kRows;  // ring rows in buffer order
+            if (kLean || a.win_pos0 == nullptr) return (lt - a.T_sel) * kRows;  // ring rows in buffer order
             return (int)(inf.i - a.W + 1 + (int64_t)(lt - a.T_sel) * kRows - a.win_pos0[inf.seq]);
         };
         // The next live TMA-tile (not gathered) after global tile g within this
@@ -515,10 +524,10 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
                 const int64_t qi = idiv(g, a.T);
                 const int lt = (int)(g - qi * a.T);
                 const QueryInfo inf = query_info(a, qi);
-                if (!tile_live(a, inf, lt)) continue;
-                if (a.pre) {
+                if (!tile_live<kLean>(a, inf, lt)) continue;
+                if (!kLean && a.pre) {
                     if (lane < 8) tc::tma_prefetch_3d(&tm_sel, lane * 64, lt * kRows, (int)qi);
-                } else if (!is_gathered(a, lt) && lane < 8) {
+                } else if (!is_gathered<kLean>(a, lt) && lane < 8) {
                     const int r0 = box_row0(inf, lt);
                     if (r0 >= 0)  // a window box that starts before row 0 is not prefetched
                         tc::tma_prefetch_3d(lt < a.T_sel ? &tm_sel : &tm_win, lane * 64, r0, inf.seq);
@@ -530,19 +539,19 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
             const int64_t qi = idiv(g, a.T);
             const int lt = (int)(g - qi * a.T);
             const QueryInfo inf = query_info(a, qi);
-            if (!tile_live(a, inf, lt)) continue;
+            if (!tile_live<kLean>(a, inf, lt)) continue;
             const int st = tcount & 1;
             prefetch_after(g);
             // every use of a stage is waited for here, in order, whoever fills it
             if (!warp_wait(&empty[st], ((tcount >> 1) & 1u) ^ 1u, abort_flag, a.status, lane)) break;
             if (lane == 0) tc::mbar_arrive_expect_tx(&full[st], kStageBytes);
-            if (is_gathered(a, lt)) {
+            if (is_gathered<kLean>(a, lt)) {
                 if (lane == 0) tc::mbar_arrive(&go[st]);  // the gather warps join in
             } else {
                 uint8_t* dst = sE + st * kStageBytes;
                 __syncwarp();
                 if (lane < 8) {
-                    if (a.pre)
+                    if (!kLean && a.pre)
                         tc::tma_load_3d(dst + lane * kBoxBytes, &tm_sel, &full[st], lane * 64, lt * kRows, (int)qi);
                     else
                         tc::tma_load_3d(dst + lane * kBoxBytes, lt < a.T_sel ? &tm_sel : &tm_win, &full[st],
@@ -594,11 +603,11 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
                         if (g >= cur_end) {
                             cur_q = qi;
                             inf = query_info(a, qi);
-                            cur_end = seg_end_of(a, g, g_end);
-                            lt_last = last_live(a, inf, (int)(g - qi * a.T), (int)(cur_end - qi * a.T));
+                            cur_end = seg_end_of<kLean>(a, g, g_end);
+                            lt_last = last_live<kLean>(a, inf, (int)(g - qi * a.T), (int)(cur_end - qi * a.T));
                             at_seg_start = true;
                         }
-                        if (tile_live(a, inf, (int)(g - qi * a.T))) return true;
+                        if (tile_live<kLean>(a, inf, (int)(g - qi * a.T))) return true;
                     }
                     return false;
                 };
@@ -678,11 +687,11 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
                         if (g >= cur_end) {
                             cur_q = qi;
                             inf = query_info(a, qi);
-                            cur_end = seg_end_of(a, g, g_end);
-                            lt_last = last_live(a, inf, (int)(g - qi * a.T), (int)(cur_end - qi * a.T));
+                            cur_end = seg_end_of<kLean>(a, g, g_end);
+                            lt_last = last_live<kLean>(a, inf, (int)(g - qi * a.T), (int)(cur_end - qi * a.T));
                             at_seg_start = true;
                         }
-                        if (tile_live(a, inf, (int)(g - qi * a.T))) return true;
+                        if (tile_live<kLean>(a, inf, (int)(g - qi * a.T))) return true;
                     }
                     return false;
                 };
@@ -784,7 +793,7 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
         // normalised and rotated in place.  Lane l of a warp holds dims
         // 16l .. 16l+15 of a head: two 16-byte chunks of box l/4 of that
         // head's 128-byte row.
-        uint32_t qraw_issued = next_live_query(a, g_begin, g_end) >= 0 ? 1u : 0u, qraw_done = 0;
+        uint32_t qraw_issued = next_live_query<kLean>(a, g_begin, g_end) >= 0 ? 1u : 0u, qraw_done = 0;
         auto load_q = [&](int64_t qi) {  // by one thread
             tc::mbar_arrive_expect_tx(&q_raw, kQBytes);
             for (int bx = 0; bx < 8; bx++)
@@ -849,7 +858,7 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
 
 
         {
-            const int64_t q0 = next_live_query(a, g_begin, g_end);
+            const int64_t q0 = next_live_query<kLean>(a, g_begin, g_end);
             if (q0 >= 0) prep_q(q0);
         }
         uint32_t tcount = 0, nseg = 0;
@@ -858,13 +867,13 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
         const float* mref = mref_s + h0;  // running reference of this warp's heads (valid once ref_set)
         for (int64_t g = g_begin; g < g_end && !stop;) {
             const int64_t qi = idiv(g, a.T);
-            const int64_t seg_end = seg_end_of(a, g, g_end);
+            const int64_t seg_end = seg_end_of<kLean>(a, g, g_end);
             const QueryInfo inf = query_info(a, qi);
             const int lt0 = (int)(g - qi * a.T), lt1 = (int)(seg_end - qi * a.T);
-            const int lt_last = last_live(a, inf, lt0, lt1);
+            const int lt_last = last_live<kLean>(a, inf, lt0, lt1);
             if (tid == 0 && blocks_of(inf.i, a.m) > a.n_cap) atomicOr(a.status, CSA_DEV_BAD_POSITION);
             // the next query's q rows head for L2 while this segment runs
-            const int64_t qn = next_live_query(a, seg_end, g_end);
+            const int64_t qn = next_live_query<kLean>(a, seg_end, g_end);
             const bool q_next = qn >= 0 && qn != qi;  // a further split of this query keeps q'
             if (q_next) prefetch_l2(a.q + (qn * kH + sw * (kH / kSoftWarps) + (lane >> 3)) * kD + (lane & 7) * 64);
 #pragma unroll
@@ -872,7 +881,7 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
             int seg_tiles = 0;
             bool ref_set = false;  // mref_s holds this segment's reference
             for (int lt = lt0; lt <= lt_last; ++lt) {
-                if (!tile_live(a, inf, lt)) continue;
+                if (!tile_live<kLean>(a, inf, lt)) continue;
                 const int b = tcount & 1;
                 // row validity (and the device-side checks of the row list)
                 bool valid = false;
@@ -893,7 +902,7 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
                         }
                     } else {
                         const int r = (lt - a.T_sel) * kRows + row;
-                        if (a.win_pos0 == nullptr) {  // ring row r: valid when its position is in the window
+                        if (kLean || a.win_pos0 == nullptr) {  // ring row r: valid when its position is in the window
                             const int64_t wpos = r < a.n_win ? ring_pos(inf.i, r, a.n_win) : -1;
                             valid = wpos >= 0 && wpos >= inf.i - a.W + 1;
                         } else {
@@ -1000,10 +1009,11 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
             // partial slot: the split's index, or the CTA's rank among those
             // meeting the query; a query no other CTA meets is finished here
             // (never with fixed splits: their merge order is the same in any batch)
-            const int64_t c_first = a.seg ? 0 : cta_of(a, qi * a.T);
-            const int64_t c_last = a.seg ? 0 : cta_of(a, (qi + 1) * a.T - 1);
-            const int64_t slot = a.seg ? idiv(lt0, a.seg) : (int64_t)blockIdx.x - c_first;
-            const bool whole = !a.seg && c_first == c_last;
+            const int seg = kLean ? 0 : a.seg;
+            const int64_t c_first = seg ? 0 : cta_of(a, qi * a.T);
+            const int64_t c_last = seg ? 0 : cta_of(a, (qi + 1) * a.T - 1);
+            const int64_t slot = seg ? idiv(lt0, seg) : (int64_t)blockIdx.x - c_first;
+            const bool whole = !seg && c_first == c_last;
             // the CTA holding the query's first tile tells the combine how many partials it has
             if (a.nslots && lt0 == 0 && tid == 0) a.nslots[qi] = whole ? 0 : (int32_t)(c_last - c_first + 1);
             {
@@ -1100,10 +1110,10 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
                 qi = idiv(g, a.T);
                 lt = (int)(g - qi * a.T);
                 const QueryInfo inf = query_info(a, qi);
-                if (!tile_live(a, inf, lt)) continue;
+                if (!tile_live<kLean>(a, inf, lt)) continue;
                 st = tcount & 1;
                 ++tcount;
-                if (is_gathered(a, lt)) {
+                if (is_gathered<kLean>(a, lt)) {
                     ++g;
                     return true;
                 }
@@ -1312,8 +1322,10 @@ cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool spars
     a.status = status;
     a.theta = rope_theta(g);
     {
-        cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(attend_tc_kernel<true>), kSmem);
-        if (e == cudaSuccess) e = set_smem_attr(reinterpret_cast<const void*>(attend_tc_kernel<false>), kSmem);
+        cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(attend_tc_kernel<true, true>), kSmem);
+        if (e == cudaSuccess) e = set_smem_attr(reinterpret_cast<const void*>(attend_tc_kernel<true, false>), kSmem);
+        if (e == cudaSuccess) e = set_smem_attr(reinterpret_cast<const void*>(attend_tc_kernel<false, true>), kSmem);
+        if (e == cudaSuccess) e = set_smem_attr(reinterpret_cast<const void*>(attend_tc_kernel<false, false>), kSmem);
         if (e != cudaSuccess) return e;
     }
     CUtensorMap tm_q;
@@ -1323,12 +1335,23 @@ cudaError_t launch_attend_tc(const Geometry& g, const AttendPlan& pl, bool spars
         const uint32_t box[3] = {64, (uint32_t)kH, 1};
         if (!make_tmap_bf16(&tm_q, q, 3, d, sd, box)) return cudaErrorInvalidValue;
     }
-    // the split issue layout where no tile is gathered
-    const cudaError_t e = (a.pre || a.topk_idx == nullptr)
-        ? launch_dependent(attend_tc_kernel<true>, dim3(pl.tc_grid), dim3(Roles<true>::kThreads), kSmem, st,
-                           tm_sel, tm_win, tm_q, a)
-        : launch_dependent(attend_tc_kernel<false>, dim3(pl.tc_grid), dim3(Roles<false>::kThreads), kSmem, st,
-                           tm_sel, tm_win, tm_q, a);
+    // the split issue layout where no tile is gathered; the lean build
+    // where there are no fixed splits, no pre-gathered rows and the window
+    // (if any) is a ring
+    const bool split = a.pre || a.topk_idx == nullptr;
+    const bool lean = a.seg == 0 && !a.pre && a.win_pos0 == nullptr;
+    const dim3 grid(pl.tc_grid);
+    cudaError_t e;
+    if (split)
+        e = lean ? launch_dependent(attend_tc_kernel<true, true>, grid, dim3(Roles<true>::kThreads), kSmem, st,
+                                    tm_sel, tm_win, tm_q, a)
+                 : launch_dependent(attend_tc_kernel<true, false>, grid, dim3(Roles<true>::kThreads), kSmem, st,
+                                    tm_sel, tm_win, tm_q, a);
+    else
+        e = lean ? launch_dependent(attend_tc_kernel<false, true>, grid, dim3(Roles<false>::kThreads), kSmem, st,
+                                    tm_sel, tm_win, tm_q, a)
+                 : launch_dependent(attend_tc_kernel<false, false>, grid, dim3(Roles<false>::kThreads), kSmem, st,
+                                    tm_sel, tm_win, tm_q, a);
     note_launch();
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
