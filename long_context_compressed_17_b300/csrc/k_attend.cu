@@ -414,6 +414,7 @@ cudaError_t launch_attend(const Geometry& g, const AttendPlan& pl, bool sparse, 
     const int64_t items = (!ranges || by_query) ? (int64_t)Q * H : (int64_t)(pl.tc_grid - 1) * H;
     if (items == 0) return cudaSuccess;  // every query was finished by its only CTA
     if (g.D % 128 != 0 || g.D > 512) return cudaErrorInvalidValue;  // the combine's lane layout
+    if (items >= (1LL << 31)) return cudaErrorInvalidValue;         // its item arithmetic is 32-bit
     const int64_t blocks = (items + kCombineWarps - 1) / kCombineWarps;
     // launched in stream order: as a programmatic dependent of the attention
     // kernel it took 2-4 us longer a step (CSA decode 128K, HCA decode 1M)
