@@ -18,14 +18,22 @@
 namespace csa {
 
 constexpr int kCompressThreads = 256;
+
+// This thread's RoPE frequency when it is one of the 32 that rotate a pair.
+__device__ __forceinline__ double rope_theta_of(const RopeTheta& theta) {
+    return threadIdx.x < kRopeDims / 2 ? theta.t[threadIdx.x] : 0.0;
+}
 constexpr size_t kCompressStageMax = 160 * 1024;  // raw block staged in smem up to this size
 
 // row[0, D) holds a pooled vector (shared memory) and ss each thread's partial
 // sum of its squares: RMSNorm it, rotate its last 64 dims at position pos and
-// store it into a cache row at dst (whole CTA; red: 32 floats of scratch).
+// store it into a cache row at dst (whole CTA; red: 32 floats of scratch;
+// theta_j: thread j < 32's RoPE frequency).  Out of line: the kernels call it
+// from up to four places, and the inlined copies (with the sine, cosine and
+// FP8 packing code) made them 77-111 KB of code that each CTA runs once.
 template <int NT>
-__device__ void norm_rope_store(float* row, float ss, float* red, int D, float eps, double pos,
-                                const RopeTheta& theta, int kvfmt, uint8_t* dst) {
+__device__ __noinline__ void norm_rope_store(float* row, float ss, float* red, int D, float eps, double pos,
+                                             double theta_j, int kvfmt, uint8_t* dst) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int nwarps = NT / 32;
     ss = warp_sum(ss);
@@ -43,7 +51,7 @@ __device__ void norm_rope_store(float* row, float ss, float* red, int D, float e
     if (tid < kRopeDims / 2) {
         const int j = tid;
         float c, s;
-        rope_cs(pos, theta.t[j], &c, &s);
+        rope_cs(pos, theta_j, &c, &s);
         const int d0 = D - kRopeDims + 2 * j;
         const float x0 = row[d0], x1 = row[d0 + 1];
         row[d0] = x0 * c - x1 * s;
@@ -64,7 +72,7 @@ __device__ void window_row(const uint8_t* tok, int act, float* row, float* red, 
         row[d] = c;
         ss = fmaf(c, c, ss);
     }
-    norm_rope_store<NT>(row, ss, red, D, eps, pos, theta, kvfmt, dst);
+    norm_rope_store<NT>(row, ss, red, D, eps, pos, rope_theta_of(theta), kvfmt, dst);
 }
 
 // The block of m raw rows at src (shared memory or global) pooled into one
@@ -115,7 +123,7 @@ __device__ __forceinline__ void pool_block_store(const uint8_t* src, int act, in
         ss = fmaf(c, c, ss);
     }
     // RMSNorm, partial RoPE at the block's last position, store
-    norm_rope_store<NT>(row, ss, red, D, eps, pos, theta, kvfmt, dst);
+    norm_rope_store<NT>(row, ss, red, D, eps, pos, rope_theta_of(theta), kvfmt, dst);
 }
 
 // grid (n_blocks_out, B).  Dynamic smem: (m + D + 32) floats, rounded up to
@@ -252,7 +260,7 @@ __device__ __forceinline__ void cluster_pool_store(const ClusterSmem& c, int ran
         row[d] = cc;
         ss = fmaf(cc, cc, ss);
     }
-    norm_rope_store<kCompressThreads>(row, ss, red, D, eps, pos, theta, kvfmt, entry_dst);
+    norm_rope_store<kCompressThreads>(row, ss, red, D, eps, pos, rope_theta_of(theta), kvfmt, entry_dst);
 }
 
 __global__ void __launch_bounds__(kCompressThreads)
