@@ -220,6 +220,25 @@ __global__ void __launch_bounds__(kAttThreads) attend_generic_kernel(AttendArgs 
 //   otherwise there are (grid-1)*H items and item (b-1, h) handles the query
 //   cut by boundary b, if b is the first boundary inside it.
 constexpr int kCombineWarps = 4;
+
+// The query cut by CTA boundary b (first tile of CTA b inside it) whose
+// first boundary it is, and its partial count, or qi = -1 (the boundary
+// falls between queries, or the query was met at an earlier boundary).  Out
+// of line: only prefill-sized batches take it, and inlined it was 40% of the
+// combine's code.  Tile counts are below 2^31.
+__device__ __noinline__ void boundary_query(int64_t b, int64_t tiles, int64_t total, int grid, int qcta, int qrem,
+                                            int qc, int64_t* qi_out, int* sq_out) {
+    const TileDeal deal{total, tiles, grid, qcta, qrem, qc};
+    const int64_t g = deal.begin(b);  // first tile of CTA b
+    const uint32_t qi = (uint32_t)g / (uint32_t)tiles;
+    *qi_out = -1;
+    if ((int64_t)qi * tiles == g) return;  // the boundary falls between queries
+    const int64_t c0 = deal.cta_of((int64_t)qi * tiles);
+    if (c0 + 1 != b) return;               // handled at the query's first boundary
+    *qi_out = qi;
+    *sq_out = (int)(deal.cta_of(((int64_t)qi + 1) * tiles - 1) - c0 + 1);
+}
+
 __global__ void __launch_bounds__(32 * kCombineWarps)
     attend_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                           const int32_t* __restrict__ nslots, int S_alloc, int H, int D,
@@ -234,14 +253,8 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
     int64_t qi = unit;
     int Sq = S_alloc;  // an upper bound until nslots is read
     if (tiles > 0 && !by_query) {
-        const TileDeal deal{total, tiles, grid, qcta, qrem, qc};
-        const int64_t b = unit + 1;
-        const int64_t g = deal.begin(b);         // first tile of CTA b
-        if (g % tiles == 0) return;              // the boundary falls between queries
-        qi = g / tiles;
-        const int64_t c0 = deal.cta_of(qi * tiles);
-        if (c0 + 1 != b) return;                 // handled at the query's first boundary
-        Sq = (int)(deal.cta_of((qi + 1) * tiles - 1) - c0 + 1);
+        boundary_query(unit + 1, tiles, total, grid, qcta, qrem, qc, &qi, &Sq);
+        if (qi < 0) return;
     }
     const int S = S_alloc;
     const float* ml = part_ml + (qi * S * H + h) * 2;  // slot s: ml[s * 2H], ml[s * 2H + 1]
