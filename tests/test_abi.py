@@ -180,6 +180,24 @@ def _inv_splits(T):
     return -(-T // s)
 
 
+def test_attend_workspace_partial_counts_and_wide_fallback(L):
+    """Tensor-core ranges (bf16, D = 512, 64 heads, k = 1024, W = 128: 18 tiles
+    a query): at Q = 32 on 148 SMs the ranges are query-aligned, 4 or 5 CTAs
+    a query, so 5 partial slots, plus one int32 partial count per query.  At
+    Q*(18 + 5) >= 2^31 tile units the planner hands the call to the CUDA-core
+    kernel: one split of all 1152 rows, no partial counts."""
+    import torch
+    if torch.cuda.is_available() and torch.cuda.get_device_properties(0).multi_processor_count != 148:
+        pytest.skip("the expected ranges assume 148 SMs")
+    p = L.params(512, 4, topk=1024, window=128)
+    Q = 32
+    want = 256 + _al(Q * 5 * 64 * 512 * 4) + _al(Q * 5 * 64 * 2 * 4) + _al(Q * 4)
+    assert L.csa_workspace_bytes(p, L.OP_ATTEND, Q, Q, 64, 0, 32768, 128) == want
+    Q = (1 << 31) // 23 + 1
+    want = 256 + _al(Q * 64 * 512 * 4) + _al(Q * 64 * 2 * 4)
+    assert L.csa_workspace_bytes(p, L.OP_ATTEND, Q, Q, 64, 0, 32768, 128) == want
+
+
 @pytest.mark.parametrize("k,W,n_cap,Q,B", [(1024, 128, 32768, 32, 32), (1024, 128, 4096, 5, 5),
                                            (64, 0, 4096, 3, 3), (100, 128, 4096, 8, 2)])
 def test_batch_invariant_csa_workspace_follows_the_split_rule(L, k, W, n_cap, Q, B):
